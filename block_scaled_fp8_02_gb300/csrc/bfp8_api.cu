@@ -1,0 +1,449 @@
+// bfp8_api.cu -- the libbfp8 C ABI: argument validation, device checks,
+// schedule planning, TMA tensor maps and kernel launches.  See include/bfp8.h
+// for the contract of every entry point.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+
+#include "../../include/bfp8.h"
+#include "bfp8_gemm_kernel.cuh"
+#include "bfp8_internal.h"
+#include "bfp8_ptx.cuh"
+
+namespace bfp8 {
+namespace {
+
+// Library-owned device state: the failure word kernels report into.
+__device__ int g_dev_err;
+__device__ unsigned long long g_selftest_elapsed;
+__device__ int g_selftest_ok;
+
+constexpr unsigned long long kWaitLimitCycles = 1ull << 31;  // ~1 s at 2 GHz
+constexpr int kMaxDevices = 64;
+
+thread_local std::string t_last_error;
+
+bfp8_status fail(bfp8_status st, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  t_last_error = buf;
+  return st;
+}
+
+bfp8_status ok() {
+  t_last_error.clear();
+  return BFP8_OK;
+}
+
+struct DevInfo {
+  bool ready = false;
+  int cc_major = 0, cc_minor = 0, sms = 0;
+  int* err = nullptr;
+};
+DevInfo g_dev[kMaxDevices];
+std::mutex g_dev_mu;
+
+// Checks the current device is an sm_103 part and caches its properties.
+bfp8_status current_device(DevInfo* out, int* dev_out) {
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return fail(BFP8_ERR_UNSUPPORTED, "no CUDA device: %s", cudaGetErrorString(e));
+  }
+  if (dev < 0 || dev >= kMaxDevices) return fail(BFP8_ERR_UNSUPPORTED, "device index %d", dev);
+  std::lock_guard<std::mutex> lk(g_dev_mu);
+  DevInfo& d = g_dev[dev];
+  if (!d.ready) {
+    if (cudaDeviceGetAttribute(&d.cc_major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&d.cc_minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+      cudaGetLastError();
+      return fail(BFP8_ERR_CUDA, "cudaDeviceGetAttribute failed on device %d", dev);
+    }
+    if (d.cc_major == 10 && d.cc_minor == 3) {
+      void* p = nullptr;
+      e = cudaGetSymbolAddress(&p, g_dev_err);
+      if (e != cudaSuccess) {
+        cudaGetLastError();
+        return fail(BFP8_ERR_CUDA, "cudaGetSymbolAddress(failure word): %s", cudaGetErrorString(e));
+      }
+      d.err = static_cast<int*>(p);
+    }
+    d.ready = true;
+  }
+  if (!(d.cc_major == 10 && d.cc_minor == 3))
+    return fail(BFP8_ERR_UNSUPPORTED, "device %d is sm_%d%d; libbfp8 is built for sm_103a only", dev,
+                d.cc_major, d.cc_minor);
+  *out = d;
+  if (dev_out) *dev_out = dev;
+  return BFP8_OK;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+bfp8_status get_encoder(PFN_cuTensorMapEncodeTiled_v12000* fn) {
+  std::call_once(g_encode_once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    cudaGetLastError();
+  });
+  if (!g_encode) return fail(BFP8_ERR_CUDA, "cuTensorMapEncodeTiled is not available");
+  *fn = g_encode;
+  return BFP8_OK;
+}
+
+// Tensor map over a [rows, inner] uint8 matrix (row stride `inner` bytes),
+// box 128 (K) x box_rows, 128-byte swizzle, zero fill outside the matrix.
+bfp8_status encode_operand(CUtensorMap* map, const void* ptr, int64_t rows, int64_t inner,
+                           int box_rows) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc;
+  bfp8_status st = get_encoder(&enc);
+  if (st != BFP8_OK) return st;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(inner)};
+  const cuuint32_t box[2] = {128u, static_cast<cuuint32_t>(box_rows)};
+  const cuuint32_t estr[2] = {1u, 1u};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(ptr), dims, strides, box,
+                   estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    return fail(BFP8_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d) for [%lld x %lld] box %d", (int)r,
+                (long long)rows, (long long)inner, box_rows);
+  return BFP8_OK;
+}
+
+inline int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+inline size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+struct Plan {
+  bool swap = false;
+  int bn = 0;
+  bool relayout = false;
+  int64_t kp = 0;            // inner extent of the operand tensor maps
+  Sched sched{};
+  size_t off_counters = 0, off_partials = 0, off_a = 0, off_b = 0, total = 0;
+};
+
+bfp8_status check_options(const bfp8_gemm_options* opt) {
+  if (!opt) return BFP8_OK;
+  if (opt->schedule < 0 || opt->schedule > 2)
+    return fail(BFP8_ERR_INVALID_ARG, "options.schedule = %d (expected 0, 1 or 2)", opt->schedule);
+  if (opt->max_ctas < 0) return fail(BFP8_ERR_INVALID_ARG, "options.max_ctas = %d", opt->max_ctas);
+  if (opt->tile_n != 0 && opt->tile_n != 128 && opt->tile_n != 256)
+    return fail(BFP8_ERR_INVALID_ARG, "options.tile_n = %d (expected 0, 128 or 256)", opt->tile_n);
+  return BFP8_OK;
+}
+
+// Small M: the weights fill the 128-row MMA slot and the activation rows the
+// N slot, padded to the next supported width.
+int swap_tile_n(int64_t M) {
+  if (M <= 16) return 16;
+  if (M <= 32) return 32;
+  if (M <= 64) return 64;
+  if (M <= 128) return 128;
+  return 256;
+}
+
+constexpr int64_t kSwapMaxM = 256;
+
+bfp8_status make_plan(int64_t M, int64_t N, int64_t K, int num_sms, const bfp8_gemm_options* opt,
+                      bool unaligned, Plan* p) {
+  const int schedule = opt ? opt->schedule : BFP8_SCHEDULE_AUTO;
+  p->swap = schedule == BFP8_SCHEDULE_SWAP_AB ||
+            (schedule == BFP8_SCHEDULE_AUTO && M <= kSwapMaxM);
+  p->bn = p->swap ? swap_tile_n(M) : ((opt && opt->tile_n == 128) ? 128 : 256);
+  const int64_t G = cdiv(K, 128);
+  const int64_t p_tiles = p->swap ? cdiv(N, 128) : cdiv(M, 128);
+  const int64_t q_tiles = p->swap ? cdiv(M, p->bn) : cdiv(N, p->bn);
+  int max_ctas = num_sms;
+  if (opt && opt->max_ctas > 0 && opt->max_ctas < max_ctas) max_ctas = opt->max_ctas;
+  p->sched = make_sched(p_tiles, q_tiles, static_cast<int32_t>(G), max_ctas);
+  p->relayout = unaligned || (K % 16) != 0;
+  p->kp = p->relayout ? cdiv(K, 16) * 16 : K;
+  size_t off = 0;
+  const int64_t sk_tiles = p->sched.tiles - p->sched.dp_tiles;
+  p->off_counters = off;
+  off += align256(static_cast<size_t>(sk_tiles) * sizeof(int));
+  p->off_partials = off;
+  if (p->sched.sk_units > 0)
+    off += align256(static_cast<size_t>(p->sched.grid) * 2 * 128 * p->bn * sizeof(float));
+  p->off_a = off;
+  if (p->relayout) off += align256(static_cast<size_t>(M) * p->kp);
+  p->off_b = off;
+  if (p->relayout) off += align256(static_cast<size_t>(N) * p->kp);
+  p->total = off;
+  return BFP8_OK;
+}
+
+bfp8_status check_gemm_sizes(int64_t M, int64_t N, int64_t K) {
+  const int64_t lim = 0x7FFFFFFF;
+  if (M < 1 || N < 1 || K < 1)
+    return fail(BFP8_ERR_INVALID_ARG, "M, N, K must be >= 1 (got %lld, %lld, %lld)", (long long)M,
+                (long long)N, (long long)K);
+  if (M > lim || N > lim || K > lim)
+    return fail(BFP8_ERR_INVALID_ARG, "M, N, K must be < 2^31");
+  return BFP8_OK;
+}
+
+bool misaligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) != 0; }
+
+// One bounded wait on a barrier nothing arrives on.
+__global__ void selftest_wait_kernel(unsigned long long limit) {
+  __shared__ __align__(8) uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_addr(&bar), 1);
+    fence_barrier_init();
+  }
+  __syncwarp();
+  if (threadIdx.x == 0) {
+    const long long t0 = clock64();
+    const bool done = mbar_wait_bounded(smem_addr(&bar), 0, limit);
+    g_selftest_elapsed = static_cast<unsigned long long>(clock64() - t0);
+    g_selftest_ok = done ? 1 : 0;
+  }
+}
+
+}  // namespace
+}  // namespace bfp8
+
+using namespace bfp8;
+
+extern "C" {
+
+int bfp8_version(void) { return BFP8_VERSION; }
+
+const char* bfp8_last_error(void) { return t_last_error.c_str(); }
+
+const char* bfp8_status_string(int status) {
+  switch (status) {
+    case BFP8_OK: return "BFP8_OK";
+    case BFP8_ERR_INVALID_ARG: return "BFP8_ERR_INVALID_ARG";
+    case BFP8_ERR_ALIGNMENT: return "BFP8_ERR_ALIGNMENT";
+    case BFP8_ERR_UNSUPPORTED: return "BFP8_ERR_UNSUPPORTED";
+    case BFP8_ERR_CUDA: return "BFP8_ERR_CUDA";
+    case BFP8_ERR_WORKSPACE: return "BFP8_ERR_WORKSPACE";
+    case BFP8_ERR_DEVICE_TIMEOUT: return "BFP8_ERR_DEVICE_TIMEOUT";
+    default: return "BFP8_ERR_UNKNOWN";
+  }
+}
+
+int64_t bfp8_scale_ld(int64_t M) { return M <= 0 ? 0 : (M + 3) / 4 * 4; }
+
+bfp8_status bfp8_group_quant(const void* x, int in_dtype, int64_t M, int64_t K, int64_t ld_x,
+                             int group, int col_major, void* q, int64_t ld_q, float* s,
+                             int64_t ld_s, void* stream) {
+  if (in_dtype != BFP8_IN_BF16 && in_dtype != BFP8_IN_F32)
+    return fail(BFP8_ERR_INVALID_ARG, "in_dtype = %d (expected BFP8_IN_BF16 or BFP8_IN_F32)", in_dtype);
+  if (group != 128) return fail(BFP8_ERR_INVALID_ARG, "group = %d: only 128 is supported", group);
+  if (col_major != 0 && col_major != 1)
+    return fail(BFP8_ERR_INVALID_ARG, "col_major = %d (expected 0 or 1)", col_major);
+  if (M < 0 || K < 0) return fail(BFP8_ERR_INVALID_ARG, "negative size M=%lld K=%lld", (long long)M, (long long)K);
+  if (M == 0 || K == 0) return ok();
+  const int64_t G = (K + 127) / 128;
+  if (!x || !q || !s) return fail(BFP8_ERR_INVALID_ARG, "null pointer (x=%p q=%p s=%p)", x, q, (void*)s);
+  if (ld_x < K) return fail(BFP8_ERR_INVALID_ARG, "ld_x = %lld < K = %lld", (long long)ld_x, (long long)K);
+  if (ld_q < K) return fail(BFP8_ERR_INVALID_ARG, "ld_q = %lld < K = %lld", (long long)ld_q, (long long)K);
+  if (col_major ? ld_s < M : ld_s < G)
+    return fail(BFP8_ERR_INVALID_ARG, "ld_s = %lld too small for the %s layout", (long long)ld_s,
+                col_major ? "column-major" : "row-major");
+  if (misaligned(x, in_dtype == BFP8_IN_F32 ? 4 : 2))
+    return fail(BFP8_ERR_ALIGNMENT, "x is not aligned to its element size");
+  if (misaligned(s, 4)) return fail(BFP8_ERR_ALIGNMENT, "s is not 4-byte aligned");
+  DevInfo d;
+  bfp8_status st = current_device(&d, nullptr);
+  if (st != BFP8_OK) return st;
+  cudaError_t e = launch_group_quant(x, in_dtype == BFP8_IN_F32, M, K, ld_x, static_cast<uint8_t*>(q),
+                                     ld_q, s, col_major, ld_s, d.sms,
+                                     static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail(BFP8_ERR_CUDA, "quantisation launch: %s", cudaGetErrorString(e));
+  return ok();
+}
+
+bfp8_status bfp8_gemm_plan(int64_t M, int64_t N, int64_t K, int num_sms,
+                           const bfp8_gemm_options* opt, int operands_unaligned,
+                           bfp8_plan_info* info) {
+  bfp8_status st = check_gemm_sizes(M, N, K);
+  if (st != BFP8_OK) return st;
+  if ((st = check_options(opt)) != BFP8_OK) return st;
+  if (num_sms < 1) return fail(BFP8_ERR_INVALID_ARG, "num_sms = %d", num_sms);
+  if (!info) return fail(BFP8_ERR_INVALID_ARG, "info is null");
+  Plan p;
+  make_plan(M, N, K, num_sms, opt, operands_unaligned != 0, &p);
+  info->swap_ab = p.swap;
+  info->tile_n = p.bn;
+  info->stages = gemm_stages(p.swap, p.bn);
+  info->grid = p.sched.grid;
+  info->tiles = p.sched.tiles;
+  info->k_blocks = p.sched.G;
+  info->dp_tiles = p.sched.dp_tiles;
+  info->sk_units = p.sched.sk_units;
+  info->relayout = p.relayout;
+  info->workspace_bytes = p.total;
+  return ok();
+}
+
+bfp8_status bfp8_plan_unit(int64_t M, int64_t N, int64_t K, int num_sms,
+                           const bfp8_gemm_options* opt, int cta, int64_t j, int64_t* num_units_out,
+                           int64_t* tile, int64_t* k_block) {
+  bfp8_status st = check_gemm_sizes(M, N, K);
+  if (st != BFP8_OK) return st;
+  if ((st = check_options(opt)) != BFP8_OK) return st;
+  if (num_sms < 1) return fail(BFP8_ERR_INVALID_ARG, "num_sms = %d", num_sms);
+  Plan p;
+  make_plan(M, N, K, num_sms, opt, false, &p);
+  if (cta < 0 || cta >= p.sched.grid) return fail(BFP8_ERR_INVALID_ARG, "cta %d out of range", cta);
+  const int64_t n = num_units(p.sched, cta);
+  if (num_units_out) *num_units_out = n;
+  if (j >= 0) {
+    if (j >= n) return fail(BFP8_ERR_INVALID_ARG, "unit %lld out of range", (long long)j);
+    const Unit u = unit_at(p.sched, cta, j);
+    if (tile) *tile = u.tile;
+    if (k_block) *k_block = u.kb;
+  }
+  return ok();
+}
+
+bfp8_status bfp8_gemm_workspace_size(int64_t M, int64_t N, int64_t K,
+                                     const bfp8_gemm_options* opt, int operands_unaligned,
+                                     size_t* bytes) {
+  bfp8_status st = check_gemm_sizes(M, N, K);
+  if (st != BFP8_OK) return st;
+  if ((st = check_options(opt)) != BFP8_OK) return st;
+  if (!bytes) return fail(BFP8_ERR_INVALID_ARG, "bytes is null");
+  DevInfo d;
+  if ((st = current_device(&d, nullptr)) != BFP8_OK) return st;
+  Plan p;
+  make_plan(M, N, K, d.sms, opt, operands_unaligned != 0, &p);
+  *bytes = p.total;
+  return ok();
+}
+
+bfp8_status bfp8_gemm_ex(const void* A, const void* B, const float* As, int as_col_major,
+                         int64_t ld_as, const float* Bs, void* out, int64_t M, int64_t N,
+                         int64_t K, void* workspace, size_t workspace_bytes,
+                         const bfp8_gemm_options* opt, void* stream) {
+  bfp8_status st = check_gemm_sizes(M, N, K);
+  if (st != BFP8_OK) return st;
+  if ((st = check_options(opt)) != BFP8_OK) return st;
+  if (!A || !B || !As || !Bs || !out)
+    return fail(BFP8_ERR_INVALID_ARG, "null pointer (A=%p B=%p As=%p Bs=%p out=%p)", A, B,
+                (const void*)As, (const void*)Bs, out);
+  if (as_col_major != 0 && as_col_major != 1)
+    return fail(BFP8_ERR_INVALID_ARG, "as_col_major = %d (expected 0 or 1)", as_col_major);
+  const int64_t G = cdiv(K, 128);
+  if (as_col_major ? ld_as < M : ld_as < G)
+    return fail(BFP8_ERR_INVALID_ARG, "ld_as = %lld too small for the %s layout", (long long)ld_as,
+                as_col_major ? "column-major" : "row-major");
+  if (misaligned(As, 4) || misaligned(Bs, 4))
+    return fail(BFP8_ERR_ALIGNMENT, "As and Bs must be 4-byte aligned");
+  if (misaligned(out, 2)) return fail(BFP8_ERR_ALIGNMENT, "out must be 2-byte aligned");
+  DevInfo d;
+  if ((st = current_device(&d, nullptr)) != BFP8_OK) return st;
+  const bool unaligned = misaligned(A, 16) || misaligned(B, 16);
+  Plan p;
+  make_plan(M, N, K, d.sms, opt, unaligned, &p);
+  if (p.total > 0) {
+    if (!workspace)
+      return fail(BFP8_ERR_WORKSPACE, "this problem needs %zu workspace bytes; got none", p.total);
+    if (workspace_bytes < p.total)
+      return fail(BFP8_ERR_WORKSPACE, "workspace of %zu bytes is smaller than the %zu needed",
+                  workspace_bytes, p.total);
+    if (misaligned(workspace, 256))
+      return fail(BFP8_ERR_WORKSPACE, "workspace must be 256-byte aligned");
+  }
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  const void* a_op = A;
+  const void* b_op = B;
+  if (p.relayout) {
+    cudaError_t e = launch_relayout(static_cast<const uint8_t*>(A), M, K, ws + p.off_a, p.kp, d.sms, cs);
+    if (e == cudaSuccess)
+      e = launch_relayout(static_cast<const uint8_t*>(B), N, K, ws + p.off_b, p.kp, d.sms, cs);
+    if (e != cudaSuccess) return fail(BFP8_ERR_CUDA, "operand re-layout launch: %s", cudaGetErrorString(e));
+    a_op = ws + p.off_a;
+    b_op = ws + p.off_b;
+  }
+  CUtensorMap tmP, tmQ;
+  const void* p_ptr = p.swap ? b_op : a_op;
+  const void* q_ptr = p.swap ? a_op : b_op;
+  const int64_t p_rows = p.swap ? N : M;
+  const int64_t q_rows = p.swap ? M : N;
+  if ((st = encode_operand(&tmP, p_ptr, p_rows, p.kp, 128)) != BFP8_OK) return st;
+  if ((st = encode_operand(&tmQ, q_ptr, q_rows, p.kp, p.bn)) != BFP8_OK) return st;
+
+  GemmArgs a{};
+  a.As = As;
+  a.ld_as = ld_as;
+  a.as_col_major = as_col_major;
+  a.NT = static_cast<int32_t>(cdiv(N, 128));
+  a.Bs = Bs;
+  a.out = static_cast<__nv_bfloat16*>(out);
+  a.M = M;
+  a.N = N;
+  a.sched = p.sched;
+  a.counters = reinterpret_cast<int*>(ws ? ws + p.off_counters : nullptr);
+  a.partials = reinterpret_cast<float*>(ws ? ws + p.off_partials : nullptr);
+  a.vec_store = (!misaligned(out, 16) && (N % 8) == 0) ? 1 : 0;
+  a.err = d.err;
+  a.wait_limit = kWaitLimitCycles;
+  cudaError_t e = p.swap ? launch_gemm_swap(p.bn, tmP, tmQ, a, cs) : launch_gemm_wide(p.bn, tmP, tmQ, a, cs);
+  if (e != cudaSuccess) return fail(BFP8_ERR_CUDA, "GEMM launch: %s", cudaGetErrorString(e));
+  return ok();
+}
+
+bfp8_status bfp8_gemm(const void* A, const void* B, const float* As, int as_col_major,
+                      int64_t ld_as, const float* Bs, void* out, int64_t M, int64_t N, int64_t K,
+                      void* workspace, size_t workspace_bytes, void* stream) {
+  return bfp8_gemm_ex(A, B, As, as_col_major, ld_as, Bs, out, M, N, K, workspace, workspace_bytes,
+                      nullptr, stream);
+}
+
+bfp8_status bfp8_device_status(int* code, int clear) {
+  if (!code) return fail(BFP8_ERR_INVALID_ARG, "code is null");
+  DevInfo d;
+  bfp8_status st = current_device(&d, nullptr);
+  if (st != BFP8_OK) return st;
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e == cudaSuccess) e = cudaMemcpyFromSymbol(code, g_dev_err, sizeof(int));
+  if (e == cudaSuccess && clear) {
+    const int zero = 0;
+    e = cudaMemcpyToSymbol(g_dev_err, &zero, sizeof(int));
+  }
+  if (e != cudaSuccess) return fail(BFP8_ERR_CUDA, "reading the failure word: %s", cudaGetErrorString(e));
+  return ok();
+}
+
+bfp8_status bfp8_selftest_bounded_wait(uint64_t limit_cycles, uint64_t* elapsed, void* stream) {
+  DevInfo d;
+  bfp8_status st = current_device(&d, nullptr);
+  if (st != BFP8_OK) return st;
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  selftest_wait_kernel<<<1, 32, 0, cs>>>(limit_cycles);
+  cudaError_t e = cudaGetLastError();
+  unsigned long long el = 0;
+  int done = 0;
+  if (e == cudaSuccess) e = cudaMemcpyFromSymbolAsync(&el, g_selftest_elapsed, sizeof(el), 0, cudaMemcpyDeviceToHost, cs);
+  if (e == cudaSuccess) e = cudaMemcpyFromSymbolAsync(&done, g_selftest_ok, sizeof(done), 0, cudaMemcpyDeviceToHost, cs);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(cs);
+  if (e != cudaSuccess) return fail(BFP8_ERR_CUDA, "bounded-wait self-test: %s", cudaGetErrorString(e));
+  if (elapsed) *elapsed = el;
+  if (!done) return fail(BFP8_ERR_DEVICE_TIMEOUT, "the wait gave up after %llu cycles", el);
+  return ok();
+}
+
+}  // extern "C"

@@ -1,0 +1,414 @@
+// bfp8_gemm_kernel.cuh -- blocked W8A8 FP8 GEMM for sm_103a (tcgen05 + TMA).
+//
+//   out[m, n] = bf16( sum_kb (A[m, kb] . B[n, kb]) * As[m, kb] * Bs[n / 128, kb] )
+//
+// with A [M, K] and B [N, K] float8_e4m3fn (K-major), As the per-token-group
+// activation scales (1 x 128) and Bs the per-tile weight scales (128 x 128), as
+// in native_w8a8_block_matmul / apply_block_scaled_mm of the vLLM PR 49932
+// digest ("implementation breakdown", "key source snippet").
+//
+// The fp32 scales are arbitrary (not powers of two), so the tensor core's
+// block-scaled MMA cannot apply them.  Each 128-wide K block is therefore its
+// own MMA problem: the tensor core writes the block's exact-product fp32 sum
+// into TMEM, and CUDA-core warps read it back, multiply by As * Bs and add it
+// to an fp32 accumulator held in registers (the "promotion" of the DeepGEMM
+// design the lmdeploy PR 4830 page follows for large M).
+//
+// Roles (one CTA per SM, persistent):
+//   warps 0 .. NE-1  promotion / epilogue warps; warp w reads TMEM lanes
+//                    32*(w%4) .. +31 and column half w/4
+//   warp  NE         TMA producer (one lane): A/B tiles into a STAGES-deep ring
+//   warp  NE+1       TMEM owner and MMA issuer (one lane)
+// TMEM holds two partial buffers of BN columns, so the MMA of block kb+1 runs
+// while block kb is promoted.
+//
+// SWAP = false: MMA M slot = 128 activation rows, N slot = BN weight rows
+//               (large M).
+// SWAP = true:  MMA M slot = 128 weight rows, N slot = BN >= M activation rows
+//               ("swap AB": the transposed schedule the lmdeploy page uses for
+//               small M, so the 128-row MMA is filled by weights).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+
+#include <cstdint>
+
+#include "bfp8_ptx.cuh"
+#include "bfp8_sched.h"
+
+namespace bfp8 {
+
+// Device-side failure codes (the first failure of a launch wins).
+enum : int {
+  kDevOk = 0,
+  kDevTimeoutProducer = 1,
+  kDevTimeoutMma = 2,
+  kDevTimeoutEpilogue = 3,
+  kDevTimeoutTail = 4,
+};
+
+struct GemmArgs {
+  const float* As;       // activation scales
+  int64_t ld_as;         // leading dimension of As
+  int32_t as_col_major;  // 1: As[kb * ld_as + m], 0: As[m * ld_as + kb]
+  int32_t NT;            // rows of Bs = ceil(N / 128); Bs row stride = G
+  const float* Bs;
+  __nv_bfloat16* out;    // [M, N] row-major
+  int64_t M, N;
+  Sched sched;
+  int* counters;         // one per stream-K tile, zero between launches
+  float* partials;       // grid * 2 slots of 128 x BN fp32
+  int32_t vec_store;     // out rows may be written 16 bytes at a time
+  int* err;              // device failure word
+  unsigned long long wait_limit;  // cycles before a wait gives up
+};
+
+__host__ __device__ constexpr int tmem_cols_for(int n) {
+  return n <= 32 ? 32 : n <= 64 ? 64 : n <= 128 ? 128 : n <= 256 ? 256 : 512;
+}
+
+template <int BN, bool SWAP>
+struct GemmCfg {
+  static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "MMA N for M=128 is 16..256 step 16");
+  static_assert(SWAP || BN % 128 == 0, "wide tiles cover whole 128-column weight-scale blocks");
+  static constexpr int kNE = BN > 128 ? 8 : 4;   // promotion warps
+  static constexpr int kNH = kNE / 4;            // column halves
+  static constexpr int kCPT = BN / kNH;          // accumulator columns per thread
+  // 16-column TMEM loads when two warps share a lane quadrant: 10 warps put three
+  // on some SM sub-partitions, which caps a thread at 168 registers.
+  static constexpr int kCH = (kCPT % 32 == 0 && kNH == 1) ? 32 : 16;
+  static constexpr int kThreads = (kNE + 2) * 32;
+  static constexpr int kPBytes = 128 * 128;
+  static constexpr int kQBytes = BN * 128;
+  static constexpr int kStageBytes = kPBytes + kQBytes;
+  static constexpr int kD = 3;                   // scale prefetch distance in units
+  static constexpr int kR = kD + 2;              // scale ring slots
+  static constexpr int kScaleBytes = kR * (128 + BN) * 4;
+  static constexpr int kSmemLimit = 232448;      // 227 KB per CTA
+  static constexpr int kFixed = 1024 /*align slack*/ + 256 /*barriers, flags*/ + kScaleBytes;
+  static constexpr int kStagesFit = (kSmemLimit - kFixed) / kStageBytes;
+  static constexpr int kStages = kStagesFit > 10 ? 10 : kStagesFit;
+  static_assert(kStages >= 2, "ring too small");
+  static constexpr int kOffBars = kStages * kStageBytes;
+  static constexpr int kOffTmemPtr = kOffBars + (2 * kStages + 4) * 8;
+  static constexpr int kOffFlags = kOffTmemPtr + 8;
+  static constexpr int kOffScaleP = (kOffFlags + 8 + 15) / 16 * 16;
+  static constexpr int kOffScaleQ = kOffScaleP + kR * 128 * 4;
+  static constexpr int kSmemBytes = kOffScaleQ + kR * BN * 4 + 1024;
+  static constexpr int kTmemCols = tmem_cols_for(2 * BN);
+  static constexpr uint32_t kIdesc = idesc_e4m3_f32(128, BN);
+};
+
+__device__ __forceinline__ void report_failure(int* err, int code) {
+  if (err != nullptr) atomicCAS(err, 0, code);
+}
+
+template <int BN, bool SWAP>
+__global__ void __launch_bounds__(GemmCfg<BN, SWAP>::kThreads, 1)
+    gemm_kernel(const __grid_constant__ CUtensorMap tmP, const __grid_constant__ CUtensorMap tmQ,
+                const GemmArgs a) {
+#if defined(__CUDA_ARCH__)
+  using C = GemmCfg<BN, SWAP>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_addr(smem_raw);
+  uint8_t* smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
+  const uint32_t sbase = smem_addr(smem);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const Sched& s = a.sched;
+  const int64_t cta = blockIdx.x;
+  const int nunits = static_cast<int>(num_units(s, cta));
+
+  auto bar_full = [&](int i) { return sbase + C::kOffBars + 8u * i; };
+  auto bar_empty = [&](int i) { return sbase + C::kOffBars + 8u * (C::kStages + i); };
+  auto bar_tfull = [&](int b) { return sbase + C::kOffBars + 8u * (2 * C::kStages + b); };
+  auto bar_tempty = [&](int b) { return sbase + C::kOffBars + 8u * (2 * C::kStages + 2 + b); };
+  auto stage_p = [&](int i) { return sbase + static_cast<uint32_t>(i * C::kStageBytes); };
+  auto stage_q = [&](int i) { return sbase + static_cast<uint32_t>(i * C::kStageBytes + C::kPBytes); };
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffTmemPtr);
+  volatile int* s_last_flag = reinterpret_cast<volatile int*>(smem + C::kOffFlags);
+  float* sP = reinterpret_cast<float*>(smem + C::kOffScaleP);
+  float* sQ = reinterpret_cast<float*>(smem + C::kOffScaleQ);
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < C::kStages; ++i) {
+      mbar_init(bar_full(i), 1);
+      mbar_init(bar_empty(i), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(bar_tfull(b), 1);
+      mbar_init(bar_tempty(b), C::kNE * 32);
+    }
+    *s_last_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == C::kNE + 1) {
+    tmem_alloc(smem_addr(tmem_slot), C::kTmemCols);
+    tmem_relinquish();
+  }
+  if (warp == C::kNE && lane == 0) {
+    tma_prefetch_desc(&tmP);
+    tma_prefetch_desc(&tmQ);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == C::kNE) {
+    // ------------------------------------------------------- TMA producer
+    if (lane == 0) {
+      int st = 0;
+      uint32_t ph = 0;
+      int issued = 0;
+      bool ok = true;
+      for (int j = 0; j < nunits; ++j) {
+        const Unit u = unit_at(s, cta, j);
+        if (!mbar_wait_bounded(bar_empty(st), ph ^ 1u, a.wait_limit)) {
+          report_failure(a.err, kDevTimeoutProducer);
+          ok = false;
+          break;
+        }
+        const int64_t p_tile = u.tile % s.p_tiles;
+        const int64_t q_tile = u.tile / s.p_tiles;
+        mbar_arrive_expect_tx(bar_full(st), C::kStageBytes);
+        tma_load_2d(stage_p(st), &tmP, bar_full(st), u.kb * 128, static_cast<int32_t>(p_tile * 128));
+        tma_load_2d(stage_q(st), &tmQ, bar_full(st), u.kb * 128, static_cast<int32_t>(q_tile * BN));
+        ++issued;
+        if (++st == C::kStages) { st = 0; ph ^= 1u; }
+      }
+      // Do not leave while copies into this CTA's shared memory may be in flight.
+      const int tail = issued < C::kStages ? issued : C::kStages;
+      for (int t = 0; t < tail; ++t) {
+        const int j = issued - 1 - t;
+        if (!mbar_wait_bounded(bar_full(j % C::kStages), (j / C::kStages) & 1, a.wait_limit)) {
+          report_failure(a.err, kDevTimeoutTail);
+          break;
+        }
+      }
+      (void)ok;
+    }
+    __syncwarp();
+  } else if (warp == C::kNE + 1) {
+    // ---------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      int st = 0;
+      uint32_t ph = 0;
+      int done = 0;
+      for (int j = 0; j < nunits; ++j) {
+        const int b = j & 1;
+        const uint32_t tph = (j >> 1) & 1;
+        if (!mbar_wait_bounded(bar_tempty(b), tph ^ 1u, a.wait_limit) ||
+            !mbar_wait_bounded(bar_full(st), ph, a.wait_limit)) {
+          report_failure(a.err, kDevTimeoutMma);
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem + static_cast<uint32_t>(b * BN);
+        const uint64_t adesc = sdesc_k_sw128(stage_p(st));
+        const uint64_t bdesc = sdesc_k_sw128(stage_q(st));
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          // advancing 32 fp8 elements along K = 32 bytes = 2 descriptor units
+          mma_f8f6f4(d_tmem, adesc + 2u * k, bdesc + 2u * k, C::kIdesc, k > 0 ? 1u : 0u);
+        }
+        mma_commit(bar_empty(st));
+        mma_commit(bar_tfull(b));
+        done = j + 1;
+        if (++st == C::kStages) { st = 0; ph ^= 1u; }
+      }
+      // The last commit fires when every MMA issued above has completed.
+      if (done > 0 && done < nunits) {
+        const int j = done - 1;
+        if (!mbar_wait_bounded(bar_tfull(j & 1), (j >> 1) & 1, a.wait_limit))
+          report_failure(a.err, kDevTimeoutTail);
+      }
+    }
+    __syncwarp();
+  } else {
+    // ---------------------------------------------- promotion and epilogue
+    const int quad = warp & 3;
+    const int half = warp >> 2;
+    const int r = quad * 32 + lane;          // TMEM lane = row of the P tile
+    const int col0 = half * C::kCPT;         // first TMEM column of this thread
+    const int etid = threadIdx.x;            // 0 .. NE*32-1
+    const uint32_t sP_addr = smem_addr(sP);
+    const uint32_t sQ_addr = smem_addr(sQ);
+
+    // Stages the scales of unit jj into ring slot jj % R (one cp.async group
+    // per unit, empty past the end so the group count stays uniform).
+    auto stage_scales = [&](int jj) {
+      if (jj < nunits) {
+        const Unit u = unit_at(s, cta, jj);
+        const int slot = jj % C::kR;
+        const int64_t p_tile = u.tile % s.p_tiles;
+        const int64_t q_tile = u.tile / s.p_tiles;
+        const int64_t kb = u.kb;
+        if (!SWAP) {
+          if (etid < 128) {
+            const int64_t m = p_tile * 128 + etid;
+            const bool ok = m < a.M;
+            const float* src =
+                ok ? a.As + (a.as_col_major ? kb * a.ld_as + m : m * a.ld_as + kb) : a.As;
+            cp_async_4(sP_addr + 4u * (slot * 128 + etid), src, ok ? 4u : 0u);
+          }
+          if (etid < BN / 128) {
+            const int64_t nb = q_tile * (BN / 128) + etid;
+            const bool ok = nb < a.NT;
+            const float* src = ok ? a.Bs + nb * s.G + kb : a.Bs;
+            cp_async_4(sQ_addr + 4u * (slot * BN + etid), src, ok ? 4u : 0u);
+          }
+        } else {
+          if (etid < BN) {
+            const int64_t m = q_tile * BN + etid;
+            const bool ok = m < a.M;
+            const float* src =
+                ok ? a.As + (a.as_col_major ? kb * a.ld_as + m : m * a.ld_as + kb) : a.As;
+            cp_async_4(sQ_addr + 4u * (slot * BN + etid), src, ok ? 4u : 0u);
+          }
+          if (etid == 0) cp_async_4(sP_addr + 4u * (slot * 128), a.Bs + p_tile * s.G + kb, 4u);
+        }
+      }
+      cp_async_commit();
+    };
+
+    float acc[C::kCPT];
+#pragma unroll
+    for (int i = 0; i < C::kCPT; ++i) acc[i] = 0.f;
+
+#pragma unroll
+    for (int d = 0; d < C::kD; ++d) stage_scales(d);
+
+    for (int j = 0; j < nunits; ++j) {
+      stage_scales(j + C::kD);
+      cp_async_wait<C::kD>();
+      named_bar_sync(1, C::kNE * 32);
+
+      const Unit u = unit_at(s, cta, j);
+      const int slot = j % C::kR;
+      const int b = j & 1;
+      if (!mbar_wait_bounded(bar_tfull(b), (j >> 1) & 1, a.wait_limit)) {
+        report_failure(a.err, kDevTimeoutEpilogue);
+        break;
+      }
+      tc_fence_after();
+
+      if (u.first) {
+#pragma unroll
+        for (int i = 0; i < C::kCPT; ++i) acc[i] = 0.f;
+      }
+      const uint32_t taddr = tmem + static_cast<uint32_t>(b * BN + col0) +
+                             (static_cast<uint32_t>(quad * 32) << 16);
+      if (!SWAP) {
+        const float sc = sP[slot * 128 + r] * sQ[slot * BN + col0 / 128];
+#pragma unroll
+        for (int c = 0; c < C::kCPT / C::kCH; ++c) {
+          uint32_t v[C::kCH];
+          if constexpr (C::kCH == 32) tmem_ld32(taddr + c * 32, v); else tmem_ld16(taddr + c * 16, v);
+          tmem_wait_ld_regs(v);
+#pragma unroll
+          for (int i = 0; i < C::kCH; ++i)
+            acc[c * C::kCH + i] = fmaf(__uint_as_float(v[i]), sc, acc[c * C::kCH + i]);
+        }
+      } else {
+        const float sb = sP[slot * 128];
+        const float* sq = sQ + slot * BN + col0;
+#pragma unroll
+        for (int c = 0; c < C::kCPT / C::kCH; ++c) {
+          uint32_t v[C::kCH];
+          if constexpr (C::kCH == 32) tmem_ld32(taddr + c * 32, v); else tmem_ld16(taddr + c * 16, v);
+          tmem_wait_ld_regs(v);
+#pragma unroll
+          for (int i = 0; i < C::kCH; ++i)
+            acc[c * C::kCH + i] =
+                fmaf(__uint_as_float(v[i]), sb * sq[c * C::kCH + i], acc[c * C::kCH + i]);
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(bar_tempty(b));
+
+      if (!u.last) continue;
+
+      // ---- the segment is complete: emit it
+      const int64_t p_tile = u.tile % s.p_tiles;
+      const int64_t q_tile = u.tile / s.p_tiles;
+      int64_t pf = cta, pl = cta;
+      if (u.sk_tile >= 0) {
+        pf = sk_first_cta(s, u.sk_tile);
+        pl = sk_last_cta(s, u.sk_tile);
+      }
+      if (pl > pf) {
+        // stream-K fixup: publish this CTA's partial, the last arrival adds all
+        float* mine = a.partials +
+                      static_cast<size_t>(cta * 2 + sk_slot(s, cta, u.sk_tile)) * (128 * BN);
+#pragma unroll
+        for (int c = 0; c < C::kCPT; ++c) mine[(col0 + c) * 128 + r] = acc[c];
+        __threadfence();
+        named_bar_sync(1, C::kNE * 32);
+        if (etid == 0) {
+          const int old = atomicAdd(a.counters + u.sk_tile, 1);
+          *s_last_flag = (old == static_cast<int>(pl - pf)) ? 1 : 0;
+        }
+        named_bar_sync(1, C::kNE * 32);
+        const bool is_last = *s_last_flag != 0;
+        if (!is_last) continue;
+        __threadfence();
+        for (int64_t pp = pf; pp <= pl; ++pp) {
+          const float* part = a.partials +
+                              static_cast<size_t>(pp * 2 + sk_slot(s, pp, u.sk_tile)) * (128 * BN);
+          if (pp == pf) {
+#pragma unroll
+            for (int c = 0; c < C::kCPT; ++c) acc[c] = __ldcg(part + (col0 + c) * 128 + r);
+          } else {
+#pragma unroll
+            for (int c = 0; c < C::kCPT; ++c) acc[c] += __ldcg(part + (col0 + c) * 128 + r);
+          }
+        }
+        if (etid == 0) a.counters[u.sk_tile] = 0;  // every contributor has arrived
+      }
+
+      if (!SWAP) {
+        const int64_t m = p_tile * 128 + r;
+        if (m < a.M) {
+          __nv_bfloat16* row = a.out + m * a.N;
+          const int64_t nbase = q_tile * BN + col0;
+#pragma unroll
+          for (int g = 0; g < C::kCPT / 8; ++g) {
+            const int64_t n = nbase + g * 8;
+            if (a.vec_store && n + 8 <= a.N) {
+              st_global_v4(row + n, pack_bf16x2(acc[g * 8 + 0], acc[g * 8 + 1]),
+                           pack_bf16x2(acc[g * 8 + 2], acc[g * 8 + 3]),
+                           pack_bf16x2(acc[g * 8 + 4], acc[g * 8 + 5]),
+                           pack_bf16x2(acc[g * 8 + 6], acc[g * 8 + 7]));
+            } else {
+#pragma unroll
+              for (int i = 0; i < 8; ++i)
+                if (n + i < a.N) row[n + i] = __float2bfloat16_rn(acc[g * 8 + i]);
+            }
+          }
+        }
+      } else {
+        const int64_t n = p_tile * 128 + r;
+        if (n < a.N) {
+          const int64_t mbase = q_tile * BN + col0;
+#pragma unroll
+          for (int c = 0; c < C::kCPT; ++c) {
+            const int64_t m = mbase + c;
+            if (m < a.M) a.out[m * a.N + n] = __float2bfloat16_rn(acc[c]);
+          }
+        }
+      }
+    }
+    cp_async_wait<0>();
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == C::kNE + 1) tmem_dealloc(tmem, C::kTmemCols);
+#endif
+}
+
+}  // namespace bfp8

@@ -1,0 +1,77 @@
+// bfp8_gemm_swap.cu -- swap-AB instantiations of the blocked FP8 GEMM (small
+// M: 128 weight rows fill the MMA M slot, BN >= M activation rows the N slot)
+// and the operand re-layout kernel for rows whose stride TMA cannot take.
+#include <atomic>
+
+#include "bfp8_gemm_kernel.cuh"
+#include "bfp8_internal.h"
+
+namespace bfp8 {
+
+namespace {
+
+template <int BN, bool SWAP>
+cudaError_t launch_one(const CUtensorMap& tmP, const CUtensorMap& tmQ, const GemmArgs& a,
+                       cudaStream_t stream) {
+  using C = GemmCfg<BN, SWAP>;
+  // The shared-memory opt-in is per device; set it once (a launch captured
+  // into a CUDA graph then needs no attribute call).
+  static std::atomic<uint64_t> configured{0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const uint64_t bit = 1ull << (dev & 63);
+  if (!(configured.load(std::memory_order_acquire) & bit)) {
+    e = cudaFuncSetAttribute(gemm_kernel<BN, SWAP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             C::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    configured.fetch_or(bit, std::memory_order_acq_rel);
+  }
+  gemm_kernel<BN, SWAP><<<a.sched.grid, C::kThreads, C::kSmemBytes, stream>>>(tmP, tmQ, a);
+  return cudaGetLastError();
+}
+
+__global__ void relayout_kernel(const uint8_t* __restrict__ src, int64_t rows, int64_t K,
+                                uint8_t* __restrict__ dst, int64_t kp) {
+  const int64_t chunks_per_row = kp / 16;
+  const int64_t total = rows * chunks_per_row;
+  for (int64_t c = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; c < total;
+       c += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t r = c / chunks_per_row;
+    const int64_t k0 = (c - r * chunks_per_row) * 16;
+    uint32_t w[4] = {0, 0, 0, 0};
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const int64_t k = k0 + i;
+      const uint32_t b = k < K ? src[r * K + k] : 0u;
+      w[i / 4] |= b << (8 * (i % 4));
+    }
+    *reinterpret_cast<uint4*>(dst + r * kp + k0) = make_uint4(w[0], w[1], w[2], w[3]);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_gemm_swap(int bn, const CUtensorMap& tmP, const CUtensorMap& tmQ,
+                             const GemmArgs& a, cudaStream_t stream) {
+  switch (bn) {
+    case 16: return launch_one<16, true>(tmP, tmQ, a, stream);
+    case 32: return launch_one<32, true>(tmP, tmQ, a, stream);
+    case 64: return launch_one<64, true>(tmP, tmQ, a, stream);
+    case 128: return launch_one<128, true>(tmP, tmQ, a, stream);
+    case 256: return launch_one<256, true>(tmP, tmQ, a, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+cudaError_t launch_relayout(const uint8_t* src, int64_t rows, int64_t K, uint8_t* dst, int64_t kp,
+                            int num_sms, cudaStream_t stream) {
+  const int64_t total = rows * (kp / 16);
+  int64_t blocks = (total + 255) / 256;
+  if (blocks > static_cast<int64_t>(num_sms) * 8) blocks = static_cast<int64_t>(num_sms) * 8;
+  if (blocks < 1) blocks = 1;
+  relayout_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(src, rows, K, dst, kp);
+  return cudaGetLastError();
+}
+
+}  // namespace bfp8

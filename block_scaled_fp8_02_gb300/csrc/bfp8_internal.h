@@ -1,0 +1,39 @@
+// bfp8_internal.h -- declarations shared by the library's translation units
+// (host side).  Not part of the public ABI.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstddef>
+#include <cstdint>
+
+#include "bfp8_sched.h"
+
+namespace bfp8 {
+
+struct GemmArgs;
+
+// Per-token group quantisation launcher (bfp8_quant.cu).
+cudaError_t launch_group_quant(const void* x, int in_f32, int64_t M, int64_t K, int64_t ld_x,
+                               uint8_t* q, int64_t ld_q, float* s, int col_major, int64_t ld_s,
+                               int num_sms, cudaStream_t stream);
+
+// GEMM launchers (bfp8_gemm_swap.cu, bfp8_gemm_wide.cu).  `bn` selects the
+// instantiation; returns cudaErrorInvalidValue for one that does not exist.
+cudaError_t launch_gemm_swap(int bn, const CUtensorMap& tmP, const CUtensorMap& tmQ,
+                             const GemmArgs& a, cudaStream_t stream);
+cudaError_t launch_gemm_wide(int bn, const CUtensorMap& tmP, const CUtensorMap& tmQ,
+                             const GemmArgs& a, cudaStream_t stream);
+
+// Pipeline depth and dynamic shared memory of an instantiation (0 if none).
+int gemm_stages(bool swap, int bn);
+int gemm_threads(bool swap, int bn);
+size_t gemm_smem_bytes(bool swap, int bn);
+
+// Copies rows x K bytes (row stride K) into rows x kp bytes (row stride kp,
+// kp = K rounded up to 16) with zeros in columns K .. kp-1 (bfp8_gemm_swap.cu).
+cudaError_t launch_relayout(const uint8_t* src, int64_t rows, int64_t K, uint8_t* dst, int64_t kp,
+                            int num_sms, cudaStream_t stream);
+
+}  // namespace bfp8

@@ -1,0 +1,203 @@
+/*
+ * bfp8.h -- libbfp8: DeepSeek-style blocked W8A8 FP8 linear layer on GB300
+ * (sm_103a).  Plain C ABI: raw pointers, sizes and an opaque stream handle.
+ *
+ * The layer has two steps (vLLM PR 49932 digest, "implementation breakdown"
+ * and "key source snippet"; lmdeploy PR 4830, "Kernel design"):
+ *   1. per-token group quantisation of the activations to float8_e4m3fn in
+ *      1 x 128 groups, with one fp32 scale per group (amax / 448);
+ *   2. the block-scaled GEMM
+ *        out[m, n] = sum over 128-wide K blocks kb of
+ *                    (A[m, kb] . B[n, kb]) * As[m, kb] * Bs[n / 128, kb]
+ *      with 128 x 128 weight-scale tiles and a bf16 output.
+ *
+ * Conventions for every entry point:
+ *   - Device pointers are CUDA device (or managed) addresses on the current
+ *     device; the caller owns every buffer, including the GEMM workspace.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
+ *     stream).  Calls only enqueue work: they neither allocate device memory
+ *     nor synchronise.
+ *   - Every argument is validated on the host before anything is launched; a
+ *     rejected call returns a status other than BFP8_OK, launches nothing and
+ *     leaves a reason in bfp8_last_error().  Nothing is thrown across the ABI.
+ *   - Inputs must be finite.  NaN or infinite inputs give unspecified outputs
+ *     (never a fault).
+ *   - Only GB300-class devices (compute capability 10.3) are supported.
+ */
+#ifndef BFP8_H_
+#define BFP8_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define BFP8_VERSION 1
+
+typedef enum {
+  BFP8_OK = 0,
+  BFP8_ERR_INVALID_ARG = 1,     /* null pointer, bad size, bad leading dimension */
+  BFP8_ERR_ALIGNMENT = 2,       /* a pointer or stride breaks a stated alignment rule */
+  BFP8_ERR_UNSUPPORTED = 3,     /* no device, or a device that is not sm_103 */
+  BFP8_ERR_CUDA = 4,            /* a CUDA runtime / driver call failed */
+  BFP8_ERR_WORKSPACE = 5,       /* workspace missing, too small or misaligned */
+  BFP8_ERR_DEVICE_TIMEOUT = 6   /* a kernel-side wait gave up (see bfp8_device_status) */
+} bfp8_status;
+
+typedef enum { BFP8_IN_BF16 = 0, BFP8_IN_F32 = 1 } bfp8_in_dtype;
+
+/* ------------------------------------------------------------------------ */
+/* Step 1: per-token group quantisation                                      */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * bfp8_group_quant -- per_token_group_quant_fp8(x, group_size=128,
+ * column_major_scales) as called in the vLLM PR 49932 digest's test.
+ *
+ *   x      [M, K] row-major activations, bf16 or fp32 (in_dtype), leading
+ *          dimension ld_x elements (ld_x >= K).
+ *   group  must be 128 (the only activation block shape the pages use).
+ *   q      [M, K] float8_e4m3fn codes, leading dimension ld_q bytes (>= K).
+ *   s      G = ceil(K / 128) fp32 scales per row:
+ *            col_major = 0: s[m * ld_s + g], ld_s >= G
+ *            col_major = 1: s[g * ld_s + m], ld_s >= M
+ *          (bfp8_scale_ld(M) gives the 16-byte-aligned column-major stride the
+ *          GEMM prefers).  Entries of a padded layout that hold no scale are
+ *          not written.
+ * For each group: amax = max |x| over the group's real elements (the last
+ * group of a row has K - 128 * (G - 1) elements), scale = max(amax, 1e-10)
+ * / 448 (IEEE fp32 division), q = round-to-nearest-even, saturating
+ * e4m3(x / scale) with an IEEE fp32 division per element; a zero or an
+ * underflow to zero keeps its sign.
+ * Any M >= 0 and K >= 0 (empty inputs launch nothing).  No alignment is
+ * required; 16-byte aligned rows take the vectorised path.
+ */
+bfp8_status bfp8_group_quant(const void* x, int in_dtype, int64_t M, int64_t K, int64_t ld_x,
+                             int group, int col_major, void* q, int64_t ld_q, float* s,
+                             int64_t ld_s, void* stream);
+
+/* Column-major scale stride the GEMM prefers: M rounded up to a multiple of 4
+ * (16 bytes of fp32, the TMA stride rule lmdeploy PR 4830 pads for). */
+int64_t bfp8_scale_ld(int64_t M);
+
+/* ------------------------------------------------------------------------ */
+/* Step 2: block-scaled GEMM                                                 */
+/* ------------------------------------------------------------------------ */
+
+typedef enum {
+  BFP8_SCHEDULE_AUTO = 0,
+  BFP8_SCHEDULE_SWAP_AB = 1,  /* weights fill the 128-row MMA slot (small M) */
+  BFP8_SCHEDULE_WIDE = 2      /* activations fill it; 128 x 256 output tiles */
+} bfp8_schedule;
+
+/* Optional tuning / test controls; a NULL options pointer means all zero. */
+typedef struct {
+  int schedule;        /* bfp8_schedule */
+  int max_ctas;        /* cap on persistent CTAs; 0 = one per SM */
+  int tile_n;          /* BFP8_SCHEDULE_WIDE only: 128 or 256 (0 = 256) */
+  int reserved[5];
+} bfp8_gemm_options;
+
+/*
+ * bfp8_gemm -- out = blocked_fp8_gemm(A, B, As, Bs), the computation of
+ * native_w8a8_block_matmul / apply_block_scaled_mm in the vLLM PR 49932
+ * digest, without its padding of M to a multiple of 4: ragged M, N and K
+ * (including a partial last K block) are handled by the library.
+ *
+ *   A    [M, K] float8_e4m3fn, row-major, row stride K bytes.
+ *   B    [N, K] float8_e4m3fn, row-major, row stride K bytes (the "NT" form:
+ *        out = A @ B^T).
+ *   As   activation scales, G = ceil(K / 128) per row:
+ *          as_col_major = 1: As[kb * ld_as + m], ld_as >= M
+ *          as_col_major = 0: As[m * ld_as + kb], ld_as >= G
+ *   Bs   [ceil(N / 128), G] fp32, row-major, one scale per 128 x 128 weight tile.
+ *   out  [M, N] bfloat16, row-major; each element is the fp32 accumulation of
+ *        the scaled block partial sums, rounded to nearest even.
+ *   workspace / workspace_bytes
+ *        caller-owned device scratch of at least the size bfp8_gemm_workspace_size
+ *        reports for the same (M, N, K, options), 256-byte aligned.  It must be
+ *        zero-filled once after allocation; every call that completes leaves it
+ *        ready for the next (its counters return to zero).  Concurrent calls
+ *        must not share a workspace.  After BFP8_ERR_DEVICE_TIMEOUT, zero it
+ *        again.  A workspace of 0 bytes is valid when 0 is reported.
+ * Results are deterministic: the same inputs give bitwise the same output on
+ * every call, whichever SM finishes first.
+ * Requirements: M, N, K >= 1; A and B 16-byte aligned with K % 16 == 0 for the
+ * direct path (otherwise the operands are first re-laid out into the
+ * workspace, which the size query accounts for); As, Bs 4-byte aligned.
+ */
+bfp8_status bfp8_gemm(const void* A, const void* B, const float* As, int as_col_major,
+                      int64_t ld_as, const float* Bs, void* out, int64_t M, int64_t N, int64_t K,
+                      void* workspace, size_t workspace_bytes, void* stream);
+
+/* bfp8_gemm with explicit schedule controls (opt may be NULL).  Every
+ * schedule computes the same function; they differ only in speed. */
+bfp8_status bfp8_gemm_ex(const void* A, const void* B, const float* As, int as_col_major,
+                         int64_t ld_as, const float* Bs, void* out, int64_t M, int64_t N,
+                         int64_t K, void* workspace, size_t workspace_bytes,
+                         const bfp8_gemm_options* opt, void* stream);
+
+/* Workspace bytes bfp8_gemm / bfp8_gemm_ex need for this problem on the
+ * current device.  Writes *bytes; returns BFP8_ERR_UNSUPPORTED without a
+ * suitable device. A, B alignment is not known here: the size assumes the
+ * re-layout path when K % 16 != 0 or `operands_unaligned` is nonzero. */
+bfp8_status bfp8_gemm_workspace_size(int64_t M, int64_t N, int64_t K,
+                                     const bfp8_gemm_options* opt, int operands_unaligned,
+                                     size_t* bytes);
+
+/* Host-only description of the schedule bfp8_gemm_ex would run on a device
+ * with `num_sms` SMs (no device needed; used for planning and tests). */
+typedef struct {
+  int swap_ab;          /* 1: weights in the MMA M slot */
+  int tile_n;           /* MMA N (rows of the second operand per tile) */
+  int stages;           /* shared-memory pipeline depth */
+  int grid;             /* persistent CTAs */
+  int64_t tiles;        /* output tiles */
+  int64_t k_blocks;     /* G = ceil(K / 128) */
+  int64_t dp_tiles;     /* tiles computed whole, round-robin */
+  int64_t sk_units;     /* (tile, k-block) units split across CTAs */
+  int relayout;         /* operands re-laid out into the workspace first */
+  size_t workspace_bytes;
+} bfp8_plan_info;
+
+bfp8_status bfp8_gemm_plan(int64_t M, int64_t N, int64_t K, int num_sms,
+                           const bfp8_gemm_options* opt, int operands_unaligned,
+                           bfp8_plan_info* info);
+
+/* Host-only view of the stream-K work split of a plan: for CTA `cta`, the
+ * number of (tile, k-block) units it processes and, for unit j, its tile and
+ * k-block.  Returns BFP8_ERR_INVALID_ARG for indices out of range. */
+bfp8_status bfp8_plan_unit(int64_t M, int64_t N, int64_t K, int num_sms,
+                           const bfp8_gemm_options* opt, int cta, int64_t j,
+                           int64_t* num_units, int64_t* tile, int64_t* k_block);
+
+/* ------------------------------------------------------------------------ */
+/* Status and diagnostics                                                    */
+/* ------------------------------------------------------------------------ */
+
+/* Reason for the last failure on the calling thread ("" if none). */
+const char* bfp8_last_error(void);
+
+/* Static name of a status code. */
+const char* bfp8_status_string(int status);
+
+/* Synchronises the current device and reads the library's device-side failure
+ * word for it (0 = no kernel-side wait has given up since the last clear);
+ * clears it when `clear` is nonzero. */
+bfp8_status bfp8_device_status(int* code, int clear);
+
+/* Self-test of the bounded wait every kernel uses: launches one warp that
+ * waits on a shared-memory barrier nothing ever arrives on, giving up after
+ * `limit_cycles` SM cycles.  Synchronises the stream and returns
+ * BFP8_ERR_DEVICE_TIMEOUT when the wait gave up as designed (and *elapsed
+ * holds the cycles it waited), BFP8_OK if the barrier completed. */
+bfp8_status bfp8_selftest_bounded_wait(uint64_t limit_cycles, uint64_t* elapsed, void* stream);
+
+int bfp8_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* BFP8_H_ */

@@ -1,0 +1,139 @@
+"""The C ABI without a GPU: the library loads, exports every symbol the header
+declares, rejects bad arguments on the host before touching a device, and
+plans schedules whose work split covers every (tile, k-block) unit once."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import block_scaled_fp8_02_gb300 as bf
+from block_scaled_fp8_02_gb300 import build as bfbuild
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "bfp8.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    bfbuild.build()
+    return bf.lib()
+
+
+def _declared():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(bfp8_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_header_declares_what_the_binding_expects():
+    assert _declared() == sorted(bf.EXPORTS)
+
+
+def test_library_exports_every_declared_symbol(L):
+    for name in _declared():
+        assert hasattr(L, name), name
+        assert ctypes.cast(getattr(L, name), ctypes.c_void_p).value
+
+
+def test_status_strings_and_helpers(L):
+    assert bf.bfp8_version() == 1
+    assert L.bfp8_status_string(0) == b"BFP8_OK"
+    assert L.bfp8_status_string(6) == b"BFP8_ERR_DEVICE_TIMEOUT"
+    assert [bf.bfp8_scale_ld(m) for m in (0, 1, 4, 5, 83, 84)] == [0, 4, 4, 8, 84, 84]
+
+
+def _quant(L, **kw):
+    a = dict(x=16, in_dtype=0, M=4, K=256, ld_x=256, group=128, col_major=1, q=16, ld_q=256,
+             s=16, ld_s=4, stream=None)
+    a.update(kw)
+    return L.bfp8_group_quant(a["x"], a["in_dtype"], a["M"], a["K"], a["ld_x"], a["group"],
+                              a["col_major"], a["q"], a["ld_q"], a["s"], a["ld_s"], a["stream"])
+
+
+def test_group_quant_rejects_bad_arguments_on_the_host(L):
+    assert _quant(L, group=64) == 1
+    assert _quant(L, in_dtype=7) == 1
+    assert _quant(L, col_major=2) == 1
+    assert _quant(L, M=-1) == 1
+    assert _quant(L, x=None) == 1
+    assert _quant(L, ld_x=100) == 1
+    assert _quant(L, ld_q=10) == 1
+    assert _quant(L, ld_s=3) == 1                     # column-major needs ld_s >= M
+    assert _quant(L, col_major=0, ld_s=1) == 1        # row-major needs ld_s >= G = 2
+    assert _quant(L, x=17) == 2                       # bf16 input must be 2-byte aligned
+    assert _quant(L, s=18) == 2
+    assert "ld_s" in bf.bfp8_last_error() or "aligned" in bf.bfp8_last_error()
+    assert _quant(L, M=0) == 0 and _quant(L, K=0, x=None) == 0   # empty: nothing to do
+
+
+def _gemm(L, **kw):
+    a = dict(A=256, B=256, As=256, col=1, ld_as=4, Bs=256, out=256, M=4, N=128, K=256, ws=256,
+             wsb=1 << 30, opt=None, stream=None)
+    a.update(kw)
+    return L.bfp8_gemm_ex(a["A"], a["B"], a["As"], a["col"], a["ld_as"], a["Bs"], a["out"], a["M"],
+                          a["N"], a["K"], a["ws"], a["wsb"], a["opt"], a["stream"])
+
+
+def test_gemm_rejects_bad_arguments_on_the_host(L):
+    assert _gemm(L, M=0) == 1
+    assert _gemm(L, K=-5) == 1
+    assert _gemm(L, N=1 << 31) == 1
+    assert _gemm(L, A=None) == 1
+    assert _gemm(L, out=None) == 1
+    assert _gemm(L, col=3) == 1
+    assert _gemm(L, ld_as=3) == 1                     # column-major ld_as >= M
+    assert _gemm(L, col=0, ld_as=1) == 1              # row-major ld_as >= G = 2
+    assert _gemm(L, As=258) == 2
+    assert _gemm(L, out=257) == 2
+    bad = bf.GemmOptions()
+    bad.schedule = 9
+    assert _gemm(L, opt=ctypes.pointer(bad)) == 1
+    bad.schedule, bad.tile_n = 0, 64
+    assert _gemm(L, opt=ctypes.pointer(bad)) == 1
+    # a valid call reaches the device check, which fails cleanly without a GPU
+    import torch
+    if not torch.cuda.is_available():
+        assert _gemm(L) == 3
+        assert "device" in bf.bfp8_last_error().lower() or "driver" in bf.bfp8_last_error().lower()
+
+
+def _cover(M, N, K, sms, options=None):
+    plan = bf.bfp8_gemm_plan(M, N, K, sms, options)
+    seen = {}
+    for cta in range(plan["grid"]):
+        n, _, _ = bf.bfp8_plan_unit(M, N, K, sms, cta, -1, options)
+        prev = None
+        for j in range(n):
+            _, t, kb = bf.bfp8_plan_unit(M, N, K, sms, cta, j, options)
+            assert 0 <= t < plan["tiles"] and 0 <= kb < plan["k_blocks"]
+            assert (t, kb) not in seen, (t, kb, cta, seen.get((t, kb)))
+            seen[(t, kb)] = cta
+            if prev is not None and prev[0] == t:
+                assert kb == prev[1] + 1          # a CTA's units within a tile are contiguous
+            prev = (t, kb)
+    assert len(seen) == plan["tiles"] * plan["k_blocks"]
+    return plan
+
+
+@pytest.mark.parametrize("M,N,K,sms,opts", [
+    (1, 4096, 4096, 152, None), (83, 576, 7168, 152, None), (83, 576, 7168, 7, None),
+    (2048, 4096, 4096, 152, None), (1000, 1000, 1000, 152, None), (3, 576, 1000, 152, None),
+    (300, 1000, 7168, 152, {"schedule": 1}), (16, 512, 256, 152, {"schedule": 2}),
+    (1, 1, 1, 152, None), (4096, 4096, 512, 19, {"tile_n": 128}),
+])
+def test_work_split_covers_every_unit_once(L, M, N, K, sms, opts):
+    _cover(M, N, K, sms, opts)
+
+
+def test_plans_choose_the_documented_schedules(L):
+    p = bf.bfp8_gemm_plan(1, 4096, 4096, 152)
+    assert p["swap_ab"] == 1 and p["tile_n"] == 16 and p["grid"] == 152 and p["dp_tiles"] == 0
+    p = bf.bfp8_gemm_plan(64, 4096, 4096, 152)
+    assert p["swap_ab"] == 1 and p["tile_n"] == 64
+    p = bf.bfp8_gemm_plan(8192, 4096, 4096, 152)
+    assert p["swap_ab"] == 0 and p["tile_n"] == 256 and p["tiles"] == 64 * 16
+    assert p["dp_tiles"] % 152 == 0 and p["dp_tiles"] > 0
+    p = bf.bfp8_gemm_plan(3, 1000, 1000, 152)
+    assert p["relayout"] == 1                       # 1000-byte rows break the TMA stride rule
+    assert bf.bfp8_gemm_plan(3, 1000, 1024, 152)["relayout"] == 0
+    assert bf.bfp8_gemm_plan(3, 1000, 1024, 152, operands_unaligned=True)["relayout"] == 1

@@ -1,0 +1,83 @@
+"""GPU parity of the per-token group quantisation kernel: codes and fp32 scales
+must equal the oracle's bit for bit, for both scale layouts, on the pages'
+workloads (fp32 page inputs, bf16 N(0,1) activations at the sweep and
+Qwen3-32B shapes, heavy-tailed ragged inputs) and on edge shapes."""
+import numpy as np
+import pytest
+import torch
+
+import block_scaled_fp8_02_gb300 as bf
+from block_scaled_fp8_02_gb300 import build as bfbuild
+from block_scaled_fp8_02_gb300 import workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def dev():
+    bfbuild.build()
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    return torch.device("cuda:0")
+
+
+def _oracle_quant(oracle_mod, x: torch.Tensor, col_major: bool):
+    if x.dtype == torch.float32:
+        return oracle_mod.group_quant(x.numpy(), True, col_major)
+    return oracle_mod.group_quant(x.view(torch.int16).numpy().view(np.uint16), False, col_major)
+
+
+def _check(oracle_mod, dev, x_cpu: torch.Tensor, col_major: bool, x_dev=None):
+    M, K = x_cpu.shape
+    q_ref, s_ref = _oracle_quant(oracle_mod, x_cpu, col_major)
+    x_dev = x_cpu.to(dev) if x_dev is None else x_dev
+    q, s = bf.bfp8_group_quant(x_dev, col_major=col_major)
+    torch.cuda.synchronize()
+    q_np = q.view(torch.uint8).cpu().numpy()
+    G = (K + 127) // 128
+    s_np = s.cpu().numpy()                       # [M, G] view in either layout
+    s_want = s_ref[:, :M].T if col_major else s_ref[:, :G]
+    bad = np.nonzero(q_np != q_ref)
+    assert bad[0].size == 0, f"{bad[0].size} codes differ, first at {bad[0][0], bad[1][0]}"
+    assert (s_np.view(np.uint32) == np.ascontiguousarray(s_want).view(np.uint32)).all()
+
+
+CASES = [(m, 4096, "normal") for m in (1, 9, 64, 256, 2048)] + \
+        [(64, k, "normal") for k in (5120, 8192, 25600)] + \
+        [(m, k, "student_t3") for m in (3, 83, 127, 1000) for k in (7168, 1000)] + \
+        [(1, 1, "normal"), (5, 127, "student_t3"), (2, 129, "normal"), (7, 16, "normal"),
+         (3, 200, "student_t3")]
+
+
+@pytest.mark.parametrize("M,K,dist", CASES)
+@pytest.mark.parametrize("col_major", [True, False])
+def test_quant_bitwise_vs_oracle(oracle_mod, dev, M, K, dist, col_major):
+    x = wl.activations(M, K, seed=M * 31 + K, dist=dist)
+    _check(oracle_mod, dev, x, col_major)
+
+
+@pytest.mark.parametrize("col_major", [True, False])
+def test_quant_page_fp32_inputs(oracle_mod, dev, col_major):
+    c = wl.correctness_case()
+    _check(oracle_mod, dev, c["x"], col_major)
+
+
+def test_quant_full_size_prefill(oracle_mod, dev):
+    x = wl.activations(8192, 4096, seed=5)
+    _check(oracle_mod, dev, x, True)
+
+
+def test_quant_unaligned_rows_take_the_scalar_path(oracle_mod, dev):
+    M, K = 9, 1000
+    x = wl.activations(M, K + 1, seed=9, dist="student_t3")
+    x_dev = x.to(dev)[:, 1:]                     # row stride K+1 elements: not 16-byte aligned
+    _check(oracle_mod, dev, x[:, 1:].contiguous(), True, x_dev=x_dev)
+
+
+def test_quant_special_groups(oracle_mod, dev):
+    x = torch.zeros(3, 384, dtype=torch.float32)
+    x[1, 128:256] = -0.0
+    x[1, 200] = 1e-12                            # below the 1e-10 floor
+    x[2, :] = torch.linspace(-1000, 1000, 384)   # max element encodes to +-448
+    x[2, 300] = 3.0e-8
+    _check(oracle_mod, dev, x, True)
+    _check(oracle_mod, dev, x.to(torch.bfloat16), False)
