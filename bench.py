@@ -98,10 +98,27 @@ class ClockSampler:
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
     def __init__(self, gpu_index: int):
-        self.gpu = gpu_index
+        self.gpu = self._nvsmi_id(gpu_index)
         self.proc = None
         self.lines = []
         self.thread = None
+
+    @staticmethod
+    def _nvsmi_id(local: int) -> str:
+        """nvidia-smi's id of torch device `local` (its UUID when torch knows it)."""
+        try:
+            import torch
+            u = str(torch.cuda.get_device_properties(local).uuid)
+            if u:
+                return u if u.startswith("GPU-") else "GPU-" + u
+        except Exception:
+            pass
+        vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+        if vis:
+            parts = [v.strip() for v in vis.split(",") if v.strip()]
+            if local < len(parts):
+                return parts[local]
+        return str(local)
 
     def start(self):
         try:

@@ -160,6 +160,7 @@ int swap_tile_n(int64_t M) {
 }
 
 constexpr int64_t kSwapMaxM = 256;
+constexpr size_t kCounterHeaderBytes = 16384;   // 4096 stream-K tile counters
 
 bfp8_status make_plan(int64_t M, int64_t N, int64_t K, int num_sms, const bfp8_gemm_options* opt,
                       bool unaligned, Plan* p) {
@@ -177,8 +178,12 @@ bfp8_status make_plan(int64_t M, int64_t N, int64_t K, int num_sms, const bfp8_g
   p->kp = p->relayout ? cdiv(K, 16) * 16 : K;
   size_t off = 0;
   const int64_t sk_tiles = p->sched.tiles - p->sched.dp_tiles;
+  // The counters live in a fixed-size header at the start of every workspace,
+  // whatever the problem: a later call with a different shape must find zeros
+  // there, never an earlier call's partial sums.  Stream-K always covers fewer
+  // than 2 x grid tiles (whole waves are handed out round-robin first).
   p->off_counters = off;
-  off += align256(static_cast<size_t>(sk_tiles) * sizeof(int));
+  if (sk_tiles > 0) off += kCounterHeaderBytes;
   p->off_partials = off;
   if (p->sched.sk_units > 0)
     off += align256(static_cast<size_t>(p->sched.grid) * 2 * 128 * p->bn * sizeof(float));
@@ -284,6 +289,8 @@ bfp8_status bfp8_gemm_plan(int64_t M, int64_t N, int64_t K, int num_sms,
   if (!info) return fail(BFP8_ERR_INVALID_ARG, "info is null");
   Plan p;
   make_plan(M, N, K, num_sms, opt, operands_unaligned != 0, &p);
+  if (p.sched.tiles - p.sched.dp_tiles > static_cast<int64_t>(kCounterHeaderBytes / sizeof(int)))
+    return fail(BFP8_ERR_UNSUPPORTED, "more stream-K tiles than the workspace header holds");
   info->swap_ab = p.swap;
   info->tile_n = p.bn;
   info->stages = gemm_stages(p.swap, p.bn);
@@ -357,6 +364,8 @@ bfp8_status bfp8_gemm_ex(const void* A, const void* B, const float* As, int as_c
   const bool unaligned = misaligned(A, 16) || misaligned(B, 16);
   Plan p;
   make_plan(M, N, K, d.sms, opt, unaligned, &p);
+  if (p.sched.tiles - p.sched.dp_tiles > static_cast<int64_t>(kCounterHeaderBytes / sizeof(int)))
+    return fail(BFP8_ERR_UNSUPPORTED, "more stream-K tiles than the workspace header holds");
   if (p.total > 0) {
     if (!workspace)
       return fail(BFP8_ERR_WORKSPACE, "this problem needs %zu workspace bytes; got none", p.total);

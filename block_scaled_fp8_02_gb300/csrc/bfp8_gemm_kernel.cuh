@@ -355,15 +355,38 @@ __global__ void __launch_bounds__(GemmCfg<BN, SWAP>::kThreads, 1)
         const bool is_last = *s_last_flag != 0;
         if (!is_last) continue;
         __threadfence();
-        for (int64_t pp = pf; pp <= pl; ++pp) {
-          const float* part = a.partials +
-                              static_cast<size_t>(pp * 2 + sk_slot(s, pp, u.sk_tile)) * (128 * BN);
-          if (pp == pf) {
+        // Sum the contributors in ascending K order.  Loads are issued in
+        // batches of kFixBatch contributors x kFixCols columns so that one L2
+        // round trip serves a whole batch
+        // (two contributors x 8 columns when 128 accumulators already fill the
+        // register budget of the 10-warp configuration)
+        constexpr int kFixBatch = C::kNH == 2 ? 2 : 4;
+        constexpr int kFixCols = C::kNH == 2 ? 8 : 16;
+        const float* part0 = a.partials +
+                             static_cast<size_t>(pf * 2 + sk_slot(s, pf, u.sk_tile)) * (128 * BN);
 #pragma unroll
-            for (int c = 0; c < C::kCPT; ++c) acc[c] = __ldcg(part + (col0 + c) * 128 + r);
-          } else {
+        for (int c = 0; c < C::kCPT; ++c) acc[c] = __ldcg(part0 + (col0 + c) * 128 + r);
+        for (int64_t pb = pf + 1; pb <= pl; pb += kFixBatch) {
+          const float* parts[kFixBatch];
 #pragma unroll
-            for (int c = 0; c < C::kCPT; ++c) acc[c] += __ldcg(part + (col0 + c) * 128 + r);
+          for (int i = 0; i < kFixBatch; ++i) {
+            const int64_t pp = pb + i <= pl ? pb + i : pl;
+            parts[i] = a.partials + static_cast<size_t>(pp * 2 + sk_slot(s, pp, u.sk_tile)) * (128 * BN);
+          }
+#pragma unroll
+          for (int c0 = 0; c0 < C::kCPT; c0 += kFixCols) {
+            float t[kFixBatch][kFixCols];
+#pragma unroll
+            for (int i = 0; i < kFixBatch; ++i)
+#pragma unroll
+              for (int c = 0; c < kFixCols; ++c)
+                t[i][c] = (pb + i <= pl) ? __ldcg(parts[i] + (col0 + c0 + c) * 128 + r) : 0.f;
+#pragma unroll
+            for (int i = 0; i < kFixBatch; ++i)
+              if (pb + i <= pl) {
+#pragma unroll
+                for (int c = 0; c < kFixCols; ++c) acc[c0 + c] += t[i][c];
+              }
           }
         }
         if (etid == 0) a.counters[u.sk_tile] = 0;  // every contributor has arrived
