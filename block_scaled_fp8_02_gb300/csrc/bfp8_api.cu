@@ -171,9 +171,13 @@ bfp8_status make_plan(int64_t M, int64_t N, int64_t K, int num_sms, const bfp8_g
   const int64_t G = cdiv(K, 128);
   const int64_t p_tiles = p->swap ? cdiv(N, 128) : cdiv(M, 128);
   const int64_t q_tiles = p->swap ? cdiv(M, p->bn) : cdiv(N, p->bn);
+  if (p_tiles * q_tiles * G >= (int64_t{1} << 31))
+    return fail(BFP8_ERR_UNSUPPORTED, "problem too large: %lld tiles x %lld k-blocks",
+                (long long)(p_tiles * q_tiles), (long long)G);
   int max_ctas = num_sms;
   if (opt && opt->max_ctas > 0 && opt->max_ctas < max_ctas) max_ctas = opt->max_ctas;
-  p->sched = make_sched(p_tiles, q_tiles, static_cast<int32_t>(G), max_ctas);
+  p->sched = make_sched(static_cast<uint32_t>(p_tiles), static_cast<uint32_t>(q_tiles),
+                        static_cast<uint32_t>(G), static_cast<uint32_t>(max_ctas));
   p->relayout = unaligned || (K % 16) != 0;
   p->kp = p->relayout ? cdiv(K, 16) * 16 : K;
   size_t off = 0;
@@ -182,8 +186,10 @@ bfp8_status make_plan(int64_t M, int64_t N, int64_t K, int num_sms, const bfp8_g
   // whatever the problem: a later call with a different shape must find zeros
   // there, never an earlier call's partial sums.  Stream-K always covers fewer
   // than 2 x grid tiles (whole waves are handed out round-robin first).
+  // It is reserved whenever the workspace is used at all, so that nothing but
+  // counters (which every completed call returns to zero) is ever written there.
   p->off_counters = off;
-  if (sk_tiles > 0) off += kCounterHeaderBytes;
+  if (sk_tiles > 0 || p->relayout) off += kCounterHeaderBytes;
   p->off_partials = off;
   if (p->sched.sk_units > 0)
     off += align256(static_cast<size_t>(p->sched.grid) * 2 * 128 * p->bn * sizeof(float));
@@ -269,6 +275,8 @@ bfp8_status bfp8_group_quant(const void* x, int in_dtype, int64_t M, int64_t K, 
   if (misaligned(x, in_dtype == BFP8_IN_F32 ? 4 : 2))
     return fail(BFP8_ERR_ALIGNMENT, "x is not aligned to its element size");
   if (misaligned(s, 4)) return fail(BFP8_ERR_ALIGNMENT, "s is not 4-byte aligned");
+  if (M * ((G + 1) / 2) >= (int64_t{1} << 30))
+    return fail(BFP8_ERR_UNSUPPORTED, "M x K too large for one quantisation launch");
   DevInfo d;
   bfp8_status st = current_device(&d, nullptr);
   if (st != BFP8_OK) return st;
@@ -288,7 +296,7 @@ bfp8_status bfp8_gemm_plan(int64_t M, int64_t N, int64_t K, int num_sms,
   if (num_sms < 1) return fail(BFP8_ERR_INVALID_ARG, "num_sms = %d", num_sms);
   if (!info) return fail(BFP8_ERR_INVALID_ARG, "info is null");
   Plan p;
-  make_plan(M, N, K, num_sms, opt, operands_unaligned != 0, &p);
+  if ((st = make_plan(M, N, K, num_sms, opt, operands_unaligned != 0, &p)) != BFP8_OK) return st;
   if (p.sched.tiles - p.sched.dp_tiles > static_cast<int64_t>(kCounterHeaderBytes / sizeof(int)))
     return fail(BFP8_ERR_UNSUPPORTED, "more stream-K tiles than the workspace header holds");
   info->swap_ab = p.swap;
@@ -312,15 +320,19 @@ bfp8_status bfp8_plan_unit(int64_t M, int64_t N, int64_t K, int num_sms,
   if ((st = check_options(opt)) != BFP8_OK) return st;
   if (num_sms < 1) return fail(BFP8_ERR_INVALID_ARG, "num_sms = %d", num_sms);
   Plan p;
-  make_plan(M, N, K, num_sms, opt, false, &p);
-  if (cta < 0 || cta >= p.sched.grid) return fail(BFP8_ERR_INVALID_ARG, "cta %d out of range", cta);
-  const int64_t n = num_units(p.sched, cta);
+  if ((st = make_plan(M, N, K, num_sms, opt, false, &p)) != BFP8_OK) return st;
+  if (cta < 0 || static_cast<uint32_t>(cta) >= p.sched.grid)
+    return fail(BFP8_ERR_INVALID_ARG, "cta %d out of range", cta);
+  const int64_t n = num_units(p.sched, static_cast<uint32_t>(cta));
   if (num_units_out) *num_units_out = n;
   if (j >= 0) {
     if (j >= n) return fail(BFP8_ERR_INVALID_ARG, "unit %lld out of range", (long long)j);
-    const Unit u = unit_at(p.sched, cta, j);
-    if (tile) *tile = u.tile;
-    if (k_block) *k_block = u.kb;
+    // walk the same cursor the kernel's roles walk
+    Cursor c;
+    c.init(p.sched, static_cast<uint32_t>(cta));
+    for (int64_t i = 0; i < j; ++i) c.next();
+    if (tile) *tile = c.tile;
+    if (k_block) *k_block = c.kb;
   }
   return ok();
 }
@@ -335,7 +347,7 @@ bfp8_status bfp8_gemm_workspace_size(int64_t M, int64_t N, int64_t K,
   DevInfo d;
   if ((st = current_device(&d, nullptr)) != BFP8_OK) return st;
   Plan p;
-  make_plan(M, N, K, d.sms, opt, operands_unaligned != 0, &p);
+  if ((st = make_plan(M, N, K, d.sms, opt, operands_unaligned != 0, &p)) != BFP8_OK) return st;
   *bytes = p.total;
   return ok();
 }
@@ -363,7 +375,7 @@ bfp8_status bfp8_gemm_ex(const void* A, const void* B, const float* As, int as_c
   if ((st = current_device(&d, nullptr)) != BFP8_OK) return st;
   const bool unaligned = misaligned(A, 16) || misaligned(B, 16);
   Plan p;
-  make_plan(M, N, K, d.sms, opt, unaligned, &p);
+  if ((st = make_plan(M, N, K, d.sms, opt, unaligned, &p)) != BFP8_OK) return st;
   if (p.sched.tiles - p.sched.dp_tiles > static_cast<int64_t>(kCounterHeaderBytes / sizeof(int)))
     return fail(BFP8_ERR_UNSUPPORTED, "more stream-K tiles than the workspace header holds");
   if (p.total > 0) {

@@ -9,16 +9,18 @@
 //
 // The fp32 scales are arbitrary (not powers of two), so the tensor core's
 // block-scaled MMA cannot apply them.  Each 128-wide K block is therefore its
-// own MMA problem: the tensor core writes the block's exact-product fp32 sum
-// into TMEM, and CUDA-core warps read it back, multiply by As * Bs and add it
-// to an fp32 accumulator held in registers (the "promotion" of the DeepGEMM
-// design the lmdeploy PR 4830 page follows for large M).
+// own MMA problem: the tensor core writes the block's fp32 sum into TMEM, and
+// CUDA-core warps read it back, multiply by As * Bs and add it to an fp32
+// accumulator held in registers (the "promotion" of the DeepGEMM design the
+// lmdeploy PR 4830 page follows for large M).
 //
 // Roles (one CTA per SM, persistent):
 //   warps 0 .. NE-1  promotion / epilogue warps; warp w reads TMEM lanes
 //                    32*(w%4) .. +31 and column half w/4
 //   warp  NE         TMA producer (one lane): A/B tiles into a STAGES-deep ring
 //   warp  NE+1       TMEM owner and MMA issuer (one lane)
+//   (the 256-wide tile adds two idle warps so that the non-epilogue warps form
+//   a whole warpgroup that can hand registers to the epilogue via setmaxnreg)
 // TMEM holds two partial buffers of BN columns, so the MMA of block kb+1 runs
 // while block kb is promoted.
 //
@@ -75,16 +77,23 @@ struct GemmCfg {
   static constexpr int kNE = BN > 128 ? 8 : 4;   // promotion warps
   static constexpr int kNH = kNE / 4;            // column halves
   static constexpr int kCPT = BN / kNH;          // accumulator columns per thread
-  // 16-column TMEM loads when two warps share a lane quadrant: 10 warps put three
-  // on some SM sub-partitions, which caps a thread at 168 registers.
-  static constexpr int kCH = (kCPT % 32 == 0 && kNH == 1) ? 32 : 16;
-  static constexpr int kThreads = (kNE + 2) * 32;
+  static constexpr int kCH = kCPT >= 32 ? 32 : 16;   // columns per tcgen05.ld
+  static constexpr int kBatch = kCPT >= 64 ? 64 : kCPT;  // columns loaded per wait
+  // 8 promotion warps: 12 warps in all so that warps 8..11 are one warpgroup
+  // that gives registers to the promotion warpgroups (setmaxnreg).
+  static constexpr int kWarps = kNE == 8 ? 12 : kNE + 2;
+  static constexpr int kThreads = kWarps * 32;
+  static constexpr bool kRebalance = kNE == 8;
+  static constexpr int kRegsEpi = 232, kRegsOther = 40;  // 256*232 + 128*40 = 384*168
   static constexpr int kPBytes = 128 * 128;
   static constexpr int kQBytes = BN * 128;
   static constexpr int kStageBytes = kPBytes + kQBytes;
   static constexpr int kD = 3;                   // scale prefetch distance in units
   static constexpr int kR = kD + 2;              // scale ring slots
-  static constexpr int kScaleBytes = kR * (128 + BN) * 4;
+  // per warp and slot: swap -> the warp's column scales + the weight scale;
+  // wide -> one activation scale per lane + the weight scale
+  static constexpr int kScaleStride = SWAP ? (kCPT + 4) : 36;
+  static constexpr int kScaleBytes = kR * kNE * kScaleStride * 4;
   static constexpr int kSmemLimit = 232448;      // 227 KB per CTA
   static constexpr int kFixed = 1024 /*align slack*/ + 256 /*barriers, flags*/ + kScaleBytes;
   static constexpr int kStagesFit = (kSmemLimit - kFixed) / kStageBytes;
@@ -93,15 +102,30 @@ struct GemmCfg {
   static constexpr int kOffBars = kStages * kStageBytes;
   static constexpr int kOffTmemPtr = kOffBars + (2 * kStages + 4) * 8;
   static constexpr int kOffFlags = kOffTmemPtr + 8;
-  static constexpr int kOffScaleP = (kOffFlags + 8 + 15) / 16 * 16;
-  static constexpr int kOffScaleQ = kOffScaleP + kR * 128 * 4;
-  static constexpr int kSmemBytes = kOffScaleQ + kR * BN * 4 + 1024;
+  static constexpr int kOffScale = (kOffFlags + 8 + 15) / 16 * 16;
+  static constexpr int kSmemBytes = kOffScale + kScaleBytes + 1024;
   static constexpr int kTmemCols = tmem_cols_for(2 * BN);
   static constexpr uint32_t kIdesc = idesc_e4m3_f32(128, BN);
 };
 
 __device__ __forceinline__ void report_failure(int* err, int code) {
   if (err != nullptr) atomicCAS(err, 0, code);
+}
+
+template <int N>
+__device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, uint32_t* v) {
+  if constexpr (N == 32) {
+    tmem_ld32(taddr, *reinterpret_cast<uint32_t(*)[32]>(v));
+  } else {
+    tmem_ld16(taddr, *reinterpret_cast<uint32_t(*)[16]>(v));
+  }
+}
+
+template <int N>
+__device__ __forceinline__ void reg_fence(uint32_t* v) {
+  static_assert(N % 16 == 0, "");
+#pragma unroll
+  for (int i = 0; i < N; i += 16) reg_fence16(*reinterpret_cast<uint32_t(*)[16]>(v + i));
 }
 
 template <int BN, bool SWAP>
@@ -118,8 +142,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, SWAP>::kThreads, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const Sched& s = a.sched;
-  const int64_t cta = blockIdx.x;
-  const int nunits = static_cast<int>(num_units(s, cta));
+  const uint32_t cta = blockIdx.x;
 
   auto bar_full = [&](int i) { return sbase + C::kOffBars + 8u * i; };
   auto bar_empty = [&](int i) { return sbase + C::kOffBars + 8u * (C::kStages + i); };
@@ -129,8 +152,6 @@ __global__ void __launch_bounds__(GemmCfg<BN, SWAP>::kThreads, 1)
   auto stage_q = [&](int i) { return sbase + static_cast<uint32_t>(i * C::kStageBytes + C::kPBytes); };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffTmemPtr);
   volatile int* s_last_flag = reinterpret_cast<volatile int*>(smem + C::kOffFlags);
-  float* sP = reinterpret_cast<float*>(smem + C::kOffScaleP);
-  float* sQ = reinterpret_cast<float*>(smem + C::kOffScaleQ);
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::kStages; ++i) {
@@ -157,47 +178,43 @@ __global__ void __launch_bounds__(GemmCfg<BN, SWAP>::kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == C::kNE) {
-    // ------------------------------------------------------- TMA producer
-    if (lane == 0) {
+  if (warp >= C::kNE) {
+    if constexpr (C::kRebalance) setmaxnreg_dec<C::kRegsOther>();
+    if (warp == C::kNE && lane == 0) {
+      // ----------------------------------------------------- TMA producer
+      Cursor cur;
+      cur.init(s, cta);
       int st = 0;
       uint32_t ph = 0;
-      int issued = 0;
-      bool ok = true;
-      for (int j = 0; j < nunits; ++j) {
-        const Unit u = unit_at(s, cta, j);
+      uint32_t issued = 0;
+      for (; cur.valid(); cur.next()) {
         if (!mbar_wait_bounded(bar_empty(st), ph ^ 1u, a.wait_limit)) {
           report_failure(a.err, kDevTimeoutProducer);
-          ok = false;
           break;
         }
-        const int64_t p_tile = u.tile % s.p_tiles;
-        const int64_t q_tile = u.tile / s.p_tiles;
         mbar_arrive_expect_tx(bar_full(st), C::kStageBytes);
-        tma_load_2d(stage_p(st), &tmP, bar_full(st), u.kb * 128, static_cast<int32_t>(p_tile * 128));
-        tma_load_2d(stage_q(st), &tmQ, bar_full(st), u.kb * 128, static_cast<int32_t>(q_tile * BN));
+        const int32_t x = static_cast<int32_t>(cur.kb * 128);
+        tma_load_2d(stage_p(st), &tmP, bar_full(st), x, static_cast<int32_t>(cur.p_tile * 128));
+        tma_load_2d(stage_q(st), &tmQ, bar_full(st), x, static_cast<int32_t>(cur.q_tile * BN));
         ++issued;
         if (++st == C::kStages) { st = 0; ph ^= 1u; }
       }
       // Do not leave while copies into this CTA's shared memory may be in flight.
-      const int tail = issued < C::kStages ? issued : C::kStages;
-      for (int t = 0; t < tail; ++t) {
-        const int j = issued - 1 - t;
-        if (!mbar_wait_bounded(bar_full(j % C::kStages), (j / C::kStages) & 1, a.wait_limit)) {
+      const uint32_t tail = issued < static_cast<uint32_t>(C::kStages) ? issued : C::kStages;
+      for (uint32_t t = 0; t < tail; ++t) {
+        const uint32_t j = issued - 1 - t;
+        if (!mbar_wait_bounded(bar_full(j % C::kStages), (j / C::kStages) & 1u, a.wait_limit)) {
           report_failure(a.err, kDevTimeoutTail);
           break;
         }
       }
-      (void)ok;
-    }
-    __syncwarp();
-  } else if (warp == C::kNE + 1) {
-    // ---------------------------------------------------------- MMA issuer
-    if (lane == 0) {
+    } else if (warp == C::kNE + 1 && lane == 0) {
+      // -------------------------------------------------------- MMA issuer
+      const uint32_t n = num_units(s, cta);
       int st = 0;
       uint32_t ph = 0;
-      int done = 0;
-      for (int j = 0; j < nunits; ++j) {
+      uint32_t done = 0;
+      for (uint32_t j = 0; j < n; ++j) {
         const int b = j & 1;
         const uint32_t tph = (j >> 1) & 1;
         if (!mbar_wait_bounded(bar_tempty(b), tph ^ 1u, a.wait_limit) ||
@@ -220,8 +237,8 @@ __global__ void __launch_bounds__(GemmCfg<BN, SWAP>::kThreads, 1)
         if (++st == C::kStages) { st = 0; ph ^= 1u; }
       }
       // The last commit fires when every MMA issued above has completed.
-      if (done > 0 && done < nunits) {
-        const int j = done - 1;
+      if (done > 0 && done < n) {
+        const uint32_t j = done - 1;
         if (!mbar_wait_bounded(bar_tfull(j & 1), (j >> 1) & 1, a.wait_limit))
           report_failure(a.err, kDevTimeoutTail);
       }
@@ -229,46 +246,46 @@ __global__ void __launch_bounds__(GemmCfg<BN, SWAP>::kThreads, 1)
     __syncwarp();
   } else {
     // ---------------------------------------------- promotion and epilogue
+    if constexpr (C::kRebalance) setmaxnreg_inc<C::kRegsEpi>();
     const int quad = warp & 3;
     const int half = warp >> 2;
     const int r = quad * 32 + lane;          // TMEM lane = row of the P tile
     const int col0 = half * C::kCPT;         // first TMEM column of this thread
     const int etid = threadIdx.x;            // 0 .. NE*32-1
-    const uint32_t sP_addr = smem_addr(sP);
-    const uint32_t sQ_addr = smem_addr(sQ);
+    float* sScale = reinterpret_cast<float*>(smem + C::kOffScale);
+    const uint32_t sScale_addr = smem_addr(sScale);
 
-    // Stages the scales of unit jj into ring slot jj % R (one cp.async group
-    // per unit, empty past the end so the group count stays uniform).
-    auto stage_scales = [&](int jj) {
-      if (jj < nunits) {
-        const Unit u = unit_at(s, cta, jj);
-        const int slot = jj % C::kR;
-        const int64_t p_tile = u.tile % s.p_tiles;
-        const int64_t q_tile = u.tile / s.p_tiles;
+    // Stages the scales unit `u` needs into this warp's slot of the ring (one
+    // cp.async group per unit, empty past the end so the group count stays
+    // uniform).  Each warp stages what its own lanes read, so a __syncwarp is
+    // the only synchronisation.
+    auto stage_scales = [&](const Cursor& u) {
+      if (u.valid()) {
+        const int slot = u.j % C::kR;
+        const uint32_t base = sScale_addr + 4u * ((slot * C::kNE + warp) * C::kScaleStride);
         const int64_t kb = u.kb;
         if (!SWAP) {
-          if (etid < 128) {
-            const int64_t m = p_tile * 128 + etid;
-            const bool ok = m < a.M;
-            const float* src =
-                ok ? a.As + (a.as_col_major ? kb * a.ld_as + m : m * a.ld_as + kb) : a.As;
-            cp_async_4(sP_addr + 4u * (slot * 128 + etid), src, ok ? 4u : 0u);
-          }
-          if (etid < BN / 128) {
-            const int64_t nb = q_tile * (BN / 128) + etid;
-            const bool ok = nb < a.NT;
-            const float* src = ok ? a.Bs + nb * s.G + kb : a.Bs;
-            cp_async_4(sQ_addr + 4u * (slot * BN + etid), src, ok ? 4u : 0u);
+          const int64_t m = static_cast<int64_t>(u.p_tile) * 128 + r;
+          const bool ok = m < a.M;
+          const float* src =
+              ok ? a.As + (a.as_col_major ? kb * a.ld_as + m : m * a.ld_as + kb) : a.As;
+          cp_async_4(base + 4u * lane, src, ok ? 4u : 0u);
+          if (lane == 0) {
+            const int64_t nb = static_cast<int64_t>(u.q_tile) * (BN / 128) + half;
+            const bool okb = nb < a.NT;
+            cp_async_4(base + 4u * 32, okb ? a.Bs + nb * s.G + kb : a.Bs, okb ? 4u : 0u);
           }
         } else {
-          if (etid < BN) {
-            const int64_t m = q_tile * BN + etid;
+#pragma unroll
+          for (int c = lane; c < C::kCPT; c += 32) {
+            const int64_t m = static_cast<int64_t>(u.q_tile) * BN + col0 + c;
             const bool ok = m < a.M;
             const float* src =
                 ok ? a.As + (a.as_col_major ? kb * a.ld_as + m : m * a.ld_as + kb) : a.As;
-            cp_async_4(sQ_addr + 4u * (slot * BN + etid), src, ok ? 4u : 0u);
+            cp_async_4(base + 4u * c, src, ok ? 4u : 0u);
           }
-          if (etid == 0) cp_async_4(sP_addr + 4u * (slot * 128), a.Bs + p_tile * s.G + kb, 4u);
+          if (lane == 0)
+            cp_async_4(base + 4u * C::kCPT, a.Bs + static_cast<int64_t>(u.p_tile) * s.G + kb, 4u);
         }
       }
       cp_async_commit();
@@ -278,16 +295,23 @@ __global__ void __launch_bounds__(GemmCfg<BN, SWAP>::kThreads, 1)
 #pragma unroll
     for (int i = 0; i < C::kCPT; ++i) acc[i] = 0.f;
 
+    Cursor cur, ahead;
+    cur.init(s, cta);
+    ahead = cur;
 #pragma unroll
-    for (int d = 0; d < C::kD; ++d) stage_scales(d);
+    for (int d = 0; d < C::kD; ++d) {
+      stage_scales(ahead);
+      ahead.next();
+    }
 
-    for (int j = 0; j < nunits; ++j) {
-      stage_scales(j + C::kD);
+    for (; cur.valid(); cur.next()) {
+      stage_scales(ahead);
+      ahead.next();
       cp_async_wait<C::kD>();
-      named_bar_sync(1, C::kNE * 32);
+      __syncwarp();
 
-      const Unit u = unit_at(s, cta, j);
-      const int slot = j % C::kR;
+      const uint32_t j = cur.j;
+      const float* sc_slot = sScale + ((j % C::kR) * C::kNE + warp) * C::kScaleStride;
       const int b = j & 1;
       if (!mbar_wait_bounded(bar_tfull(b), (j >> 1) & 1, a.wait_limit)) {
         report_failure(a.err, kDevTimeoutEpilogue);
@@ -295,60 +319,48 @@ __global__ void __launch_bounds__(GemmCfg<BN, SWAP>::kThreads, 1)
       }
       tc_fence_after();
 
-      if (u.first) {
+      if (cur.first()) {
 #pragma unroll
         for (int i = 0; i < C::kCPT; ++i) acc[i] = 0.f;
       }
       const uint32_t taddr = tmem + static_cast<uint32_t>(b * BN + col0) +
                              (static_cast<uint32_t>(quad * 32) << 16);
-      if (!SWAP) {
-        const float sc = sP[slot * 128 + r] * sQ[slot * BN + col0 / 128];
+      // scale of element (row r, column c): sr * column scale (swap) or sr
+      const float sr = SWAP ? sc_slot[C::kCPT] : sc_slot[lane] * sc_slot[32];
 #pragma unroll
-        for (int c = 0; c < C::kCPT / C::kCH; ++c) {
-          uint32_t v[C::kCH];
-          if constexpr (C::kCH == 32) tmem_ld32(taddr + c * 32, v); else tmem_ld16(taddr + c * 16, v);
-          tmem_wait_ld_regs(v);
+      for (int c0 = 0; c0 < C::kCPT; c0 += C::kBatch) {
+        uint32_t v[C::kBatch];
 #pragma unroll
-          for (int i = 0; i < C::kCH; ++i)
-            acc[c * C::kCH + i] = fmaf(__uint_as_float(v[i]), sc, acc[c * C::kCH + i]);
-        }
-      } else {
-        const float sb = sP[slot * 128];
-        const float* sq = sQ + slot * BN + col0;
+        for (int h = 0; h < C::kBatch; h += C::kCH) tmem_ld_cols<C::kCH>(taddr + c0 + h, v + h);
+        tmem_wait_ld();
+        reg_fence<C::kBatch>(v);
 #pragma unroll
-        for (int c = 0; c < C::kCPT / C::kCH; ++c) {
-          uint32_t v[C::kCH];
-          if constexpr (C::kCH == 32) tmem_ld32(taddr + c * 32, v); else tmem_ld16(taddr + c * 16, v);
-          tmem_wait_ld_regs(v);
-#pragma unroll
-          for (int i = 0; i < C::kCH; ++i)
-            acc[c * C::kCH + i] =
-                fmaf(__uint_as_float(v[i]), sb * sq[c * C::kCH + i], acc[c * C::kCH + i]);
+        for (int i = 0; i < C::kBatch; ++i) {
+          const float sc = SWAP ? sr * sc_slot[c0 + i] : sr;
+          acc[c0 + i] = fmaf(__uint_as_float(v[i]), sc, acc[c0 + i]);
         }
       }
       tc_fence_before();
       mbar_arrive(bar_tempty(b));
 
-      if (!u.last) continue;
+      if (!cur.last()) continue;
 
       // ---- the segment is complete: emit it
-      const int64_t p_tile = u.tile % s.p_tiles;
-      const int64_t q_tile = u.tile / s.p_tiles;
-      int64_t pf = cta, pl = cta;
-      if (u.sk_tile >= 0) {
-        pf = sk_first_cta(s, u.sk_tile);
-        pl = sk_last_cta(s, u.sk_tile);
+      const int32_t ts = cur.sk_tile();
+      uint32_t pf = cta, pl = cta;
+      if (ts >= 0) {
+        pf = sk_first_cta(s, ts);
+        pl = sk_last_cta(s, ts);
       }
       if (pl > pf) {
         // stream-K fixup: publish this CTA's partial, the last arrival adds all
-        float* mine = a.partials +
-                      static_cast<size_t>(cta * 2 + sk_slot(s, cta, u.sk_tile)) * (128 * BN);
+        float* mine = a.partials + static_cast<size_t>(cta * 2 + sk_slot(s, cta, ts)) * (128 * BN);
 #pragma unroll
         for (int c = 0; c < C::kCPT; ++c) mine[(col0 + c) * 128 + r] = acc[c];
         __threadfence();
         named_bar_sync(1, C::kNE * 32);
         if (etid == 0) {
-          const int old = atomicAdd(a.counters + u.sk_tile, 1);
+          const int old = atomicAdd(a.counters + ts, 1);
           *s_last_flag = (old == static_cast<int>(pl - pf)) ? 1 : 0;
         }
         named_bar_sync(1, C::kNE * 32);
@@ -357,21 +369,19 @@ __global__ void __launch_bounds__(GemmCfg<BN, SWAP>::kThreads, 1)
         __threadfence();
         // Sum the contributors in ascending K order.  Loads are issued in
         // batches of kFixBatch contributors x kFixCols columns so that one L2
-        // round trip serves a whole batch
-        // (two contributors x 8 columns when 128 accumulators already fill the
-        // register budget of the 10-warp configuration)
-        constexpr int kFixBatch = C::kNH == 2 ? 2 : 4;
-        constexpr int kFixCols = C::kNH == 2 ? 8 : 16;
-        const float* part0 = a.partials +
-                             static_cast<size_t>(pf * 2 + sk_slot(s, pf, u.sk_tile)) * (128 * BN);
+        // round trip serves a whole batch.
+        constexpr int kFixBatch = 4;
+        constexpr int kFixCols = 16;
+        const float* part0 =
+            a.partials + static_cast<size_t>(pf * 2 + sk_slot(s, pf, ts)) * (128 * BN);
 #pragma unroll
         for (int c = 0; c < C::kCPT; ++c) acc[c] = __ldcg(part0 + (col0 + c) * 128 + r);
-        for (int64_t pb = pf + 1; pb <= pl; pb += kFixBatch) {
+        for (uint32_t pb = pf + 1; pb <= pl; pb += kFixBatch) {
           const float* parts[kFixBatch];
 #pragma unroll
           for (int i = 0; i < kFixBatch; ++i) {
-            const int64_t pp = pb + i <= pl ? pb + i : pl;
-            parts[i] = a.partials + static_cast<size_t>(pp * 2 + sk_slot(s, pp, u.sk_tile)) * (128 * BN);
+            const uint32_t pp = pb + i <= pl ? pb + i : pl;
+            parts[i] = a.partials + static_cast<size_t>(pp * 2 + sk_slot(s, pp, ts)) * (128 * BN);
           }
 #pragma unroll
           for (int c0 = 0; c0 < C::kCPT; c0 += kFixCols) {
@@ -389,14 +399,14 @@ __global__ void __launch_bounds__(GemmCfg<BN, SWAP>::kThreads, 1)
               }
           }
         }
-        if (etid == 0) a.counters[u.sk_tile] = 0;  // every contributor has arrived
+        if (etid == 0) a.counters[ts] = 0;  // every contributor has arrived
       }
 
       if (!SWAP) {
-        const int64_t m = p_tile * 128 + r;
+        const int64_t m = static_cast<int64_t>(cur.p_tile) * 128 + r;
         if (m < a.M) {
           __nv_bfloat16* row = a.out + m * a.N;
-          const int64_t nbase = q_tile * BN + col0;
+          const int64_t nbase = static_cast<int64_t>(cur.q_tile) * BN + col0;
 #pragma unroll
           for (int g = 0; g < C::kCPT / 8; ++g) {
             const int64_t n = nbase + g * 8;
@@ -413,9 +423,9 @@ __global__ void __launch_bounds__(GemmCfg<BN, SWAP>::kThreads, 1)
           }
         }
       } else {
-        const int64_t n = p_tile * 128 + r;
+        const int64_t n = static_cast<int64_t>(cur.p_tile) * 128 + r;
         if (n < a.N) {
-          const int64_t mbase = q_tile * BN + col0;
+          const int64_t mbase = static_cast<int64_t>(cur.q_tile) * BN + col0;
 #pragma unroll
           for (int c = 0; c < C::kCPT; ++c) {
             const int64_t m = mbase + c;

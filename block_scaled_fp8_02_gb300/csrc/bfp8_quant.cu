@@ -14,8 +14,8 @@
 // Memory-bound: each warp streams 512 input bytes per step with 16-byte loads
 // (one 128-element group for fp32 input, two for bf16 input: a half-warp per
 // group), reduces amax with warp shuffles inside the group's lanes and packs
-// pairs of codes with cvt.rn.satfinite.e4m3x2.f32.  Two steps are in flight per
-// warp to keep enough bytes outstanding.
+// pairs of codes with cvt.rn.satfinite.e4m3x2.f32.  Four steps (2 KB) are in
+// flight per warp to keep enough bytes outstanding.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -66,34 +66,37 @@ __device__ __forceinline__ void load_vec(const void* x, int64_t idx, float (&v)[
   }
 }
 
-constexpr int kUnroll = 2;
+constexpr int kUnroll = 4;
 constexpr int kWarpsPerBlock = 8;
 
 template <bool kF32>
-__global__ void __launch_bounds__(kWarpsPerBlock * 32)
+__global__ void __launch_bounds__(kWarpsPerBlock * 32, 4)
     group_quant_kernel(const void* __restrict__ x, int64_t M, int64_t K, int64_t ld_x,
                        uint8_t* __restrict__ q, int64_t ld_q, float* __restrict__ s,
                        int32_t col_major, int64_t ld_s, int32_t vec_x, int32_t vec_q) {
   using S = QuantShape<kF32>;
   constexpr int EPL = S::kEPL, LPG = S::kLPG, GPW = S::kGPW;
-  const int64_t G = (K + 127) / 128;
-  const int64_t chunks_per_row = (G + GPW - 1) / GPW;
-  const int64_t total = M * chunks_per_row;
+  // chunk indices fit in 32 bits (the host checks M * chunks_per_row < 2^31),
+  // so the row / chunk split is a 32-bit division, not a 64-bit one
+  const uint32_t G = static_cast<uint32_t>((K + 127) / 128);
+  const uint32_t chunks_per_row = (G + GPW - 1) / GPW;
+  const uint32_t total = static_cast<uint32_t>(M) * chunks_per_row;
   const int lane = threadIdx.x & 31;
   const int gi = lane / LPG;       // group within the warp step
   const int li = lane % LPG;       // lane within the group
-  const int64_t warp0 = static_cast<int64_t>(blockIdx.x) * kWarpsPerBlock + (threadIdx.x >> 5);
-  const int64_t nwarps = static_cast<int64_t>(gridDim.x) * kWarpsPerBlock;
+  const uint32_t warp0 = blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
+  const uint32_t nwarps = gridDim.x * kWarpsPerBlock;
 
-  for (int64_t base = warp0; base < total; base += nwarps * kUnroll) {
+  for (uint32_t base = warp0; base < total; base += nwarps * kUnroll) {
     float v[kUnroll][EPL];
     int64_t row[kUnroll], k[kUnroll], g[kUnroll];
     bool valid[kUnroll];
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u) {
-      const int64_t c = base + u * nwarps;
-      row[u] = c / chunks_per_row;
-      g[u] = (c - row[u] * chunks_per_row) * GPW + gi;
+      const uint32_t c = base + u * nwarps;
+      const uint32_t rr = c / chunks_per_row;
+      row[u] = rr;
+      g[u] = static_cast<int64_t>(c - rr * chunks_per_row) * GPW + gi;
       k[u] = g[u] * 128 + li * EPL;
       valid[u] = (c < total) && (g[u] < G);
       if (valid[u] && vec_x && k[u] + EPL <= K) {
@@ -154,6 +157,8 @@ cudaError_t launch_group_quant(const void* x, int in_f32, int64_t M, int64_t K, 
   const int vec_x = (reinterpret_cast<uintptr_t>(x) % 16 == 0) && ((ld_x * esize) % 16 == 0);
   const int vec_q = (reinterpret_cast<uintptr_t>(q) % epl == 0) && (ld_q % epl == 0);
   const int64_t total = M * ((G + gpw - 1) / gpw);
+  if (total >= (int64_t{1} << 31) - static_cast<int64_t>(num_sms) * 8 * kWarpsPerBlock * kUnroll)
+    return cudaErrorInvalidValue;
   int64_t blocks = (total + kWarpsPerBlock - 1) / kWarpsPerBlock;
   const int64_t cap = static_cast<int64_t>(num_sms) * 8;
   if (blocks > cap) blocks = cap;

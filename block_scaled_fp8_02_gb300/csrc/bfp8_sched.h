@@ -14,6 +14,10 @@
 // finished by the last of them to arrive, which adds the others' fp32
 // partial sums in ascending K order, so the result does not depend on which
 // CTA arrives last.
+//
+// All counts fit in 32 bits (the planner rejects larger problems); the device
+// walks its units with an incremental cursor, so the steady state performs no
+// integer division at all.
 #pragma once
 
 #include <cstdint>
@@ -27,97 +31,138 @@
 namespace bfp8 {
 
 struct Sched {
-  int64_t p_tiles;   // tiles along P (128 rows each)
-  int64_t q_tiles;   // tiles along Q (BN rows each)
-  int64_t tiles;     // p_tiles * q_tiles
-  int32_t G;         // k-blocks per tile
-  int32_t grid;      // persistent CTAs
-  int64_t dp_tiles;  // whole tiles handed out round-robin; a multiple of grid
-  int64_t sk_units;  // (tiles - dp_tiles) * G
-  int64_t sk_q;      // units per CTA in the stream-K part ...
-  int64_t sk_r;      // ... plus one for CTAs p < sk_r
+  uint32_t p_tiles;   // tiles along P (128 rows each)
+  uint32_t q_tiles;   // tiles along Q (BN rows each)
+  uint32_t tiles;     // p_tiles * q_tiles
+  uint32_t G;         // k-blocks per tile
+  uint32_t grid;      // persistent CTAs
+  uint32_t dp_tiles;  // whole tiles handed out round-robin; a multiple of grid
+  uint32_t sk_units;  // (tiles - dp_tiles) * G
+  uint32_t sk_q;      // stream-K units per CTA ...
+  uint32_t sk_r;      // ... plus one for CTAs p < sk_r
 };
 
-struct Unit {
-  int64_t tile;      // tile index; p_tile = tile % p_tiles, q_tile = tile / p_tiles
-  int32_t kb;        // k-block
-  int32_t first;     // first unit of a segment (accumulator starts from zero)
-  int32_t last;      // last unit of a segment (the segment's result is emitted)
-  int64_t sk_tile;   // index among stream-K tiles, or -1 for a whole (data-parallel) tile
-};
-
-BFP8_HD int64_t sk_begin(const Sched& s, int64_t p) {
+BFP8_HD uint32_t sk_begin(const Sched& s, uint32_t p) {
   return p * s.sk_q + (p < s.sk_r ? p : s.sk_r);
 }
 
 // CTA that owns stream-K unit u.
-BFP8_HD int64_t sk_owner(const Sched& s, int64_t u) {
-  const int64_t big = s.sk_r * (s.sk_q + 1);
+BFP8_HD uint32_t sk_owner(const Sched& s, uint32_t u) {
+  const uint32_t big = s.sk_r * (s.sk_q + 1);
   return u < big ? u / (s.sk_q + 1) : s.sk_r + (u - big) / s.sk_q;
 }
 
-BFP8_HD int64_t dp_units(const Sched& s) { return (s.dp_tiles / s.grid) * s.G; }
+BFP8_HD uint32_t dp_units(const Sched& s) { return (s.dp_tiles / s.grid) * s.G; }
 
-BFP8_HD int64_t num_units(const Sched& s, int64_t p) {
+BFP8_HD uint32_t num_units(const Sched& s, uint32_t p) {
   return dp_units(s) + sk_begin(s, p + 1) - sk_begin(s, p);
 }
 
-BFP8_HD Unit unit_at(const Sched& s, int64_t p, int64_t j) {
-  Unit u;
-  const int64_t dpu = dp_units(s);
-  if (j < dpu) {
-    const int64_t t = j / s.G;
-    u.kb = static_cast<int32_t>(j - t * s.G);
-    u.tile = p + t * s.grid;
-    u.sk_tile = -1;
-    u.first = u.kb == 0;
-    u.last = u.kb == s.G - 1;
-  } else {
-    const int64_t uu = sk_begin(s, p) + (j - dpu);
-    const int64_t ts = uu / s.G;
-    u.kb = static_cast<int32_t>(uu - ts * s.G);
-    u.tile = s.dp_tiles + ts;
-    u.sk_tile = ts;
-    u.first = (u.kb == 0) || (j == dpu);
-    u.last = (u.kb == s.G - 1) || (j == num_units(s, p) - 1);
-  }
-  return u;
-}
-
 // CTAs that contribute to stream-K tile ts, in ascending K order.
-BFP8_HD int64_t sk_first_cta(const Sched& s, int64_t ts) { return sk_owner(s, ts * s.G); }
-BFP8_HD int64_t sk_last_cta(const Sched& s, int64_t ts) {
+BFP8_HD uint32_t sk_first_cta(const Sched& s, uint32_t ts) { return sk_owner(s, ts * s.G); }
+BFP8_HD uint32_t sk_last_cta(const Sched& s, uint32_t ts) {
   return sk_owner(s, ts * s.G + s.G - 1);
 }
 
 // Which of CTA p's two partial slots holds its contribution to tile ts: slot 0
 // for the segment its stream-K range starts in, slot 1 for the one it ends in.
-BFP8_HD int32_t sk_slot(const Sched& s, int64_t p, int64_t ts) {
-  return (sk_begin(s, p) / s.G == ts) ? 0 : 1;
+BFP8_HD uint32_t sk_slot(const Sched& s, uint32_t p, uint32_t ts) {
+  return (sk_begin(s, p) / s.G == ts) ? 0u : 1u;
 }
 
-// Builds the decomposition for `tiles` tiles of G k-blocks on at most
-// `max_ctas` CTAs.
-inline Sched make_sched(int64_t p_tiles, int64_t q_tiles, int32_t G, int32_t max_ctas) {
+// Sequential walk over one CTA's units, in the order every role processes
+// them.  Divisions happen only when a new tile starts.
+struct Cursor {
+  uint32_t G, grid, p_tiles, dp_tiles, dp_per_cta, sk_beg;
+  uint32_t n;        // units of this CTA
+  uint32_t j;        // current unit index
+  uint32_t tile, kb, p_tile, q_tile;
+  uint32_t dp_t;     // whole tiles finished
+  uint32_t u;        // current stream-K unit (when in_sk)
+  bool in_sk;
+
+  BFP8_HD void set_pq() {
+    q_tile = tile / p_tiles;
+    p_tile = tile - q_tile * p_tiles;
+  }
+  BFP8_HD void enter_sk() {
+    in_sk = true;
+    u = sk_beg;
+    const uint32_t ts = u / G;
+    tile = dp_tiles + ts;
+    kb = u - ts * G;
+    set_pq();
+  }
+  BFP8_HD void init(const Sched& s, uint32_t cta) {
+    G = s.G;
+    grid = s.grid;
+    p_tiles = s.p_tiles;
+    dp_tiles = s.dp_tiles;
+    dp_per_cta = s.dp_tiles / s.grid;
+    sk_beg = sk_begin(s, cta);
+    n = dp_per_cta * s.G + sk_begin(s, cta + 1) - sk_beg;
+    j = 0;
+    dp_t = 0;
+    u = 0;
+    in_sk = false;
+    if (n == 0) { tile = kb = p_tile = q_tile = 0; return; }
+    if (dp_per_cta > 0) {
+      tile = cta;
+      kb = 0;
+      set_pq();
+    } else {
+      enter_sk();
+    }
+  }
+  BFP8_HD void next() {
+    if (++j >= n) return;
+    if (!in_sk) {
+      if (++kb == G) {
+        kb = 0;
+        if (++dp_t < dp_per_cta) {
+          tile += grid;
+          set_pq();
+        } else {
+          enter_sk();
+        }
+      }
+    } else {
+      ++u;
+      if (++kb == G) {
+        kb = 0;
+        ++tile;
+        if (++p_tile == p_tiles) { p_tile = 0; ++q_tile; }
+      }
+    }
+  }
+  BFP8_HD bool valid() const { return j < n; }
+  BFP8_HD bool first() const { return kb == 0 || (in_sk && u == sk_beg); }
+  BFP8_HD bool last() const { return kb + 1 == G || j + 1 == n; }
+  BFP8_HD int32_t sk_tile() const { return in_sk ? static_cast<int32_t>(tile - dp_tiles) : -1; }
+};
+
+// Builds the decomposition for p_tiles x q_tiles tiles of G k-blocks on at
+// most `max_ctas` CTAs.  The caller checks that tiles * G fits in 31 bits.
+inline Sched make_sched(uint32_t p_tiles, uint32_t q_tiles, uint32_t G, uint32_t max_ctas) {
   Sched s{};
   s.p_tiles = p_tiles;
   s.q_tiles = q_tiles;
   s.tiles = p_tiles * q_tiles;
   s.G = G;
-  const int64_t units = s.tiles * G;
-  int64_t grid = max_ctas;
+  const uint64_t units = static_cast<uint64_t>(s.tiles) * G;
+  uint64_t grid = max_ctas;
   if (grid > units) grid = units;
   if (grid < 1) grid = 1;
-  s.grid = static_cast<int32_t>(grid);
-  if (s.tiles % grid == 0) {
+  s.grid = static_cast<uint32_t>(grid);
+  if (s.tiles % s.grid == 0) {
     s.dp_tiles = s.tiles;                        // whole waves: no stream-K
   } else {
-    const int64_t waves = s.tiles / grid;
-    s.dp_tiles = waves >= 2 ? (waves - 1) * grid : 0;
+    const uint32_t waves = s.tiles / s.grid;
+    s.dp_tiles = waves >= 2 ? (waves - 1) * s.grid : 0;
   }
   s.sk_units = (s.tiles - s.dp_tiles) * G;
-  s.sk_q = s.sk_units / grid;
-  s.sk_r = s.sk_units % grid;
+  s.sk_q = s.sk_units / s.grid;
+  s.sk_r = s.sk_units % s.grid;
   return s;
 }
 

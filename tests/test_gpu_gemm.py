@@ -149,3 +149,21 @@ def test_deterministic_across_calls(dev, options):
     torch.cuda.synchronize()
     for o in outs[1:]:
         assert torch.equal(o.view(torch.int16), outs[0].view(torch.int16))
+
+
+def test_one_workspace_serves_problems_of_every_layout(oracle_mod, dev):
+    """Calls with different workspace layouts (whole tiles only, stream-K,
+    re-laid-out operands) share one workspace in turn; every result must stay
+    correct, i.e. no call may leave non-zero counters for the next."""
+    ws = torch.zeros(64 << 20, dtype=torch.uint8, device=dev)
+    shapes = [(1, 8, 1), (2, 130, 129), (83, 576, 7168), (1, 8, 1), (300, 1000, 1000),
+              (16, 4096, 512), (2, 130, 129), (1000, 576, 7168)]
+    for M, N, K in shapes:
+        case = wl.ragged_case(M, N, K, seed=M + N + K)
+        A, As, B, Bs = _prepare(oracle_mod, case, True)
+        A_d, As_d, B_d, Bs_d = _to_dev(dev, A, As, B, Bs, True, M)
+        out = bf.bfp8_gemm(A_d, B_d, As_d, Bs_d, workspace=ws)
+        torch.cuda.synchronize()
+        rows = None if M <= 128 else sample_rows(M, 16, seed=M)
+        ref = oracle_mod.blocked_gemm(A, B, As, True, Bs, rows=rows, want_abs=True)
+        check_gemm(out, ref, (K + 127) // 128, rows=rows, label=f"shared ws {M}x{N}x{K}")
