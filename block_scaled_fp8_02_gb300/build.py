@@ -42,17 +42,25 @@ def _stale(target: str, deps: list[str]) -> bool:
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def build(force: bool = False, verbose_ptxas: bool = False, jobs: int | None = None) -> str:
-    """Compile (if needed) and return the path of libbfp8.so."""
+def build(force: bool = False, verbose_ptxas: bool = False, jobs: int | None = None,
+          trace: bool = False, out: str | None = None) -> str:
+    """Compile (if needed) and return the path of libbfp8.so.
+
+    trace=True builds a separate timeline-tracing variant (kernels record
+    %globaltimer at role milestones; see bfp8_trace_read) into `out`."""
+    lib = out or LIB
     deps = _deps()
-    if not force and not _stale(LIB, deps):
-        return LIB
+    if not force and not _stale(lib, deps):
+        return lib
     os.makedirs(BUILD, exist_ok=True)
     nvcc = _nvcc()
     extra = ["-Xptxas", "-v"] if verbose_ptxas else []
+    if trace:
+        extra += ["-DBFP8_TRACE"]
+    tag = "_trace" if trace else ""
 
     def compile_one(src: str) -> tuple[str, str]:
-        obj = os.path.join(BUILD, src.replace(".cu", ".o"))
+        obj = os.path.join(BUILD, src.replace(".cu", tag + ".o"))
         cmd = [nvcc, *ARCH, *FLAGS, *extra, "-c", os.path.join(CSRC, src), "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
@@ -65,13 +73,13 @@ def build(force: bool = False, verbose_ptxas: bool = False, jobs: int | None = N
         with open(os.path.join(BUILD, "ptxas.log"), "w") as f:
             for (_, log), src in zip(results, SOURCES):
                 f.write(f"==== {src}\n{log}\n")
-    tmp = LIB + ".tmp"
+    tmp = lib + ".tmp"
     cmd = [nvcc, *ARCH, "-shared", "-o", tmp, *[o for o, _ in results], "-cudart", "static"]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stderr}\n{r.stdout}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":

@@ -230,9 +230,26 @@ __global__ void selftest_wait_kernel(unsigned long long limit) {
 }
 
 }  // namespace
+
+#if defined(BFP8_TRACE)
+__device__ unsigned long long g_bfp8_trace[1024 * kTraceEvents];
+#endif
+
 }  // namespace bfp8
 
 using namespace bfp8;
+
+#if defined(BFP8_TRACE)
+// Trace builds only: copies the per-CTA milestone timestamps of the last
+// traced launch (kTraceEvents per CTA, up to 1024 CTAs) to host memory.
+extern "C" int bfp8_trace_events(void) { return kTraceEvents; }
+extern "C" int bfp8_trace_read(unsigned long long* host, int max_ctas) {
+  if (max_ctas > 1024) max_ctas = 1024;
+  if (cudaDeviceSynchronize() != cudaSuccess) return -1;
+  return cudaMemcpyFromSymbol(host, g_bfp8_trace, sizeof(unsigned long long) * kTraceEvents * max_ctas) ==
+                 cudaSuccess ? 0 : -1;
+}
+#endif
 
 extern "C" {
 
@@ -422,6 +439,14 @@ bfp8_status bfp8_gemm_ex(const void* A, const void* B, const float* As, int as_c
   a.vec_store = (!misaligned(out, 16) && (N % 8) == 0) ? 1 : 0;
   a.err = d.err;
   a.wait_limit = kWaitLimitCycles;
+  a.trace = nullptr;
+#if defined(BFP8_TRACE)
+  {
+    void* tp = nullptr;
+    if (cudaGetSymbolAddress(&tp, g_bfp8_trace) == cudaSuccess) a.trace = static_cast<unsigned long long*>(tp);
+    cudaGetLastError();
+  }
+#endif
   cudaError_t e = p.swap ? launch_gemm_swap(p.bn, tmP, tmQ, a, cs) : launch_gemm_wide(p.bn, tmP, tmQ, a, cs);
   if (e != cudaSuccess) return fail(BFP8_ERR_CUDA, "GEMM launch: %s", cudaGetErrorString(e));
   return ok();

@@ -64,6 +64,7 @@ struct GemmArgs {
   int32_t vec_store;     // out rows may be written 16 bytes at a time
   int* err;              // device failure word
   unsigned long long wait_limit;  // cycles before a wait gives up
+  unsigned long long* trace;      // milestone timestamps (trace builds only)
 };
 
 __host__ __device__ constexpr int tmem_cols_for(int n) {
@@ -107,6 +108,46 @@ struct GemmCfg {
   static constexpr int kTmemCols = tmem_cols_for(2 * BN);
   static constexpr uint32_t kIdesc = idesc_e4m3_f32(128, BN);
 };
+
+// Optional timeline trace (compiled in only with -DBFP8_TRACE): %globaltimer
+// nanoseconds at role milestones, one row of kTraceEvents per CTA.
+enum : int {
+  kTrStart = 0,        // after set-up
+  kTrProdFirst = 1,    // producer issued its first load
+  kTrProdDone = 2,     // producer issued its last load
+  kTrMmaFirst = 3,     // first stage of data seen by the MMA issuer
+  kTrMmaDone = 4,      // last MMA issued
+  kTrEpiFirst = 5,     // first TMEM partial seen by the promotion warps
+  kTrEpiLoop = 6,      // last unit promoted
+  kTrEpiEnd = 7,       // promotion warps done (after fixups and stores)
+  // accumulated SM cycles (not timestamps)
+  kTrEpiWaitCyc = 8,   // promotion warp 0 waiting for TMEM partials
+  kTrEpiWorkCyc = 9,   // promotion warp 0 from partial ready to TMEM release
+  kTrMmaWaitTmem = 10, // MMA issuer waiting for a free TMEM buffer
+  kTrMmaWaitData = 11, // MMA issuer waiting for operand tiles
+  kTrProdWait = 12,    // producer waiting for a free stage
+  kTrEpiScaleCyc = 13, // promotion warp 0 staging / waiting for scales
+  kTrEpiFixCyc = 14,   // promotion warp 0 in segment epilogues (fixup + stores)
+  kTraceEvents = 16
+};
+#if defined(BFP8_TRACE)
+__device__ __forceinline__ void trace_event(unsigned long long* tr, uint32_t cta, int e) {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  if (tr != nullptr && cta < 1024) tr[cta * kTraceEvents + e] = t;
+}
+__device__ __forceinline__ void trace_value(unsigned long long* tr, uint32_t cta, int e,
+                                            unsigned long long v) {
+  if (tr != nullptr && cta < 1024) tr[cta * kTraceEvents + e] = v;
+}
+#define BFP8_CLK(var) const long long var = clock64()
+#define BFP8_ACC(acc, since) acc += static_cast<unsigned long long>(clock64() - (since))
+#else
+__device__ __forceinline__ void trace_event(unsigned long long*, uint32_t, int) {}
+__device__ __forceinline__ void trace_value(unsigned long long*, uint32_t, int, unsigned long long) {}
+#define BFP8_CLK(var)
+#define BFP8_ACC(acc, since)
+#endif
 
 __device__ __forceinline__ void report_failure(int* err, int code) {
   if (err != nullptr) atomicCAS(err, 0, code);
@@ -160,23 +201,34 @@ __global__ void __launch_bounds__(GemmCfg<BN, SWAP>::kThreads, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(bar_tfull(b), 1);
-      mbar_init(bar_tempty(b), C::kNE * 32);
+      mbar_init(bar_tempty(b), C::kNE);      // one arrival per promotion warp
     }
     *s_last_flag = 0;
     fence_barrier_init();
-  }
-  if (warp == C::kNE + 1) {
-    tmem_alloc(smem_addr(tmem_slot), C::kTmemCols);
-    tmem_relinquish();
   }
   if (warp == C::kNE && lane == 0) {
     tma_prefetch_desc(&tmP);
     tma_prefetch_desc(&tmQ);
   }
-  tc_fence_before();
+  // Barriers are initialised before anyone uses them; the producer then starts
+  // streaming while the MMA warp allocates TMEM.  The TMEM address reaches the
+  // MMA and promotion warps through named barrier 2 (producer not included).
   __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = *tmem_slot;
+  if (threadIdx.x == 0) trace_event(a.trace, cta, kTrStart);
+  constexpr uint32_t kTmemSyncThreads = (C::kNE + 1) * 32;
+  uint32_t tmem = 0;
+  if (warp == C::kNE + 1) {
+    tmem_alloc(smem_addr(tmem_slot), C::kTmemCols);
+    tmem_relinquish();
+    tc_fence_before();
+    named_bar_sync(2, kTmemSyncThreads);
+    tc_fence_after();
+    tmem = *tmem_slot;
+  } else if (warp < C::kNE) {
+    named_bar_sync(2, kTmemSyncThreads);
+    tc_fence_after();
+    tmem = *tmem_slot;
+  }
 
   if (warp >= C::kNE) {
     if constexpr (C::kRebalance) setmaxnreg_dec<C::kRegsOther>();
@@ -187,18 +239,25 @@ __global__ void __launch_bounds__(GemmCfg<BN, SWAP>::kThreads, 1)
       int st = 0;
       uint32_t ph = 0;
       uint32_t issued = 0;
+      unsigned long long t_wait = 0;
+      (void)t_wait;
       for (; cur.valid(); cur.next()) {
+        BFP8_CLK(c0);
         if (!mbar_wait_bounded(bar_empty(st), ph ^ 1u, a.wait_limit)) {
           report_failure(a.err, kDevTimeoutProducer);
           break;
         }
+        BFP8_ACC(t_wait, c0);
         mbar_arrive_expect_tx(bar_full(st), C::kStageBytes);
         const int32_t x = static_cast<int32_t>(cur.kb * 128);
         tma_load_2d(stage_p(st), &tmP, bar_full(st), x, static_cast<int32_t>(cur.p_tile * 128));
         tma_load_2d(stage_q(st), &tmQ, bar_full(st), x, static_cast<int32_t>(cur.q_tile * BN));
+        if (issued == 0) trace_event(a.trace, cta, kTrProdFirst);
         ++issued;
         if (++st == C::kStages) { st = 0; ph ^= 1u; }
       }
+      trace_event(a.trace, cta, kTrProdDone);
+      trace_value(a.trace, cta, kTrProdWait, t_wait);
       // Do not leave while copies into this CTA's shared memory may be in flight.
       const uint32_t tail = issued < static_cast<uint32_t>(C::kStages) ? issued : C::kStages;
       for (uint32_t t = 0; t < tail; ++t) {
@@ -214,15 +273,22 @@ __global__ void __launch_bounds__(GemmCfg<BN, SWAP>::kThreads, 1)
       int st = 0;
       uint32_t ph = 0;
       uint32_t done = 0;
+      unsigned long long t_tmem = 0, t_data = 0;
+      (void)t_tmem; (void)t_data;
       for (uint32_t j = 0; j < n; ++j) {
         const int b = j & 1;
         const uint32_t tph = (j >> 1) & 1;
-        if (!mbar_wait_bounded(bar_tempty(b), tph ^ 1u, a.wait_limit) ||
-            !mbar_wait_bounded(bar_full(st), ph, a.wait_limit)) {
+        BFP8_CLK(c0);
+        const bool ok_t = mbar_wait_bounded(bar_tempty(b), tph ^ 1u, a.wait_limit);
+        BFP8_ACC(t_tmem, c0);
+        BFP8_CLK(c1);
+        if (!ok_t || !mbar_wait_bounded(bar_full(st), ph, a.wait_limit)) {
           report_failure(a.err, kDevTimeoutMma);
           break;
         }
+        BFP8_ACC(t_data, c1);
         tc_fence_after();
+        if (j == 0) trace_event(a.trace, cta, kTrMmaFirst);
         const uint32_t d_tmem = tmem + static_cast<uint32_t>(b * BN);
         const uint64_t adesc = sdesc_k_sw128(stage_p(st));
         const uint64_t bdesc = sdesc_k_sw128(stage_q(st));
@@ -236,6 +302,9 @@ __global__ void __launch_bounds__(GemmCfg<BN, SWAP>::kThreads, 1)
         done = j + 1;
         if (++st == C::kStages) { st = 0; ph ^= 1u; }
       }
+      trace_event(a.trace, cta, kTrMmaDone);
+      trace_value(a.trace, cta, kTrMmaWaitTmem, t_tmem);
+      trace_value(a.trace, cta, kTrMmaWaitData, t_data);
       // The last commit fires when every MMA issued above has completed.
       if (done > 0 && done < n) {
         const uint32_t j = done - 1;
@@ -304,11 +373,16 @@ __global__ void __launch_bounds__(GemmCfg<BN, SWAP>::kThreads, 1)
       ahead.next();
     }
 
+    unsigned long long t_ewait = 0, t_ework = 0, t_escale = 0, t_efix = 0;
+    (void)t_ewait; (void)t_ework; (void)t_escale; (void)t_efix;
     for (; cur.valid(); cur.next()) {
+      BFP8_CLK(e0);
       stage_scales(ahead);
       ahead.next();
       cp_async_wait<C::kD>();
       __syncwarp();
+      BFP8_ACC(t_escale, e0);
+      BFP8_CLK(e1);
 
       const uint32_t j = cur.j;
       const float* sc_slot = sScale + ((j % C::kR) * C::kNE + warp) * C::kScaleStride;
@@ -318,6 +392,10 @@ __global__ void __launch_bounds__(GemmCfg<BN, SWAP>::kThreads, 1)
         break;
       }
       tc_fence_after();
+      BFP8_ACC(t_ewait, e1);
+      BFP8_CLK(e2);
+      if (j == 0 && etid == 0) trace_event(a.trace, cta, kTrEpiFirst);
+      if (j + 1 == cur.n && etid == 0) trace_event(a.trace, cta, kTrEpiLoop);
 
       if (cur.first()) {
 #pragma unroll
@@ -340,10 +418,15 @@ __global__ void __launch_bounds__(GemmCfg<BN, SWAP>::kThreads, 1)
           acc[c0 + i] = fmaf(__uint_as_float(v[i]), sc, acc[c0 + i]);
         }
       }
+      // every lane's TMEM reads are complete (wait::ld above); order them before
+      // the release, then one lane per warp arrives
       tc_fence_before();
-      mbar_arrive(bar_tempty(b));
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_tempty(b));
+      BFP8_ACC(t_ework, e2);
 
       if (!cur.last()) continue;
+      BFP8_CLK(e3);
 
       // ---- the segment is complete: emit it
       const int32_t ts = cur.sk_tile();
@@ -365,7 +448,10 @@ __global__ void __launch_bounds__(GemmCfg<BN, SWAP>::kThreads, 1)
         }
         named_bar_sync(1, C::kNE * 32);
         const bool is_last = *s_last_flag != 0;
-        if (!is_last) continue;
+        if (!is_last) {
+          BFP8_ACC(t_efix, e3);
+          continue;
+        }
         __threadfence();
         // Sum the contributors in ascending K order.  Loads are issued in
         // batches of kFixBatch contributors x kFixCols columns so that one L2
@@ -376,6 +462,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, SWAP>::kThreads, 1)
             a.partials + static_cast<size_t>(pf * 2 + sk_slot(s, pf, ts)) * (128 * BN);
 #pragma unroll
         for (int c = 0; c < C::kCPT; ++c) acc[c] = __ldcg(part0 + (col0 + c) * 128 + r);
+#pragma unroll 1
         for (uint32_t pb = pf + 1; pb <= pl; pb += kFixBatch) {
           const float* parts[kFixBatch];
 #pragma unroll
@@ -433,8 +520,16 @@ __global__ void __launch_bounds__(GemmCfg<BN, SWAP>::kThreads, 1)
           }
         }
       }
+      BFP8_ACC(t_efix, e3);
     }
     cp_async_wait<0>();
+    if (etid == 0) {
+      trace_event(a.trace, cta, kTrEpiEnd);
+      trace_value(a.trace, cta, kTrEpiWaitCyc, t_ewait);
+      trace_value(a.trace, cta, kTrEpiWorkCyc, t_ework);
+      trace_value(a.trace, cta, kTrEpiScaleCyc, t_escale);
+      trace_value(a.trace, cta, kTrEpiFixCyc, t_efix);
+    }
   }
 
   tc_fence_before();
