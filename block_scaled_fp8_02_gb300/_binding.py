@@ -28,7 +28,7 @@ STATUS_NAMES = {0: "BFP8_OK", 1: "BFP8_ERR_INVALID_ARG", 2: "BFP8_ERR_ALIGNMENT"
 EXPORTS = ("bfp8_group_quant", "bfp8_scale_ld", "bfp8_gemm", "bfp8_gemm_ex",
            "bfp8_gemm_workspace_size", "bfp8_gemm_plan", "bfp8_plan_unit", "bfp8_last_error",
            "bfp8_status_string", "bfp8_device_status", "bfp8_selftest_bounded_wait",
-           "bfp8_version")
+           "bfp8_version", "bfp8_gemm_noalloc")
 
 
 class BFP8Error(RuntimeError):
@@ -92,6 +92,8 @@ def lib():
             L.bfp8_selftest_bounded_wait.argtypes = [ctypes.c_uint64, ctypes.POINTER(ctypes.c_uint64), P]
             L.bfp8_version.restype = i32
             L.bfp8_version.argtypes = []
+            L.bfp8_gemm_noalloc.restype = i32
+            L.bfp8_gemm_noalloc.argtypes = [P, P, P, i32, i64, P, P, i64, i64, i64, P]
             _lib = L
     return _lib
 

@@ -44,6 +44,15 @@ bfp8_status ok() {
   return BFP8_OK;
 }
 
+}  // namespace
+
+bfp8_status set_last_error(bfp8_status st, const char* msg) {
+  t_last_error = msg ? msg : "";
+  return st;
+}
+
+namespace {
+
 struct DevInfo {
   bool ready = false;
   int cc_major = 0, cc_minor = 0, sms = 0;

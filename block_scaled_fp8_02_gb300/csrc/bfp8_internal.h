@@ -8,9 +8,13 @@
 #include <cstddef>
 #include <cstdint>
 
+#include "../../include/bfp8.h"
 #include "bfp8_sched.h"
 
 namespace bfp8 {
+
+// Records `msg` as the calling thread's bfp8_last_error() and returns st.
+bfp8_status set_last_error(bfp8_status st, const char* msg);
 
 struct GemmArgs;
 

@@ -173,6 +173,43 @@ bfp8_status bfp8_plan_unit(int64_t M, int64_t N, int64_t K, int num_sms,
                            const bfp8_gemm_options* opt, int cta, int64_t j,
                            int64_t* num_units, int64_t* tile, int64_t* k_block);
 
+/*
+ * bfp8_gemm_noalloc -- bfp8_gemm for callers that cannot allocate device
+ * memory.  (Not from the pages: they have no counterpart; this is a
+ * convenience of this library.)
+ *
+ * Some callers have no way to provide the GEMM workspace: code running while a
+ * stream is being captured into a CUDA graph in a mode that forbids
+ * cudaMalloc, plug-ins living inside a host framework that owns every device
+ * allocation through its own pool and exposes no hook to them, and
+ * latency-critical loops that must not pay for an allocation or risk one
+ * failing.  This entry point computes exactly what bfp8_gemm computes (same
+ * arguments minus the workspace, same kernels, same results) but takes its
+ * scratch from a fixed array built into the library: BFP8_NOALLOC_SCRATCH_BYTES
+ * (16 MiB) of device memory that every GPU which loads the library holds until
+ * the process exits.  It never calls cudaMalloc, cudaFree or any allocating
+ * routine.
+ *
+ * Limits and rules:
+ *   - Problems whose workspace (bfp8_gemm_workspace_size with default
+ *     options) exceeds BFP8_NOALLOC_SCRATCH_BYTES are rejected with
+ *     BFP8_ERR_WORKSPACE and a reason in bfp8_last_error(); nothing is
+ *     launched.  Decode-sized problems fit (e.g. M <= 64 at N = K = 4096);
+ *     large-M problems generally do not.
+ *   - The first call on each device looks up the scratch's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before any stream capture begins.
+ *   - Every call on a device shares the one scratch array, and it keeps the
+ *     previous call's contents: each call first clears (cudaMemsetAsync on
+ *     `stream`) the part that must start at zero.  Calls whose kernels can
+ *     overlap on the GPU (different streams without ordering between them)
+ *     race on the scratch and give wrong results; serialise them.
+ */
+#define BFP8_NOALLOC_SCRATCH_BYTES ((size_t)16 << 20)
+bfp8_status bfp8_gemm_noalloc(const void* A, const void* B, const float* As, int as_col_major,
+                              int64_t ld_as, const float* Bs, void* out, int64_t M, int64_t N,
+                              int64_t K, void* stream);
+
 /* ------------------------------------------------------------------------ */
 /* Status and diagnostics                                                    */
 /* ------------------------------------------------------------------------ */
