@@ -145,7 +145,8 @@ struct Plan {
   bool relayout = false;
   int64_t kp = 0;            // inner extent of the operand tensor maps
   Sched sched{};
-  size_t off_counters = 0, off_partials = 0, off_a = 0, off_b = 0, total = 0;
+  size_t off_counters = 0, off_partials = 0, off_a = 0, off_b = 0, off_as = 0, off_bs = 0,
+         total = 0;
 };
 
 bfp8_status check_options(const bfp8_gemm_options* opt) {
@@ -193,12 +194,13 @@ bfp8_status make_plan(int64_t M, int64_t N, int64_t K, int num_sms, const bfp8_g
   const int64_t sk_tiles = p->sched.tiles - p->sched.dp_tiles;
   // The counters live in a fixed-size header at the start of every workspace,
   // whatever the problem: a later call with a different shape must find zeros
-  // there, never an earlier call's partial sums.  Stream-K always covers fewer
-  // than 2 x grid tiles (whole waves are handed out round-robin first).
-  // It is reserved whenever the workspace is used at all, so that nothing but
-  // counters (which every completed call returns to zero) is ever written there.
+  // there, never an earlier call's partial sums.  Stream-K covers fewer tiles
+  // than the grid has CTAs (whole waves are handed out round-robin first).
+  // It is always reserved, so that nothing but counters (which every
+  // completed call returns to zero) is ever written there.
+  (void)sk_tiles;
   p->off_counters = off;
-  if (sk_tiles > 0 || p->relayout) off += kCounterHeaderBytes;
+  off += kCounterHeaderBytes;
   p->off_partials = off;
   if (p->sched.sk_units > 0)
     off += align256(static_cast<size_t>(p->sched.grid) * 2 * 128 * p->bn * sizeof(float));
@@ -206,6 +208,12 @@ bfp8_status make_plan(int64_t M, int64_t N, int64_t K, int num_sms, const bfp8_g
   if (p->relayout) off += align256(static_cast<size_t>(M) * p->kp);
   p->off_b = off;
   if (p->relayout) off += align256(static_cast<size_t>(N) * p->kp);
+  // room for the scales in the kernel's layout (used when the caller's As is
+  // row-major or not 16-byte aligned, or Bs does not meet the 16-byte rules)
+  p->off_as = off;
+  off += align256(static_cast<size_t>(G) * static_cast<size_t>(cdiv(M, 4) * 4) * sizeof(float));
+  p->off_bs = off;
+  off += align256(static_cast<size_t>(cdiv(N, 128) * G + 4) * sizeof(float));
   p->total = off;
   return BFP8_OK;
 }
@@ -425,6 +433,23 @@ bfp8_status bfp8_gemm_ex(const void* A, const void* B, const float* As, int as_c
     a_op = ws + p.off_a;
     b_op = ws + p.off_b;
   }
+  // scales in the layout the kernel bulk-copies
+  const int64_t NTv = cdiv(N, 128);
+  const bool as_ok = as_col_major && ld_as % 4 == 0 && !misaligned(As, 16);
+  const bool bs_ok = !misaligned(Bs, 16) && (NTv * G) % 4 == 0;
+  const float* as_k = As;
+  int64_t ld_k = ld_as;
+  const float* bs_k = Bs;
+  if (!as_ok || !bs_ok) {
+    float* as_out = as_ok ? nullptr : reinterpret_cast<float*>(ws + p.off_as);
+    float* bs_out = bs_ok ? nullptr : reinterpret_cast<float*>(ws + p.off_bs);
+    const int64_t ld_out = cdiv(M, 4) * 4;
+    cudaError_t e = launch_scale_relayout(As, as_col_major, ld_as, M, G, as_out, ld_out, Bs,
+                                          NTv * G, bs_out, d.sms, cs);
+    if (e != cudaSuccess) return fail(BFP8_ERR_CUDA, "scale re-layout launch: %s", cudaGetErrorString(e));
+    if (as_out) { as_k = as_out; ld_k = ld_out; }
+    if (bs_out) bs_k = bs_out;
+  }
   CUtensorMap tmP, tmQ;
   const void* p_ptr = p.swap ? b_op : a_op;
   const void* q_ptr = p.swap ? a_op : b_op;
@@ -434,11 +459,10 @@ bfp8_status bfp8_gemm_ex(const void* A, const void* B, const float* As, int as_c
   if ((st = encode_operand(&tmQ, q_ptr, q_rows, p.kp, p.bn)) != BFP8_OK) return st;
 
   GemmArgs a{};
-  a.As = As;
-  a.ld_as = ld_as;
-  a.as_col_major = as_col_major;
-  a.NT = static_cast<int32_t>(cdiv(N, 128));
-  a.Bs = Bs;
+  a.As = as_k;
+  a.ld_as = ld_k;
+  a.NT = static_cast<int32_t>(NTv);
+  a.Bs = bs_k;
   a.out = static_cast<__nv_bfloat16*>(out);
   a.M = M;
   a.N = N;

@@ -51,11 +51,10 @@ enum : int {
 };
 
 struct GemmArgs {
-  const float* As;       // activation scales
-  int64_t ld_as;         // leading dimension of As
-  int32_t as_col_major;  // 1: As[kb * ld_as + m], 0: As[m * ld_as + kb]
+  const float* As;       // activation scales, column-major As[kb * ld_as + m],
+  int64_t ld_as;         //   16-byte aligned, ld_as % 4 == 0
   int32_t NT;            // rows of Bs = ceil(N / 128); Bs row stride = G
-  const float* Bs;
+  const float* Bs;       // 16-byte aligned; NT * G rounded up to 4 floats readable
   __nv_bfloat16* out;    // [M, N] row-major
   int64_t M, N;
   Sched sched;
@@ -75,33 +74,53 @@ template <int BN, bool SWAP>
 struct GemmCfg {
   static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "MMA N for M=128 is 16..256 step 16");
   static_assert(SWAP || BN % 128 == 0, "wide tiles cover whole 128-column weight-scale blocks");
-  static constexpr int kNE = BN > 128 ? 8 : 4;   // promotion warps
-  static constexpr int kNH = kNE / 4;            // column halves
+#ifndef BFP8_WIDE_WARPS
+#define BFP8_WIDE_WARPS 8
+#endif
+  // promotion warps: 4 per 128 TMEM columns; the wide 256-column tile may use
+  // 16 (four per SM sub-partition, 64 columns each) to hide TMEM load latency
+  static constexpr int kNE = (!SWAP && BN == 256) ? BFP8_WIDE_WARPS : (BN > 128 ? 8 : 4);
+  static constexpr int kNH = kNE / 4;            // column groups per lane quadrant
   static constexpr int kCPT = BN / kNH;          // accumulator columns per thread
   static constexpr int kCH = kCPT >= 32 ? 32 : 16;   // columns per tcgen05.ld
-  static constexpr int kBatch = kCPT >= 64 ? 64 : kCPT;  // columns loaded per wait
+  // columns loaded per tcgen05.wait::ld: every wait costs a full TMEM load
+  // latency, so batches are as large as the register budget allows
+#ifndef BFP8_WIDE_BATCH
+#define BFP8_WIDE_BATCH 64
+#endif
+  static constexpr int kBatch =
+      kNH == 4 ? 32 : (kNH == 2 ? BFP8_WIDE_BATCH : (kCPT >= 64 ? 64 : kCPT));
   // 8 promotion warps: 12 warps in all so that warps 8..11 are one warpgroup
   // that gives registers to the promotion warpgroups (setmaxnreg).
-  static constexpr int kWarps = kNE == 8 ? 12 : kNE + 2;
+  static constexpr int kWarps = kNE >= 8 ? kNE + 4 : kNE + 2;
   static constexpr int kThreads = kWarps * 32;
-  static constexpr bool kRebalance = kNE == 8;
-  static constexpr int kRegsEpi = 232, kRegsOther = 40;  // 256*232 + 128*40 = 384*168
+  static constexpr bool kRebalance = kNE >= 8;
+  // 8: 256*232 + 128*40 <= 384*168;  16: 512*112 + 128*24 <= 640*96
+  static constexpr int kRegsEpi = kNE == 16 ? 112 : 232;
+  static constexpr int kRegsOther = kNE == 16 ? 24 : 40;
   static constexpr int kPBytes = 128 * 128;
   static constexpr int kQBytes = BN * 128;
   static constexpr int kStageBytes = kPBytes + kQBytes;
-  static constexpr int kD = 3;                   // scale prefetch distance in units
-  static constexpr int kR = kD + 2;              // scale ring slots
-  // per warp and slot: swap -> the warp's column scales + the weight scale;
-  // wide -> one activation scale per lane + the weight scale
-  static constexpr int kScaleStride = SWAP ? (kCPT + 4) : 36;
-  static constexpr int kScaleBytes = kR * kNE * kScaleStride * 4;
+  // Scales: the producer bulk-copies each unit's activation-scale slice
+  // (column-major, contiguous) and a 16-byte chunk holding each weight scale
+  // into a kSR-deep ring of slots, independent of the operand ring so that it
+  // runs further ahead (the library hands the kernel scales in that layout).
+  // Slot layout (floats):
+  //   [0, kAsFloats)                       As of the tile's rows (wide) / columns (swap)
+  //   [kAsFloats + 4h, kAsFloats + 4h + 4) 16-byte chunk containing Bs of block h
+  static constexpr int kSR = 8;
+  static constexpr int kAsFloats = SWAP ? BN : 128;
+  static constexpr int kBsChunks = SWAP ? 1 : BN / 128;
+  static constexpr int kSlotFloats = kAsFloats + 4 * kBsChunks;
+  static constexpr int kScaleBytes = kSR * kSlotFloats * 4;
   static constexpr int kSmemLimit = 232448;      // 227 KB per CTA
-  static constexpr int kFixed = 1024 /*align slack*/ + 256 /*barriers, flags*/ + kScaleBytes;
-  static constexpr int kStagesFit = (kSmemLimit - kFixed) / kStageBytes;
+  static constexpr int kStagesFit =
+      (kSmemLimit - 1024 /*align*/ - 384 /*barriers*/ - kScaleBytes) / kStageBytes;
   static constexpr int kStages = kStagesFit > 10 ? 10 : kStagesFit;
   static_assert(kStages >= 2, "ring too small");
+  // barriers: full, empty [kStages]; sfull, sempty [kSR]; tfull, tempty [2]
   static constexpr int kOffBars = kStages * kStageBytes;
-  static constexpr int kOffTmemPtr = kOffBars + (2 * kStages + 4) * 8;
+  static constexpr int kOffTmemPtr = kOffBars + (2 * kStages + 2 * kSR + 4) * 8;
   static constexpr int kOffFlags = kOffTmemPtr + 8;
   static constexpr int kOffScale = (kOffFlags + 8 + 15) / 16 * 16;
   static constexpr int kSmemBytes = kOffScale + kScaleBytes + 1024;
@@ -187,8 +206,12 @@ __global__ void __launch_bounds__(GemmCfg<BN, SWAP>::kThreads, 1)
 
   auto bar_full = [&](int i) { return sbase + C::kOffBars + 8u * i; };
   auto bar_empty = [&](int i) { return sbase + C::kOffBars + 8u * (C::kStages + i); };
-  auto bar_tfull = [&](int b) { return sbase + C::kOffBars + 8u * (2 * C::kStages + b); };
-  auto bar_tempty = [&](int b) { return sbase + C::kOffBars + 8u * (2 * C::kStages + 2 + b); };
+  auto bar_sfull = [&](int i) { return sbase + C::kOffBars + 8u * (2 * C::kStages + i); };
+  auto bar_sempty = [&](int i) { return sbase + C::kOffBars + 8u * (2 * C::kStages + C::kSR + i); };
+  auto bar_tfull = [&](int b) { return sbase + C::kOffBars + 8u * (2 * C::kStages + 2 * C::kSR + b); };
+  auto bar_tempty = [&](int b) {
+    return sbase + C::kOffBars + 8u * (2 * C::kStages + 2 * C::kSR + 2 + b);
+  };
   auto stage_p = [&](int i) { return sbase + static_cast<uint32_t>(i * C::kStageBytes); };
   auto stage_q = [&](int i) { return sbase + static_cast<uint32_t>(i * C::kStageBytes + C::kPBytes); };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffTmemPtr);
@@ -198,6 +221,10 @@ __global__ void __launch_bounds__(GemmCfg<BN, SWAP>::kThreads, 1)
     for (int i = 0; i < C::kStages; ++i) {
       mbar_init(bar_full(i), 1);
       mbar_init(bar_empty(i), 1);
+    }
+    for (int i = 0; i < C::kSR; ++i) {
+      mbar_init(bar_sfull(i), 1);
+      mbar_init(bar_sempty(i), C::kNE);    // one arrival per promotion warp
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(bar_tfull(b), 1);
@@ -241,8 +268,36 @@ __global__ void __launch_bounds__(GemmCfg<BN, SWAP>::kThreads, 1)
       uint32_t issued = 0;
       unsigned long long t_wait = 0;
       (void)t_wait;
+      int ss = 0;
+      uint32_t sph = 0;
+      const uint32_t sring = smem_addr(smem + C::kOffScale);
       for (; cur.valid(); cur.next()) {
         BFP8_CLK(c0);
+        {
+          if (!mbar_wait_bounded(bar_sempty(ss), sph ^ 1u, a.wait_limit)) {
+            report_failure(a.err, kDevTimeoutProducer);
+            break;
+          }
+          const int64_t kb = cur.kb;
+          const uint32_t slot = sring + 4u * (ss * C::kSlotFloats);
+          const int64_t m0 = SWAP ? static_cast<int64_t>(cur.q_tile) * BN
+                                  : static_cast<int64_t>(cur.p_tile) * 128;
+          int64_t n_as = a.ld_as - m0;                 // stay inside the As allocation
+          if (n_as > C::kAsFloats) n_as = C::kAsFloats;
+          const uint32_t as_bytes = static_cast<uint32_t>(n_as) * 4u;
+          mbar_arrive_expect_tx(bar_sfull(ss), as_bytes + 16u * C::kBsChunks);
+          bulk_load(slot, a.As + kb * a.ld_as + m0, as_bytes, bar_sfull(ss));
+#pragma unroll
+          for (int h = 0; h < C::kBsChunks; ++h) {
+            int64_t nb = SWAP ? static_cast<int64_t>(cur.p_tile)
+                              : static_cast<int64_t>(cur.q_tile) * (BN / 128) + h;
+            if (nb >= a.NT) nb = a.NT - 1;             // block past N: any in-bounds value
+            const int64_t e = nb * s.G + kb;
+            bulk_load(slot + 4u * (C::kAsFloats + 4 * h), a.Bs + (e & ~int64_t{3}), 16u,
+                      bar_sfull(ss));
+          }
+          if (++ss == C::kSR) { ss = 0; sph ^= 1u; }
+        }
         if (!mbar_wait_bounded(bar_empty(st), ph ^ 1u, a.wait_limit)) {
           report_failure(a.err, kDevTimeoutProducer);
           break;
@@ -265,6 +320,16 @@ __global__ void __launch_bounds__(GemmCfg<BN, SWAP>::kThreads, 1)
         if (!mbar_wait_bounded(bar_full(j % C::kStages), (j / C::kStages) & 1u, a.wait_limit)) {
           report_failure(a.err, kDevTimeoutTail);
           break;
+        }
+      }
+      {
+        const uint32_t stail = issued < static_cast<uint32_t>(C::kSR) ? issued : C::kSR;
+        for (uint32_t t = 0; t < stail; ++t) {
+          const uint32_t j = issued - 1 - t;
+          if (!mbar_wait_bounded(bar_sfull(j % C::kSR), (j / C::kSR) & 1u, a.wait_limit)) {
+            report_failure(a.err, kDevTimeoutTail);
+            break;
+          }
         }
       }
     } else if (warp == C::kNE + 1 && lane == 0) {
@@ -321,71 +386,42 @@ __global__ void __launch_bounds__(GemmCfg<BN, SWAP>::kThreads, 1)
     const int r = quad * 32 + lane;          // TMEM lane = row of the P tile
     const int col0 = half * C::kCPT;         // first TMEM column of this thread
     const int etid = threadIdx.x;            // 0 .. NE*32-1
-    float* sScale = reinterpret_cast<float*>(smem + C::kOffScale);
-    const uint32_t sScale_addr = smem_addr(sScale);
-
-    // Stages the scales unit `u` needs into this warp's slot of the ring (one
-    // cp.async group per unit, empty past the end so the group count stays
-    // uniform).  Each warp stages what its own lanes read, so a __syncwarp is
-    // the only synchronisation.
-    auto stage_scales = [&](const Cursor& u) {
-      if (u.valid()) {
-        const int slot = u.j % C::kR;
-        const uint32_t base = sScale_addr + 4u * ((slot * C::kNE + warp) * C::kScaleStride);
-        const int64_t kb = u.kb;
-        if (!SWAP) {
-          const int64_t m = static_cast<int64_t>(u.p_tile) * 128 + r;
-          const bool ok = m < a.M;
-          const float* src =
-              ok ? a.As + (a.as_col_major ? kb * a.ld_as + m : m * a.ld_as + kb) : a.As;
-          cp_async_4(base + 4u * lane, src, ok ? 4u : 0u);
-          if (lane == 0) {
-            const int64_t nb = static_cast<int64_t>(u.q_tile) * (BN / 128) + half;
-            const bool okb = nb < a.NT;
-            cp_async_4(base + 4u * 32, okb ? a.Bs + nb * s.G + kb : a.Bs, okb ? 4u : 0u);
-          }
-        } else {
-#pragma unroll
-          for (int c = lane; c < C::kCPT; c += 32) {
-            const int64_t m = static_cast<int64_t>(u.q_tile) * BN + col0 + c;
-            const bool ok = m < a.M;
-            const float* src =
-                ok ? a.As + (a.as_col_major ? kb * a.ld_as + m : m * a.ld_as + kb) : a.As;
-            cp_async_4(base + 4u * c, src, ok ? 4u : 0u);
-          }
-          if (lane == 0)
-            cp_async_4(base + 4u * C::kCPT, a.Bs + static_cast<int64_t>(u.p_tile) * s.G + kb, 4u);
-        }
-      }
-      cp_async_commit();
-    };
-
+    const float* sRing = reinterpret_cast<const float*>(smem + C::kOffScale);
+    int ss = 0;
+    uint32_t sph = 0;
+    // fp32 accumulators, one per column of this thread's TMEM lane
+    constexpr int kP = C::kCPT / 2;          // column pairs
     float acc[C::kCPT];
 #pragma unroll
     for (int i = 0; i < C::kCPT; ++i) acc[i] = 0.f;
 
-    Cursor cur, ahead;
+    Cursor cur;
     cur.init(s, cta);
-    ahead = cur;
-#pragma unroll
-    for (int d = 0; d < C::kD; ++d) {
-      stage_scales(ahead);
-      ahead.next();
-    }
 
     unsigned long long t_ewait = 0, t_ework = 0, t_escale = 0, t_efix = 0;
     (void)t_ewait; (void)t_ework; (void)t_escale; (void)t_efix;
     for (; cur.valid(); cur.next()) {
       BFP8_CLK(e0);
-      stage_scales(ahead);
-      ahead.next();
-      cp_async_wait<C::kD>();
-      __syncwarp();
+      const uint32_t j = cur.j;
+      if (!mbar_wait_bounded(bar_sfull(ss), sph, a.wait_limit)) {
+        report_failure(a.err, kDevTimeoutEpilogue);
+        break;
+      }
+      const float* slot = sRing + ss * C::kSlotFloats;
+      float sr;                 // row scale (wide: As * Bs; swap: Bs)
+      if (!SWAP) {
+        const uint32_t hb = col0 / 128;         // this thread's 128-column weight block
+        const uint32_t nb = cur.q_tile * (BN / 128) + hb;
+        const float bsv = nb < static_cast<uint32_t>(a.NT)
+                              ? slot[C::kAsFloats + 4 * hb + ((nb * s.G + cur.kb) & 3)]
+                              : 0.f;
+        sr = slot[r] * bsv;
+      } else {
+        sr = slot[C::kAsFloats + ((cur.p_tile * s.G + cur.kb) & 3)];
+      }
+      const float* sq = slot + col0;          // column scales (swap)
       BFP8_ACC(t_escale, e0);
       BFP8_CLK(e1);
-
-      const uint32_t j = cur.j;
-      const float* sc_slot = sScale + ((j % C::kR) * C::kNE + warp) * C::kScaleStride;
       const int b = j & 1;
       if (!mbar_wait_bounded(bar_tfull(b), (j >> 1) & 1, a.wait_limit)) {
         report_failure(a.err, kDevTimeoutEpilogue);
@@ -403,8 +439,6 @@ __global__ void __launch_bounds__(GemmCfg<BN, SWAP>::kThreads, 1)
       }
       const uint32_t taddr = tmem + static_cast<uint32_t>(b * BN + col0) +
                              (static_cast<uint32_t>(quad * 32) << 16);
-      // scale of element (row r, column c): sr * column scale (swap) or sr
-      const float sr = SWAP ? sc_slot[C::kCPT] : sc_slot[lane] * sc_slot[32];
 #pragma unroll
       for (int c0 = 0; c0 < C::kCPT; c0 += C::kBatch) {
         uint32_t v[C::kBatch];
@@ -412,9 +446,10 @@ __global__ void __launch_bounds__(GemmCfg<BN, SWAP>::kThreads, 1)
         for (int h = 0; h < C::kBatch; h += C::kCH) tmem_ld_cols<C::kCH>(taddr + c0 + h, v + h);
         tmem_wait_ld();
         reg_fence<C::kBatch>(v);
+        // element (row r, column c) gets scale sr (wide) or sr * As[c] (swap)
 #pragma unroll
         for (int i = 0; i < C::kBatch; ++i) {
-          const float sc = SWAP ? sr * sc_slot[c0 + i] : sr;
+          const float sc = SWAP ? sr * sq[c0 + i] : sr;
           acc[c0 + i] = fmaf(__uint_as_float(v[i]), sc, acc[c0 + i]);
         }
       }
@@ -422,7 +457,11 @@ __global__ void __launch_bounds__(GemmCfg<BN, SWAP>::kThreads, 1)
       // the release, then one lane per warp arrives
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar_tempty(b));
+      if (lane == 0) {
+        mbar_arrive(bar_tempty(b));
+        mbar_arrive(bar_sempty(ss));
+      }
+      if (++ss == C::kSR) { ss = 0; sph ^= 1u; }
       BFP8_ACC(t_ework, e2);
 
       if (!cur.last()) continue;
@@ -436,10 +475,17 @@ __global__ void __launch_bounds__(GemmCfg<BN, SWAP>::kThreads, 1)
         pl = sk_last_cta(s, ts);
       }
       if (pl > pf) {
-        // stream-K fixup: publish this CTA's partial, the last arrival adds all
-        float* mine = a.partials + static_cast<size_t>(cta * 2 + sk_slot(s, cta, ts)) * (128 * BN);
+        // stream-K fixup: publish this CTA's partial, the last arrival adds all.
+        // Partial layout: column pairs interleaved, pair k of row r at
+        // [(k * 128 + r) * 2, +2), so each lane moves 8 contiguous bytes.
+        auto part = [&](uint32_t pp) {
+          return reinterpret_cast<float2*>(
+                     a.partials + static_cast<size_t>(pp * 2 + sk_slot(s, pp, ts)) * (128 * BN)) +
+                 (col0 / 2) * 128 + r;
+        };
+        float2* mine = part(cta);
 #pragma unroll
-        for (int c = 0; c < C::kCPT; ++c) mine[(col0 + c) * 128 + r] = acc[c];
+        for (int k = 0; k < kP; ++k) mine[k * 128] = make_float2(acc[2 * k], acc[2 * k + 1]);
         __threadfence();
         named_bar_sync(1, C::kNE * 32);
         if (etid == 0) {
@@ -453,37 +499,31 @@ __global__ void __launch_bounds__(GemmCfg<BN, SWAP>::kThreads, 1)
           continue;
         }
         __threadfence();
-        // Sum the contributors in ascending K order.  Loads are issued in
-        // batches of kFixBatch contributors x kFixCols columns so that one L2
-        // round trip serves a whole batch.
-        constexpr int kFixBatch = 4;
-        constexpr int kFixCols = 16;
-        const float* part0 =
-            a.partials + static_cast<size_t>(pf * 2 + sk_slot(s, pf, ts)) * (128 * BN);
+        // Sum the contributors in ascending K order; each contributor's pairs
+        // are loaded in chunks of kFixPairs so one L2 round trip serves many.
+        constexpr int kFixPairs = C::kNH >= 2 ? 16 : (kP >= 32 ? 32 : kP);
+        {
+          const float2* p0 = part(pf);
 #pragma unroll
-        for (int c = 0; c < C::kCPT; ++c) acc[c] = __ldcg(part0 + (col0 + c) * 128 + r);
-#pragma unroll 1
-        for (uint32_t pb = pf + 1; pb <= pl; pb += kFixBatch) {
-          const float* parts[kFixBatch];
-#pragma unroll
-          for (int i = 0; i < kFixBatch; ++i) {
-            const uint32_t pp = pb + i <= pl ? pb + i : pl;
-            parts[i] = a.partials + static_cast<size_t>(pp * 2 + sk_slot(s, pp, ts)) * (128 * BN);
+          for (int k = 0; k < kP; ++k) {
+            const float2 t = __ldcg(p0 + k * 128);
+            acc[2 * k] = t.x;
+            acc[2 * k + 1] = t.y;
           }
+        }
+#pragma unroll 1
+        for (uint32_t pp = pf + 1; pp <= pl; ++pp) {
+          const float2* pq = part(pp);
 #pragma unroll
-          for (int c0 = 0; c0 < C::kCPT; c0 += kFixCols) {
-            float t[kFixBatch][kFixCols];
+          for (int k0 = 0; k0 < kP; k0 += kFixPairs) {
+            float2 t[kFixPairs];
 #pragma unroll
-            for (int i = 0; i < kFixBatch; ++i)
+            for (int k = 0; k < kFixPairs; ++k) t[k] = __ldcg(pq + (k0 + k) * 128);
 #pragma unroll
-              for (int c = 0; c < kFixCols; ++c)
-                t[i][c] = (pb + i <= pl) ? __ldcg(parts[i] + (col0 + c0 + c) * 128 + r) : 0.f;
-#pragma unroll
-            for (int i = 0; i < kFixBatch; ++i)
-              if (pb + i <= pl) {
-#pragma unroll
-                for (int c = 0; c < kFixCols; ++c) acc[c0 + c] += t[i][c];
-              }
+            for (int k = 0; k < kFixPairs; ++k) {
+              acc[2 * (k0 + k)] += t[k].x;
+              acc[2 * (k0 + k) + 1] += t[k].y;
+            }
           }
         }
         if (etid == 0) a.counters[ts] = 0;  // every contributor has arrived
@@ -497,15 +537,14 @@ __global__ void __launch_bounds__(GemmCfg<BN, SWAP>::kThreads, 1)
 #pragma unroll
           for (int g = 0; g < C::kCPT / 8; ++g) {
             const int64_t n = nbase + g * 8;
+            const float* f = acc + g * 8;
             if (a.vec_store && n + 8 <= a.N) {
-              st_global_v4(row + n, pack_bf16x2(acc[g * 8 + 0], acc[g * 8 + 1]),
-                           pack_bf16x2(acc[g * 8 + 2], acc[g * 8 + 3]),
-                           pack_bf16x2(acc[g * 8 + 4], acc[g * 8 + 5]),
-                           pack_bf16x2(acc[g * 8 + 6], acc[g * 8 + 7]));
+              st_global_v4(row + n, pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]),
+                           pack_bf16x2(f[4], f[5]), pack_bf16x2(f[6], f[7]));
             } else {
 #pragma unroll
               for (int i = 0; i < 8; ++i)
-                if (n + i < a.N) row[n + i] = __float2bfloat16_rn(acc[g * 8 + i]);
+                if (n + i < a.N) row[n + i] = __float2bfloat16_rn(f[i]);
             }
           }
         }
@@ -522,7 +561,6 @@ __global__ void __launch_bounds__(GemmCfg<BN, SWAP>::kThreads, 1)
       }
       BFP8_ACC(t_efix, e3);
     }
-    cp_async_wait<0>();
     if (etid == 0) {
       trace_event(a.trace, cta, kTrEpiEnd);
       trace_value(a.trace, cta, kTrEpiWaitCyc, t_ewait);

@@ -50,7 +50,40 @@ __global__ void relayout_kernel(const uint8_t* __restrict__ src, int64_t rows, i
   }
 }
 
+// Scales in the layout the GEMM kernel bulk-copies: As column-major
+// [G][ld_out] (ld_out = M rounded up to 4; padding zero) and Bs contiguous
+// with four zero floats after it.
+__global__ void scale_relayout_kernel(const float* __restrict__ As, int32_t as_col_major,
+                                      int64_t ld_as, int64_t M, int64_t G, float* __restrict__ As_out,
+                                      int64_t ld_out, const float* __restrict__ Bs, int64_t nbs,
+                                      float* __restrict__ Bs_out) {
+  const int64_t n_as = As_out ? G * ld_out : 0;
+  const int64_t total = n_as + (Bs_out ? nbs + 4 : 0);
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    if (i < n_as) {
+      const int64_t kb = i / ld_out, m = i - kb * ld_out;
+      As_out[i] = m < M ? (as_col_major ? As[kb * ld_as + m] : As[m * ld_as + kb]) : 0.f;
+    } else {
+      const int64_t e = i - n_as;
+      Bs_out[e] = e < nbs ? Bs[e] : 0.f;
+    }
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_scale_relayout(const float* As, int as_col_major, int64_t ld_as, int64_t M,
+                                  int64_t G, float* As_out, int64_t ld_out, const float* Bs,
+                                  int64_t nbs, float* Bs_out, int num_sms, cudaStream_t stream) {
+  const int64_t total = (As_out ? G * ld_out : 0) + (Bs_out ? nbs + 4 : 0);
+  if (total == 0) return cudaSuccess;
+  int64_t blocks = (total + 255) / 256;
+  if (blocks > static_cast<int64_t>(num_sms) * 4) blocks = static_cast<int64_t>(num_sms) * 4;
+  scale_relayout_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
+      As, as_col_major, ld_as, M, G, As_out, ld_out, Bs, nbs, Bs_out);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_gemm_swap(int bn, const CUtensorMap& tmP, const CUtensorMap& tmQ,
                              const GemmArgs& a, cudaStream_t stream) {

@@ -40,4 +40,11 @@ size_t gemm_smem_bytes(bool swap, int bn);
 cudaError_t launch_relayout(const uint8_t* src, int64_t rows, int64_t K, uint8_t* dst, int64_t kp,
                             int num_sms, cudaStream_t stream);
 
+// Copies the scales into the layout the GEMM kernel reads: As column-major
+// [G][ld_out] with ld_out = M rounded up to 4 (when As_out != nullptr) and Bs
+// with four zero floats appended (when Bs_out != nullptr).
+cudaError_t launch_scale_relayout(const float* As, int as_col_major, int64_t ld_as, int64_t M,
+                                  int64_t G, float* As_out, int64_t ld_out, const float* Bs,
+                                  int64_t nbs, float* Bs_out, int num_sms, cudaStream_t stream);
+
 }  // namespace bfp8

@@ -119,14 +119,17 @@ typedef struct {
  *        caller-owned device scratch of at least the size bfp8_gemm_workspace_size
  *        reports for the same (M, N, K, options), 256-byte aligned.  It must be
  *        zero-filled once after allocation; every call that completes leaves it
- *        ready for the next (its counters return to zero).  Concurrent calls
- *        must not share a workspace.  After BFP8_ERR_DEVICE_TIMEOUT, zero it
- *        again.  A workspace of 0 bytes is valid when 0 is reported.
+ *        ready for the next (its counters return to zero), whatever the shapes
+ *        of later calls.  Concurrent calls must not share a workspace.  After
+ *        BFP8_ERR_DEVICE_TIMEOUT, zero it again.
  * Results are deterministic: the same inputs give bitwise the same output on
  * every call, whichever SM finishes first.
- * Requirements: M, N, K >= 1; A and B 16-byte aligned with K % 16 == 0 for the
- * direct path (otherwise the operands are first re-laid out into the
- * workspace, which the size query accounts for); As, Bs 4-byte aligned.
+ * Requirements: M, N, K >= 1; As, Bs 4-byte aligned.  Fast path: A and B
+ * 16-byte aligned with K % 16 == 0, As column-major with ld_as % 4 == 0 and
+ * 16-byte aligned, Bs 16-byte aligned with ceil(N/128) * G % 4 == 0 (what
+ * bfp8_group_quant and bfp8_scale_ld produce for column-major scales).  Other
+ * inputs are first re-laid out into the workspace by the library, in the
+ * same call, at the cost of one or two small extra kernels.
  */
 bfp8_status bfp8_gemm(const void* A, const void* B, const float* As, int as_col_major,
                       int64_t ld_as, const float* Bs, void* out, int64_t M, int64_t N, int64_t K,
@@ -140,9 +143,10 @@ bfp8_status bfp8_gemm_ex(const void* A, const void* B, const float* As, int as_c
                          const bfp8_gemm_options* opt, void* stream);
 
 /* Workspace bytes bfp8_gemm / bfp8_gemm_ex need for this problem on the
- * current device.  Writes *bytes; returns BFP8_ERR_UNSUPPORTED without a
- * suitable device. A, B alignment is not known here: the size assumes the
- * re-layout path when K % 16 != 0 or `operands_unaligned` is nonzero. */
+ * current device: a 16 KB counter header, the stream-K partial sums, room for
+ * re-laid-out scales and, when K % 16 != 0 or `operands_unaligned` is nonzero
+ * (A or B not 16-byte aligned), room for re-laid-out operands.  Writes
+ * *bytes; returns BFP8_ERR_UNSUPPORTED without a suitable device. */
 bfp8_status bfp8_gemm_workspace_size(int64_t M, int64_t N, int64_t K,
                                      const bfp8_gemm_options* opt, int operands_unaligned,
                                      size_t* bytes);
