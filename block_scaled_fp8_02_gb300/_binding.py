@@ -39,7 +39,7 @@ class BFP8Error(RuntimeError):
 
 class GemmOptions(ctypes.Structure):
     _fields_ = [("schedule", ctypes.c_int), ("max_ctas", ctypes.c_int), ("tile_n", ctypes.c_int),
-                ("reserved", ctypes.c_int * 5)]
+                ("prefetch_weights", ctypes.c_int), ("reserved", ctypes.c_int * 4)]
 
 
 class PlanInfo(ctypes.Structure):
@@ -124,6 +124,7 @@ def _opts(options) -> ctypes.POINTER(GemmOptions) | None:
     o.schedule = int(options.get("schedule", 0))
     o.max_ctas = int(options.get("max_ctas", 0))
     o.tile_n = int(options.get("tile_n", 0))
+    o.prefetch_weights = int(options.get("prefetch_weights", 0))
     return ctypes.pointer(o)
 
 
@@ -274,4 +275,6 @@ def linear(x: torch.Tensor, B: torch.Tensor, Bs: torch.Tensor, out: torch.Tensor
     """The whole W8A8 blocked linear layer: quantise x per 128-group (column-major
     scales) and run the blocked GEMM against e4m3 weights B with scales Bs."""
     q, s = bfp8_group_quant(x, col_major=True, stream=stream)
-    return bfp8_gemm(q, B, s, Bs, out=out, stream=stream)
+    # the quantisation kernel writes neither B nor Bs: the GEMM may start
+    # streaming the weights while it runs
+    return bfp8_gemm(q, B, s, Bs, out=out, options={"prefetch_weights": 1}, stream=stream)

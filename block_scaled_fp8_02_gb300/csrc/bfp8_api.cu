@@ -156,6 +156,9 @@ bfp8_status check_options(const bfp8_gemm_options* opt) {
   if (opt->max_ctas < 0) return fail(BFP8_ERR_INVALID_ARG, "options.max_ctas = %d", opt->max_ctas);
   if (opt->tile_n != 0 && opt->tile_n != 128 && opt->tile_n != 256)
     return fail(BFP8_ERR_INVALID_ARG, "options.tile_n = %d (expected 0, 128 or 256)", opt->tile_n);
+  if (opt->prefetch_weights != 0 && opt->prefetch_weights != 1)
+    return fail(BFP8_ERR_INVALID_ARG, "options.prefetch_weights = %d (expected 0 or 1)",
+                opt->prefetch_weights);
   return BFP8_OK;
 }
 
@@ -470,6 +473,8 @@ bfp8_status bfp8_gemm_ex(const void* A, const void* B, const float* As, int as_c
   a.counters = reinterpret_cast<int*>(ws ? ws + p.off_counters : nullptr);
   a.partials = reinterpret_cast<float*>(ws ? ws + p.off_partials : nullptr);
   a.vec_store = (!misaligned(out, 16) && (N % 8) == 0) ? 1 : 0;
+  // weight prefetch also needs the weight operand untouched by re-layout
+  a.prefetch_b = (opt && opt->prefetch_weights == 1 && !p.relayout && bs_ok) ? 1 : 0;
   a.err = d.err;
   a.wait_limit = kWaitLimitCycles;
   a.trace = nullptr;

@@ -64,6 +64,7 @@ struct GemmArgs {
   int* err;              // device failure word
   unsigned long long wait_limit;  // cycles before a wait gives up
   unsigned long long* trace;      // milestone timestamps (trace builds only)
+  int32_t prefetch_b;    // stream B tiles before the preceding grid completes
 };
 
 __host__ __device__ constexpr int tmem_cols_for(int n) {
@@ -242,6 +243,11 @@ __global__ void __launch_bounds__(GemmCfg<BN, SWAP>::kThreads, 1)
   // MMA and promotion warps through named barrier 2 (producer not included).
   __syncthreads();
   if (threadIdx.x == 0) trace_event(a.trace, cta, kTrStart);
+  // Everything above overlaps the tail of the preceding kernel in the stream
+  // (programmatic dependent launch).  Global memory that kernel may have
+  // written (A, As, the workspace; B and Bs unless prefetch_b) is touched only
+  // after this wait; the producer waits inside its loop instead.
+  if (warp != C::kNE) griddep_wait();
   constexpr uint32_t kTmemSyncThreads = (C::kNE + 1) * 32;
   uint32_t tmem = 0;
   if (warp == C::kNE + 1) {
@@ -271,6 +277,22 @@ __global__ void __launch_bounds__(GemmCfg<BN, SWAP>::kThreads, 1)
       int ss = 0;
       uint32_t sph = 0;
       const uint32_t sring = smem_addr(smem + C::kOffScale);
+      // With prefetch_b, the weight tiles of the first stages are requested
+      // before waiting for the preceding grid; their stages are then completed
+      // with the activation tiles below.
+      uint32_t pre = 0;
+      if (a.prefetch_b) {
+        Cursor pc = cur;
+        for (; pre < static_cast<uint32_t>(C::kStages) && pc.valid(); ++pre, pc.next()) {
+          mbar_arrive_expect_tx(bar_full(pre), C::kStageBytes);
+          const int32_t x = static_cast<int32_t>(pc.kb * 128);
+          if (SWAP)
+            tma_load_2d(stage_p(pre), &tmP, bar_full(pre), x, static_cast<int32_t>(pc.p_tile * 128));
+          else
+            tma_load_2d(stage_q(pre), &tmQ, bar_full(pre), x, static_cast<int32_t>(pc.q_tile * BN));
+        }
+      }
+      griddep_wait();
       for (; cur.valid(); cur.next()) {
         BFP8_CLK(c0);
         {
@@ -303,10 +325,18 @@ __global__ void __launch_bounds__(GemmCfg<BN, SWAP>::kThreads, 1)
           break;
         }
         BFP8_ACC(t_wait, c0);
-        mbar_arrive_expect_tx(bar_full(st), C::kStageBytes);
         const int32_t x = static_cast<int32_t>(cur.kb * 128);
-        tma_load_2d(stage_p(st), &tmP, bar_full(st), x, static_cast<int32_t>(cur.p_tile * 128));
-        tma_load_2d(stage_q(st), &tmQ, bar_full(st), x, static_cast<int32_t>(cur.q_tile * BN));
+        if (issued < pre) {
+          // weight tile already requested: add the activation tile
+          if (SWAP)
+            tma_load_2d(stage_q(st), &tmQ, bar_full(st), x, static_cast<int32_t>(cur.q_tile * BN));
+          else
+            tma_load_2d(stage_p(st), &tmP, bar_full(st), x, static_cast<int32_t>(cur.p_tile * 128));
+        } else {
+          mbar_arrive_expect_tx(bar_full(st), C::kStageBytes);
+          tma_load_2d(stage_p(st), &tmP, bar_full(st), x, static_cast<int32_t>(cur.p_tile * 128));
+          tma_load_2d(stage_q(st), &tmQ, bar_full(st), x, static_cast<int32_t>(cur.q_tile * BN));
+        }
         if (issued == 0) trace_event(a.trace, cta, kTrProdFirst);
         ++issued;
         if (++st == C::kStages) { st = 0; ph ^= 1u; }

@@ -27,8 +27,19 @@ cudaError_t launch_one(const CUtensorMap& tmP, const CUtensorMap& tmQ, const Gem
     if (e != cudaSuccess) return e;
     configured.fetch_or(bit, std::memory_order_acq_rel);
   }
-  gemm_kernel<BN, SWAP><<<a.sched.grid, C::kThreads, C::kSmemBytes, stream>>>(tmP, tmQ, a);
-  return cudaGetLastError();
+  // programmatic dependent launch: the prologue may overlap the preceding
+  // kernel; the kernel waits for it (griddepcontrol.wait) before reading inputs
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(a.sched.grid);
+  cfg.blockDim = dim3(C::kThreads);
+  cfg.dynamicSmemBytes = C::kSmemBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, gemm_kernel<BN, SWAP>, tmP, tmQ, a);
 }
 
 }  // namespace

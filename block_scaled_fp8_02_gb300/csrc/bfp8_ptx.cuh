@@ -251,6 +251,18 @@ __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
+// ------------------------------------------ programmatic dependent launch ---
+
+// Waits until the grids this grid depends on (launched before it in the stream)
+// have completed and their memory is visible.  A no-op without PDL.
+__device__ __forceinline__ void griddep_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+// Lets the next grid in the stream (if launched with PDL) begin launching.
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // -------------------------------------------------------- named barrier ---
 
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {

@@ -22,6 +22,7 @@
 #include <cstdint>
 
 #include "bfp8_internal.h"
+#include "bfp8_ptx.cuh"
 
 namespace bfp8 {
 
@@ -86,6 +87,11 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32, 4)
   const int li = lane % LPG;       // lane within the group
   const uint32_t warp0 = blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
   const uint32_t nwarps = gridDim.x * kWarpsPerBlock;
+  // x may come from the kernel before this one; once it is visible, the next
+  // kernel (the GEMM, which waits for this grid before reading q and s) may
+  // start its prologue
+  griddep_wait();
+  griddep_launch_dependents();
 
   for (uint32_t base = warp0; base < total; base += nwarps * kUnroll) {
     float v[kUnroll][EPL];
@@ -163,14 +169,21 @@ cudaError_t launch_group_quant(const void* x, int in_f32, int64_t M, int64_t K, 
   const int64_t cap = static_cast<int64_t>(num_sms) * 8;
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
-  const dim3 grid(static_cast<unsigned>(blocks)), block(kWarpsPerBlock * 32);
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(static_cast<unsigned>(blocks));
+  cfg.blockDim = dim3(kWarpsPerBlock * 32);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const int32_t cm = col_major;
   if (in_f32)
-    group_quant_kernel<true><<<grid, block, 0, stream>>>(x, M, K, ld_x, q, ld_q, s, col_major, ld_s,
-                                                          vec_x, vec_q);
-  else
-    group_quant_kernel<false><<<grid, block, 0, stream>>>(x, M, K, ld_x, q, ld_q, s, col_major, ld_s,
-                                                           vec_x, vec_q);
-  return cudaGetLastError();
+    return cudaLaunchKernelEx(&cfg, group_quant_kernel<true>, x, M, K, ld_x, q, ld_q, s, cm, ld_s,
+                              vec_x, vec_q);
+  return cudaLaunchKernelEx(&cfg, group_quant_kernel<false>, x, M, K, ld_x, q, ld_q, s, cm, ld_s,
+                            vec_x, vec_q);
 }
 
 }  // namespace bfp8

@@ -97,7 +97,12 @@ typedef struct {
   int schedule;        /* bfp8_schedule */
   int max_ctas;        /* cap on persistent CTAs; 0 = one per SM */
   int tile_n;          /* BFP8_SCHEDULE_WIDE only: 128 or 256 (0 = 256) */
-  int reserved[5];
+  int prefetch_weights;/* 1: the GEMM may start streaming B and Bs before the
+                          kernel launched just before it on the stream has
+                          finished (programmatic dependent launch).  Only valid
+                          when that kernel does not write B or Bs, e.g. when it
+                          is the bfp8_group_quant of this layer's activations. */
+  int reserved[4];
 } bfp8_gemm_options;
 
 /*

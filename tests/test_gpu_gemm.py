@@ -167,3 +167,24 @@ def test_one_workspace_serves_problems_of_every_layout(oracle_mod, dev):
         rows = None if M <= 128 else sample_rows(M, 16, seed=M)
         ref = oracle_mod.blocked_gemm(A, B, As, True, Bs, rows=rows, want_abs=True)
         check_gemm(out, ref, (K + 127) // 128, rows=rows, label=f"shared ws {M}x{N}x{K}")
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 4096, 4096), (64, 4096, 4096), (300, 1024, 2048),
+                                   (2048, 4096, 4096), (83, 576, 7168)])
+def test_weight_prefetch_right_after_quantisation(oracle_mod, dev, M, N, K):
+    """prefetch_weights=1: the GEMM requests weight tiles before the
+    quantisation kernel launched just before it has finished (programmatic
+    dependent launch), then waits for it before reading the activations."""
+    case = wl.linear_case(M, N, K, seed=M + 17)
+    x = case["x"].to(dev)
+    B = case["B"].to(dev)
+    Bs = case["Bs"].to(dev)
+    for _ in range(3):
+        q, s = bf.bfp8_group_quant(x)
+        out = bf.bfp8_gemm(q, B, s, Bs, options={"prefetch_weights": 1})
+    torch.cuda.synchronize()
+    A, As = oracle_mod.group_quant(case["x"].view(torch.int16).numpy().view(np.uint16), False, True)
+    rows = None if M <= 128 else sample_rows(M, 16, seed=M)
+    ref = oracle_mod.blocked_gemm(A, case["B"].view(torch.uint8).numpy(), As, True,
+                                  case["Bs"].numpy(), rows=rows, want_abs=True)
+    check_gemm(out, ref, (K + 127) // 128, rows=rows, label=f"prefetch {M}x{N}x{K}")
