@@ -5,7 +5,10 @@
 // source snippet"):
 //   amax  = max |x[m, k]| over the group's real elements
 //   scale = max(amax, 1e-10) / 448           (one IEEE fp32 division)
-//   q     = e4m3_rn_satfinite(x / scale)     (one IEEE fp32 division each)
+//   q     = e4m3_rn_satfinite(x / scale)     (x / scale as one IEEE fp32 division;
+//                                             computed as x * (1/scale) except
+//                                             near e4m3 rounding boundaries,
+//                                             which gives the same codes)
 // and the scale is stored row-major s[m * ld_s + g] or column-major
 // s[g * ld_s + m] (the layout the GEMM kernels read; lmdeploy PR 4830 pads its
 // stride to 16 bytes for TMA, transformers' _coerce_sf_for_kernel calls it
@@ -34,6 +37,22 @@ struct QuantShape {
   static constexpr int kLPG = 128 / kEPL;       // lanes per group
   static constexpr int kGPW = 32 / kLPG;        // groups per warp step
 };
+
+// fl32(x / scale) as far as its e4m3 code is concerned.  y = x * rcp, with
+// rcp = 1/scale rounded to nearest, differs from x / scale by at most 2 ulp
+// and from its correctly rounded value by at most 2.5 ulp.  The e4m3 code of
+// a value with |y| >= 2^-6 only changes at the midpoints between e4m3 values,
+// fp32 numbers whose low 20 mantissa bits are exactly 0x80000; so unless y is
+// within 3 ulp of such a midpoint (or in the e4m3 subnormal range, where the
+// spacing is fixed) both round to the same code, and the IEEE division is
+// only needed for those rare cases.
+__device__ __forceinline__ float quotient_for_e4m3(float x, float scale, float rcp) {
+  const float y = __fmul_rn(x, rcp);
+  const uint32_t b = __float_as_uint(y) & 0x7FFFFFFFu;
+  const bool tiny = b < 0x3C800000u;                            // |y| < 2^-6
+  const bool near_mid = ((b - 0x80000u + 3u) & 0xFFFFFu) <= 6u;  // within 3 ulp of a midpoint
+  return (tiny || near_mid) ? __fdiv_rn(x, scale) : y;
+}
 
 __device__ __forceinline__ uint16_t cvt_e4m3x2(float lo, float hi) {
   uint16_t r;
@@ -123,10 +142,12 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32, 4)
         amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
       if (!valid[u]) continue;
       const float scale = __fdiv_rn(fmaxf(amax, 1e-10f), 448.0f);
+      const float rcp = __frcp_rn(scale);
       uint16_t pk[EPL / 2];
 #pragma unroll
       for (int e = 0; e < EPL; e += 2)
-        pk[e / 2] = cvt_e4m3x2(__fdiv_rn(v[u][e], scale), __fdiv_rn(v[u][e + 1], scale));
+        pk[e / 2] = cvt_e4m3x2(quotient_for_e4m3(v[u][e], scale, rcp),
+                               quotient_for_e4m3(v[u][e + 1], scale, rcp));
       uint8_t* qrow = q + row[u] * ld_q;
       if (vec_q && k[u] + EPL <= K) {
         if constexpr (kF32) {

@@ -81,3 +81,36 @@ def test_quant_special_groups(oracle_mod, dev):
     x[2, 300] = 3.0e-8
     _check(oracle_mod, dev, x, True)
     _check(oracle_mod, dev, x.to(torch.bfloat16), False)
+
+
+def test_quotients_next_to_e4m3_rounding_boundaries(oracle_mod, dev):
+    """Elements placed so that x / scale falls within a few fp32 ulps of the
+    midpoints between e4m3 values (and in the e4m3 subnormal range), where a
+    quotient that is not correctly rounded would change the code."""
+    rng = np.random.default_rng(7)
+    tab = oracle_mod.e4m3_table()
+    mags = np.sort(np.unique(np.abs(tab[np.isfinite(tab)])))
+    mids = (mags[:-1] + mags[1:]) / 2                       # every rounding boundary
+    rows = []
+    for amax in rng.uniform(0.5, 50.0, size=24).astype(np.float32):
+        scale = np.float32(amax) / np.float32(448.0)          # the group's scale
+        vals = []
+        for mid in mids:
+            base = np.float32(mid * np.float64(scale))
+            for k in (-3, -2, -1, 0, 1, 2, 3):
+                v = base
+                step = np.float32(np.inf) if k > 0 else np.float32(-np.inf)
+                for _ in range(abs(k)):
+                    v = np.nextafter(v, step)
+                vals.append(v if rng.random() < 0.5 else -v)
+        vals = np.array(vals, dtype=np.float32)
+        vals = vals[np.abs(vals) < amax]
+        for i in range(0, vals.size, 127):
+            row = np.zeros(128, dtype=np.float32)
+            chunk = vals[i:i + 127]
+            row[:chunk.size] = chunk
+            row[127] = amax                                   # fixes the group's scale
+            rows.append(row)
+    x = torch.from_numpy(np.stack(rows))
+    _check(oracle_mod, dev, x, True)
+    _check(oracle_mod, dev, x, False)
