@@ -262,6 +262,7 @@ def run_ours(args, rank, world, local):
     B0 = base["B"].to(dev)
     Bs0 = base["Bs"].to(dev)
     bufs = []
+    gemm_opts = {"prefetch_weights": 1}   # each GEMM follows its own quantisation kernel
     for M in Ms:
         x = wl.activations(M, K, seed=1000 + M + 7919 * rank).to(dev)
         ld = bf.bfp8_scale_ld(M)
@@ -272,9 +273,7 @@ def run_ours(args, rank, world, local):
             q=torch.empty((M, K), dtype=torch.float8_e4m3fn, device=dev), s_st=s_st,
             s=s_st[:, :M].t(), out=torch.empty((M, N), dtype=torch.bfloat16, device=dev),
             ws=torch.zeros(max(wsb, 256), dtype=torch.uint8, device=dev),
-            plan=bf.bfp8_gemm_plan(M, N, K, torch.cuda.get_device_properties(dev).multi_processor_count)))
-
-    gemm_opts = {"prefetch_weights": 1}   # each GEMM follows its own quantisation kernel
+            plan=bf.bfp8_gemm_plan(M, N, K, 0, gemm_opts)))
 
     def step(events=None):
         if events is not None:
@@ -398,7 +397,9 @@ def run_ours(args, rank, world, local):
             "gemm_roofline_frac": round(roof / pg, 3),
             "quant_p50_us": round(pq, 3),
             "quant_gbs": round(mt.quant_bytes(M, K) / (pq * 1e-6) / 1e9, 1),
-            "schedule": ("swap_ab" if b["plan"]["swap_ab"] else "wide") + f"/n{b['plan']['tile_n']}",
+            "schedule": ("swap_ab" if b["plan"]["swap_ab"] else "wide") + f"/n{b['plan']['tile_n']}"
+                        + (f"/cluster{b['plan']['cluster']}" if b["plan"]["cluster"] > 1
+                           else ("/stream-k" if b["plan"]["sk_units"] else "")),
         }
         gname = "gemm_swap_ab" if b["plan"]["swap_ab"] else "gemm_wide"
         for name, ds, fl, by in (("quant", dq, 0.0, mt.quant_bytes(M, K)),

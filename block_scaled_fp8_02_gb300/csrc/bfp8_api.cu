@@ -5,6 +5,7 @@
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
+#include <cmath>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
@@ -53,10 +54,14 @@ bfp8_status set_last_error(bfp8_status st, const char* msg) {
 
 namespace {
 
+constexpr int kMaxCluster = 8;   // portable cluster size
+
 struct DevInfo {
   bool ready = false;
   int cc_major = 0, cc_minor = 0, sms = 0;
   int* err = nullptr;
+  bool caps_ready = false;
+  int cluster_cap[kMaxCluster + 1] = {};   // co-resident GEMM clusters of each size
 };
 DevInfo g_dev[kMaxDevices];
 std::mutex g_dev_mu;
@@ -95,6 +100,29 @@ bfp8_status current_device(DevInfo* out, int* dev_out) {
                 d.cc_major, d.cc_minor);
   *out = d;
   if (dev_out) *dev_out = dev;
+  return BFP8_OK;
+}
+
+// current_device plus the device's GEMM cluster capacities (asked once).
+bfp8_status current_device_with_caps(DevInfo* out) {
+  int dev = 0;
+  bfp8_status st = current_device(out, &dev);
+  if (st != BFP8_OK) return st;
+  if (out->caps_ready) return BFP8_OK;
+  int cap[kMaxCluster + 1] = {};
+  cap[0] = cap[1] = out->sms;
+  for (int cs = 2; cs <= kMaxCluster; ++cs) {
+    const cudaError_t e = gemm_cluster_capacity(cs, &cap[cs]);
+    if (e != cudaSuccess) {
+      cudaGetLastError();
+      return fail(BFP8_ERR_CUDA, "cluster occupancy query (size %d): %s", cs, cudaGetErrorString(e));
+    }
+  }
+  std::lock_guard<std::mutex> lk(g_dev_mu);
+  DevInfo& d = g_dev[dev];
+  std::memcpy(d.cluster_cap, cap, sizeof(cap));
+  d.caps_ready = true;
+  *out = d;
   return BFP8_OK;
 }
 
@@ -159,7 +187,68 @@ bfp8_status check_options(const bfp8_gemm_options* opt) {
   if (opt->prefetch_weights != 0 && opt->prefetch_weights != 1)
     return fail(BFP8_ERR_INVALID_ARG, "options.prefetch_weights = %d (expected 0 or 1)",
                 opt->prefetch_weights);
+  if (opt->k_split < 0 || opt->k_split > 2)
+    return fail(BFP8_ERR_INVALID_ARG, "options.k_split = %d (expected 0, 1 or 2)", opt->k_split);
+  if (opt->cluster_size != 0 && (opt->cluster_size < 2 || opt->cluster_size > kMaxCluster))
+    return fail(BFP8_ERR_INVALID_ARG, "options.cluster_size = %d (expected 0 or 2..8)",
+                opt->cluster_size);
   return BFP8_OK;
+}
+
+// Co-resident clusters of each size on a device with `sms` SMs when the
+// device itself cannot be asked (host-only planning): its GPCs are not all
+// alike, so a little less than sms / cs, and clearly less for 7 and 8.
+void estimate_cluster_caps(int sms, int* cap) {
+  for (int cs = 0; cs <= kMaxCluster; ++cs)
+    cap[cs] = cs < 2 ? sms : static_cast<int>(sms * (cs >= 7 ? 0.75 : 0.94) / cs);
+}
+
+// Relative time of the two ways of sharing K among CTAs, in units of one
+// (tile, k-block) step of one CTA.  Stream-K: the busiest CTA's steps plus
+// the fixup of a tile whose steps are spread over c CTAs, which reads the
+// c - 1 other partial tiles (128 x bn fp32 each) one after another from L2,
+// each costing about 1.5 steps of latency plus bn / 128 steps of transfer.
+// Cluster split-K of size cs: ceil(G / cs) steps per wave of co-resident
+// clusters, plus the reduction through distributed shared memory.
+double stream_k_cost(int64_t tiles, int64_t G, int bn, int64_t grid) {
+  const double per_cta = static_cast<double>(tiles * G) / static_cast<double>(grid);
+  const double ctas_per_tile = per_cta >= static_cast<double>(G) ? 1.0 : G / per_cta + 1.0;
+  return std::ceil(per_cta) + (ctas_per_tile - 1.0) * (1.5 + bn / 128.0);
+}
+double cluster_cost(int64_t tiles, int64_t G, int bn, int cs, int cap) {
+  const int64_t waves = cap > 0 ? (tiles + cap - 1) / cap : tiles;
+  return static_cast<double>(waves) *
+         (static_cast<double>((G + cs - 1) / cs) + 0.5 + 0.5 * bn / 128.0);
+}
+
+// CTAs per tile for cluster split-K, or 0 for the persistent stream-K
+// schedule.  Clusters are considered only when the tiles alone would leave
+// SMs idle, with tiles * cs <= max_ctas and cs <= G.  An explicit
+// cluster_size is taken as given (clamped to G); otherwise the size with the
+// lowest cost above, and under AUTO only when it beats stream-K.
+uint32_t choose_cluster(int64_t tiles, int64_t G, int bn, int64_t max_ctas,
+                        const bfp8_gemm_options* opt, const int* cap) {
+  const int ks = opt ? opt->k_split : BFP8_KSPLIT_AUTO;
+  if (ks == BFP8_KSPLIT_STREAM_K || tiles >= max_ctas || G < 2) return 0;
+  if (opt && opt->cluster_size > 0)
+    return static_cast<uint32_t>(opt->cluster_size < G ? opt->cluster_size : G);
+  int best = 0;
+  double best_cost = 0.0;
+  for (int cs = 2; cs <= kMaxCluster && cs <= G && tiles * cs <= max_ctas; ++cs) {
+    const double c = cluster_cost(tiles, G, bn, cs, cap[cs]);
+    if (best == 0 || c < best_cost) {
+      best = cs;
+      best_cost = c;
+    }
+  }
+  if (best == 0) return 0;
+  if (ks == BFP8_KSPLIT_AUTO && best_cost >= stream_k_cost(tiles, G, bn, max_ctas)) return 0;
+  return static_cast<uint32_t>(best);
+}
+
+// Stream-K tiles of a schedule (they each need a counter in the header).
+int64_t stream_k_tiles(const Sched& s) {
+  return s.cluster > 1 ? 0 : static_cast<int64_t>(s.tiles) - s.dp_tiles;
 }
 
 // Small M: the weights fill the 128-row MMA slot and the activation rows the
@@ -175,8 +264,9 @@ int swap_tile_n(int64_t M) {
 constexpr int64_t kSwapMaxM = 256;
 constexpr size_t kCounterHeaderBytes = 16384;   // 4096 stream-K tile counters
 
+// `cap` = co-resident clusters of each size (nullptr: estimated from num_sms).
 bfp8_status make_plan(int64_t M, int64_t N, int64_t K, int num_sms, const bfp8_gemm_options* opt,
-                      bool unaligned, Plan* p) {
+                      bool unaligned, const int* cap, Plan* p) {
   const int schedule = opt ? opt->schedule : BFP8_SCHEDULE_AUTO;
   p->swap = schedule == BFP8_SCHEDULE_SWAP_AB ||
             (schedule == BFP8_SCHEDULE_AUTO && M <= kSwapMaxM);
@@ -189,19 +279,27 @@ bfp8_status make_plan(int64_t M, int64_t N, int64_t K, int num_sms, const bfp8_g
                 (long long)(p_tiles * q_tiles), (long long)G);
   int max_ctas = num_sms;
   if (opt && opt->max_ctas > 0 && opt->max_ctas < max_ctas) max_ctas = opt->max_ctas;
-  p->sched = make_sched(static_cast<uint32_t>(p_tiles), static_cast<uint32_t>(q_tiles),
-                        static_cast<uint32_t>(G), static_cast<uint32_t>(max_ctas));
+  int est[kMaxCluster + 1];
+  if (!cap) {
+    estimate_cluster_caps(num_sms, est);
+    cap = est;
+  }
+  const uint32_t cs = choose_cluster(p_tiles * q_tiles, G, p->bn, max_ctas, opt, cap);
+  if (cs > 1)
+    p->sched = make_sched_cluster(static_cast<uint32_t>(p_tiles), static_cast<uint32_t>(q_tiles),
+                                  static_cast<uint32_t>(G), cs);
+  else
+    p->sched = make_sched(static_cast<uint32_t>(p_tiles), static_cast<uint32_t>(q_tiles),
+                          static_cast<uint32_t>(G), static_cast<uint32_t>(max_ctas));
   p->relayout = unaligned || (K % 16) != 0;
   p->kp = p->relayout ? cdiv(K, 16) * 16 : K;
   size_t off = 0;
-  const int64_t sk_tiles = p->sched.tiles - p->sched.dp_tiles;
   // The counters live in a fixed-size header at the start of every workspace,
   // whatever the problem: a later call with a different shape must find zeros
   // there, never an earlier call's partial sums.  Stream-K covers fewer tiles
   // than the grid has CTAs (whole waves are handed out round-robin first).
   // It is always reserved, so that nothing but counters (which every
   // completed call returns to zero) is ever written there.
-  (void)sk_tiles;
   p->off_counters = off;
   off += kCounterHeaderBytes;
   p->off_partials = off;
@@ -330,11 +428,18 @@ bfp8_status bfp8_gemm_plan(int64_t M, int64_t N, int64_t K, int num_sms,
   bfp8_status st = check_gemm_sizes(M, N, K);
   if (st != BFP8_OK) return st;
   if ((st = check_options(opt)) != BFP8_OK) return st;
-  if (num_sms < 1) return fail(BFP8_ERR_INVALID_ARG, "num_sms = %d", num_sms);
+  if (num_sms < 0) return fail(BFP8_ERR_INVALID_ARG, "num_sms = %d", num_sms);
   if (!info) return fail(BFP8_ERR_INVALID_ARG, "info is null");
+  DevInfo d;
+  const int* cap = nullptr;
+  if (num_sms == 0) {
+    if ((st = current_device_with_caps(&d)) != BFP8_OK) return st;
+    num_sms = d.sms;
+    cap = d.cluster_cap;
+  }
   Plan p;
-  if ((st = make_plan(M, N, K, num_sms, opt, operands_unaligned != 0, &p)) != BFP8_OK) return st;
-  if (p.sched.tiles - p.sched.dp_tiles > static_cast<int64_t>(kCounterHeaderBytes / sizeof(int)))
+  if ((st = make_plan(M, N, K, num_sms, opt, operands_unaligned != 0, cap, &p)) != BFP8_OK) return st;
+  if (stream_k_tiles(p.sched) > static_cast<int64_t>(kCounterHeaderBytes / sizeof(int)))
     return fail(BFP8_ERR_UNSUPPORTED, "more stream-K tiles than the workspace header holds");
   info->swap_ab = p.swap;
   info->tile_n = p.bn;
@@ -346,6 +451,7 @@ bfp8_status bfp8_gemm_plan(int64_t M, int64_t N, int64_t K, int num_sms,
   info->sk_units = p.sched.sk_units;
   info->relayout = p.relayout;
   info->workspace_bytes = p.total;
+  info->cluster = p.sched.cluster > 1 ? static_cast<int>(p.sched.cluster) : 1;
   return ok();
 }
 
@@ -355,9 +461,16 @@ bfp8_status bfp8_plan_unit(int64_t M, int64_t N, int64_t K, int num_sms,
   bfp8_status st = check_gemm_sizes(M, N, K);
   if (st != BFP8_OK) return st;
   if ((st = check_options(opt)) != BFP8_OK) return st;
-  if (num_sms < 1) return fail(BFP8_ERR_INVALID_ARG, "num_sms = %d", num_sms);
+  if (num_sms < 0) return fail(BFP8_ERR_INVALID_ARG, "num_sms = %d", num_sms);
+  DevInfo d;
+  const int* cap = nullptr;
+  if (num_sms == 0) {
+    if ((st = current_device_with_caps(&d)) != BFP8_OK) return st;
+    num_sms = d.sms;
+    cap = d.cluster_cap;
+  }
   Plan p;
-  if ((st = make_plan(M, N, K, num_sms, opt, false, &p)) != BFP8_OK) return st;
+  if ((st = make_plan(M, N, K, num_sms, opt, false, cap, &p)) != BFP8_OK) return st;
   if (cta < 0 || static_cast<uint32_t>(cta) >= p.sched.grid)
     return fail(BFP8_ERR_INVALID_ARG, "cta %d out of range", cta);
   const int64_t n = num_units(p.sched, static_cast<uint32_t>(cta));
@@ -382,9 +495,10 @@ bfp8_status bfp8_gemm_workspace_size(int64_t M, int64_t N, int64_t K,
   if ((st = check_options(opt)) != BFP8_OK) return st;
   if (!bytes) return fail(BFP8_ERR_INVALID_ARG, "bytes is null");
   DevInfo d;
-  if ((st = current_device(&d, nullptr)) != BFP8_OK) return st;
+  if ((st = current_device_with_caps(&d)) != BFP8_OK) return st;
   Plan p;
-  if ((st = make_plan(M, N, K, d.sms, opt, operands_unaligned != 0, &p)) != BFP8_OK) return st;
+  if ((st = make_plan(M, N, K, d.sms, opt, operands_unaligned != 0, d.cluster_cap, &p)) != BFP8_OK)
+    return st;
   *bytes = p.total;
   return ok();
 }
@@ -409,11 +523,11 @@ bfp8_status bfp8_gemm_ex(const void* A, const void* B, const float* As, int as_c
     return fail(BFP8_ERR_ALIGNMENT, "As and Bs must be 4-byte aligned");
   if (misaligned(out, 2)) return fail(BFP8_ERR_ALIGNMENT, "out must be 2-byte aligned");
   DevInfo d;
-  if ((st = current_device(&d, nullptr)) != BFP8_OK) return st;
+  if ((st = current_device_with_caps(&d)) != BFP8_OK) return st;
   const bool unaligned = misaligned(A, 16) || misaligned(B, 16);
   Plan p;
-  if ((st = make_plan(M, N, K, d.sms, opt, unaligned, &p)) != BFP8_OK) return st;
-  if (p.sched.tiles - p.sched.dp_tiles > static_cast<int64_t>(kCounterHeaderBytes / sizeof(int)))
+  if ((st = make_plan(M, N, K, d.sms, opt, unaligned, d.cluster_cap, &p)) != BFP8_OK) return st;
+  if (stream_k_tiles(p.sched) > static_cast<int64_t>(kCounterHeaderBytes / sizeof(int)))
     return fail(BFP8_ERR_UNSUPPORTED, "more stream-K tiles than the workspace header holds");
   if (p.total > 0) {
     if (!workspace)

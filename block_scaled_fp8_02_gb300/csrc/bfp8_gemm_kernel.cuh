@@ -34,6 +34,7 @@
 #include <cuda.h>
 #include <cuda_bf16.h>
 
+#include <atomic>
 #include <cstdint>
 
 #include "bfp8_ptx.cuh"
@@ -125,7 +126,15 @@ struct GemmCfg {
   static constexpr int kOffFlags = kOffTmemPtr + 8;
   static constexpr int kOffScale = (kOffFlags + 8 + 15) / 16 * 16;
   static constexpr int kSmemBytes = kOffScale + kScaleBytes + 1024;
+  // one CTA per SM (the planner's cluster capacities assume it)
+  static_assert(2 * kSmemBytes > kSmemLimit + 1024, "two CTAs would fit on one SM");
   static constexpr int kTmemCols = tmem_cols_for(2 * BN);
+  // Cluster split-K: a CTA's partial tile goes into its (then idle) operand
+  // ring as [column][row] fp32 with a 132-float column pitch, so that the
+  // promotion warps write it without bank conflicts and 16-byte reads of
+  // neighbouring columns fall in different banks.
+  static constexpr int kPartPitch = 132;
+  static_assert(BN * kPartPitch * 4 <= kStages * kStageBytes, "partial tile does not fit the ring");
   static constexpr uint32_t kIdesc = idesc_e4m3_f32(128, BN);
 };
 
@@ -408,6 +417,12 @@ __global__ void __launch_bounds__(GemmCfg<BN, SWAP>::kThreads, 1)
       }
     }
     __syncwarp();
+    if (s.cluster > 1) {
+      // every thread of the cluster takes part in both cluster barriers of
+      // the split-K reduction (see the promotion warps)
+      cluster_sync();
+      cluster_sync();
+    }
   } else {
     // ---------------------------------------------- promotion and epilogue
     if constexpr (C::kRebalance) setmaxnreg_inc<C::kRegsEpi>();
@@ -496,6 +511,17 @@ __global__ void __launch_bounds__(GemmCfg<BN, SWAP>::kThreads, 1)
 
       if (!cur.last()) continue;
       BFP8_CLK(e3);
+
+      if (s.cluster > 1) {
+        // cluster split-K: park this CTA's partial tile in its own shared
+        // memory; the cluster adds the partials after the loop.  Every MMA
+        // has completed (tfull of the last unit), so the operand ring is idle.
+        float* part = reinterpret_cast<float*>(smem);
+#pragma unroll
+        for (int i = 0; i < C::kCPT; ++i) part[(col0 + i) * C::kPartPitch + r] = acc[i];
+        BFP8_ACC(t_efix, e3);
+        continue;
+      }
 
       // ---- the segment is complete: emit it
       const int32_t ts = cur.sk_tile();
@@ -591,6 +617,81 @@ __global__ void __launch_bounds__(GemmCfg<BN, SWAP>::kThreads, 1)
       }
       BFP8_ACC(t_efix, e3);
     }
+    if (s.cluster > 1) {
+      // ---- cluster split-K reduction.  After the first cluster barrier every
+      // CTA's partial is in its shared memory.  The output tile's valid part,
+      // cut into runs of 4 rows of one column, is divided evenly among the
+      // cluster's CTAs; each adds the cs partials of its runs in rank order
+      // (deterministic) through distributed shared memory and stores bf16.
+      // The second barrier keeps every CTA (and its shared memory) alive
+      // until all reads of it are done.
+      cluster_sync();
+      const uint32_t cs = s.cluster;
+      const uint32_t rank = cta % cs;            // 1-D clusters of consecutive CTAs
+      const uint32_t tile = cta / cs;
+      const uint32_t q_tile = tile / s.p_tiles;
+      const uint32_t p_tile = tile - q_tile * s.p_tiles;
+      const int64_t p0 = static_cast<int64_t>(p_tile) * 128;   // first row (TMEM lane)
+      const int64_t q0 = static_cast<int64_t>(q_tile) * BN;    // first column
+      const int64_t qlim = SWAP ? a.M : a.N;
+      const int64_t plim = SWAP ? a.N : a.M;
+      const uint32_t qv = static_cast<uint32_t>(qlim - q0 < BN ? qlim - q0 : BN);
+      const int64_t pv64 = plim - p0 < 128 ? plim - p0 : 128;
+      const uint32_t runs_per_col = static_cast<uint32_t>((pv64 + 3) / 4);
+      const uint32_t items = qv * runs_per_col;
+      const uint32_t beg = static_cast<uint32_t>((static_cast<uint64_t>(rank) * items) / cs);
+      const uint32_t end = static_cast<uint32_t>((static_cast<uint64_t>(rank + 1) * items) / cs);
+      const uint32_t part0 = smem_addr(smem);
+      for (uint32_t i = beg + etid; i < end; i += C::kNE * 32) {
+        // swap: lanes walk down a column (rows = output columns n, contiguous);
+        // wide: lanes walk across columns (output columns n) of one row run
+        uint32_t c, r4;
+        if (SWAP) {
+          c = i / runs_per_col;
+          r4 = (i - c * runs_per_col) * 4;
+        } else {
+          const uint32_t run = i / qv;
+          c = i - run * qv;
+          r4 = run * 4;
+        }
+        const uint32_t addr = part0 + 4u * (c * C::kPartPitch + r4);
+        float4 t[8];
+#pragma unroll
+        for (uint32_t q = 0; q < 8; ++q)
+          if (q < cs) t[q] = ld_dsmem_v4(mapa_shared(addr, q));
+        float4 v = t[0];
+#pragma unroll
+        for (uint32_t q = 1; q < 8; ++q) {
+          if (q < cs) {
+            v.x += t[q].x;
+            v.y += t[q].y;
+            v.z += t[q].z;
+            v.w += t[q].w;
+          }
+        }
+        const float f[4] = {v.x, v.y, v.z, v.w};
+        if (SWAP) {
+          const int64_t m = q0 + c;
+          const int64_t n = p0 + r4;
+          __nv_bfloat16* row = a.out + m * a.N;
+          if (a.vec_store && n + 4 <= a.N) {
+            st_global_v2(row + n, pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]));
+          } else {
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              if (n + e < a.N) row[n + e] = __float2bfloat16_rn(f[e]);
+          }
+        } else {
+          const int64_t n = q0 + c;
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int64_t m = p0 + r4 + e;
+            if (m < a.M) a.out[m * a.N + n] = __float2bfloat16_rn(f[e]);
+          }
+        }
+      }
+      cluster_sync();
+    }
     if (etid == 0) {
       trace_event(a.trace, cta, kTrEpiEnd);
       trace_value(a.trace, cta, kTrEpiWaitCyc, t_ewait);
@@ -605,6 +706,76 @@ __global__ void __launch_bounds__(GemmCfg<BN, SWAP>::kThreads, 1)
   tc_fence_after();
   if (warp == C::kNE + 1) tmem_dealloc(tmem, C::kTmemCols);
 #endif
+}
+
+// Host side.  The dynamic shared-memory opt-in is per device and set once (a
+// launch captured into a CUDA graph then needs no attribute call).
+template <int BN, bool SWAP>
+cudaError_t configure_instance() {
+  using C = GemmCfg<BN, SWAP>;
+  static std::atomic<uint64_t> configured{0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const uint64_t bit = 1ull << (dev & 63);
+  if (!(configured.load(std::memory_order_acquire) & bit)) {
+    e = cudaFuncSetAttribute(gemm_kernel<BN, SWAP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             C::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    configured.fetch_or(bit, std::memory_order_acq_rel);
+  }
+  return cudaSuccess;
+}
+
+// How many clusters of `cs` CTAs of this instantiation the current device
+// runs at once (the GPCs' sizes decide it, not just the SM count).
+template <int BN, bool SWAP>
+cudaError_t cluster_capacity_instance(int cs, int* clusters) {
+  using C = GemmCfg<BN, SWAP>;
+  cudaError_t e = configure_instance<BN, SWAP>();
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(cs);
+  cfg.blockDim = dim3(C::kThreads);
+  cfg.dynamicSmemBytes = C::kSmemBytes;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = cs;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaOccupancyMaxActiveClusters(clusters, gemm_kernel<BN, SWAP>, &cfg);
+}
+
+// Launches one instantiation with programmatic dependent launch (the
+// prologue may overlap the preceding kernel in the stream; the kernel waits
+// for it before reading its inputs) and, for cluster split-K, as 1-D
+// clusters of sched.cluster consecutive CTAs.
+template <int BN, bool SWAP>
+cudaError_t launch_instance(const CUtensorMap& tmP, const CUtensorMap& tmQ, const GemmArgs& a,
+                            cudaStream_t stream) {
+  using C = GemmCfg<BN, SWAP>;
+  cudaError_t e = configure_instance<BN, SWAP>();
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(a.sched.grid);
+  cfg.blockDim = dim3(C::kThreads);
+  cfg.dynamicSmemBytes = C::kSmemBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (a.sched.cluster > 1) {
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = a.sched.cluster;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.numAttrs = 2;
+  }
+  return cudaLaunchKernelEx(&cfg, gemm_kernel<BN, SWAP>, tmP, tmQ, a);
 }
 
 }  // namespace bfp8

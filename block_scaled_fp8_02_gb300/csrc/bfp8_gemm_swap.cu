@@ -1,46 +1,12 @@
 // bfp8_gemm_swap.cu -- swap-AB instantiations of the blocked FP8 GEMM (small
 // M: 128 weight rows fill the MMA M slot, BN >= M activation rows the N slot)
 // and the operand re-layout kernel for rows whose stride TMA cannot take.
-#include <atomic>
-
 #include "bfp8_gemm_kernel.cuh"
 #include "bfp8_internal.h"
 
 namespace bfp8 {
 
 namespace {
-
-template <int BN, bool SWAP>
-cudaError_t launch_one(const CUtensorMap& tmP, const CUtensorMap& tmQ, const GemmArgs& a,
-                       cudaStream_t stream) {
-  using C = GemmCfg<BN, SWAP>;
-  // The shared-memory opt-in is per device; set it once (a launch captured
-  // into a CUDA graph then needs no attribute call).
-  static std::atomic<uint64_t> configured{0};
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  const uint64_t bit = 1ull << (dev & 63);
-  if (!(configured.load(std::memory_order_acquire) & bit)) {
-    e = cudaFuncSetAttribute(gemm_kernel<BN, SWAP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             C::kSmemBytes);
-    if (e != cudaSuccess) return e;
-    configured.fetch_or(bit, std::memory_order_acq_rel);
-  }
-  // programmatic dependent launch: the prologue may overlap the preceding
-  // kernel; the kernel waits for it (griddepcontrol.wait) before reading inputs
-  cudaLaunchConfig_t cfg{};
-  cfg.gridDim = dim3(a.sched.grid);
-  cfg.blockDim = dim3(C::kThreads);
-  cfg.dynamicSmemBytes = C::kSmemBytes;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, gemm_kernel<BN, SWAP>, tmP, tmQ, a);
-}
 
 __global__ void relayout_kernel(const uint8_t* __restrict__ src, int64_t rows, int64_t K,
                                 uint8_t* __restrict__ dst, int64_t kp) {
@@ -99,13 +65,18 @@ cudaError_t launch_scale_relayout(const float* As, int as_col_major, int64_t ld_
 cudaError_t launch_gemm_swap(int bn, const CUtensorMap& tmP, const CUtensorMap& tmQ,
                              const GemmArgs& a, cudaStream_t stream) {
   switch (bn) {
-    case 16: return launch_one<16, true>(tmP, tmQ, a, stream);
-    case 32: return launch_one<32, true>(tmP, tmQ, a, stream);
-    case 64: return launch_one<64, true>(tmP, tmQ, a, stream);
-    case 128: return launch_one<128, true>(tmP, tmQ, a, stream);
-    case 256: return launch_one<256, true>(tmP, tmQ, a, stream);
+    case 16: return launch_instance<16, true>(tmP, tmQ, a, stream);
+    case 32: return launch_instance<32, true>(tmP, tmQ, a, stream);
+    case 64: return launch_instance<64, true>(tmP, tmQ, a, stream);
+    case 128: return launch_instance<128, true>(tmP, tmQ, a, stream);
+    case 256: return launch_instance<256, true>(tmP, tmQ, a, stream);
     default: return cudaErrorInvalidValue;
   }
+}
+
+cudaError_t gemm_cluster_capacity(int cs, int* clusters) {
+  // every instantiation holds one CTA per SM, so one of them answers for all
+  return cluster_capacity_instance<16, true>(cs, clusters);
 }
 
 cudaError_t launch_relayout(const uint8_t* src, int64_t rows, int64_t K, uint8_t* dst, int64_t kp,

@@ -30,6 +30,9 @@ cudaError_t launch_gemm_swap(int bn, const CUtensorMap& tmP, const CUtensorMap& 
 cudaError_t launch_gemm_wide(int bn, const CUtensorMap& tmP, const CUtensorMap& tmQ,
                              const GemmArgs& a, cudaStream_t stream);
 
+// Clusters of `cs` GEMM CTAs the current device runs at once (bfp8_gemm_swap.cu).
+cudaError_t gemm_cluster_capacity(int cs, int* clusters);
+
 // Pipeline depth and dynamic shared memory of an instantiation (0 if none).
 int gemm_stages(bool swap, int bn);
 int gemm_threads(bool swap, int bn);

@@ -6,7 +6,7 @@
 // blocks of 128 (one block = one set of fp32 scales, so one promotion).  A
 // unit of work is one (tile, k-block) pair.
 //
-// CTAs are persistent (grid <= SM count).  Tiles [0, dp_tiles) are handed out
+// Default: CTAs are persistent (grid <= SM count).  Tiles [0, dp_tiles) are handed out
 // whole, round-robin (CTA p takes tiles p, p+grid, ...): neighbouring CTAs
 // work on neighbouring tiles at the same time, which keeps shared operand
 // rows in L2.  The remaining tiles' units are split evenly and contiguously
@@ -14,6 +14,10 @@
 // finished by the last of them to arrive, which adds the others' fp32
 // partial sums in ascending K order, so the result does not depend on which
 // CTA arrives last.
+//
+// Cluster split-K (for problems with fewer tiles than SMs): each tile is
+// given to a thread-block cluster of cs CTAs, rank r taking a contiguous
+// slice of the k-blocks; see make_sched_cluster.
 //
 // All counts fit in 32 bits (the planner rejects larger problems); the device
 // walks its units with an incremental cursor, so the steady state performs no
@@ -40,7 +44,20 @@ struct Sched {
   uint32_t sk_units;  // (tiles - dp_tiles) * G
   uint32_t sk_q;      // stream-K units per CTA ...
   uint32_t sk_r;      // ... plus one for CTAs p < sk_r
+  uint32_t cluster;   // > 1: cluster split-K; CTA p works on tile p / cluster,
+                      // k-blocks of slice p % cluster; partials are summed in
+                      // distributed shared memory (no stream-K, no workspace)
 };
+
+// k-blocks [begin, end) of slice `rank` when G blocks are split `cs` ways
+// (balanced: every slice has floor or ceil of G / cs blocks, so none is empty
+// when cs <= G).
+BFP8_HD uint32_t cluster_kb_begin(uint32_t G, uint32_t cs, uint32_t rank) {
+  return static_cast<uint32_t>((static_cast<uint64_t>(rank) * G) / cs);
+}
+BFP8_HD uint32_t cluster_kb_end(uint32_t G, uint32_t cs, uint32_t rank) {
+  return cluster_kb_begin(G, cs, rank + 1);
+}
 
 BFP8_HD uint32_t sk_begin(const Sched& s, uint32_t p) {
   return p * s.sk_q + (p < s.sk_r ? p : s.sk_r);
@@ -55,6 +72,8 @@ BFP8_HD uint32_t sk_owner(const Sched& s, uint32_t u) {
 BFP8_HD uint32_t dp_units(const Sched& s) { return (s.dp_tiles / s.grid) * s.G; }
 
 BFP8_HD uint32_t num_units(const Sched& s, uint32_t p) {
+  if (s.cluster > 1)
+    return cluster_kb_end(s.G, s.cluster, p % s.cluster) - cluster_kb_begin(s.G, s.cluster, p % s.cluster);
   return dp_units(s) + sk_begin(s, p + 1) - sk_begin(s, p);
 }
 
@@ -80,6 +99,8 @@ struct Cursor {
   uint32_t dp_t;     // whole tiles finished
   uint32_t u;        // current stream-K unit (when in_sk)
   bool in_sk;
+  bool clustered;    // cluster split-K: one partial tile, kb from kb0
+  uint32_t kb0;
 
   BFP8_HD void set_pq() {
     q_tile = tile / p_tiles;
@@ -105,6 +126,17 @@ struct Cursor {
     dp_t = 0;
     u = 0;
     in_sk = false;
+    clustered = s.cluster > 1;
+    kb0 = 0;
+    if (clustered) {
+      const uint32_t rank = cta % s.cluster;
+      kb0 = cluster_kb_begin(G, s.cluster, rank);
+      n = cluster_kb_end(G, s.cluster, rank) - kb0;
+      tile = cta / s.cluster;
+      kb = kb0;
+      set_pq();
+      return;
+    }
     if (n == 0) { tile = kb = p_tile = q_tile = 0; return; }
     if (dp_per_cta > 0) {
       tile = cta;
@@ -116,6 +148,10 @@ struct Cursor {
   }
   BFP8_HD void next() {
     if (++j >= n) return;
+    if (clustered) {
+      ++kb;
+      return;
+    }
     if (!in_sk) {
       if (++kb == G) {
         kb = 0;
@@ -136,7 +172,7 @@ struct Cursor {
     }
   }
   BFP8_HD bool valid() const { return j < n; }
-  BFP8_HD bool first() const { return kb == 0 || (in_sk && u == sk_beg); }
+  BFP8_HD bool first() const { return kb == kb0 || (in_sk && u == sk_beg); }
   BFP8_HD bool last() const { return kb + 1 == G || j + 1 == n; }
   BFP8_HD int32_t sk_tile() const { return in_sk ? static_cast<int32_t>(tile - dp_tiles) : -1; }
 };
@@ -169,6 +205,25 @@ inline Sched make_sched(uint32_t p_tiles, uint32_t q_tiles, uint32_t G, uint32_t
   s.sk_units = (s.tiles - s.dp_tiles) * G;
   s.sk_q = s.sk_units / s.grid;
   s.sk_r = s.sk_units % s.grid;
+  s.cluster = 0;
+  return s;
+}
+
+// Cluster split-K: tiles x cs CTAs (2 <= cs <= min(8, G)); the cs CTAs of a
+// thread-block cluster share one tile, each summing a contiguous slice of its
+// k-blocks, and add their partial tiles through distributed shared memory.
+inline Sched make_sched_cluster(uint32_t p_tiles, uint32_t q_tiles, uint32_t G, uint32_t cs) {
+  Sched s{};
+  s.p_tiles = p_tiles;
+  s.q_tiles = q_tiles;
+  s.tiles = p_tiles * q_tiles;
+  s.G = G;
+  s.grid = s.tiles * cs;
+  s.dp_tiles = 0;
+  s.sk_units = 0;
+  s.sk_q = 0;
+  s.sk_r = 0;
+  s.cluster = cs;
   return s;
 }
 

@@ -92,17 +92,37 @@ typedef enum {
   BFP8_SCHEDULE_WIDE = 2      /* activations fill it; 128 x 256 output tiles */
 } bfp8_schedule;
 
+/* How the K dimension is shared out when the output has fewer tiles than the
+ * device has SMs (decode-sized M, or few weight rows). */
+typedef enum {
+  BFP8_KSPLIT_AUTO = 0,      /* whichever a cost model of the two expects to be
+                                faster for the problem */
+  BFP8_KSPLIT_STREAM_K = 1,  /* persistent CTAs; tiles left after whole waves are
+                                split into (tile, k-block) units, partial sums
+                                meet in the workspace */
+  BFP8_KSPLIT_CLUSTER = 2    /* thread-block clusters of 2..8 CTAs share a tile,
+                                each takes a slice of its k-blocks, and the
+                                partial tiles are added in distributed shared
+                                memory (no workspace traffic) */
+} bfp8_ksplit;
+
 /* Optional tuning / test controls; a NULL options pointer means all zero. */
 typedef struct {
   int schedule;        /* bfp8_schedule */
-  int max_ctas;        /* cap on persistent CTAs; 0 = one per SM */
+  int max_ctas;        /* cap on CTAs; 0 = one per SM */
   int tile_n;          /* BFP8_SCHEDULE_WIDE only: 128 or 256 (0 = 256) */
   int prefetch_weights;/* 1: the GEMM may start streaming B and Bs before the
                           kernel launched just before it on the stream has
                           finished (programmatic dependent launch).  Only valid
                           when that kernel does not write B or Bs, e.g. when it
                           is the bfp8_group_quant of this layer's activations. */
-  int reserved[4];
+  int k_split;         /* bfp8_ksplit.  CLUSTER applies only when the output
+                          has fewer tiles than max_ctas and K > 128; otherwise
+                          stream-K runs. */
+  int cluster_size;    /* CLUSTER: CTAs per tile, 2..8, clamped to ceil(K/128);
+                          0 = the size the cost model prefers among those with
+                          tiles * size <= max_ctas */
+  int reserved[2];
 } bfp8_gemm_options;
 
 /*
@@ -156,8 +176,12 @@ bfp8_status bfp8_gemm_workspace_size(int64_t M, int64_t N, int64_t K,
                                      const bfp8_gemm_options* opt, int operands_unaligned,
                                      size_t* bytes);
 
-/* Host-only description of the schedule bfp8_gemm_ex would run on a device
- * with `num_sms` SMs (no device needed; used for planning and tests). */
+/* Description of the schedule bfp8_gemm_ex runs.  num_sms = 0: for the
+ * current device (its SM count and how many GEMM clusters of each size it
+ * runs at once; needs the device).  num_sms > 0: host-only, for a device with
+ * that many SMs whose cluster capacity is estimated (a little below
+ * num_sms / size, since GPCs differ in size), so the cluster size may differ
+ * from the one the current device would get. */
 typedef struct {
   int swap_ab;          /* 1: weights in the MMA M slot */
   int tile_n;           /* MMA N (rows of the second operand per tile) */
@@ -169,15 +193,17 @@ typedef struct {
   int64_t sk_units;     /* (tile, k-block) units split across CTAs */
   int relayout;         /* operands re-laid out into the workspace first */
   size_t workspace_bytes;
+  int cluster;          /* CTAs per tile: > 1 for cluster split-K (grid =
+                           tiles * cluster, dp_tiles = sk_units = 0), else 1 */
 } bfp8_plan_info;
 
 bfp8_status bfp8_gemm_plan(int64_t M, int64_t N, int64_t K, int num_sms,
                            const bfp8_gemm_options* opt, int operands_unaligned,
                            bfp8_plan_info* info);
 
-/* Host-only view of the stream-K work split of a plan: for CTA `cta`, the
- * number of (tile, k-block) units it processes and, for unit j, its tile and
- * k-block.  Returns BFP8_ERR_INVALID_ARG for indices out of range. */
+/* The work split of a plan (num_sms as for bfp8_gemm_plan): for CTA `cta`,
+ * the number of (tile, k-block) units it processes and, for unit j, its tile
+ * and k-block.  Returns BFP8_ERR_INVALID_ARG for indices out of range. */
 bfp8_status bfp8_plan_unit(int64_t M, int64_t N, int64_t K, int num_sms,
                            const bfp8_gemm_options* opt, int cta, int64_t j,
                            int64_t* num_units, int64_t* tile, int64_t* k_block);

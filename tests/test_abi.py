@@ -90,6 +90,12 @@ def test_gemm_rejects_bad_arguments_on_the_host(L):
     assert _gemm(L, opt=ctypes.pointer(bad)) == 1
     bad.schedule, bad.tile_n = 0, 64
     assert _gemm(L, opt=ctypes.pointer(bad)) == 1
+    bad.tile_n, bad.k_split = 0, 3
+    assert _gemm(L, opt=ctypes.pointer(bad)) == 1
+    for cs in (1, 9, -2):
+        bad.k_split, bad.cluster_size = 2, cs
+        assert _gemm(L, opt=ctypes.pointer(bad)) == 1
+    bad.cluster_size = 0
     # a valid call reaches the device check, which fails cleanly without a GPU
     import torch
     if not torch.cuda.is_available():
@@ -120,14 +126,65 @@ def _cover(M, N, K, sms, options=None):
     (2048, 4096, 4096, 152, None), (1000, 1000, 1000, 152, None), (3, 576, 1000, 152, None),
     (300, 1000, 7168, 152, {"schedule": 1}), (16, 512, 256, 152, {"schedule": 2}),
     (1, 1, 1, 152, None), (4096, 4096, 512, 19, {"tile_n": 128}),
+    (1, 4096, 4096, 152, {"k_split": 1}), (3, 576, 7168, 152, {"k_split": 2}),
+    (1, 4096, 300, 152, {"k_split": 2}), (5, 256, 1024, 152, {"k_split": 2, "cluster_size": 5}),
+    (600, 512, 4096, 152, {"schedule": 2}), (7, 1000, 1000, 152, {"k_split": 2, "cluster_size": 7}),
 ])
 def test_work_split_covers_every_unit_once(L, M, N, K, sms, opts):
     _cover(M, N, K, sms, opts)
 
 
+def _cluster_units(M, N, K, sms, options):
+    """Per tile, the k-blocks each cluster rank takes, from the plan's walk."""
+    plan = bf.bfp8_gemm_plan(M, N, K, sms, options)
+    cs = plan["cluster"]
+    per_tile = {}
+    for cta in range(plan["grid"]):
+        n, _, _ = bf.bfp8_plan_unit(M, N, K, sms, cta, -1, options)
+        kbs = []
+        for j in range(n):
+            _, t, kb = bf.bfp8_plan_unit(M, N, K, sms, cta, j, options)
+            assert t == cta // cs                    # a cluster's CTAs share one tile
+            kbs.append(kb)
+        per_tile.setdefault(cta // cs, []).append(kbs)
+    return plan, per_tile
+
+
+@pytest.mark.parametrize("M,N,K,opts,cs", [
+    (1, 4096, 4096, None, 4), (200, 4096, 4096, None, 4), (3, 576, 7168, {"k_split": 2}, 8),
+    (1, 4096, 300, {"k_split": 2}, 3), (600, 512, 4096, {"schedule": 2}, 8),
+    (5, 256, 1024, {"k_split": 2, "cluster_size": 5}, 5),
+])
+def test_cluster_split_gives_each_rank_one_nonempty_contiguous_slice(L, M, N, K, opts, cs):
+    plan, per_tile = _cluster_units(M, N, K, 152, opts)
+    assert plan["cluster"] == cs and plan["grid"] == plan["tiles"] * cs
+    assert plan["dp_tiles"] == 0 and plan["sk_units"] == 0
+    G = plan["k_blocks"]
+    for t, slices in per_tile.items():
+        assert len(slices) == cs
+        assert [kb for sl in slices for kb in sl] == list(range(G))     # rank order = K order
+        sizes = [len(sl) for sl in slices]
+        assert min(sizes) >= 1 and max(sizes) - min(sizes) <= 1
+
+
 def test_plans_choose_the_documented_schedules(L):
     p = bf.bfp8_gemm_plan(1, 4096, 4096, 152)
-    assert p["swap_ab"] == 1 and p["tile_n"] == 16 and p["grid"] == 152 and p["dp_tiles"] == 0
+    assert p["swap_ab"] == 1 and p["tile_n"] == 16 and p["cluster"] == 4 and p["grid"] == 128
+    p = bf.bfp8_gemm_plan(1, 4096, 4096, 152, {"k_split": 1})
+    assert p["cluster"] == 1 and p["grid"] == 152 and p["dp_tiles"] == 0
+    # the cost model: five tiles of 56 k-blocks would be spread over ~30 CTAs
+    # each by stream-K (a long fixup chain); clusters of 8 win
+    assert bf.bfp8_gemm_plan(83, 576, 7168, 152)["cluster"] == 8
+    # 40 tiles of 200 k-blocks: stream-K's 53 steps per CTA beat 67 in clusters of 3
+    assert bf.bfp8_gemm_plan(1, 5120, 25600, 152)["cluster"] == 1
+    # wide tiles: 64 of them at M = 512, clusters of 2
+    p = bf.bfp8_gemm_plan(512, 4096, 4096, 152)
+    assert p["swap_ab"] == 0 and p["cluster"] == 2 and p["grid"] == 128
+    # 80 tiles: not even clusters of 2 fit in one wave
+    assert bf.bfp8_gemm_plan(1, 10240, 5120, 152)["cluster"] == 1
+    # cluster schedules need no stream-K partials in the workspace
+    assert (bf.bfp8_gemm_plan(1, 4096, 4096, 152)["workspace_bytes"]
+            < bf.bfp8_gemm_plan(1, 4096, 4096, 152, {"k_split": 1})["workspace_bytes"])
     p = bf.bfp8_gemm_plan(64, 4096, 4096, 152)
     assert p["swap_ab"] == 1 and p["tile_n"] == 64
     p = bf.bfp8_gemm_plan(8192, 4096, 4096, 152)

@@ -1,7 +1,8 @@
 """GPU parity of the blocked FP8 GEMM against the oracle.
 
 Every schedule computes the same function, so the page's correctness case is
-run through each of them and through forced stream-K splits.  The sweep at
+run through each of them, through forced stream-K splits and through cluster
+split-K at several cluster sizes.  The sweep at
 N=K=4096 is compared in full for the decode sizes and on sampled rows for the
 prefill sizes (the launch configuration the bench times); the Qwen3-32B
 layer shapes and the ragged/tail shapes (heavy-tailed activations,
@@ -71,7 +72,9 @@ PAGE = wl.correctness_case()
 @pytest.mark.parametrize("col_major", [True, False])
 @pytest.mark.parametrize("options", [None, {"schedule": 1}, {"schedule": 2},
                                      {"schedule": 2, "tile_n": 128}, {"max_ctas": 7},
-                                     {"schedule": 2, "max_ctas": 3}, {"schedule": 1, "max_ctas": 150}])
+                                     {"schedule": 2, "max_ctas": 3}, {"schedule": 1, "max_ctas": 150},
+                                     {"k_split": 1}, {"k_split": 2}, {"k_split": 2, "cluster_size": 3},
+                                     {"schedule": 2, "k_split": 2}])
 def test_page_correctness_case_every_schedule(oracle_mod, dev, col_major, options):
     stats, _ = _run(oracle_mod, dev, PAGE, col_major, options, label=f"page {options}")
     assert stats["rel_diff"] < 1e-3
@@ -138,7 +141,29 @@ def test_unaligned_operands_and_output(oracle_mod, dev):
     assert float(out_big[0]) == 0.0
 
 
-@pytest.mark.parametrize("options", [None, {"max_ctas": 5}, {"schedule": 2}])
+@pytest.mark.parametrize("M,N,K", [(1, 4096, 4096), (16, 4096, 4096), (83, 576, 7168),
+                                   (100, 1000, 1000), (129, 16, 300), (256, 4096, 1024),
+                                   (600, 512, 4096), (257, 384, 256), (2, 130, 129)])
+@pytest.mark.parametrize("cs", [0, 2, 3, 5, 8])
+def test_cluster_split_k(oracle_mod, dev, M, N, K, cs):
+    """Cluster split-K at every cluster size the planner may pick (0 = its
+    own choice; explicit sizes are clamped to the tile's k-blocks): swap and
+    wide tiles, ragged M, N and K, re-laid-out operands."""
+    opts = {"k_split": 2, "cluster_size": cs}
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    plan = bf.bfp8_gemm_plan(M, N, K, 0, opts)          # this device's plan
+    G = plan["k_blocks"]
+    if cs:
+        assert plan["cluster"] == (min(cs, G) if G >= 2 else 1)
+    elif G >= 2 and 2 * plan["tiles"] <= sms:
+        assert 2 <= plan["cluster"] <= min(8, G) and plan["grid"] <= sms
+    case = wl.ragged_case(M, N, K, seed=5 * M + N + K + cs)
+    rows = None if M <= 128 else sample_rows(M, 24, seed=M + cs)
+    _run(oracle_mod, dev, case, options=opts, rows=rows, label=f"cluster {cs} {M}x{N}x{K}")
+
+
+@pytest.mark.parametrize("options", [None, {"max_ctas": 5}, {"schedule": 2}, {"k_split": 2},
+                                     {"k_split": 2, "cluster_size": 8}, {"k_split": 1}])
 def test_deterministic_across_calls(dev, options):
     case = wl.linear_case(96, 1024, 2048, seed=3)
     x = case["x"].to(dev)
