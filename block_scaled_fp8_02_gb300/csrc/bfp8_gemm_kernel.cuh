@@ -130,11 +130,15 @@ struct GemmCfg {
   static_assert(2 * kSmemBytes > kSmemLimit + 1024, "two CTAs would fit on one SM");
   static constexpr int kTmemCols = tmem_cols_for(2 * BN);
   // Cluster split-K: a CTA's partial tile goes into its (then idle) operand
-  // ring as [column][row] fp32 with a 132-float column pitch, so that the
-  // promotion warps write it without bank conflicts and 16-byte reads of
-  // neighbouring columns fall in different banks.
-  static constexpr int kPartPitch = 132;
-  static_assert(BN * kPartPitch * 4 <= kStages * kStageBytes, "partial tile does not fit the ring");
+  // ring, laid out so that the reduction reads it contiguously along the
+  // output's inner dimension (n): swap tiles as [column][row] with a 132-float
+  // column pitch (TMEM rows are output columns), wide tiles as [row][column]
+  // with a BN + 4 float row pitch (written 16 bytes at a time; the padding
+  // spreads neighbouring rows over the banks).
+  static constexpr int kPartPitch = SWAP ? 132 : BN + 4;
+  static constexpr int kPartLines = SWAP ? BN : 128;
+  static_assert(kPartLines * kPartPitch * 4 <= kStages * kStageBytes,
+                "partial tile does not fit the ring");
   static constexpr uint32_t kIdesc = idesc_e4m3_f32(128, BN);
 };
 
@@ -157,7 +161,12 @@ enum : int {
   kTrProdWait = 12,    // producer waiting for a free stage
   kTrEpiScaleCyc = 13, // promotion warp 0 staging / waiting for scales
   kTrEpiFixCyc = 14,   // promotion warp 0 in segment epilogues (fixup + stores)
-  kTraceEvents = 16
+  kTrClusterSync = 15, // cluster split-K: first cluster barrier passed
+  kTrProdAtSync = 16,  // producer lane reaches the first cluster barrier
+  kTrMmaAtSync = 17,   // MMA lane reaches it
+  kTrEpiAtSync = 18,   // promotion warp 0 reaches it (partial parked)
+  kTrEpiReduced = 19,  // promotion warp 0 done with its share of the reduction
+  kTraceEvents = 24
 };
 #if defined(BFP8_TRACE)
 __device__ __forceinline__ void trace_event(unsigned long long* tr, uint32_t cta, int e) {
@@ -226,6 +235,14 @@ __global__ void __launch_bounds__(GemmCfg<BN, SWAP>::kThreads, 1)
   auto stage_q = [&](int i) { return sbase + static_cast<uint32_t>(i * C::kStageBytes + C::kPBytes); };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffTmemPtr);
   volatile int* s_last_flag = reinterpret_cast<volatile int*>(smem + C::kOffFlags);
+  // set by any role of this CTA that gives up on a wait (copies may then still
+  // be in flight into shared memory when the roles end)
+  volatile int* s_fail = reinterpret_cast<volatile int*>(smem + C::kOffFlags + 4);
+  auto fail = [&](int code) {
+    report_failure(a.err, code);
+    *s_fail = 1;
+  };
+  uint32_t prod_issued = 0, prod_sissued = 0;   // producer lane: copies requested
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::kStages; ++i) {
@@ -241,6 +258,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, SWAP>::kThreads, 1)
       mbar_init(bar_tempty(b), C::kNE);      // one arrival per promotion warp
     }
     *s_last_flag = 0;
+    *s_fail = 0;
     fence_barrier_init();
   }
   if (warp == C::kNE && lane == 0) {
@@ -306,7 +324,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, SWAP>::kThreads, 1)
         BFP8_CLK(c0);
         {
           if (!mbar_wait_bounded(bar_sempty(ss), sph ^ 1u, a.wait_limit)) {
-            report_failure(a.err, kDevTimeoutProducer);
+            fail(kDevTimeoutProducer);
             break;
           }
           const int64_t kb = cur.kb;
@@ -327,10 +345,11 @@ __global__ void __launch_bounds__(GemmCfg<BN, SWAP>::kThreads, 1)
             bulk_load(slot + 4u * (C::kAsFloats + 4 * h), a.Bs + (e & ~int64_t{3}), 16u,
                       bar_sfull(ss));
           }
+          ++prod_sissued;
           if (++ss == C::kSR) { ss = 0; sph ^= 1u; }
         }
         if (!mbar_wait_bounded(bar_empty(st), ph ^ 1u, a.wait_limit)) {
-          report_failure(a.err, kDevTimeoutProducer);
+          fail(kDevTimeoutProducer);
           break;
         }
         BFP8_ACC(t_wait, c0);
@@ -352,25 +371,10 @@ __global__ void __launch_bounds__(GemmCfg<BN, SWAP>::kThreads, 1)
       }
       trace_event(a.trace, cta, kTrProdDone);
       trace_value(a.trace, cta, kTrProdWait, t_wait);
-      // Do not leave while copies into this CTA's shared memory may be in flight.
-      const uint32_t tail = issued < static_cast<uint32_t>(C::kStages) ? issued : C::kStages;
-      for (uint32_t t = 0; t < tail; ++t) {
-        const uint32_t j = issued - 1 - t;
-        if (!mbar_wait_bounded(bar_full(j % C::kStages), (j / C::kStages) & 1u, a.wait_limit)) {
-          report_failure(a.err, kDevTimeoutTail);
-          break;
-        }
-      }
-      {
-        const uint32_t stail = issued < static_cast<uint32_t>(C::kSR) ? issued : C::kSR;
-        for (uint32_t t = 0; t < stail; ++t) {
-          const uint32_t j = issued - 1 - t;
-          if (!mbar_wait_bounded(bar_sfull(j % C::kSR), (j / C::kSR) & 1u, a.wait_limit)) {
-            report_failure(a.err, kDevTimeoutTail);
-            break;
-          }
-        }
-      }
+      // When every role finishes normally, every copy has landed (the MMA
+      // issuer waited for each operand stage, the promotion warps for each
+      // scale slot); otherwise the copies are drained at the end.
+      prod_issued = issued;
     } else if (warp == C::kNE + 1 && lane == 0) {
       // -------------------------------------------------------- MMA issuer
       const uint32_t n = num_units(s, cta);
@@ -387,7 +391,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, SWAP>::kThreads, 1)
         BFP8_ACC(t_tmem, c0);
         BFP8_CLK(c1);
         if (!ok_t || !mbar_wait_bounded(bar_full(st), ph, a.wait_limit)) {
-          report_failure(a.err, kDevTimeoutMma);
+          fail(kDevTimeoutMma);
           break;
         }
         BFP8_ACC(t_data, c1);
@@ -412,14 +416,15 @@ __global__ void __launch_bounds__(GemmCfg<BN, SWAP>::kThreads, 1)
       // The last commit fires when every MMA issued above has completed.
       if (done > 0 && done < n) {
         const uint32_t j = done - 1;
-        if (!mbar_wait_bounded(bar_tfull(j & 1), (j >> 1) & 1, a.wait_limit))
-          report_failure(a.err, kDevTimeoutTail);
+        if (!mbar_wait_bounded(bar_tfull(j & 1), (j >> 1) & 1, a.wait_limit)) fail(kDevTimeoutTail);
       }
     }
     __syncwarp();
     if (s.cluster > 1) {
       // every thread of the cluster takes part in both cluster barriers of
       // the split-K reduction (see the promotion warps)
+      if (lane == 0 && warp == C::kNE) trace_event(a.trace, cta, kTrProdAtSync);
+      if (lane == 0 && warp == C::kNE + 1) trace_event(a.trace, cta, kTrMmaAtSync);
       cluster_sync();
       cluster_sync();
     }
@@ -449,7 +454,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, SWAP>::kThreads, 1)
       BFP8_CLK(e0);
       const uint32_t j = cur.j;
       if (!mbar_wait_bounded(bar_sfull(ss), sph, a.wait_limit)) {
-        report_failure(a.err, kDevTimeoutEpilogue);
+        fail(kDevTimeoutEpilogue);
         break;
       }
       const float* slot = sRing + ss * C::kSlotFloats;
@@ -469,7 +474,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, SWAP>::kThreads, 1)
       BFP8_CLK(e1);
       const int b = j & 1;
       if (!mbar_wait_bounded(bar_tfull(b), (j >> 1) & 1, a.wait_limit)) {
-        report_failure(a.err, kDevTimeoutEpilogue);
+        fail(kDevTimeoutEpilogue);
         break;
       }
       tc_fence_after();
@@ -517,8 +522,15 @@ __global__ void __launch_bounds__(GemmCfg<BN, SWAP>::kThreads, 1)
         // memory; the cluster adds the partials after the loop.  Every MMA
         // has completed (tfull of the last unit), so the operand ring is idle.
         float* part = reinterpret_cast<float*>(smem);
+        if (SWAP) {
 #pragma unroll
-        for (int i = 0; i < C::kCPT; ++i) part[(col0 + i) * C::kPartPitch + r] = acc[i];
+          for (int i = 0; i < C::kCPT; ++i) part[(col0 + i) * C::kPartPitch + r] = acc[i];
+        } else {
+          float4* row = reinterpret_cast<float4*>(part + r * C::kPartPitch + col0);
+#pragma unroll
+          for (int i = 0; i < C::kCPT / 4; ++i)
+            row[i] = make_float4(acc[4 * i], acc[4 * i + 1], acc[4 * i + 2], acc[4 * i + 3]);
+        }
         BFP8_ACC(t_efix, e3);
         continue;
       }
@@ -620,12 +632,15 @@ __global__ void __launch_bounds__(GemmCfg<BN, SWAP>::kThreads, 1)
     if (s.cluster > 1) {
       // ---- cluster split-K reduction.  After the first cluster barrier every
       // CTA's partial is in its shared memory.  The output tile's valid part,
-      // cut into runs of 4 rows of one column, is divided evenly among the
+      // cut into runs of 4 elements along n, is divided evenly among the
       // cluster's CTAs; each adds the cs partials of its runs in rank order
       // (deterministic) through distributed shared memory and stores bf16.
       // The second barrier keeps every CTA (and its shared memory) alive
       // until all reads of it are done.
+      if (etid == 0) trace_event(a.trace, cta, kTrEpiAtSync);
       cluster_sync();
+      if (etid == 0) trace_event(a.trace, cta, kTrClusterSync);
+      BFP8_CLK(e4);
       const uint32_t cs = s.cluster;
       const uint32_t rank = cta % cs;            // 1-D clusters of consecutive CTAs
       const uint32_t tile = cta / cs;
@@ -636,43 +651,63 @@ __global__ void __launch_bounds__(GemmCfg<BN, SWAP>::kThreads, 1)
       const int64_t qlim = SWAP ? a.M : a.N;
       const int64_t plim = SWAP ? a.N : a.M;
       const uint32_t qv = static_cast<uint32_t>(qlim - q0 < BN ? qlim - q0 : BN);
-      const int64_t pv64 = plim - p0 < 128 ? plim - p0 : 128;
-      const uint32_t runs_per_col = static_cast<uint32_t>((pv64 + 3) / 4);
-      const uint32_t items = qv * runs_per_col;
-      const uint32_t beg = static_cast<uint32_t>((static_cast<uint64_t>(rank) * items) / cs);
-      const uint32_t end = static_cast<uint32_t>((static_cast<uint64_t>(rank + 1) * items) / cs);
+      const uint32_t pv = static_cast<uint32_t>(plim - p0 < 128 ? plim - p0 : 128);
+      // swap: runs of 4 TMEM rows in each valid column; wide: runs of 4
+      // columns in each valid row
+      const uint32_t runs_per_line = SWAP ? (pv + 3) / 4 : (qv + 3) / 4;
+      const uint32_t items = (SWAP ? qv : pv) * runs_per_line;
+      const uint32_t beg = rank * items / cs;         // items <= 256 * 32: no overflow
+      const uint32_t end = (rank + 1) * items / cs;
       const uint32_t part0 = smem_addr(smem);
-      for (uint32_t i = beg + etid; i < end; i += C::kNE * 32) {
-        // swap: lanes walk down a column (rows = output columns n, contiguous);
-        // wide: lanes walk across columns (output columns n) of one row run
-        uint32_t c, r4;
-        if (SWAP) {
-          c = i / runs_per_col;
-          r4 = (i - c * runs_per_col) * 4;
-        } else {
-          const uint32_t run = i / qv;
-          c = i - run * qv;
-          r4 = run * 4;
+      // kU runs per thread per round, all their loads issued before any is
+      // used: distributed shared memory has a long round trip.
+      constexpr int kU = 4;
+      constexpr uint32_t kStride = C::kNE * 32;
+      for (uint32_t i0 = beg + etid; i0 < end; i0 += kU * kStride) {
+        uint32_t addr[kU];
+        uint32_t cc[kU], rr[kU];
+#pragma unroll
+        for (int u = 0; u < kU; ++u) {
+          const uint32_t i = i0 + u * kStride;
+          // lanes walk along n: swap, down a column of TMEM rows; wide, across
+          // the columns of one row
+          const uint32_t line = i / runs_per_line;
+          const uint32_t off4 = (i - line * runs_per_line) * 4;
+          cc[u] = line;
+          rr[u] = off4;
+          addr[u] = part0 + 4u * (line * C::kPartPitch + off4);
         }
-        const uint32_t addr = part0 + 4u * (c * C::kPartPitch + r4);
-        float4 t[8];
+        float4 v[kU];
 #pragma unroll
-        for (uint32_t q = 0; q < 8; ++q)
-          if (q < cs) t[q] = ld_dsmem_v4(mapa_shared(addr, q));
-        float4 v = t[0];
+        for (int u = 0; u < kU; ++u) v[u] = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-        for (uint32_t q = 1; q < 8; ++q) {
-          if (q < cs) {
-            v.x += t[q].x;
-            v.y += t[q].y;
-            v.z += t[q].z;
-            v.w += t[q].w;
+        for (uint32_t q = 0; q < 8; ++q) {
+          if (q >= cs) break;
+          float4 t[kU];
+#pragma unroll
+          for (int u = 0; u < kU; ++u)
+            if (i0 + u * kStride < end) t[u] = ld_dsmem_v4(mapa_shared(addr[u], q));
+#pragma unroll
+          for (int u = 0; u < kU; ++u) {
+            if (i0 + u * kStride < end) {
+              if (q == 0) {
+                v[u] = t[u];
+              } else {
+                v[u].x += t[u].x;
+                v[u].y += t[u].y;
+                v[u].z += t[u].z;
+                v[u].w += t[u].w;
+              }
+            }
           }
         }
-        const float f[4] = {v.x, v.y, v.z, v.w};
-        if (SWAP) {
-          const int64_t m = q0 + c;
-          const int64_t n = p0 + r4;
+#pragma unroll
+        for (int u = 0; u < kU; ++u) {
+          if (i0 + u * kStride >= end) continue;
+          const float f[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+          // output row m and first column n of the run
+          const int64_t m = SWAP ? q0 + cc[u] : p0 + cc[u];
+          const int64_t n = SWAP ? p0 + rr[u] : q0 + rr[u];
           __nv_bfloat16* row = a.out + m * a.N;
           if (a.vec_store && n + 4 <= a.N) {
             st_global_v2(row + n, pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]));
@@ -681,15 +716,10 @@ __global__ void __launch_bounds__(GemmCfg<BN, SWAP>::kThreads, 1)
             for (int e = 0; e < 4; ++e)
               if (n + e < a.N) row[n + e] = __float2bfloat16_rn(f[e]);
           }
-        } else {
-          const int64_t n = q0 + c;
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int64_t m = p0 + r4 + e;
-            if (m < a.M) a.out[m * a.N + n] = __float2bfloat16_rn(f[e]);
-          }
         }
       }
+      BFP8_ACC(t_efix, e4);
+      if (etid == 0) trace_event(a.trace, cta, kTrEpiReduced);
       cluster_sync();
     }
     if (etid == 0) {
@@ -704,6 +734,26 @@ __global__ void __launch_bounds__(GemmCfg<BN, SWAP>::kThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  if (warp == C::kNE && lane == 0 && *s_fail) {
+    // a role gave up: do not leave while copies into this CTA's shared memory
+    // may still be in flight
+    const uint32_t tail = prod_issued < static_cast<uint32_t>(C::kStages) ? prod_issued : C::kStages;
+    for (uint32_t t = 0; t < tail; ++t) {
+      const uint32_t j = prod_issued - 1 - t;
+      if (!mbar_wait_bounded(bar_full(j % C::kStages), (j / C::kStages) & 1u, a.wait_limit)) {
+        report_failure(a.err, kDevTimeoutTail);
+        break;
+      }
+    }
+    const uint32_t stail = prod_sissued < static_cast<uint32_t>(C::kSR) ? prod_sissued : C::kSR;
+    for (uint32_t t = 0; t < stail; ++t) {
+      const uint32_t j = prod_sissued - 1 - t;
+      if (!mbar_wait_bounded(bar_sfull(j % C::kSR), (j / C::kSR) & 1u, a.wait_limit)) {
+        report_failure(a.err, kDevTimeoutTail);
+        break;
+      }
+    }
+  }
   if (warp == C::kNE + 1) tmem_dealloc(tmem, C::kTmemCols);
 #endif
 }
