@@ -6,9 +6,9 @@
 //   amax  = max |x[m, k]| over the group's real elements
 //   scale = max(amax, 1e-10) / 448           (one IEEE fp32 division)
 //   q     = e4m3_rn_satfinite(x / scale)     (x / scale as one IEEE fp32 division;
-//                                             computed as x * (1/scale) except
-//                                             near e4m3 rounding boundaries,
-//                                             which gives the same codes)
+//                                             its code is found from two
+//                                             products that bracket it, with the
+//                                             division only where they disagree)
 // and the scale is stored row-major s[m * ld_s + g] or column-major
 // s[g * ld_s + m] (the layout the GEMM kernels read; lmdeploy PR 4830 pads its
 // stride to 16 bytes for TMA, transformers' _coerce_sf_for_kernel calls it
@@ -17,8 +17,9 @@
 // Memory-bound: each warp streams 512 input bytes per step with 16-byte loads
 // (one 128-element group for fp32 input, two for bf16 input: a half-warp per
 // group), reduces amax with warp shuffles inside the group's lanes and packs
-// pairs of codes with cvt.rn.satfinite.e4m3x2.f32.  Four steps (2 KB) are in
-// flight per warp to keep enough bytes outstanding.
+// pairs of codes with cvt.rn.satfinite.e4m3x2.f32.  One wave of persistent
+// blocks; each warp keeps the loads of its next kUnroll steps in flight while
+// it quantises the current ones.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -38,20 +39,11 @@ struct QuantShape {
   static constexpr int kGPW = 32 / kLPG;        // groups per warp step
 };
 
-// fl32(x / scale) as far as its e4m3 code is concerned.  y = x * rcp, with
-// rcp = 1/scale rounded to nearest, differs from x / scale by at most 2 ulp
-// and from its correctly rounded value by at most 2.5 ulp.  The e4m3 code of
-// a value with |y| >= 2^-6 only changes at the midpoints between e4m3 values,
-// fp32 numbers whose low 20 mantissa bits are exactly 0x80000; so unless y is
-// within 3 ulp of such a midpoint (or in the e4m3 subnormal range, where the
-// spacing is fixed) both round to the same code, and the IEEE division is
-// only needed for those rare cases.
-__device__ __forceinline__ float quotient_for_e4m3(float x, float scale, float rcp) {
-  const float y = __fmul_rn(x, rcp);
-  const uint32_t b = __float_as_uint(y) & 0x7FFFFFFFu;
-  const bool tiny = b < 0x3C800000u;                            // |y| < 2^-6
-  const bool near_mid = ((b - 0x80000u + 3u) & 0xFFFFFu) <= 6u;  // within 3 ulp of a midpoint
-  return (tiny || near_mid) ? __fdiv_rn(x, scale) : y;
+// Approximate reciprocal (PTX rcp.approx: at most 1 ulp from 1/s).
+__device__ __forceinline__ float rcp_approx(float s) {
+  float r;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(s));
+  return r;
 }
 
 __device__ __forceinline__ uint16_t cvt_e4m3x2(float lo, float hi) {
@@ -60,115 +52,211 @@ __device__ __forceinline__ uint16_t cvt_e4m3x2(float lo, float hi) {
   return r;
 }
 
+// A lane's 16 input bytes as four raw 32-bit words (bf16: two elements per
+// word, element 2i in the low half), kept packed until they are used.
 template <bool kF32>
-__device__ __forceinline__ float load_elem(const void* x, int64_t idx) {
+__device__ __forceinline__ void load_words(const void* x, int64_t idx, uint32_t (&w)[4]) {
+  const uint4 t = kF32 ? __ldg(reinterpret_cast<const uint4*>(static_cast<const float*>(x) + idx))
+                       : __ldg(reinterpret_cast<const uint4*>(static_cast<const unsigned short*>(x) + idx));
+  w[0] = t.x; w[1] = t.y; w[2] = t.z; w[3] = t.w;
+}
+
+// Same for a lane whose elements run past K or whose row is not 16-byte
+// aligned: element by element, zeros beyond `n`.
+template <bool kF32>
+__device__ __forceinline__ void load_words_tail(const void* x, int64_t idx, int64_t n, uint32_t (&w)[4]) {
+#pragma unroll
+  for (int i = 0; i < 4; ++i) w[i] = 0u;
   if constexpr (kF32) {
-    return __ldg(static_cast<const float*>(x) + idx);
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+      if (e < n) w[e] = __float_as_uint(__ldg(static_cast<const float*>(x) + idx + e));
   } else {
-    const unsigned short b = __ldg(static_cast<const unsigned short*>(x) + idx);
-    return __uint_as_float(static_cast<uint32_t>(b) << 16);
+#pragma unroll
+    for (int e = 0; e < 8; ++e)
+      if (e < n) w[e / 2] |= static_cast<uint32_t>(__ldg(static_cast<const unsigned short*>(x) + idx + e))
+                             << (16 * (e & 1));
   }
 }
 
 template <bool kF32>
-__device__ __forceinline__ void load_vec(const void* x, int64_t idx, float (&v)[QuantShape<kF32>::kEPL]) {
+__device__ __forceinline__ void unpack(const uint32_t (&w)[4], float (&v)[QuantShape<kF32>::kEPL]) {
   if constexpr (kF32) {
-    const float4 f = __ldg(reinterpret_cast<const float4*>(static_cast<const float*>(x) + idx));
-    v[0] = f.x; v[1] = f.y; v[2] = f.z; v[3] = f.w;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) v[i] = __uint_as_float(w[i]);
   } else {
-    const uint4 w = __ldg(reinterpret_cast<const uint4*>(static_cast<const unsigned short*>(x) + idx));
-    const uint32_t words[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      v[2 * i] = __uint_as_float(words[i] << 16);
-      v[2 * i + 1] = __uint_as_float(words[i] & 0xFFFF0000u);
+      v[2 * i] = __uint_as_float(w[i] << 16);
+      v[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
     }
   }
 }
 
-constexpr int kUnroll = 4;
+#ifndef BFP8_QUANT_UNROLL
+#define BFP8_QUANT_UNROLL 2
+#endif
+#ifndef BFP8_QUANT_MIN_BLOCKS
+#define BFP8_QUANT_MIN_BLOCKS 4
+#endif
+constexpr int kUnroll = BFP8_QUANT_UNROLL;       // warp steps per batch
 constexpr int kWarpsPerBlock = 8;
+constexpr int kBlocksPerSm = BFP8_QUANT_MIN_BLOCKS;
+
+// Walks one warp's chunks, kUnroll at a time: chunk c = row * chunks_per_row
+// + col; warp w takes chunks w, w + nwarps, ... (a chunk is one warp step:
+// GPW groups of one row).  Positions advance without division (the host
+// checks M * chunks_per_row < 2^31).
+struct ChunkWalk {
+  uint32_t rw[kUnroll], cl[kUnroll];
+  uint32_t cpr, srow, scol;
+  __device__ __forceinline__ void init(uint32_t warp0, uint32_t nwarps, uint32_t chunks_per_row) {
+    cpr = chunks_per_row;
+    const uint32_t stride = nwarps * kUnroll;
+    srow = stride / cpr;
+    scol = stride - srow * cpr;
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const uint32_t c = warp0 + u * nwarps;
+      rw[u] = c / cpr;
+      cl[u] = c - rw[u] * cpr;
+    }
+  }
+  __device__ __forceinline__ void advance() {
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      cl[u] += scol;
+      rw[u] += srow;
+      if (cl[u] >= cpr) {
+        cl[u] -= cpr;
+        ++rw[u];
+      }
+    }
+  }
+};
 
 template <bool kF32>
-__global__ void __launch_bounds__(kWarpsPerBlock * 32, 4)
+__device__ __forceinline__ void load_batch(const void* x, const ChunkWalk& cw, uint32_t Mu, uint32_t G,
+                                           int64_t K, int64_t ld_x, int32_t vec_x, int gi, int li,
+                                           uint32_t (&w)[kUnroll][4]) {
+  constexpr int EPL = QuantShape<kF32>::kEPL, GPW = QuantShape<kF32>::kGPW;
+#pragma unroll
+  for (int u = 0; u < kUnroll; ++u) {
+    const uint32_t gu = cw.cl[u] * GPW + gi;
+    const int64_t ku = static_cast<int64_t>(gu) * 128 + li * EPL;
+    const bool ok = cw.rw[u] < Mu && gu < G;
+    const int64_t off = static_cast<int64_t>(cw.rw[u]) * ld_x + ku;
+    if (ok && vec_x && ku + EPL <= K) {
+      load_words<kF32>(x, off, w[u]);
+    } else {
+      load_words_tail<kF32>(x, off, ok ? K - ku : 0, w[u]);
+    }
+  }
+}
+
+template <bool kF32>
+__global__ void __launch_bounds__(kWarpsPerBlock * 32, kBlocksPerSm)
     group_quant_kernel(const void* __restrict__ x, int64_t M, int64_t K, int64_t ld_x,
                        uint8_t* __restrict__ q, int64_t ld_q, float* __restrict__ s,
                        int32_t col_major, int64_t ld_s, int32_t vec_x, int32_t vec_q) {
   using S = QuantShape<kF32>;
   constexpr int EPL = S::kEPL, LPG = S::kLPG, GPW = S::kGPW;
-  // chunk indices fit in 32 bits (the host checks M * chunks_per_row < 2^31),
-  // so the row / chunk split is a 32-bit division, not a 64-bit one
   const uint32_t G = static_cast<uint32_t>((K + 127) / 128);
-  const uint32_t chunks_per_row = (G + GPW - 1) / GPW;
-  const uint32_t total = static_cast<uint32_t>(M) * chunks_per_row;
+  const uint32_t Mu = static_cast<uint32_t>(M);
   const int lane = threadIdx.x & 31;
   const int gi = lane / LPG;       // group within the warp step
   const int li = lane % LPG;       // lane within the group
   const uint32_t warp0 = blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
   const uint32_t nwarps = gridDim.x * kWarpsPerBlock;
+  ChunkWalk cur, nxt;
+  cur.init(warp0, nwarps, (G + GPW - 1) / GPW);
   // x may come from the kernel before this one; once it is visible, the next
   // kernel (the GEMM, which waits for this grid before reading q and s) may
   // start its prologue
   griddep_wait();
   griddep_launch_dependents();
 
-  for (uint32_t base = warp0; base < total; base += nwarps * kUnroll) {
-    float v[kUnroll][EPL];
-    int64_t row[kUnroll], k[kUnroll], g[kUnroll];
-    bool valid[kUnroll];
+  // software pipeline: the next batch's loads are in flight while this one
+  // is quantised and stored
+  uint32_t w[kUnroll][4];
+  load_batch<kF32>(x, cur, Mu, G, K, ld_x, vec_x, gi, li, w);
+  while (cur.rw[0] < Mu) {
+    nxt = cur;
+    nxt.advance();
+    uint32_t wn[kUnroll][4];
+    if (nxt.rw[0] < Mu) load_batch<kF32>(x, nxt, Mu, G, K, ld_x, vec_x, gi, li, wn);
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u) {
-      const uint32_t c = base + u * nwarps;
-      const uint32_t rr = c / chunks_per_row;
-      row[u] = rr;
-      g[u] = static_cast<int64_t>(c - rr * chunks_per_row) * GPW + gi;
-      k[u] = g[u] * 128 + li * EPL;
-      valid[u] = (c < total) && (g[u] < G);
-      if (valid[u] && vec_x && k[u] + EPL <= K) {
-        load_vec<kF32>(x, row[u] * ld_x + k[u], v[u]);
-      } else {
-#pragma unroll
-        for (int e = 0; e < EPL; ++e)
-          v[u][e] = (valid[u] && k[u] + e < K) ? load_elem<kF32>(x, row[u] * ld_x + k[u] + e) : 0.f;
-      }
-    }
-#pragma unroll
-    for (int u = 0; u < kUnroll; ++u) {
+      const uint32_t gu = cur.cl[u] * GPW + gi;
+      const int64_t ku = static_cast<int64_t>(gu) * 128 + li * EPL;
+      const bool valid = cur.rw[u] < Mu && gu < G;
+      float v[EPL];
+      unpack<kF32>(w[u], v);
       float amax = 0.f;
 #pragma unroll
-      for (int e = 0; e < EPL; ++e) amax = fmaxf(amax, fabsf(v[u][e]));
+      for (int e = 0; e < EPL; ++e) amax = fmaxf(amax, fabsf(v[e]));
 #pragma unroll
       for (int off = LPG / 2; off > 0; off >>= 1)
         amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
-      if (!valid[u]) continue;
       const float scale = __fdiv_rn(fmaxf(amax, 1e-10f), 448.0f);
-      const float rcp = __frcp_rn(scale);
+      // The code of fl32(x / scale) without dividing.  With r = rcp_approx(scale)
+      // (relative error <= 2^-23), r_lo = RN(r (1 - 2^-19)) and r_hi =
+      // RN(r (1 + 2^-19)), the products y_lo = RN(x r_lo) and y_hi = RN(x r_hi)
+      // differ from x / scale by a factor within (1 - 2^-19 +- 2^-21) and
+      // (1 + 2^-19 +- 2^-21), while fl32(x / scale) is within a factor
+      // 1 +- 2^-24 of it, so fl32(x / scale) lies strictly between y_lo and
+      // y_hi (for |x / scale| >= 2^-126; below that all three give e4m3 +-0).
+      // Rounding to e4m3 (nearest-even, saturating) is monotone, so when y_lo
+      // and y_hi get the same code, that is the code of fl32(x / scale).  Only
+      // when an e4m3 rounding boundary falls in the 2^-18 wide bracket (about
+      // once in 30000 elements) is the IEEE division done.
+      const float r = rcp_approx(scale);
+      const float r_lo = __fmul_rn(r, 1.0f - 0x1p-19f);
+      const float r_hi = __fmul_rn(r, 1.0f + 0x1p-19f);
       uint16_t pk[EPL / 2];
+      bool need = false;
 #pragma unroll
-      for (int e = 0; e < EPL; e += 2)
-        pk[e / 2] = cvt_e4m3x2(quotient_for_e4m3(v[u][e], scale, rcp),
-                               quotient_for_e4m3(v[u][e + 1], scale, rcp));
-      uint8_t* qrow = q + row[u] * ld_q;
-      if (vec_q && k[u] + EPL <= K) {
+      for (int e = 0; e < EPL; e += 2) {
+        const uint16_t lo = cvt_e4m3x2(__fmul_rn(v[e], r_lo), __fmul_rn(v[e + 1], r_lo));
+        const uint16_t hi = cvt_e4m3x2(__fmul_rn(v[e], r_hi), __fmul_rn(v[e + 1], r_hi));
+        pk[e / 2] = lo;
+        need |= lo != hi;
+      }
+      // warp-uniform branch: the IEEE divisions run only in warps that need them
+      if (__any_sync(0xffffffffu, need)) {
+        if (need) {
+#pragma unroll
+          for (int e = 0; e < EPL; e += 2)
+            pk[e / 2] = cvt_e4m3x2(__fdiv_rn(v[e], scale), __fdiv_rn(v[e + 1], scale));
+        }
+      }
+      if (!valid) continue;
+      uint8_t* qrow = q + static_cast<int64_t>(cur.rw[u]) * ld_q;
+      if (vec_q && ku + EPL <= K) {
         if constexpr (kF32) {
-          *reinterpret_cast<uint32_t*>(qrow + k[u]) =
+          *reinterpret_cast<uint32_t*>(qrow + ku) =
               static_cast<uint32_t>(pk[0]) | (static_cast<uint32_t>(pk[1]) << 16);
         } else {
-          uint2 w;
-          w.x = static_cast<uint32_t>(pk[0]) | (static_cast<uint32_t>(pk[1]) << 16);
-          w.y = static_cast<uint32_t>(pk[2]) | (static_cast<uint32_t>(pk[3]) << 16);
-          *reinterpret_cast<uint2*>(qrow + k[u]) = w;
+          uint2 wq;
+          wq.x = static_cast<uint32_t>(pk[0]) | (static_cast<uint32_t>(pk[1]) << 16);
+          wq.y = static_cast<uint32_t>(pk[2]) | (static_cast<uint32_t>(pk[3]) << 16);
+          *reinterpret_cast<uint2*>(qrow + ku) = wq;
         }
       } else {
 #pragma unroll
         for (int e = 0; e < EPL; ++e)
-          if (k[u] + e < K) qrow[k[u] + e] = static_cast<uint8_t>(pk[e / 2] >> (8 * (e & 1)));
+          if (ku + e < K) qrow[ku + e] = static_cast<uint8_t>(pk[e / 2] >> (8 * (e & 1)));
       }
       if (li == 0) {
-        if (col_major) s[g[u] * ld_s + row[u]] = scale;
-        else s[row[u] * ld_s + g[u]] = scale;
+        if (col_major) s[static_cast<int64_t>(gu) * ld_s + cur.rw[u]] = scale;
+        else s[static_cast<int64_t>(cur.rw[u]) * ld_s + gu] = scale;
       }
     }
+    cur = nxt;
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) w[u][i] = wn[u][i];
   }
 }
 
@@ -186,8 +274,10 @@ cudaError_t launch_group_quant(const void* x, int in_f32, int64_t M, int64_t K, 
   const int64_t total = M * ((G + gpw - 1) / gpw);
   if (total >= (int64_t{1} << 31) - static_cast<int64_t>(num_sms) * 8 * kWarpsPerBlock * kUnroll)
     return cudaErrorInvalidValue;
+  // one wave of persistent blocks (each warp then walks many chunks, which
+  // keeps its software pipeline full)
   int64_t blocks = (total + kWarpsPerBlock - 1) / kWarpsPerBlock;
-  const int64_t cap = static_cast<int64_t>(num_sms) * 8;
+  const int64_t cap = static_cast<int64_t>(num_sms) * kBlocksPerSm;
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
   cudaLaunchConfig_t cfg{};
