@@ -54,8 +54,8 @@ def parse_args():
     p.add_argument("--nk", type=int, default=NK, help="N = K")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
-    p.add_argument("--cpu-budget-s", type=float, default=20.0,
-                   help="CPU seconds for the oracle baseline sample")
+    p.add_argument("--cpu-budget-s", type=float, default=12.0,
+                   help="wall seconds (on all host cores) for the oracle baseline sample")
     return p.parse_args()
 
 
@@ -209,8 +209,8 @@ def barrier(world: int):
 
 def oracle_sample(Ms, nk, budget_s, seed=1234):
     """Times the oracle (quantise + blocked GEMM, all host cores) on the first
-    rows of each M in the sweep, sized to about `budget_s` seconds of CPU work.
-    Returns (flops, seconds, cores, description)."""
+    rows of each M in the sweep, sized to about `budget_s` seconds of wall time
+    on those cores.  Returns (flops, seconds, cores, description)."""
     import numpy as np
     import oracle
     from block_scaled_fp8_02_gb300 import workloads as wl
@@ -225,8 +225,12 @@ def oracle_sample(Ms, nk, budget_s, seed=1234):
     t0 = time.perf_counter()
     oracle.blocked_gemm(A1, B, As1, True, Bs, threads=1)
     per_row_cpu = max(time.perf_counter() - t0, 1e-4)
-    rows_total = max(len(Ms), int(budget_s / per_row_cpu))
-    per_m = max(1, rows_total // len(Ms))
+    # rows the cores get through in the budget, spread evenly over the M
+    # values (small M values take all their rows; the rest go to larger ones)
+    rows_total = max(len(Ms), int(budget_s * cores / per_row_cpu))
+    per_m = 1
+    while per_m < max(Ms) and sum(min(M, per_m + 1) for M in Ms) <= rows_total:
+        per_m += 1
     flops, secs, n_rows = 0.0, 0.0, 0
     import torch
     for M in Ms:
@@ -552,7 +556,7 @@ def run_reference(args, rank, world):
     cores = None
     desc = None
     for i in range(total_steps):
-        fl, secs, cores, desc = oracle_sample(Ms, nk, budget_per_step * (cores or 1), seed=99 + i)
+        fl, secs, cores, desc = oracle_sample(Ms, nk, budget_per_step, seed=99 + i)
         if i >= args.warmup:
             times.append(secs)
             flops_list.append(fl)
