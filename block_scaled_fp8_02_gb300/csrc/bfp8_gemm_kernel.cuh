@@ -116,8 +116,13 @@ struct GemmCfg {
   static constexpr int kSlotFloats = kAsFloats + 4 * kBsChunks;
   static constexpr int kScaleBytes = kSR * kSlotFloats * 4;
   static constexpr int kSmemLimit = 232448;      // 227 KB per CTA
+  // Wide tiles stage each promotion warp's bf16 output through shared memory,
+  // 32 rows x 32 columns at a time (rows padded to 80 bytes: conflict-free),
+  // so that global stores write whole 32-byte sectors along a row.
+  static constexpr int kOutPitch = 80;
+  static constexpr int kOutBytes = SWAP ? 0 : kNE * 32 * kOutPitch;
   static constexpr int kStagesFit =
-      (kSmemLimit - 1024 /*align*/ - 384 /*barriers*/ - kScaleBytes) / kStageBytes;
+      (kSmemLimit - 1024 /*align*/ - 384 /*barriers*/ - kScaleBytes - kOutBytes) / kStageBytes;
   static constexpr int kStages = kStagesFit > 10 ? 10 : kStagesFit;
   static_assert(kStages >= 2, "ring too small");
   // barriers: full, empty [kStages]; sfull, sempty [kSR]; tfull, tempty [2]
@@ -125,7 +130,8 @@ struct GemmCfg {
   static constexpr int kOffTmemPtr = kOffBars + (2 * kStages + 2 * kSR + 4) * 8;
   static constexpr int kOffFlags = kOffTmemPtr + 8;
   static constexpr int kOffScale = (kOffFlags + 8 + 15) / 16 * 16;
-  static constexpr int kSmemBytes = kOffScale + kScaleBytes + 1024;
+  static constexpr int kOffOut = (kOffScale + kScaleBytes + 127) / 128 * 128;
+  static constexpr int kSmemBytes = kOffOut + kOutBytes + 1024;
   // one CTA per SM (the planner's cluster capacities assume it)
   static_assert(2 * kSmemBytes > kSmemLimit + 1024, "two CTAs would fit on one SM");
   static constexpr int kTmemCols = tmem_cols_for(2 * BN);
@@ -597,7 +603,35 @@ __global__ void __launch_bounds__(GemmCfg<BN, SWAP>::kThreads, 1)
         if (etid == 0) a.counters[ts] = 0;  // every contributor has arrived
       }
 
-      if (!SWAP) {
+      if (!SWAP && a.vec_store) {
+        // rows of 16-byte-aligned bf16 (N % 8 == 0): through this warp's
+        // staging rows, 32 columns at a time; lanes 4i..4i+3 then store one
+        // row's 64 contiguous bytes
+        uint8_t* stg = smem + C::kOffOut + warp * (32 * C::kOutPitch);
+        const int64_t mrow0 = static_cast<int64_t>(cur.p_tile) * 128 + quad * 32;
+        const int64_t nbase = static_cast<int64_t>(cur.q_tile) * BN + col0;
+#pragma unroll
+        for (int ch = 0; ch < C::kCPT; ch += 32) {
+#pragma unroll
+          for (int g = 0; g < 4; ++g) {
+            const float* f = acc + ch + 8 * g;
+            *reinterpret_cast<uint4*>(stg + lane * C::kOutPitch + 16 * g) =
+                make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]),
+                           pack_bf16x2(f[4], f[5]), pack_bf16x2(f[6], f[7]));
+          }
+          __syncwarp();
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int pce = i * 32 + lane;
+            const int row = pce >> 2, c16 = pce & 3;
+            const uint4 w = *reinterpret_cast<const uint4*>(stg + row * C::kOutPitch + 16 * c16);
+            const int64_t m = mrow0 + row;
+            const int64_t n = nbase + ch + 8 * c16;
+            if (m < a.M && n < a.N) st_global_v4(a.out + m * a.N + n, w.x, w.y, w.z, w.w);
+          }
+          __syncwarp();
+        }
+      } else if (!SWAP) {
         const int64_t m = static_cast<int64_t>(cur.p_tile) * 128 + r;
         if (m < a.M) {
           __nv_bfloat16* row = a.out + m * a.N;
