@@ -502,11 +502,20 @@ __global__ void __launch_bounds__(GemmCfg<BN, SWAP>::kThreads, 1)
         for (int h = 0; h < C::kBatch; h += C::kCH) tmem_ld_cols<C::kCH>(taddr + c0 + h, v + h);
         tmem_wait_ld();
         reg_fence<C::kBatch>(v);
-        // element (row r, column c) gets scale sr (wide) or sr * As[c] (swap)
+        // element (row r, column c) gets scale sr (wide) or sr * As[c] (swap);
+        // two columns per packed fp32x2 FMA (one instruction, two IEEE FMAs)
+        const uint64_t sr2 = pack_u32x2(__float_as_uint(sr), __float_as_uint(sr));
 #pragma unroll
-        for (int i = 0; i < C::kBatch; ++i) {
-          const float sc = SWAP ? sr * sq[c0 + i] : sr;
-          acc[c0 + i] = fmaf(__uint_as_float(v[i]), sc, acc[c0 + i]);
+        for (int i = 0; i < C::kBatch; i += 2) {
+          uint64_t sc2 = sr2;
+          if (SWAP) {
+            const float2 q2 = *reinterpret_cast<const float2*>(sq + c0 + i);
+            sc2 = mul_f32x2(sr2, pack_u32x2(__float_as_uint(q2.x), __float_as_uint(q2.y)));
+          }
+          const uint64_t a2 =
+              pack_u32x2(__float_as_uint(acc[c0 + i]), __float_as_uint(acc[c0 + i + 1]));
+          unpack_f32x2(fma_f32x2(pack_u32x2(v[i], v[i + 1]), sc2, a2), acc[c0 + i],
+                       acc[c0 + i + 1]);
         }
       }
       // every lane's TMEM reads are complete (wait::ld above); order them before
