@@ -279,7 +279,10 @@ __global__ void __launch_bounds__(GemmCfg<BN, SWAP>::kThreads, 1)
   // Everything above overlaps the tail of the preceding kernel in the stream
   // (programmatic dependent launch).  Global memory that kernel may have
   // written (A, As, the workspace; B and Bs unless prefetch_b) is touched only
-  // after this wait; the producer waits inside its loop instead.
+  // after this wait; the producer waits inside its loop instead.  The next
+  // kernel may be launched now: it reads what this one writes only after its
+  // own wait, which returns when this grid has completed.
+  if (threadIdx.x == 0) griddep_launch_dependents();
   if (warp != C::kNE) griddep_wait();
   constexpr uint32_t kTmemSyncThreads = (C::kNE + 1) * 32;
   uint32_t tmem = 0;

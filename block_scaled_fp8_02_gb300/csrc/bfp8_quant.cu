@@ -170,11 +170,12 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32, kBlocksPerSm)
   const uint32_t nwarps = gridDim.x * kWarpsPerBlock;
   ChunkWalk cur, nxt;
   cur.init(warp0, nwarps, (G + GPW - 1) / GPW);
-  // x may come from the kernel before this one; once it is visible, the next
-  // kernel (the GEMM, which waits for this grid before reading q and s) may
-  // start its prologue
-  griddep_wait();
+  // The next kernel (the GEMM, which waits for this grid to complete before
+  // reading q and s) may be launched at once, so that its prologue and weight
+  // prefetch overlap this kernel; x may come from the kernel before this one,
+  // so nothing is read before the wait.
   griddep_launch_dependents();
+  griddep_wait();
 
   // software pipeline: the next batch's loads are in flight while this one
   // is quantised and stored
