@@ -29,7 +29,8 @@ STATUS_NAMES = {0: "BFP8_OK", 1: "BFP8_ERR_INVALID_ARG", 2: "BFP8_ERR_ALIGNMENT"
 EXPORTS = ("bfp8_group_quant", "bfp8_scale_ld", "bfp8_gemm", "bfp8_gemm_ex",
            "bfp8_gemm_workspace_size", "bfp8_gemm_plan", "bfp8_plan_unit", "bfp8_last_error",
            "bfp8_status_string", "bfp8_device_status", "bfp8_selftest_bounded_wait",
-           "bfp8_version", "bfp8_gemm_noalloc")
+           "bfp8_version", "bfp8_gemm_noalloc", "bfp8_gemm_grouped",
+           "bfp8_gemm_grouped_workspace_size")
 
 
 class BFP8Error(RuntimeError):
@@ -97,6 +98,13 @@ def lib():
             L.bfp8_version.argtypes = []
             L.bfp8_gemm_noalloc.restype = i32
             L.bfp8_gemm_noalloc.argtypes = [P, P, P, i32, i64, P, P, i64, i64, i64, P]
+            L.bfp8_gemm_grouped.restype = i32
+            L.bfp8_gemm_grouped.argtypes = [P, P, P, i32, i64, P, P, i32, P, i64, i64, i64, P, sz,
+                                            ctypes.POINTER(GemmOptions), P]
+            L.bfp8_gemm_grouped_workspace_size.restype = i32
+            L.bfp8_gemm_grouped_workspace_size.argtypes = [i64, i64, i64, i32,
+                                                           ctypes.POINTER(GemmOptions), i32,
+                                                           ctypes.POINTER(sz)]
             _lib = L
     return _lib
 
@@ -262,6 +270,55 @@ def bfp8_gemm(A: torch.Tensor, B: torch.Tensor, As: torch.Tensor, Bs: torch.Tens
                             workspace.numel() * workspace.element_size(), _opts(options),
                             _stream_ptr(stream))
     _check(st, "bfp8_gemm")
+    return out
+
+
+def bfp8_gemm_grouped_workspace_size(M: int, N: int, K: int, num_experts: int, options=None,
+                                     operands_unaligned: bool = False) -> int:
+    n = ctypes.c_size_t(0)
+    _check(lib().bfp8_gemm_grouped_workspace_size(M, N, K, num_experts, _opts(options),
+                                                  int(operands_unaligned), ctypes.byref(n)),
+           "bfp8_gemm_grouped_workspace_size")
+    return int(n.value)
+
+
+def bfp8_gemm_grouped(A: torch.Tensor, B: torch.Tensor, As: torch.Tensor, Bs: torch.Tensor,
+                      grouped_layout: torch.Tensor, out: torch.Tensor | None = None,
+                      workspace: torch.Tensor | None = None, options=None,
+                      stream=None) -> torch.Tensor:
+    """M-grouped (mixture-of-experts) blocked-FP8 GEMM: A [M, K] rows grouped by
+    expert in 128-aligned blocks, B [E, N, K], Bs [E, ceil(N/128), G],
+    grouped_layout int32 [E] = cumulative aligned row counts (device).  Rows
+    past the last expert's block are left untouched in `out`."""
+    if A.dtype != torch.float8_e4m3fn or B.dtype != torch.float8_e4m3fn:
+        raise ValueError("A and B must be float8_e4m3fn")
+    if B.dim() != 3:
+        raise ValueError("B must be [experts, N, K]")
+    if not (A.is_contiguous() and B.is_contiguous() and Bs.is_contiguous()
+            and grouped_layout.is_contiguous()):
+        raise ValueError("A, B, Bs and grouped_layout must be contiguous")
+    M, K = A.shape
+    E, N, K2 = B.shape
+    if K2 != K:
+        raise ValueError("A and B disagree on K")
+    G = (K + 127) // 128
+    if Bs.shape != (E, (N + 127) // 128, G) or Bs.dtype != torch.float32:
+        raise ValueError(f"Bs must be float32 of shape {(E, (N + 127) // 128, G)}")
+    if grouped_layout.dtype != torch.int32 or grouped_layout.shape != (E,):
+        raise ValueError(f"grouped_layout must be int32 of shape ({E},)")
+    col, ld = _as_layout(As, M, G)
+    if out is None:
+        out = torch.zeros((M, N), dtype=torch.bfloat16, device=A.device)
+    unaligned = (A.data_ptr() % 16 != 0) or (B.data_ptr() % 16 != 0)
+    if workspace is None:
+        need = bfp8_gemm_grouped_workspace_size(M, N, K, E, options, unaligned)
+        workspace = workspace_for(need, A.device)
+    st = lib().bfp8_gemm_grouped(A.data_ptr(), B.data_ptr(), As.data_ptr(), col, ld,
+                                 Bs.data_ptr(), grouped_layout.data_ptr(), E, out.data_ptr(),
+                                 M, N, K, workspace.data_ptr(),
+                                 workspace.numel() * workspace.element_size(), _opts(options),
+                                 _stream_ptr(stream))
+    _check(st, "bfp8_gemm_grouped")
     return out
 
 

@@ -265,8 +265,9 @@ constexpr int64_t kSwapMaxM = 256;
 constexpr size_t kCounterHeaderBytes = 16384;   // 4096 stream-K tile counters
 
 // `cap` = co-resident clusters of each size (nullptr: estimated from num_sms).
+// `experts` > 1: M-grouped mode, B and Bs hold that many experts' weights.
 bfp8_status make_plan(int64_t M, int64_t N, int64_t K, int num_sms, const bfp8_gemm_options* opt,
-                      bool unaligned, const int* cap, Plan* p) {
+                      bool unaligned, const int* cap, Plan* p, int64_t experts = 1) {
   const int schedule = opt ? opt->schedule : BFP8_SCHEDULE_AUTO;
   p->swap = schedule == BFP8_SCHEDULE_SWAP_AB ||
             (schedule == BFP8_SCHEDULE_AUTO && M <= kSwapMaxM);
@@ -308,13 +309,13 @@ bfp8_status make_plan(int64_t M, int64_t N, int64_t K, int num_sms, const bfp8_g
   p->off_a = off;
   if (p->relayout) off += align256(static_cast<size_t>(M) * p->kp);
   p->off_b = off;
-  if (p->relayout) off += align256(static_cast<size_t>(N) * p->kp);
+  if (p->relayout) off += align256(static_cast<size_t>(experts * N) * p->kp);
   // room for the scales in the kernel's layout (used when the caller's As is
   // row-major or not 16-byte aligned, or Bs does not meet the 16-byte rules)
   p->off_as = off;
   off += align256(static_cast<size_t>(G) * static_cast<size_t>(cdiv(M, 4) * 4) * sizeof(float));
   p->off_bs = off;
-  off += align256(static_cast<size_t>(cdiv(N, 128) * G + 4) * sizeof(float));
+  off += align256(static_cast<size_t>(experts * cdiv(N, 128) * G + 4) * sizeof(float));
   p->total = off;
   return BFP8_OK;
 }
@@ -503,13 +504,25 @@ bfp8_status bfp8_gemm_workspace_size(int64_t M, int64_t N, int64_t K,
   return ok();
 }
 
-bfp8_status bfp8_gemm_ex(const void* A, const void* B, const float* As, int as_col_major,
-                         int64_t ld_as, const float* Bs, void* out, int64_t M, int64_t N,
-                         int64_t K, void* workspace, size_t workspace_bytes,
-                         const bfp8_gemm_options* opt, void* stream) {
+// The GEMM proper, plain (psum == nullptr) or M-grouped over `experts` experts
+// (internal linkage: not part of the exported interface).
+static bfp8_status gemm_impl(const void* A, const void* B, const float* As, int as_col_major,
+                             int64_t ld_as, const float* Bs, const int32_t* psum,
+                             int64_t experts, void* out, int64_t M, int64_t N, int64_t K,
+                             void* workspace, size_t workspace_bytes,
+                             const bfp8_gemm_options* opt_in, void* stream) {
   bfp8_status st = check_gemm_sizes(M, N, K);
   if (st != BFP8_OK) return st;
-  if ((st = check_options(opt)) != BFP8_OK) return st;
+  if ((st = check_options(opt_in)) != BFP8_OK) return st;
+  bfp8_gemm_options grouped_opt{};
+  const bfp8_gemm_options* opt = opt_in;
+  if (psum) {
+    // grouped mode runs the wide schedule (128 activation rows per tile, each
+    // tile inside one expert's aligned block)
+    if (opt_in) grouped_opt = *opt_in;
+    grouped_opt.schedule = BFP8_SCHEDULE_WIDE;
+    opt = &grouped_opt;
+  }
   if (!A || !B || !As || !Bs || !out)
     return fail(BFP8_ERR_INVALID_ARG, "null pointer (A=%p B=%p As=%p Bs=%p out=%p)", A, B,
                 (const void*)As, (const void*)Bs, out);
@@ -526,7 +539,8 @@ bfp8_status bfp8_gemm_ex(const void* A, const void* B, const float* As, int as_c
   if ((st = current_device_with_caps(&d)) != BFP8_OK) return st;
   const bool unaligned = misaligned(A, 16) || misaligned(B, 16);
   Plan p;
-  if ((st = make_plan(M, N, K, d.sms, opt, unaligned, d.cluster_cap, &p)) != BFP8_OK) return st;
+  if ((st = make_plan(M, N, K, d.sms, opt, unaligned, d.cluster_cap, &p, experts)) != BFP8_OK)
+    return st;
   if (stream_k_tiles(p.sched) > static_cast<int64_t>(kCounterHeaderBytes / sizeof(int)))
     return fail(BFP8_ERR_UNSUPPORTED, "more stream-K tiles than the workspace header holds");
   if (p.total > 0) {
@@ -545,7 +559,8 @@ bfp8_status bfp8_gemm_ex(const void* A, const void* B, const float* As, int as_c
   if (p.relayout) {
     cudaError_t e = launch_relayout(static_cast<const uint8_t*>(A), M, K, ws + p.off_a, p.kp, d.sms, cs);
     if (e == cudaSuccess)
-      e = launch_relayout(static_cast<const uint8_t*>(B), N, K, ws + p.off_b, p.kp, d.sms, cs);
+      e = launch_relayout(static_cast<const uint8_t*>(B), experts * N, K, ws + p.off_b, p.kp, d.sms,
+                          cs);
     if (e != cudaSuccess) return fail(BFP8_ERR_CUDA, "operand re-layout launch: %s", cudaGetErrorString(e));
     a_op = ws + p.off_a;
     b_op = ws + p.off_b;
@@ -553,7 +568,7 @@ bfp8_status bfp8_gemm_ex(const void* A, const void* B, const float* As, int as_c
   // scales in the layout the kernel bulk-copies
   const int64_t NTv = cdiv(N, 128);
   const bool as_ok = as_col_major && ld_as % 4 == 0 && !misaligned(As, 16);
-  const bool bs_ok = !misaligned(Bs, 16) && (NTv * G) % 4 == 0;
+  const bool bs_ok = !misaligned(Bs, 16) && (experts * NTv * G) % 4 == 0;
   const float* as_k = As;
   int64_t ld_k = ld_as;
   const float* bs_k = Bs;
@@ -562,7 +577,7 @@ bfp8_status bfp8_gemm_ex(const void* A, const void* B, const float* As, int as_c
     float* bs_out = bs_ok ? nullptr : reinterpret_cast<float*>(ws + p.off_bs);
     const int64_t ld_out = cdiv(M, 4) * 4;
     cudaError_t e = launch_scale_relayout(As, as_col_major, ld_as, M, G, as_out, ld_out, Bs,
-                                          NTv * G, bs_out, d.sms, cs);
+                                          experts * NTv * G, bs_out, d.sms, cs);
     if (e != cudaSuccess) return fail(BFP8_ERR_CUDA, "scale re-layout launch: %s", cudaGetErrorString(e));
     if (as_out) { as_k = as_out; ld_k = ld_out; }
     if (bs_out) bs_k = bs_out;
@@ -571,7 +586,7 @@ bfp8_status bfp8_gemm_ex(const void* A, const void* B, const float* As, int as_c
   const void* p_ptr = p.swap ? b_op : a_op;
   const void* q_ptr = p.swap ? a_op : b_op;
   const int64_t p_rows = p.swap ? N : M;
-  const int64_t q_rows = p.swap ? M : N;
+  const int64_t q_rows = p.swap ? M : experts * N;
   if ((st = encode_operand(&tmP, p_ptr, p_rows, p.kp, 128)) != BFP8_OK) return st;
   if ((st = encode_operand(&tmQ, q_ptr, q_rows, p.kp, p.bn)) != BFP8_OK) return st;
 
@@ -587,8 +602,11 @@ bfp8_status bfp8_gemm_ex(const void* A, const void* B, const float* As, int as_c
   a.counters = reinterpret_cast<int*>(ws ? ws + p.off_counters : nullptr);
   a.partials = reinterpret_cast<float*>(ws ? ws + p.off_partials : nullptr);
   a.vec_store = (!misaligned(out, 16) && (N % 8) == 0) ? 1 : 0;
-  // weight prefetch also needs the weight operand untouched by re-layout
-  a.prefetch_b = (opt && opt->prefetch_weights == 1 && !p.relayout && bs_ok) ? 1 : 0;
+  // weight prefetch also needs the weight operand untouched by re-layout (and,
+  // in grouped mode, the expert of each tile, known only after the wait)
+  a.prefetch_b = (opt && opt->prefetch_weights == 1 && !p.relayout && bs_ok && !psum) ? 1 : 0;
+  a.psum = psum;
+  a.experts = static_cast<int32_t>(experts);
   a.err = d.err;
   a.wait_limit = kWaitLimitCycles;
   a.trace = nullptr;
@@ -601,6 +619,61 @@ bfp8_status bfp8_gemm_ex(const void* A, const void* B, const float* As, int as_c
 #endif
   cudaError_t e = p.swap ? launch_gemm_swap(p.bn, tmP, tmQ, a, cs) : launch_gemm_wide(p.bn, tmP, tmQ, a, cs);
   if (e != cudaSuccess) return fail(BFP8_ERR_CUDA, "GEMM launch: %s", cudaGetErrorString(e));
+  return ok();
+}
+
+bfp8_status bfp8_gemm_ex(const void* A, const void* B, const float* As, int as_col_major,
+                         int64_t ld_as, const float* Bs, void* out, int64_t M, int64_t N,
+                         int64_t K, void* workspace, size_t workspace_bytes,
+                         const bfp8_gemm_options* opt, void* stream) {
+  return gemm_impl(A, B, As, as_col_major, ld_as, Bs, nullptr, 1, out, M, N, K, workspace,
+                   workspace_bytes, opt, stream);
+}
+
+static bfp8_status check_grouped(const int32_t* grouped_layout, int num_experts, int64_t N, int64_t K) {
+  if (num_experts < 1 || num_experts > kMaxExperts)
+    return fail(BFP8_ERR_INVALID_ARG, "num_experts = %d (expected 1..%d)", num_experts, kMaxExperts);
+  if (!grouped_layout) return fail(BFP8_ERR_INVALID_ARG, "grouped_layout is null");
+  if (misaligned(grouped_layout, 4))
+    return fail(BFP8_ERR_ALIGNMENT, "grouped_layout must be 4-byte aligned");
+  const int64_t G = cdiv(K, 128);
+  if (static_cast<int64_t>(num_experts) * N >= (int64_t{1} << 31) ||
+      static_cast<int64_t>(num_experts) * cdiv(N, 128) * G >= (int64_t{1} << 31))
+    return fail(BFP8_ERR_UNSUPPORTED, "num_experts x N too large");
+  return BFP8_OK;
+}
+
+bfp8_status bfp8_gemm_grouped(const void* A, const void* B, const float* As, int as_col_major,
+                              int64_t ld_as, const float* Bs, const int32_t* grouped_layout,
+                              int num_experts, void* out, int64_t M, int64_t N, int64_t K,
+                              void* workspace, size_t workspace_bytes,
+                              const bfp8_gemm_options* opt, void* stream) {
+  bfp8_status st = check_gemm_sizes(M, N, K);
+  if (st != BFP8_OK) return st;
+  if ((st = check_grouped(grouped_layout, num_experts, N, K)) != BFP8_OK) return st;
+  return gemm_impl(A, B, As, as_col_major, ld_as, Bs, grouped_layout, num_experts, out, M, N, K,
+                   workspace, workspace_bytes, opt, stream);
+}
+
+bfp8_status bfp8_gemm_grouped_workspace_size(int64_t M, int64_t N, int64_t K, int num_experts,
+                                             const bfp8_gemm_options* opt,
+                                             int operands_unaligned, size_t* bytes) {
+  bfp8_status st = check_gemm_sizes(M, N, K);
+  if (st != BFP8_OK) return st;
+  if ((st = check_options(opt)) != BFP8_OK) return st;
+  if (num_experts < 1 || num_experts > kMaxExperts)
+    return fail(BFP8_ERR_INVALID_ARG, "num_experts = %d (expected 1..%d)", num_experts, kMaxExperts);
+  if (!bytes) return fail(BFP8_ERR_INVALID_ARG, "bytes is null");
+  DevInfo d;
+  if ((st = current_device_with_caps(&d)) != BFP8_OK) return st;
+  bfp8_gemm_options g{};
+  if (opt) g = *opt;
+  g.schedule = BFP8_SCHEDULE_WIDE;
+  Plan p;
+  if ((st = make_plan(M, N, K, d.sms, &g, operands_unaligned != 0, d.cluster_cap, &p,
+                      num_experts)) != BFP8_OK)
+    return st;
+  *bytes = p.total;
   return ok();
 }
 

@@ -66,7 +66,28 @@ struct GemmArgs {
   unsigned long long wait_limit;  // cycles before a wait gives up
   unsigned long long* trace;      // milestone timestamps (trace builds only)
   int32_t prefetch_b;    // stream B tiles before the preceding grid completes
+  // M-grouped (MoE) mode, wide tiles only: B is [experts * N, K] and Bs
+  // [experts * NT, G]; rows [psum[e-1], psum[e]) use expert e (psum =
+  // cumulative per-expert row counts, each a multiple of 128); rows at or
+  // past psum[experts-1] are not stored.  psum == nullptr: one plain GEMM.
+  const int32_t* psum;
+  int32_t experts;
 };
+
+constexpr int kMaxExperts = 1024;   // psum entries cached in shared memory
+
+// Expert of the 128-row tile starting at row m0: the first e with psum[e] >
+// m0 (psum in shared memory); past the last expert, the last one (its
+// results are not stored).
+__device__ __forceinline__ uint32_t expert_of(const int32_t* spsum, int32_t experts, int64_t m0) {
+  int32_t lo = 0, hi = experts;
+  while (lo < hi) {
+    const int32_t mid = (lo + hi) >> 1;
+    if (static_cast<int64_t>(spsum[mid]) > m0) hi = mid;
+    else lo = mid + 1;
+  }
+  return static_cast<uint32_t>(lo < experts ? lo : experts - 1);
+}
 
 __host__ __device__ constexpr int tmem_cols_for(int n) {
   return n <= 32 ? 32 : n <= 64 ? 64 : n <= 128 ? 128 : n <= 256 ? 256 : 512;
@@ -121,8 +142,10 @@ struct GemmCfg {
   // so that global stores write whole 32-byte sectors along a row.
   static constexpr int kOutPitch = 80;
   static constexpr int kOutBytes = SWAP ? 0 : kNE * 32 * kOutPitch;
+  static constexpr int kPsumBytes = SWAP ? 0 : kMaxExperts * 4;   // grouped mode (wide)
   static constexpr int kStagesFit =
-      (kSmemLimit - 1024 /*align*/ - 384 /*barriers*/ - kScaleBytes - kOutBytes) / kStageBytes;
+      (kSmemLimit - 1024 /*align*/ - 384 /*barriers*/ - kScaleBytes - kOutBytes - kPsumBytes) /
+      kStageBytes;
   static constexpr int kStages = kStagesFit > 10 ? 10 : kStagesFit;
   static_assert(kStages >= 2, "ring too small");
   // barriers: full, empty [kStages]; sfull, sempty [kSR]; tfull, tempty [2]
@@ -131,7 +154,8 @@ struct GemmCfg {
   static constexpr int kOffFlags = kOffTmemPtr + 8;
   static constexpr int kOffScale = (kOffFlags + 8 + 15) / 16 * 16;
   static constexpr int kOffOut = (kOffScale + kScaleBytes + 127) / 128 * 128;
-  static constexpr int kSmemBytes = kOffOut + kOutBytes + 1024;
+  static constexpr int kOffPsum = kOffOut + kOutBytes;
+  static constexpr int kSmemBytes = kOffPsum + kPsumBytes + 1024;
   // one CTA per SM (the planner's cluster capacities assume it)
   static_assert(2 * kSmemBytes > kSmemLimit + 1024, "two CTAs would fit on one SM");
   static constexpr int kTmemCols = tmem_cols_for(2 * BN);
@@ -284,6 +308,15 @@ __global__ void __launch_bounds__(GemmCfg<BN, SWAP>::kThreads, 1)
   // own wait, which returns when this grid has completed.
   if (threadIdx.x == 0) griddep_launch_dependents();
   if (warp != C::kNE) griddep_wait();
+  const int32_t* spsum = reinterpret_cast<const int32_t*>(smem + C::kOffPsum);
+  if (!SWAP && a.psum != nullptr) {
+    // grouped mode: every role looks experts up from a shared-memory copy of
+    // psum (written by an earlier kernel, so read after the wait)
+    griddep_wait();
+    int32_t* dst = reinterpret_cast<int32_t*>(smem + C::kOffPsum);
+    for (int i = threadIdx.x; i < a.experts; i += C::kThreads) dst[i] = __ldg(a.psum + i);
+    __syncthreads();
+  }
   constexpr uint32_t kTmemSyncThreads = (C::kNE + 1) * 32;
   uint32_t tmem = 0;
   if (warp == C::kNE + 1) {
@@ -329,8 +362,16 @@ __global__ void __launch_bounds__(GemmCfg<BN, SWAP>::kThreads, 1)
         }
       }
       griddep_wait();
+      uint32_t e_tile = 0xFFFFFFFFu, e_cur = 0;   // expert of the current p tile (grouped)
       for (; cur.valid(); cur.next()) {
         BFP8_CLK(c0);
+        if (!SWAP && a.psum != nullptr && cur.p_tile != e_tile) {
+          e_tile = cur.p_tile;
+          e_cur = expert_of(spsum, a.experts, static_cast<int64_t>(cur.p_tile) * 128);
+        }
+        // B rows of this tile's expert (grouped mode) start at e_cur * N
+        const int32_t q_row = static_cast<int32_t>(static_cast<int64_t>(e_cur) * a.N) +
+                              static_cast<int32_t>(cur.q_tile * BN);
         {
           if (!mbar_wait_bounded(bar_sempty(ss), sph ^ 1u, a.wait_limit)) {
             fail(kDevTimeoutProducer);
@@ -350,7 +391,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, SWAP>::kThreads, 1)
             int64_t nb = SWAP ? static_cast<int64_t>(cur.p_tile)
                               : static_cast<int64_t>(cur.q_tile) * (BN / 128) + h;
             if (nb >= a.NT) nb = a.NT - 1;             // block past N: any in-bounds value
-            const int64_t e = nb * s.G + kb;
+            const int64_t e = (static_cast<int64_t>(e_cur) * a.NT + nb) * s.G + kb;
             bulk_load(slot + 4u * (C::kAsFloats + 4 * h), a.Bs + (e & ~int64_t{3}), 16u,
                       bar_sfull(ss));
           }
@@ -372,7 +413,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, SWAP>::kThreads, 1)
         } else {
           mbar_arrive_expect_tx(bar_full(st), C::kStageBytes);
           tma_load_2d(stage_p(st), &tmP, bar_full(st), x, static_cast<int32_t>(cur.p_tile * 128));
-          tma_load_2d(stage_q(st), &tmQ, bar_full(st), x, static_cast<int32_t>(cur.q_tile * BN));
+          tma_load_2d(stage_q(st), &tmQ, bar_full(st), x, SWAP ? static_cast<int32_t>(cur.q_tile * BN) : q_row);
         }
         if (issued == 0) trace_event(a.trace, cta, kTrProdFirst);
         ++issued;
@@ -456,6 +497,10 @@ __global__ void __launch_bounds__(GemmCfg<BN, SWAP>::kThreads, 1)
 
     Cursor cur;
     cur.init(s, cta);
+    // rows that are stored: grouped mode stops at the end of the last expert
+    const int64_t m_lim =
+        (!SWAP && a.psum != nullptr && a.M > spsum[a.experts - 1]) ? spsum[a.experts - 1] : a.M;
+    uint32_t e_tile = 0xFFFFFFFFu, e_cur = 0;      // expert of the current p tile (grouped)
 
     unsigned long long t_ewait = 0, t_ework = 0, t_escale = 0, t_efix = 0;
     (void)t_ewait; (void)t_ework; (void)t_escale; (void)t_efix;
@@ -469,11 +514,16 @@ __global__ void __launch_bounds__(GemmCfg<BN, SWAP>::kThreads, 1)
       const float* slot = sRing + ss * C::kSlotFloats;
       float sr;                 // row scale (wide: As * Bs; swap: Bs)
       if (!SWAP) {
+        if (a.psum != nullptr && cur.p_tile != e_tile) {
+          e_tile = cur.p_tile;
+          e_cur = expert_of(spsum, a.experts, static_cast<int64_t>(cur.p_tile) * 128);
+        }
         const uint32_t hb = col0 / 128;         // this thread's 128-column weight block
         const uint32_t nb = cur.q_tile * (BN / 128) + hb;
-        const float bsv = nb < static_cast<uint32_t>(a.NT)
-                              ? slot[C::kAsFloats + 4 * hb + ((nb * s.G + cur.kb) & 3)]
-                              : 0.f;
+        const float bsv =
+            nb < static_cast<uint32_t>(a.NT)
+                ? slot[C::kAsFloats + 4 * hb + (((e_cur * a.NT + nb) * s.G + cur.kb) & 3)]
+                : 0.f;
         sr = slot[r] * bsv;
       } else {
         sr = slot[C::kAsFloats + ((cur.p_tile * s.G + cur.kb) & 3)];
@@ -639,13 +689,13 @@ __global__ void __launch_bounds__(GemmCfg<BN, SWAP>::kThreads, 1)
             const uint4 w = *reinterpret_cast<const uint4*>(stg + row * C::kOutPitch + 16 * c16);
             const int64_t m = mrow0 + row;
             const int64_t n = nbase + ch + 8 * c16;
-            if (m < a.M && n < a.N) st_global_v4(a.out + m * a.N + n, w.x, w.y, w.z, w.w);
+            if (m < m_lim && n < a.N) st_global_v4(a.out + m * a.N + n, w.x, w.y, w.z, w.w);
           }
           __syncwarp();
         }
       } else if (!SWAP) {
         const int64_t m = static_cast<int64_t>(cur.p_tile) * 128 + r;
-        if (m < a.M) {
+        if (m < m_lim) {
           __nv_bfloat16* row = a.out + m * a.N;
           const int64_t nbase = static_cast<int64_t>(cur.q_tile) * BN + col0;
 #pragma unroll
@@ -695,7 +745,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, SWAP>::kThreads, 1)
       const int64_t p0 = static_cast<int64_t>(p_tile) * 128;   // first row (TMEM lane)
       const int64_t q0 = static_cast<int64_t>(q_tile) * BN;    // first column
       const int64_t qlim = SWAP ? a.M : a.N;
-      const int64_t plim = SWAP ? a.N : a.M;
+      const int64_t plim = SWAP ? a.N : m_lim;
       const uint32_t qv = static_cast<uint32_t>(qlim - q0 < BN ? qlim - q0 : BN);
       const uint32_t pv = static_cast<uint32_t>(plim - p0 < 128 ? plim - p0 : 128);
       // swap: runs of 4 TMEM rows in each valid column; wide: runs of 4

@@ -113,3 +113,30 @@ def activations(M: int, K: int, seed: int, dist: str = "normal") -> torch.Tensor
 def e4m3_codes(N: int, K: int, seed: int) -> torch.Tensor:
     """Weights only, as e4m3 codes viewed as uint8."""
     return _weights_e4m3(N, K, _gen(seed)).view(torch.uint8)
+
+
+def grouped_case(counts, N: int, K: int, seed: int, extra_rows: int = 0):
+    """Mixture-of-experts inputs in the M-grouped contiguous layout: expert e
+    owns counts[e] token rows, padded to a multiple of 128 (padding rows are
+    zero activations); `extra_rows` rows past the last expert stand for the
+    caller's upper bound on the row count.  bf16 N(0,1) activations, e4m3
+    weights from U[-448, 448] per expert, weight scales U[1e-4, 1e-2).
+
+    Returns dict(M, N, K, E, x [M,K] bf16, B [E,N,K] e4m3, Bs [E,NT,G] f32,
+    psum [E] int32, valid [M] bool (rows that hold a token))."""
+    g = _gen(seed)
+    E = len(counts)
+    aligned = [cdiv(c, 128) * 128 for c in counts]
+    psum = torch.tensor(aligned, dtype=torch.int64).cumsum(0).to(torch.int32)
+    M = int(psum[-1]) + extra_rows
+    x = torch.zeros(M, K, dtype=torch.bfloat16)
+    valid = torch.zeros(M, dtype=torch.bool)
+    start = 0
+    for c, a in zip(counts, aligned):
+        if c:
+            x[start:start + c] = torch.randn(c, K, generator=g, dtype=torch.float32).to(torch.bfloat16)
+            valid[start:start + c] = True
+        start += a
+    B = torch.stack([_weights_e4m3(N, K, g) for _ in range(E)])
+    Bs = 1e-4 + torch.rand(E, cdiv(N, 128), cdiv(K, 128), generator=g) * (1e-2 - 1e-4)
+    return dict(M=M, N=N, K=K, E=E, x=x, B=B, Bs=Bs.float(), psum=psum, valid=valid)

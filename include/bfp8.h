@@ -209,6 +209,47 @@ bfp8_status bfp8_plan_unit(int64_t M, int64_t N, int64_t K, int num_sms,
                            int64_t* num_units, int64_t* tile, int64_t* k_block);
 
 /*
+ * bfp8_gemm_grouped -- the same blocked FP8 GEMM for a mixture-of-experts
+ * layer whose token rows are grouped by expert ("M-grouped contiguous"
+ * layout: the transformers DeepGEMM integration, `_build_deepgemm_contiguous_
+ * layout` and `deepgemm_fp8_fp4_experts_forward`, in its SM100 "psum" form).
+ *
+ *   A    [M, K] e4m3, row-major: rows sorted by expert, each expert's block
+ *        padded to a multiple of 128 rows (padding rows hold anything; their
+ *        outputs are computed and may be ignored).
+ *   As   activation scales as for bfp8_gemm.
+ *   B    [num_experts, N, K] e4m3, row-major (expert e's weights are rows
+ *        e*N .. e*N+N-1 of a [num_experts*N, K] matrix).
+ *   Bs   [num_experts, ceil(N/128), G] fp32, row-major.
+ *   grouped_layout  device int32 [num_experts]: cumulative sums of the
+ *        aligned per-expert row counts (grouped_layout[e] = end of expert e's
+ *        block); non-decreasing multiples of 128.  Device memory, read by the
+ *        kernel after the preceding kernel in the stream completes, so it may
+ *        be produced on the device just before the call.
+ *   out  [M, N] bf16: row m of expert e gets
+ *          out[m, n] = sum_kb (A[m,kb] . B[e,n,kb]) * As[m,kb] * Bs[e, n/128, kb];
+ *        rows m >= grouped_layout[num_experts-1] are not written (rows the
+ *        caller's upper bound on M reserved but no expert uses).
+ * Runs the wide schedule (128-row tiles, each inside one expert); options as
+ * for bfp8_gemm_ex except `schedule` (ignored) and `prefetch_weights`
+ * (ignored: the expert of a tile is known only after the wait).  Workspace
+ * from bfp8_gemm_grouped_workspace_size.  Requirements as for bfp8_gemm plus
+ * 1 <= num_experts <= 1024 and grouped_layout 4-byte aligned; its contents
+ * are not validated (a block not a multiple of 128 rows mixes experts in one
+ * tile and gives wrong results for its rows).
+ */
+bfp8_status bfp8_gemm_grouped(const void* A, const void* B, const float* As, int as_col_major,
+                              int64_t ld_as, const float* Bs, const int32_t* grouped_layout,
+                              int num_experts, void* out, int64_t M, int64_t N, int64_t K,
+                              void* workspace, size_t workspace_bytes,
+                              const bfp8_gemm_options* opt, void* stream);
+
+/* Workspace bytes bfp8_gemm_grouped needs (current device). */
+bfp8_status bfp8_gemm_grouped_workspace_size(int64_t M, int64_t N, int64_t K, int num_experts,
+                                             const bfp8_gemm_options* opt,
+                                             int operands_unaligned, size_t* bytes);
+
+/*
  * bfp8_gemm_noalloc -- bfp8_gemm for callers that cannot allocate device
  * memory.  (Not from the pages: they have no counterpart; this is a
  * convenience of this library.)

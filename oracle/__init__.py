@@ -16,6 +16,11 @@ Functions and the passages they follow:
                              bf16 output, same snippet.
   bf16_from_f64              round-to-nearest-even to bfloat16 (the snippet's
                              out_dtype = torch.bfloat16).
+  grouped_gemm               the M-grouped contiguous layout of the transformers
+                             DeepGEMM integration (`_build_deepgemm_contiguous_
+                             layout`, SM100 "psum" form): blocked_gemm applied to
+                             each expert's block of rows with that expert's
+                             weights and weight scales.
 """
 from __future__ import annotations
 
@@ -172,6 +177,46 @@ def blocked_gemm(A: np.ndarray, B: np.ndarray, As: np.ndarray, as_col_major: boo
     res = {"bf16": out}
     if f64 is not None:
         res["f64"] = f64
+    if ab is not None:
+        res["abs"] = ab
+    return res
+
+
+def expert_of_rows(psum: np.ndarray, rows: np.ndarray) -> np.ndarray:
+    """Expert of each row under the cumulative layout psum [E] (rows
+    [psum[e-1], psum[e]) belong to expert e); -1 for rows past psum[E-1]."""
+    psum = np.asarray(psum, dtype=np.int64)
+    rows = np.asarray(rows, dtype=np.int64)
+    e = np.searchsorted(psum, rows, side="right")
+    return np.where(e < psum.size, e, -1)
+
+
+def grouped_gemm(A: np.ndarray, B: np.ndarray, As: np.ndarray, as_col_major: bool,
+                 Bs: np.ndarray, psum: np.ndarray, rows=None, want_abs: bool = False,
+                 threads: int = 0):
+    """M-grouped blocked GEMM: row m of expert e = blocked_gemm with B[e], Bs[e].
+
+    A uint8 [M, K]; B uint8 [E, N, K]; Bs float32 [E, ceil(N/128), G]; psum
+    int [E] cumulative row counts.  Returns a dict with 'bf16' [n_rows, N]
+    (rows past the last expert hold 0), 'expert' [n_rows] (-1 for those rows)
+    and, on request, 'abs'.
+    """
+    M = A.shape[0]
+    E, N, _ = B.shape
+    rows_arr = np.arange(M, dtype=np.int64) if rows is None else np.asarray(rows, dtype=np.int64)
+    experts = expert_of_rows(psum, rows_arr)
+    out = np.zeros((rows_arr.size, N), dtype=np.uint16)
+    ab = np.zeros((rows_arr.size, N), dtype=np.float64) if want_abs else None
+    for e in range(E):
+        sel = np.nonzero(experts == e)[0]
+        if sel.size == 0:
+            continue
+        r = blocked_gemm(A, B[e], As, as_col_major, Bs[e], rows=rows_arr[sel],
+                         want_abs=want_abs, threads=threads)
+        out[sel] = r["bf16"]
+        if ab is not None:
+            ab[sel] = r["abs"]
+    res = {"bf16": out, "expert": experts}
     if ab is not None:
         res["abs"] = ab
     return res

@@ -103,6 +103,20 @@ def test_gemm_rejects_bad_arguments_on_the_host(L):
         assert "device" in bf.bfp8_last_error().lower() or "driver" in bf.bfp8_last_error().lower()
 
 
+def test_grouped_gemm_rejects_bad_arguments_on_the_host(L):
+    def call(E=4, layout=512, M=256, N=128, K=256):
+        return L.bfp8_gemm_grouped(256, 256, 256, 1, 256, 256, layout, E, 256, M, N, K, 256,
+                                   1 << 30, None, None)
+    assert call(E=0) == 1
+    assert call(E=1025) == 1
+    assert call(layout=0) == 1                    # null grouped_layout
+    assert call(layout=514) == 2                  # not 4-byte aligned
+    assert call(M=0) == 1
+    import torch
+    if not torch.cuda.is_available():
+        assert call() == 3                        # valid: fails at the device check
+
+
 def _cover(M, N, K, sms, options=None):
     plan = bf.bfp8_gemm_plan(M, N, K, sms, options)
     seen = {}

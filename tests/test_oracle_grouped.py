@@ -1,0 +1,82 @@
+"""Pins for the oracle's M-grouped (mixture-of-experts) GEMM.
+
+The grouped GEMM of the transformers DeepGEMM integration (contiguous layout,
+SM100 cumulative form) applies the plain blocked GEMM to each expert's block
+of rows.  Pinned against: the row -> expert map written out by hand; brute
+force (dequantise, fp64 matmul per expert) on tiny shapes; and the fact that a
+row's result depends on its own expert's weights only."""
+import numpy as np
+import pytest
+
+pytestmark = pytest.mark.filterwarnings("ignore")
+
+
+def _case(oracle_mod, counts, N, K, seed):
+    rng = np.random.default_rng(seed)
+    E = len(counts)
+    aligned = [((c + 127) // 128) * 128 for c in counts]
+    psum = np.cumsum(aligned).astype(np.int32)
+    M = int(psum[-1]) + 64                                       # rows past the last expert
+    # integer-valued codes in [-16, 16] and power-of-two scales in [2^-2, 2^2]:
+    # every product and every partial sum is exact in fp64, so any correct
+    # evaluation order gives the same bf16
+    tab = oracle_mod.e4m3_table()
+    codes = np.array([c for c in range(256) if np.isfinite(tab[c]) and abs(tab[c]) <= 16
+                      and tab[c] == np.round(tab[c])], dtype=np.uint8)
+    A = rng.choice(codes, size=(M, K)).astype(np.uint8)
+    B = rng.choice(codes, size=(E, N, K)).astype(np.uint8)
+    G = (K + 127) // 128
+    As = (2.0 ** rng.integers(-2, 3, size=(M, G))).astype(np.float32)
+    Bs = (2.0 ** rng.integers(-2, 3, size=(E, (N + 127) // 128, G))).astype(np.float32)
+    return A, B, As, Bs, psum
+
+
+def test_rows_map_to_the_expert_whose_block_holds_them(oracle_mod):
+    psum = np.array([128, 128, 384, 512], dtype=np.int32)         # expert 1 is empty
+    rows = np.array([0, 127, 128, 383, 384, 511, 512, 900])
+    assert oracle_mod.expert_of_rows(psum, rows).tolist() == [0, 0, 2, 2, 3, 3, -1, -1]
+
+
+def test_grouped_equals_dequantised_fp64_matmul_per_expert(oracle_mod):
+    A, B, As, Bs, psum = _case(oracle_mod, [100, 0, 130, 5], N=136, K=200, seed=3)
+    res = oracle_mod.grouped_gemm(A, B, As, False, Bs, psum)
+    tab = oracle_mod.e4m3_table()
+    M = A.shape[0]
+    E, N, K = B.shape
+    G = (K + 127) // 128
+    kb = np.arange(K) // 128
+    ref_rows = 0
+    for m in range(M):
+        e = res["expert"][m]
+        if e < 0:
+            assert not res["bf16"][m].any()
+            continue
+        a = tab[A[m]] * As[m, kb].astype(np.float64)
+        b = tab[B[e]] * Bs[e][np.arange(N)[:, None] // 128, kb[None, :]].astype(np.float64)
+        want = oracle_mod.bf16_from_f64(b @ a)
+        assert np.array_equal(res["bf16"][m], want)
+        ref_rows += 1
+    assert ref_rows == int(psum[-1])
+
+
+def test_a_row_depends_on_its_own_experts_weights_only(oracle_mod):
+    A, B, As, Bs, psum = _case(oracle_mod, [128, 256, 128], N=64, K=256, seed=5)
+    base = oracle_mod.grouped_gemm(A, B, As, False, Bs, psum)["bf16"]
+    B2 = B.copy()
+    Bs2 = Bs.copy()
+    B2[1] = np.flip(B2[1], axis=0)                              # change expert 1 only
+    Bs2[1] *= 2.0
+    got = oracle_mod.grouped_gemm(A, B2, As, False, Bs2, psum)["bf16"]
+    rows_e1 = slice(int(psum[0]), int(psum[1]))
+    others = np.ones(A.shape[0], dtype=bool)
+    others[rows_e1] = False
+    assert np.array_equal(got[others], base[others])
+    assert not np.array_equal(got[rows_e1], base[rows_e1])
+
+
+def test_one_expert_is_the_plain_blocked_gemm(oracle_mod):
+    A, B, As, Bs, psum = _case(oracle_mod, [300], N=200, K=384, seed=7)
+    got = oracle_mod.grouped_gemm(A, B, As, False, Bs, psum)
+    plain = oracle_mod.blocked_gemm(A, B[0], As, False, Bs[0])["bf16"]
+    n = int(psum[0])
+    assert np.array_equal(got["bf16"][:n], plain[:n])
