@@ -30,7 +30,7 @@ EXPORTS = ("bfp8_group_quant", "bfp8_scale_ld", "bfp8_gemm", "bfp8_gemm_ex",
            "bfp8_gemm_workspace_size", "bfp8_gemm_plan", "bfp8_plan_unit", "bfp8_last_error",
            "bfp8_status_string", "bfp8_device_status", "bfp8_selftest_bounded_wait",
            "bfp8_version", "bfp8_gemm_noalloc", "bfp8_gemm_grouped",
-           "bfp8_gemm_grouped_workspace_size")
+           "bfp8_gemm_grouped_workspace_size", "bfp8_gemm_fused", "bfp8_gemm_fused_workspace_size")
 
 
 class BFP8Error(RuntimeError):
@@ -101,6 +101,12 @@ def lib():
             L.bfp8_gemm_grouped.restype = i32
             L.bfp8_gemm_grouped.argtypes = [P, P, P, i32, i64, P, P, i32, P, i64, i64, i64, P, sz,
                                             ctypes.POINTER(GemmOptions), P]
+            L.bfp8_gemm_fused.restype = i32
+            L.bfp8_gemm_fused.argtypes = [P, P, P, i32, i64, P, P, P, P, P, i32, i64, i64, i64, i64,
+                                          P, sz, ctypes.POINTER(GemmOptions), P]
+            L.bfp8_gemm_fused_workspace_size.restype = i32
+            L.bfp8_gemm_fused_workspace_size.argtypes = [i64, i64, i64, ctypes.POINTER(GemmOptions),
+                                                         i32, ctypes.POINTER(sz)]
             L.bfp8_gemm_grouped_workspace_size.restype = i32
             L.bfp8_gemm_grouped_workspace_size.argtypes = [i64, i64, i64, i32,
                                                            ctypes.POINTER(GemmOptions), i32,
@@ -320,6 +326,63 @@ def bfp8_gemm_grouped(A: torch.Tensor, B: torch.Tensor, As: torch.Tensor, Bs: to
                                  _stream_ptr(stream))
     _check(st, "bfp8_gemm_grouped")
     return out
+
+
+def bfp8_gemm_fused(A: torch.Tensor, B: torch.Tensor, As: torch.Tensor, Bs: torch.Tensor,
+                    bias: torch.Tensor | None = None, want_out: bool = True,
+                    quantise: bool = True, s_col_major: bool = True,
+                    out: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
+                    options=None, stream=None):
+    """Blocked-FP8 GEMM with the fused epilogue: y = bf16(bf16(A B^T scaled) +
+    bias), returned as (out or None, q or None, s or None); q, s = the 1x128
+    group quantisation of y (s a [M, G] view, column-major storage by default)."""
+    if A.dtype != torch.float8_e4m3fn or B.dtype != torch.float8_e4m3fn:
+        raise ValueError("A and B must be float8_e4m3fn")
+    if not (A.is_contiguous() and B.is_contiguous() and Bs.is_contiguous()):
+        raise ValueError("A, B and Bs must be contiguous")
+    M, K = A.shape
+    N, K2 = B.shape
+    if K2 != K:
+        raise ValueError("A and B disagree on K")
+    G = (K + 127) // 128
+    if Bs.shape != ((N + 127) // 128, G) or Bs.dtype != torch.float32:
+        raise ValueError(f"Bs must be float32 of shape {((N + 127) // 128, G)}")
+    if bias is not None and (bias.dtype != torch.bfloat16 or bias.shape != (N,)
+                             or not bias.is_contiguous()):
+        raise ValueError(f"bias must be a contiguous bfloat16 tensor of shape ({N},)")
+    col, ld = _as_layout(As, M, G)
+    if want_out and out is None:
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=A.device)
+    if not want_out:
+        out = None
+    q = s_view = s_st = None
+    Gn = (N + 127) // 128
+    ld_s = 0
+    if quantise:
+        q = torch.empty((M, N), dtype=torch.float8_e4m3fn, device=A.device)
+        if s_col_major:
+            ld_s = bfp8_scale_ld(M)
+            s_st = torch.zeros((Gn, ld_s), dtype=torch.float32, device=A.device)
+            s_view = s_st[:, :M].t()
+        else:
+            ld_s = Gn
+            s_st = torch.zeros((M, Gn), dtype=torch.float32, device=A.device)
+            s_view = s_st
+    unaligned = (A.data_ptr() % 16 != 0) or (B.data_ptr() % 16 != 0)
+    if workspace is None:
+        n = ctypes.c_size_t(0)
+        _check(lib().bfp8_gemm_fused_workspace_size(M, N, K, _opts(options), int(unaligned),
+                                                    ctypes.byref(n)),
+               "bfp8_gemm_fused_workspace_size")
+        workspace = workspace_for(int(n.value), A.device)
+    st = lib().bfp8_gemm_fused(
+        A.data_ptr(), B.data_ptr(), As.data_ptr(), col, ld, Bs.data_ptr(),
+        bias.data_ptr() if bias is not None else None, out.data_ptr() if out is not None else None,
+        q.data_ptr() if q is not None else None, s_st.data_ptr() if s_st is not None else None,
+        int(s_col_major), ld_s, M, N, K, workspace.data_ptr(),
+        workspace.numel() * workspace.element_size(), _opts(options), _stream_ptr(stream))
+    _check(st, "bfp8_gemm_fused")
+    return out, q, s_view
 
 
 def bfp8_device_status(clear: bool = True) -> int:

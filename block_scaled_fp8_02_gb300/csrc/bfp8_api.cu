@@ -504,26 +504,46 @@ bfp8_status bfp8_gemm_workspace_size(int64_t M, int64_t N, int64_t K,
   return ok();
 }
 
-// The GEMM proper, plain (psum == nullptr) or M-grouped over `experts` experts
-// (internal linkage: not part of the exported interface).
+// What a call adds to the plain GEMM: M-grouped experts and / or the fused
+// epilogue (bias, next-layer quantisation, optional bf16 output).
+struct GemmExtras {
+  const int32_t* psum = nullptr;
+  int64_t experts = 1;
+  const void* bias = nullptr;
+  void* q = nullptr;
+  float* s = nullptr;
+  int s_col_major = 1;
+  int64_t ld_s = 0;
+  bool store_out = true;
+};
+
+// Options a call actually runs with: grouped and fused calls use the wide
+// schedule (128 activation rows per tile, inside one expert; one 128-column
+// group per promotion thread), and fused calls the stream-K split (the
+// cluster reduction stores outside the fused epilogue).
+static bfp8_gemm_options effective_options(const bfp8_gemm_options* opt, bool grouped,
+                                           bool fused) {
+  bfp8_gemm_options o{};
+  if (opt) o = *opt;
+  if (grouped || fused) o.schedule = BFP8_SCHEDULE_WIDE;
+  if (fused) o.k_split = BFP8_KSPLIT_STREAM_K;
+  return o;
+}
+
+// The GEMM proper (internal linkage: not part of the exported interface).
 static bfp8_status gemm_impl(const void* A, const void* B, const float* As, int as_col_major,
-                             int64_t ld_as, const float* Bs, const int32_t* psum,
-                             int64_t experts, void* out, int64_t M, int64_t N, int64_t K,
-                             void* workspace, size_t workspace_bytes,
-                             const bfp8_gemm_options* opt_in, void* stream) {
+                             int64_t ld_as, const float* Bs, void* out, int64_t M, int64_t N,
+                             int64_t K, void* workspace, size_t workspace_bytes,
+                             const bfp8_gemm_options* opt_in, void* stream, const GemmExtras& x) {
   bfp8_status st = check_gemm_sizes(M, N, K);
   if (st != BFP8_OK) return st;
   if ((st = check_options(opt_in)) != BFP8_OK) return st;
-  bfp8_gemm_options grouped_opt{};
-  const bfp8_gemm_options* opt = opt_in;
-  if (psum) {
-    // grouped mode runs the wide schedule (128 activation rows per tile, each
-    // tile inside one expert's aligned block)
-    if (opt_in) grouped_opt = *opt_in;
-    grouped_opt.schedule = BFP8_SCHEDULE_WIDE;
-    opt = &grouped_opt;
-  }
-  if (!A || !B || !As || !Bs || !out)
+  const int32_t* psum = x.psum;
+  const int64_t experts = x.experts;
+  const bool fused = x.bias != nullptr || x.q != nullptr;
+  const bfp8_gemm_options eff = effective_options(opt_in, psum != nullptr, fused);
+  const bfp8_gemm_options* opt = (psum || fused) ? &eff : opt_in;
+  if (!A || !B || !As || !Bs || (!out && x.store_out))
     return fail(BFP8_ERR_INVALID_ARG, "null pointer (A=%p B=%p As=%p Bs=%p out=%p)", A, B,
                 (const void*)As, (const void*)Bs, out);
   if (as_col_major != 0 && as_col_major != 1)
@@ -607,6 +627,14 @@ static bfp8_status gemm_impl(const void* A, const void* B, const float* As, int 
   a.prefetch_b = (opt && opt->prefetch_weights == 1 && !p.relayout && bs_ok && !psum) ? 1 : 0;
   a.psum = psum;
   a.experts = static_cast<int32_t>(experts);
+  a.bias = static_cast<const __nv_bfloat16*>(x.bias);
+  a.bias_vec = (x.bias && !misaligned(x.bias, 16) && N % 8 == 0) ? 1 : 0;
+  a.store_out = x.store_out ? 1 : 0;
+  a.q_out = static_cast<uint8_t*>(x.q);
+  a.s_out = x.s;
+  a.s_col_major = x.s_col_major;
+  a.ld_s = x.ld_s;
+  a.q_vec = (x.q && !misaligned(x.q, 16) && N % 16 == 0) ? 1 : 0;
   a.err = d.err;
   a.wait_limit = kWaitLimitCycles;
   a.trace = nullptr;
@@ -626,8 +654,8 @@ bfp8_status bfp8_gemm_ex(const void* A, const void* B, const float* As, int as_c
                          int64_t ld_as, const float* Bs, void* out, int64_t M, int64_t N,
                          int64_t K, void* workspace, size_t workspace_bytes,
                          const bfp8_gemm_options* opt, void* stream) {
-  return gemm_impl(A, B, As, as_col_major, ld_as, Bs, nullptr, 1, out, M, N, K, workspace,
-                   workspace_bytes, opt, stream);
+  return gemm_impl(A, B, As, as_col_major, ld_as, Bs, out, M, N, K, workspace, workspace_bytes,
+                   opt, stream, GemmExtras{});
 }
 
 static bfp8_status check_grouped(const int32_t* grouped_layout, int num_experts, int64_t N, int64_t K) {
@@ -651,8 +679,11 @@ bfp8_status bfp8_gemm_grouped(const void* A, const void* B, const float* As, int
   bfp8_status st = check_gemm_sizes(M, N, K);
   if (st != BFP8_OK) return st;
   if ((st = check_grouped(grouped_layout, num_experts, N, K)) != BFP8_OK) return st;
-  return gemm_impl(A, B, As, as_col_major, ld_as, Bs, grouped_layout, num_experts, out, M, N, K,
-                   workspace, workspace_bytes, opt, stream);
+  GemmExtras x;
+  x.psum = grouped_layout;
+  x.experts = num_experts;
+  return gemm_impl(A, B, As, as_col_major, ld_as, Bs, out, M, N, K, workspace, workspace_bytes,
+                   opt, stream, x);
 }
 
 bfp8_status bfp8_gemm_grouped_workspace_size(int64_t M, int64_t N, int64_t K, int num_experts,
@@ -666,12 +697,63 @@ bfp8_status bfp8_gemm_grouped_workspace_size(int64_t M, int64_t N, int64_t K, in
   if (!bytes) return fail(BFP8_ERR_INVALID_ARG, "bytes is null");
   DevInfo d;
   if ((st = current_device_with_caps(&d)) != BFP8_OK) return st;
-  bfp8_gemm_options g{};
-  if (opt) g = *opt;
-  g.schedule = BFP8_SCHEDULE_WIDE;
+  const bfp8_gemm_options g = effective_options(opt, true, false);
   Plan p;
   if ((st = make_plan(M, N, K, d.sms, &g, operands_unaligned != 0, d.cluster_cap, &p,
                       num_experts)) != BFP8_OK)
+    return st;
+  *bytes = p.total;
+  return ok();
+}
+
+bfp8_status bfp8_gemm_fused(const void* A, const void* B, const float* As, int as_col_major,
+                            int64_t ld_as, const float* Bs, const void* bias, void* out, void* q,
+                            float* s, int s_col_major, int64_t ld_s, int64_t M, int64_t N,
+                            int64_t K, void* workspace, size_t workspace_bytes,
+                            const bfp8_gemm_options* opt, void* stream) {
+  bfp8_status st = check_gemm_sizes(M, N, K);
+  if (st != BFP8_OK) return st;
+  if (!out && !q) return fail(BFP8_ERR_INVALID_ARG, "out and q are both null: nothing to produce");
+  if ((q == nullptr) != (s == nullptr))
+    return fail(BFP8_ERR_INVALID_ARG, "q and s must be given together");
+  if (q) {
+    if (s_col_major != 0 && s_col_major != 1)
+      return fail(BFP8_ERR_INVALID_ARG, "s_col_major = %d (expected 0 or 1)", s_col_major);
+    const int64_t Gn = cdiv(N, 128);
+    if (s_col_major ? ld_s < M : ld_s < Gn)
+      return fail(BFP8_ERR_INVALID_ARG, "ld_s = %lld too small for the %s layout", (long long)ld_s,
+                  s_col_major ? "column-major" : "row-major");
+    if (misaligned(s, 4)) return fail(BFP8_ERR_ALIGNMENT, "s must be 4-byte aligned");
+  }
+  if (bias && misaligned(bias, 2)) return fail(BFP8_ERR_ALIGNMENT, "bias must be 2-byte aligned");
+  GemmExtras x;
+  x.bias = bias;
+  x.q = q;
+  x.s = s;
+  x.s_col_major = s_col_major;
+  x.ld_s = ld_s;
+  x.store_out = out != nullptr;
+  if (!bias && !q) {
+    // nothing to fuse: the plain GEMM
+    return gemm_impl(A, B, As, as_col_major, ld_as, Bs, out, M, N, K, workspace, workspace_bytes,
+                     opt, stream, GemmExtras{});
+  }
+  return gemm_impl(A, B, As, as_col_major, ld_as, Bs, out, M, N, K, workspace, workspace_bytes,
+                   opt, stream, x);
+}
+
+bfp8_status bfp8_gemm_fused_workspace_size(int64_t M, int64_t N, int64_t K,
+                                           const bfp8_gemm_options* opt, int operands_unaligned,
+                                           size_t* bytes) {
+  bfp8_status st = check_gemm_sizes(M, N, K);
+  if (st != BFP8_OK) return st;
+  if ((st = check_options(opt)) != BFP8_OK) return st;
+  if (!bytes) return fail(BFP8_ERR_INVALID_ARG, "bytes is null");
+  DevInfo d;
+  if ((st = current_device_with_caps(&d)) != BFP8_OK) return st;
+  const bfp8_gemm_options g = effective_options(opt, false, true);
+  Plan p;
+  if ((st = make_plan(M, N, K, d.sms, &g, operands_unaligned != 0, d.cluster_cap, &p)) != BFP8_OK)
     return st;
   *bytes = p.total;
   return ok();

@@ -1,0 +1,66 @@
+// bfp8_e4m3.cuh -- the per-token-group quantisation arithmetic shared by the
+// quantisation kernel and the fused GEMM epilogue (per_token_group_quant_fp8
+// with group 128 of the vLLM PR 49932 digest, "key source snippet"):
+//   scale = fl32(max(amax, 1e-10) / 448)      one IEEE fp32 division
+//   code  = e4m3_rn_satfinite(fl32(x / scale)) one IEEE fp32 division per element
+//
+// The codes are found without dividing.  With r = rcp.approx(scale) (relative
+// error <= 2^-23), r_lo = RN(r (1 - 2^-19)) and r_hi = RN(r (1 + 2^-19)), the
+// products y_lo = RN(x r_lo) and y_hi = RN(x r_hi) differ from x / scale by a
+// factor within (1 - 2^-19 +- 2^-21) and (1 + 2^-19 +- 2^-21), while
+// fl32(x / scale) is within a factor 1 +- 2^-24 of it, so fl32(x / scale) lies
+// strictly between y_lo and y_hi (for |x / scale| >= 2^-126; below that all
+// three give e4m3 +-0).  Rounding to e4m3 (nearest-even, saturating) is
+// monotone, so when y_lo and y_hi get the same code, that is the code of
+// fl32(x / scale).  Only when an e4m3 rounding boundary falls in the 2^-18
+// wide bracket (about once in 30000 elements) must the IEEE division be done;
+// callers do it in a warp-uniform branch.
+#pragma once
+
+#include <cstdint>
+
+namespace bfp8 {
+
+__device__ __forceinline__ float group_scale(float amax) {
+  return __fdiv_rn(fmaxf(amax, 1e-10f), 448.0f);
+}
+
+// Approximate reciprocal (PTX rcp.approx: at most 1 ulp from 1/s).
+__device__ __forceinline__ float rcp_approx(float s) {
+  float r;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(s));
+  return r;
+}
+
+__device__ __forceinline__ uint16_t cvt_e4m3x2(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// The two bracketing multipliers of a group.
+struct E4m3Bracket {
+  float lo, hi;
+  __device__ __forceinline__ explicit E4m3Bracket(float scale) {
+    const float r = rcp_approx(scale);
+    lo = __fmul_rn(r, 1.0f - 0x1p-19f);
+    hi = __fmul_rn(r, 1.0f + 0x1p-19f);
+  }
+};
+
+// Codes of fl32(x0 / scale) and fl32(x1 / scale), low byte first, when the
+// bracket decides them; sets `need` when it does not.
+__device__ __forceinline__ uint16_t e4m3_pair_bracketed(float x0, float x1, const E4m3Bracket& b,
+                                                        bool& need) {
+  const uint16_t lo = cvt_e4m3x2(__fmul_rn(x0, b.lo), __fmul_rn(x1, b.lo));
+  const uint16_t hi = cvt_e4m3x2(__fmul_rn(x0, b.hi), __fmul_rn(x1, b.hi));
+  need |= lo != hi;
+  return lo;
+}
+
+// The same codes by the IEEE division.
+__device__ __forceinline__ uint16_t e4m3_pair_divided(float x0, float x1, float scale) {
+  return cvt_e4m3x2(__fdiv_rn(x0, scale), __fdiv_rn(x1, scale));
+}
+
+}  // namespace bfp8

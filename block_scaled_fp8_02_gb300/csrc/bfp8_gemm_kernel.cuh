@@ -37,6 +37,7 @@
 #include <atomic>
 #include <cstdint>
 
+#include "bfp8_e4m3.cuh"
 #include "bfp8_ptx.cuh"
 #include "bfp8_sched.h"
 
@@ -72,6 +73,18 @@ struct GemmArgs {
   // past psum[experts-1] are not stored.  psum == nullptr: one plain GEMM.
   const int32_t* psum;
   int32_t experts;
+  // Fused epilogue (wide tiles; each promotion thread holds one 128-column
+  // group of one row): y = bf16(acc), then y = bf16(y + bias[n]) when bias is
+  // set; y is stored to out when store_out, and quantised per 1 x 128 group
+  // into q_out / s_out when q_out is set.
+  const __nv_bfloat16* bias;
+  int32_t bias_vec;      // bias may be read 16 bytes at a time
+  int32_t store_out;
+  uint8_t* q_out;        // [M, N] e4m3 codes, row-major
+  float* s_out;          // scales: s_out[g * ld_s + m] (column-major) or s_out[m * ld_s + g]
+  int32_t s_col_major;
+  int64_t ld_s;
+  int32_t q_vec;         // q_out rows may be written 16 bytes at a time
 };
 
 constexpr int kMaxExperts = 1024;   // psum entries cached in shared memory
@@ -665,7 +678,85 @@ __global__ void __launch_bounds__(GemmCfg<BN, SWAP>::kThreads, 1)
         if (etid == 0) a.counters[ts] = 0;  // every contributor has arrived
       }
 
-      if (!SWAP && a.vec_store) {
+      if (!SWAP && (a.bias != nullptr || a.q_out != nullptr)) {
+        static_assert(SWAP || C::kCPT == 128, "fused epilogue: one 128-column group per thread");
+        // ---- fused epilogue: bias, then the next layer's group quantisation
+        const int64_t m = static_cast<int64_t>(cur.p_tile) * 128 + r;
+        const int64_t nbase = static_cast<int64_t>(cur.q_tile) * BN + col0;
+        const int64_t nv = a.N - nbase < 128 ? a.N - nbase : 128;   // columns in range
+#pragma unroll
+        for (int i = 0; i < C::kCPT; ++i) acc[i] = __bfloat162float(__float2bfloat16_rn(acc[i]));
+        if (a.bias != nullptr && nv > 0) {
+          if (a.bias_vec && nv == 128) {
+#pragma unroll
+            for (int g = 0; g < 16; ++g) {
+              const uint4 w = __ldg(reinterpret_cast<const uint4*>(a.bias + nbase) + g);
+              const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+              for (int h = 0; h < 4; ++h) {
+                const float b0 = __uint_as_float(ww[h] << 16);
+                const float b1 = __uint_as_float(ww[h] & 0xFFFF0000u);
+                acc[8 * g + 2 * h] =
+                    __bfloat162float(__float2bfloat16_rn(__fadd_rn(acc[8 * g + 2 * h], b0)));
+                acc[8 * g + 2 * h + 1] =
+                    __bfloat162float(__float2bfloat16_rn(__fadd_rn(acc[8 * g + 2 * h + 1], b1)));
+              }
+            }
+          } else {
+#pragma unroll
+            for (int i = 0; i < C::kCPT; ++i)
+              if (i < nv)
+                acc[i] = __bfloat162float(
+                    __float2bfloat16_rn(__fadd_rn(acc[i], __bfloat162float(a.bias[nbase + i]))));
+          }
+        }
+        if (a.q_out != nullptr) {
+          float amax = 0.f;
+#pragma unroll
+          for (int i = 0; i < C::kCPT; ++i)
+            if (i < nv) amax = fmaxf(amax, fabsf(acc[i]));
+          const float scale = group_scale(amax);
+          const E4m3Bracket br(scale);
+          uint32_t codes[C::kCPT / 4];
+          bool need = false;
+#pragma unroll
+          for (int i = 0; i < C::kCPT; i += 4) {
+            const uint32_t lo = e4m3_pair_bracketed(acc[i], acc[i + 1], br, need);
+            const uint32_t hi = e4m3_pair_bracketed(acc[i + 2], acc[i + 3], br, need);
+            codes[i / 4] = lo | (hi << 16);
+          }
+          // warp-uniform branch: IEEE divisions only where the bracket does not decide
+          if (__any_sync(0xffffffffu, need)) {
+            if (need) {
+#pragma unroll
+              for (int i = 0; i < C::kCPT; i += 4) {
+                const uint32_t lo = e4m3_pair_divided(acc[i], acc[i + 1], scale);
+                const uint32_t hi = e4m3_pair_divided(acc[i + 2], acc[i + 3], scale);
+                codes[i / 4] = lo | (hi << 16);
+              }
+            }
+          }
+          if (m < m_lim && nv > 0) {
+            uint8_t* qrow = a.q_out + m * a.N + nbase;
+            if (a.q_vec && nv == 128) {
+#pragma unroll
+              for (int g = 0; g < C::kCPT / 16; ++g)
+                st_global_v4(qrow + 16 * g, codes[4 * g], codes[4 * g + 1], codes[4 * g + 2],
+                             codes[4 * g + 3]);
+            } else {
+#pragma unroll
+              for (int i = 0; i < C::kCPT; ++i)
+                if (i < nv) qrow[i] = static_cast<uint8_t>(codes[i / 4] >> (8 * (i & 3)));
+            }
+            const int64_t g = nbase / 128;
+            if (a.s_col_major) a.s_out[g * a.ld_s + m] = scale;
+            else a.s_out[m * a.ld_s + g] = scale;
+          }
+        }
+      }
+      if (!SWAP && !a.store_out) {
+        // fused epilogue without the bf16 output
+      } else if (!SWAP && a.vec_store) {
         // rows of 16-byte-aligned bf16 (N % 8 == 0): through this warp's
         // staging rows, 32 columns at a time; lanes 4i..4i+3 then store one
         // row's 64 contiguous bytes

@@ -25,6 +25,7 @@
 
 #include <cstdint>
 
+#include "bfp8_e4m3.cuh"
 #include "bfp8_internal.h"
 #include "bfp8_ptx.cuh"
 
@@ -39,21 +40,6 @@ struct QuantShape {
   static constexpr int kGPW = 32 / kLPG;        // groups per warp step
 };
 
-// Approximate reciprocal (PTX rcp.approx: at most 1 ulp from 1/s).
-__device__ __forceinline__ float rcp_approx(float s) {
-  float r;
-  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(s));
-  return r;
-}
-
-__device__ __forceinline__ uint16_t cvt_e4m3x2(float lo, float hi) {
-  uint16_t r;
-  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
-  return r;
-}
-
-// A lane's 16 input bytes as four raw 32-bit words (bf16: two elements per
-// word, element 2i in the low half), kept packed until they are used.
 template <bool kF32>
 __device__ __forceinline__ void load_words(const void* x, int64_t idx, uint32_t (&w)[4]) {
   const uint4 t = kF32 ? __ldg(reinterpret_cast<const uint4*>(static_cast<const float*>(x) + idx))
@@ -199,36 +185,18 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32, kBlocksPerSm)
 #pragma unroll
       for (int off = LPG / 2; off > 0; off >>= 1)
         amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
-      const float scale = __fdiv_rn(fmaxf(amax, 1e-10f), 448.0f);
-      // The code of fl32(x / scale) without dividing.  With r = rcp_approx(scale)
-      // (relative error <= 2^-23), r_lo = RN(r (1 - 2^-19)) and r_hi =
-      // RN(r (1 + 2^-19)), the products y_lo = RN(x r_lo) and y_hi = RN(x r_hi)
-      // differ from x / scale by a factor within (1 - 2^-19 +- 2^-21) and
-      // (1 + 2^-19 +- 2^-21), while fl32(x / scale) is within a factor
-      // 1 +- 2^-24 of it, so fl32(x / scale) lies strictly between y_lo and
-      // y_hi (for |x / scale| >= 2^-126; below that all three give e4m3 +-0).
-      // Rounding to e4m3 (nearest-even, saturating) is monotone, so when y_lo
-      // and y_hi get the same code, that is the code of fl32(x / scale).  Only
-      // when an e4m3 rounding boundary falls in the 2^-18 wide bracket (about
-      // once in 30000 elements) is the IEEE division done.
-      const float r = rcp_approx(scale);
-      const float r_lo = __fmul_rn(r, 1.0f - 0x1p-19f);
-      const float r_hi = __fmul_rn(r, 1.0f + 0x1p-19f);
+      const float scale = group_scale(amax);
+      // codes without dividing (bfp8_e4m3.cuh); the IEEE divisions run only
+      // in warps where the bracket does not decide a code (warp-uniform branch)
+      const E4m3Bracket br(scale);
       uint16_t pk[EPL / 2];
       bool need = false;
 #pragma unroll
-      for (int e = 0; e < EPL; e += 2) {
-        const uint16_t lo = cvt_e4m3x2(__fmul_rn(v[e], r_lo), __fmul_rn(v[e + 1], r_lo));
-        const uint16_t hi = cvt_e4m3x2(__fmul_rn(v[e], r_hi), __fmul_rn(v[e + 1], r_hi));
-        pk[e / 2] = lo;
-        need |= lo != hi;
-      }
-      // warp-uniform branch: the IEEE divisions run only in warps that need them
+      for (int e = 0; e < EPL; e += 2) pk[e / 2] = e4m3_pair_bracketed(v[e], v[e + 1], br, need);
       if (__any_sync(0xffffffffu, need)) {
         if (need) {
 #pragma unroll
-          for (int e = 0; e < EPL; e += 2)
-            pk[e / 2] = cvt_e4m3x2(__fdiv_rn(v[e], scale), __fdiv_rn(v[e + 1], scale));
+          for (int e = 0; e < EPL; e += 2) pk[e / 2] = e4m3_pair_divided(v[e], v[e + 1], scale);
         }
       }
       if (!valid) continue;

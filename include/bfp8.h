@@ -250,6 +250,40 @@ bfp8_status bfp8_gemm_grouped_workspace_size(int64_t M, int64_t N, int64_t K, in
                                              int operands_unaligned, size_t* bytes);
 
 /*
+ * bfp8_gemm_fused -- bfp8_gemm with the next steps of a linear layer folded
+ * into the GEMM's epilogue (the transformers DeepGEMM integration's
+ * `deepgemm_fp8_fp4_linear`: bias added to the bf16 product; and the next
+ * layer's per_token_group_quant_fp8 of that bf16 result, vLLM PR 49932
+ * digest, "key source snippet").  For every row m and column n:
+ *   y[m, n] = bf16(bf16(sum_kb ...) + bias[n])     (bias == NULL: bf16(sum ...))
+ * i.e. the bf16 GEMM result plus the bias as a bf16 tensor addition (one fp32
+ * addition, rounded to bf16), then, when q != NULL, the 1 x 128 group
+ * quantisation of y along n exactly as bfp8_group_quant computes it:
+ *   s[m, g] = fl32(max(amax_g |y|, 1e-10) / 448),  q[m, n] = e4m3(fl32(y / s)).
+ *   bias  bf16 [N] or NULL.
+ *   out   bf16 [M, N] row-major, or NULL to skip the bf16 output.
+ *   q     e4m3 [M, N] row-major (row stride N bytes), or NULL.
+ *   s     fp32 scales of q: s_col_major = 1: s[g * ld_s + m], ld_s >= M;
+ *         s_col_major = 0: s[m * ld_s + g], ld_s >= ceil(N / 128).  NULL iff q is.
+ * Other arguments as for bfp8_gemm_ex; the fused epilogue runs on the wide
+ * schedule with the stream-K split (options.schedule and options.k_split are
+ * ignored when bias or q is given); workspace from
+ * bfp8_gemm_fused_workspace_size.  Errors: BFP8_ERR_INVALID_ARG when out and
+ * q are both NULL, q and s are not both given, or ld_s is too small;
+ * BFP8_ERR_ALIGNMENT for s not 4-byte or bias not 2-byte aligned.
+ */
+bfp8_status bfp8_gemm_fused(const void* A, const void* B, const float* As, int as_col_major,
+                            int64_t ld_as, const float* Bs, const void* bias, void* out, void* q,
+                            float* s, int s_col_major, int64_t ld_s, int64_t M, int64_t N,
+                            int64_t K, void* workspace, size_t workspace_bytes,
+                            const bfp8_gemm_options* opt, void* stream);
+
+/* Workspace bytes bfp8_gemm_fused needs (current device). */
+bfp8_status bfp8_gemm_fused_workspace_size(int64_t M, int64_t N, int64_t K,
+                                           const bfp8_gemm_options* opt, int operands_unaligned,
+                                           size_t* bytes);
+
+/*
  * bfp8_gemm_noalloc -- bfp8_gemm for callers that cannot allocate device
  * memory.  (Not from the pages: they have no counterpart; this is a
  * convenience of this library.)

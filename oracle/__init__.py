@@ -16,6 +16,12 @@ Functions and the passages they follow:
                              bf16 output, same snippet.
   bf16_from_f64              round-to-nearest-even to bfloat16 (the snippet's
                              out_dtype = torch.bfloat16).
+  bias_add_bf16              the bias addition of the transformers DeepGEMM
+                             integration's `deepgemm_fp8_fp4_linear`
+                             (`output.add_(bias)` on bf16 tensors): one IEEE fp32
+                             addition, rounded to bf16.
+  fused_linear               blocked_gemm, bias_add_bf16, then group_quant of the
+                             bf16 result (the next layer's activations).
   grouped_gemm               the M-grouped contiguous layout of the transformers
                              DeepGEMM integration (`_build_deepgemm_contiguous_
                              layout`, SM100 "psum" form): blocked_gemm applied to
@@ -220,3 +226,26 @@ def grouped_gemm(A: np.ndarray, B: np.ndarray, As: np.ndarray, as_col_major: boo
     if ab is not None:
         res["abs"] = ab
     return res
+
+
+def bias_add_bf16(y_bits: np.ndarray, bias_bits: np.ndarray) -> np.ndarray:
+    """bf16 [.., N] + bf16 [N]: each sum is one IEEE fp32 addition of the two
+    values, rounded to nearest-even bf16 (bits in, bits out)."""
+    y = (np.asarray(y_bits, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32)
+    b = (np.asarray(bias_bits, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32)
+    s32 = (y + b).astype(np.float32)          # numpy adds float32 in float32 (IEEE)
+    return bf16_from_f64(s32.astype(np.float64))
+
+
+def fused_linear(A: np.ndarray, B: np.ndarray, As: np.ndarray, as_col_major: bool,
+                 Bs: np.ndarray, bias_bits=None, col_major_out: bool = True, rows=None,
+                 threads: int = 0):
+    """y = bf16 GEMM (+ bias as a bf16 addition), then y's 1x128 group
+    quantisation.  Returns dict(y bf16 bits [n_rows, N], q [n_rows, N] codes,
+    s scales in the requested layout, abs)."""
+    r = blocked_gemm(A, B, As, as_col_major, Bs, rows=rows, want_abs=True, threads=threads)
+    y = r["bf16"]
+    if bias_bits is not None:
+        y = bias_add_bf16(y, bias_bits)
+    q, sc = group_quant(np.ascontiguousarray(y), False, col_major_out)
+    return {"bf16": y, "q": q, "s": sc, "abs": r["abs"]}

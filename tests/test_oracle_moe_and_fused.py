@@ -1,4 +1,4 @@
-"""Pins for the oracle's M-grouped (mixture-of-experts) GEMM.
+"""Pins for the oracle's M-grouped (mixture-of-experts) GEMM and fused linear.
 
 The grouped GEMM of the transformers DeepGEMM integration (contiguous layout,
 SM100 cumulative form) applies the plain blocked GEMM to each expert's block
@@ -80,3 +80,34 @@ def test_one_expert_is_the_plain_blocked_gemm(oracle_mod):
     plain = oracle_mod.blocked_gemm(A, B[0], As, False, Bs[0])["bf16"]
     n = int(psum[0])
     assert np.array_equal(got["bf16"][:n], plain[:n])
+
+
+def test_bias_add_is_the_bf16_tensor_addition(oracle_mod):
+    """The bias step is torch's bf16 + bf16 (computed in fp32, rounded once to
+    bf16); compare with torch on CPU over random values and hand-made ties."""
+    import torch
+    rng = np.random.default_rng(11)
+    y = rng.standard_normal((64, 300)).astype(np.float32) * np.float32(2.0) ** rng.integers(-20, 20, size=(64, 300))
+    b = rng.standard_normal(300).astype(np.float32) * np.float32(2.0) ** rng.integers(-20, 20, size=300)
+    yt = torch.from_numpy(y).to(torch.bfloat16)
+    bt = torch.from_numpy(b).to(torch.bfloat16)
+    want = (yt + bt).view(torch.int16).numpy().view(np.uint16)
+    got = oracle_mod.bias_add_bf16(yt.view(torch.int16).numpy().view(np.uint16),
+                                   bt.view(torch.int16).numpy().view(np.uint16))
+    assert np.array_equal(got, want)
+    # 1 + 2^-8 is a bf16 tie between 1 and 1 + 2^-7: to even (1.0)
+    one = np.array([0x3F80], dtype=np.uint16)
+    tiny = np.array([0x3B80], dtype=np.uint16)            # 2^-8
+    assert oracle_mod.bias_add_bf16(one, tiny)[0] == 0x3F80
+
+
+def test_fused_linear_is_gemm_then_bias_then_group_quant(oracle_mod):
+    A, B, As, Bs, _ = _case(oracle_mod, [256], N=256, K=256, seed=13)
+    B0, Bs0 = B[0], Bs[0]
+    bias = np.random.default_rng(1).standard_normal(256).astype(np.float32)
+    bias_bits = (bias.view(np.uint32) >> 16).astype(np.uint16)
+    res = oracle_mod.fused_linear(A, B0, As, False, Bs0, bias_bits)
+    y = oracle_mod.bias_add_bf16(oracle_mod.blocked_gemm(A, B0, As, False, Bs0)["bf16"], bias_bits)
+    assert np.array_equal(res["bf16"], y)
+    q, s = oracle_mod.group_quant(y, False, True)
+    assert np.array_equal(res["q"], q) and np.array_equal(res["s"], s)
