@@ -54,6 +54,8 @@ def parse_args():
     p.add_argument("--nk", type=int, default=NK, help="N = K")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-extensions", action="store_true",
+                   help="skip timing the grouped (MoE) GEMM and the fused epilogue")
     p.add_argument("--cpu-budget-s", type=float, default=12.0,
                    help="wall seconds (on all host cores) for the oracle baseline sample")
     return p.parse_args()
@@ -508,6 +510,10 @@ def run_ours(args, rank, world, local):
         cpu_baseline = {"value": round(fl / secs / 1e12, 6), "unit": "TFLOP/s", "cores": cores,
                         "kind": "oracle", "sample": desc, "seconds": round(secs, 2)}
 
+    extensions = None
+    if rank == 0 and not args.no_extensions:
+        extensions = measure_extensions(dev)
+
     launches = nk_per_step * args.steps
     if rank == 0:
         line = {
@@ -535,11 +541,97 @@ def run_ours(args, rank, world, local):
             "clocks": clocks,
             "e2e": e2e,
             "cpu_baseline": cpu_baseline,
+            "extensions": extensions,
             "page_context": {"h200_gluon_sweep_gemm_us_sum": 686.64,
                              "ours_gemm_p50_us_sum": round(sum(v["gemm_p50_us"] for v in per_m.values()), 2),
                              "note": "H200, hot L2, GEMM only (lmdeploy PR 4830 table); context, not a target"},
         }
         print(json.dumps(line))
+
+
+# ------------------------------------------------------------ extensions ---
+
+def _graph_time_us(fn, reps=20, iters=5):
+    """Median device time of fn() replayed from a CUDA graph (events at the
+    ends of batches of `iters` replays); inputs are resident, no L2 flush."""
+    import torch
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        fn()
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            fn()
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    ts = []
+    for _ in range(reps):
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(s)
+        with torch.cuda.stream(s):
+            for _ in range(iters):
+                g.replay()
+        e1.record(s)
+        e1.synchronize()
+        ts.append(e0.elapsed_time(e1) * 1e3 / iters)
+    return statistics.median(ts)
+
+
+def measure_extensions(dev):
+    """The rows beyond the sweep: the M-grouped (MoE) GEMM against the plain
+    GEMM of the same total size, and the fused epilogue (bias + next-layer
+    quantisation) against the unfused GEMM -> bias add -> quantisation."""
+    import torch
+    import block_scaled_fp8_02_gb300 as bf
+    from block_scaled_fp8_02_gb300 import metrics as mt
+    from block_scaled_fp8_02_gb300 import workloads as wl
+    res = {}
+    # MoE: 8 experts x 512 tokens, expert weights N=4096, K=7168
+    counts, N, K = [512] * 8, 4096, 7168
+    case = wl.grouped_case(counts, N, K, seed=21)
+    M = case["M"]
+    x = case["x"].to(dev)
+    q, s = bf.bfp8_group_quant(x)
+    B, Bs, ps = case["B"].to(dev), case["Bs"].to(dev), case["psum"].to(dev)
+    out = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    wsg = torch.zeros(bf.bfp8_gemm_grouped_workspace_size(M, N, K, 8) + 256, dtype=torch.uint8, device=dev)
+    t_g = _graph_time_us(lambda: bf.bfp8_gemm_grouped(q, B, s, Bs, ps, out=out, workspace=wsg))
+    B0, Bs0 = B[0].contiguous(), Bs[0].contiguous()
+    wsp = torch.zeros(bf.bfp8_gemm_workspace_size(M, N, K) + 256, dtype=torch.uint8, device=dev)
+    t_p = _graph_time_us(lambda: bf.bfp8_gemm(q, B0, s, Bs0, out=out, workspace=wsp))
+    res["grouped_moe"] = {
+        "config": {"experts": 8, "tokens_per_expert": 512, "N": N, "K": K},
+        "us": round(t_g, 2), "tflops": round(mt.tflops(M, N, K, t_g), 1),
+        "plain_gemm_same_size_us": round(t_p, 2),
+        "note": "each expert's weights read once (8 x 29 MB); the plain GEMM reads one matrix"}
+    # fused epilogue: M=N=K=4096, bias + next-layer quantisation, no bf16 output
+    M = N = K = 4096
+    lc = wl.linear_case(M, N, K, seed=22)
+    x = lc["x"].to(dev)
+    q, s = bf.bfp8_group_quant(x)
+    B, Bs = lc["B"].to(dev), lc["Bs"].to(dev)
+    bias = torch.randn(N, generator=torch.Generator().manual_seed(1)).to(torch.bfloat16).to(dev)
+    y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    qn = torch.empty((M, N), dtype=torch.float8_e4m3fn, device=dev)
+    sn = torch.empty((K // 128, bf.bfp8_scale_ld(M)), dtype=torch.float32, device=dev)
+    wsf = torch.zeros(bf.bfp8_gemm_workspace_size(M, N, K, {"schedule": 2, "k_split": 1}) + 256,
+                      dtype=torch.uint8, device=dev)
+
+    def unfused():
+        bf.bfp8_gemm(q, B, s, Bs, out=y, workspace=wsf, options={"schedule": 2, "k_split": 1})
+        y.add_(bias)
+        bf.bfp8_group_quant(y, q=qn, s_storage=sn)
+
+    t_u = _graph_time_us(unfused)
+    t_f = _graph_time_us(lambda: bf.bfp8_gemm_fused(q, B, s, Bs, bias=bias, want_out=False,
+                                                    workspace=wsf))
+    res["fused_epilogue"] = {
+        "config": {"M": M, "N": N, "K": K, "bias": True, "outputs": "e4m3 codes + scales"},
+        "fused_us": round(t_f, 2), "unfused_us": round(t_u, 2),
+        "unfused": "GEMM (bf16 out) -> torch bf16 bias add -> bfp8_group_quant"}
+    return res
 
 
 # ------------------------------------------------------------ reference ----

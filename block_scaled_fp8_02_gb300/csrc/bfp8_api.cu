@@ -541,6 +541,8 @@ static bfp8_status gemm_impl(const void* A, const void* B, const float* As, int 
   const int32_t* psum = x.psum;
   const int64_t experts = x.experts;
   const bool fused = x.bias != nullptr || x.q != nullptr;
+  if (fused && psum)
+    return fail(BFP8_ERR_UNSUPPORTED, "the fused epilogue is not available for grouped GEMMs");
   const bfp8_gemm_options eff = effective_options(opt_in, psum != nullptr, fused);
   const bfp8_gemm_options* opt = (psum || fused) ? &eff : opt_in;
   if (!A || !B || !As || !Bs || (!out && x.store_out))
@@ -645,7 +647,9 @@ static bfp8_status gemm_impl(const void* A, const void* B, const float* As, int 
     cudaGetLastError();
   }
 #endif
-  cudaError_t e = p.swap ? launch_gemm_swap(p.bn, tmP, tmQ, a, cs) : launch_gemm_wide(p.bn, tmP, tmQ, a, cs);
+  const int mode = psum ? kModeGrouped : (fused ? kModeFused : kModePlain);
+  cudaError_t e = p.swap ? launch_gemm_swap(p.bn, tmP, tmQ, a, cs)
+                         : launch_gemm_wide(p.bn, mode, tmP, tmQ, a, cs);
   if (e != cudaSuccess) return fail(BFP8_ERR_CUDA, "GEMM launch: %s", cudaGetErrorString(e));
   return ok();
 }

@@ -89,6 +89,11 @@ struct GemmArgs {
 
 constexpr int kMaxExperts = 1024;   // psum entries cached in shared memory
 
+// Kernel variants (compile-time, so that the plain GEMM carries none of the
+// others' code): the plain GEMM, the M-grouped (MoE) GEMM and the GEMM with
+// the fused epilogue (the last two on wide tiles only).
+enum : int { kModePlain = 0, kModeGrouped = 1, kModeFused = 2 };
+
 // Expert of the 128-row tile starting at row m0: the first e with psum[e] >
 // m0 (psum in shared memory); past the last expert, the last one (its
 // results are not stored).
@@ -106,7 +111,7 @@ __host__ __device__ constexpr int tmem_cols_for(int n) {
   return n <= 32 ? 32 : n <= 64 ? 64 : n <= 128 ? 128 : n <= 256 ? 256 : 512;
 }
 
-template <int BN, bool SWAP>
+template <int BN, bool SWAP, int MODE = kModePlain>
 struct GemmCfg {
   static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "MMA N for M=128 is 16..256 step 16");
   static_assert(SWAP || BN % 128 == 0, "wide tiles cover whole 128-column weight-scale blocks");
@@ -155,7 +160,7 @@ struct GemmCfg {
   // so that global stores write whole 32-byte sectors along a row.
   static constexpr int kOutPitch = 80;
   static constexpr int kOutBytes = SWAP ? 0 : kNE * 32 * kOutPitch;
-  static constexpr int kPsumBytes = SWAP ? 0 : kMaxExperts * 4;   // grouped mode (wide)
+  static constexpr int kPsumBytes = MODE == kModeGrouped ? kMaxExperts * 4 : 0;
   static constexpr int kStagesFit =
       (kSmemLimit - 1024 /*align*/ - 384 /*barriers*/ - kScaleBytes - kOutBytes - kPsumBytes) /
       kStageBytes;
@@ -250,12 +255,15 @@ __device__ __forceinline__ void reg_fence(uint32_t* v) {
   for (int i = 0; i < N; i += 16) reg_fence16(*reinterpret_cast<uint32_t(*)[16]>(v + i));
 }
 
-template <int BN, bool SWAP>
-__global__ void __launch_bounds__(GemmCfg<BN, SWAP>::kThreads, 1)
+template <int BN, bool SWAP, int MODE>
+__global__ void __launch_bounds__(GemmCfg<BN, SWAP, MODE>::kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmP, const __grid_constant__ CUtensorMap tmQ,
                 const GemmArgs a) {
 #if defined(__CUDA_ARCH__)
-  using C = GemmCfg<BN, SWAP>;
+  using C = GemmCfg<BN, SWAP, MODE>;
+  static_assert(MODE == kModePlain || !SWAP, "grouped and fused variants use wide tiles");
+  constexpr bool kGrouped = MODE == kModeGrouped;
+  constexpr bool kFused = MODE == kModeFused;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_addr(smem_raw);
   uint8_t* smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
@@ -322,7 +330,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, SWAP>::kThreads, 1)
   if (threadIdx.x == 0) griddep_launch_dependents();
   if (warp != C::kNE) griddep_wait();
   const int32_t* spsum = reinterpret_cast<const int32_t*>(smem + C::kOffPsum);
-  if (!SWAP && a.psum != nullptr) {
+  if (kGrouped) {
     // grouped mode: every role looks experts up from a shared-memory copy of
     // psum (written by an earlier kernel, so read after the wait)
     griddep_wait();
@@ -378,7 +386,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, SWAP>::kThreads, 1)
       uint32_t e_tile = 0xFFFFFFFFu, e_cur = 0;   // expert of the current p tile (grouped)
       for (; cur.valid(); cur.next()) {
         BFP8_CLK(c0);
-        if (!SWAP && a.psum != nullptr && cur.p_tile != e_tile) {
+        if (kGrouped && cur.p_tile != e_tile) {
           e_tile = cur.p_tile;
           e_cur = expert_of(spsum, a.experts, static_cast<int64_t>(cur.p_tile) * 128);
         }
@@ -512,7 +520,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, SWAP>::kThreads, 1)
     cur.init(s, cta);
     // rows that are stored: grouped mode stops at the end of the last expert
     const int64_t m_lim =
-        (!SWAP && a.psum != nullptr && a.M > spsum[a.experts - 1]) ? spsum[a.experts - 1] : a.M;
+        (kGrouped && a.M > spsum[a.experts - 1]) ? spsum[a.experts - 1] : a.M;
     uint32_t e_tile = 0xFFFFFFFFu, e_cur = 0;      // expert of the current p tile (grouped)
 
     unsigned long long t_ewait = 0, t_ework = 0, t_escale = 0, t_efix = 0;
@@ -527,7 +535,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, SWAP>::kThreads, 1)
       const float* slot = sRing + ss * C::kSlotFloats;
       float sr;                 // row scale (wide: As * Bs; swap: Bs)
       if (!SWAP) {
-        if (a.psum != nullptr && cur.p_tile != e_tile) {
+        if (kGrouped && cur.p_tile != e_tile) {
           e_tile = cur.p_tile;
           e_cur = expert_of(spsum, a.experts, static_cast<int64_t>(cur.p_tile) * 128);
         }
@@ -678,7 +686,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, SWAP>::kThreads, 1)
         if (etid == 0) a.counters[ts] = 0;  // every contributor has arrived
       }
 
-      if (!SWAP && (a.bias != nullptr || a.q_out != nullptr)) {
+      if (kFused) {
         static_assert(SWAP || C::kCPT == 128, "fused epilogue: one 128-column group per thread");
         // ---- fused epilogue: bias, then the next layer's group quantisation
         const int64_t m = static_cast<int64_t>(cur.p_tile) * 128 + r;
@@ -754,7 +762,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, SWAP>::kThreads, 1)
           }
         }
       }
-      if (!SWAP && !a.store_out) {
+      if (kFused && !a.store_out) {
         // fused epilogue without the bf16 output
       } else if (!SWAP && a.vec_store) {
         // rows of 16-byte-aligned bf16 (N % 8 == 0): through this warp's
@@ -947,16 +955,16 @@ __global__ void __launch_bounds__(GemmCfg<BN, SWAP>::kThreads, 1)
 
 // Host side.  The dynamic shared-memory opt-in is per device and set once (a
 // launch captured into a CUDA graph then needs no attribute call).
-template <int BN, bool SWAP>
+template <int BN, bool SWAP, int MODE = kModePlain>
 cudaError_t configure_instance() {
-  using C = GemmCfg<BN, SWAP>;
+  using C = GemmCfg<BN, SWAP, MODE>;
   static std::atomic<uint64_t> configured{0};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   const uint64_t bit = 1ull << (dev & 63);
   if (!(configured.load(std::memory_order_acquire) & bit)) {
-    e = cudaFuncSetAttribute(gemm_kernel<BN, SWAP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(gemm_kernel<BN, SWAP, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              C::kSmemBytes);
     if (e != cudaSuccess) return e;
     configured.fetch_or(bit, std::memory_order_acq_rel);
@@ -969,7 +977,7 @@ cudaError_t configure_instance() {
 template <int BN, bool SWAP>
 cudaError_t cluster_capacity_instance(int cs, int* clusters) {
   using C = GemmCfg<BN, SWAP>;
-  cudaError_t e = configure_instance<BN, SWAP>();
+  cudaError_t e = configure_instance<BN, SWAP, kModePlain>();
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(cs);
@@ -982,18 +990,18 @@ cudaError_t cluster_capacity_instance(int cs, int* clusters) {
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaOccupancyMaxActiveClusters(clusters, gemm_kernel<BN, SWAP>, &cfg);
+  return cudaOccupancyMaxActiveClusters(clusters, gemm_kernel<BN, SWAP, kModePlain>, &cfg);
 }
 
 // Launches one instantiation with programmatic dependent launch (the
 // prologue may overlap the preceding kernel in the stream; the kernel waits
 // for it before reading its inputs) and, for cluster split-K, as 1-D
 // clusters of sched.cluster consecutive CTAs.
-template <int BN, bool SWAP>
+template <int BN, bool SWAP, int MODE = kModePlain>
 cudaError_t launch_instance(const CUtensorMap& tmP, const CUtensorMap& tmQ, const GemmArgs& a,
                             cudaStream_t stream) {
-  using C = GemmCfg<BN, SWAP>;
-  cudaError_t e = configure_instance<BN, SWAP>();
+  using C = GemmCfg<BN, SWAP, MODE>;
+  cudaError_t e = configure_instance<BN, SWAP, MODE>();
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(a.sched.grid);
@@ -1012,7 +1020,7 @@ cudaError_t launch_instance(const CUtensorMap& tmP, const CUtensorMap& tmQ, cons
     attr[1].val.clusterDim.z = 1;
     cfg.numAttrs = 2;
   }
-  return cudaLaunchKernelEx(&cfg, gemm_kernel<BN, SWAP>, tmP, tmQ, a);
+  return cudaLaunchKernelEx(&cfg, gemm_kernel<BN, SWAP, MODE>, tmP, tmQ, a);
 }
 
 }  // namespace bfp8

@@ -6,8 +6,9 @@
 
 namespace bfp8 {
 
-cudaError_t launch_gemm_wide(int bn, const CUtensorMap& tmP, const CUtensorMap& tmQ,
+cudaError_t launch_gemm_wide(int bn, int mode, const CUtensorMap& tmP, const CUtensorMap& tmQ,
                              const GemmArgs& a, cudaStream_t stream) {
+  if (mode != kModePlain) return launch_gemm_wide_ext(bn, mode, tmP, tmQ, a, stream);
   switch (bn) {
     case 128: return launch_instance<128, false>(tmP, tmQ, a, stream);
     case 256: return launch_instance<256, false>(tmP, tmQ, a, stream);

@@ -27,8 +27,12 @@ cudaError_t launch_group_quant(const void* x, int in_f32, int64_t M, int64_t K, 
 // instantiation; returns cudaErrorInvalidValue for one that does not exist.
 cudaError_t launch_gemm_swap(int bn, const CUtensorMap& tmP, const CUtensorMap& tmQ,
                              const GemmArgs& a, cudaStream_t stream);
-cudaError_t launch_gemm_wide(int bn, const CUtensorMap& tmP, const CUtensorMap& tmQ,
+// `mode` selects the plain, M-grouped or fused-epilogue variant (wide only;
+// bfp8_gemm_kernel.cuh's kMode* values; the last two live in bfp8_gemm_ext.cu).
+cudaError_t launch_gemm_wide(int bn, int mode, const CUtensorMap& tmP, const CUtensorMap& tmQ,
                              const GemmArgs& a, cudaStream_t stream);
+cudaError_t launch_gemm_wide_ext(int bn, int mode, const CUtensorMap& tmP, const CUtensorMap& tmQ,
+                                 const GemmArgs& a, cudaStream_t stream);
 
 // Clusters of `cs` GEMM CTAs the current device runs at once (bfp8_gemm_swap.cu).
 cudaError_t gemm_cluster_capacity(int cs, int* clusters);
