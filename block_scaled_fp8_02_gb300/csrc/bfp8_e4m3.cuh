@@ -13,8 +13,11 @@
 // three give e4m3 +-0).  Rounding to e4m3 (nearest-even, saturating) is
 // monotone, so when y_lo and y_hi get the same code, that is the code of
 // fl32(x / scale).  Only when an e4m3 rounding boundary falls in the 2^-18
-// wide bracket (about once in 30000 elements) must the IEEE division be done;
-// callers do it in a warp-uniform branch.
+// wide bracket must the IEEE division decide: about once in 30000 elements
+// for data with full fp32 significands, but about once in 200 for bf16 data,
+// whose quotients often fall exactly on a boundary (448 x / amax is then a
+// ratio of small integers).  Callers therefore remember which pairs were
+// undecided and divide only those, in a warp-uniform branch.
 #pragma once
 
 #include <cstdint>
@@ -49,12 +52,13 @@ struct E4m3Bracket {
 };
 
 // Codes of fl32(x0 / scale) and fl32(x1 / scale), low byte first, when the
-// bracket decides them; sets `need` when it does not.
+// bracket decides them; `undecided` is set when it does not (branch-free, so
+// that the conversions of many pairs can be interleaved).
 __device__ __forceinline__ uint16_t e4m3_pair_bracketed(float x0, float x1, const E4m3Bracket& b,
-                                                        bool& need) {
+                                                        bool& undecided) {
   const uint16_t lo = cvt_e4m3x2(__fmul_rn(x0, b.lo), __fmul_rn(x1, b.lo));
   const uint16_t hi = cvt_e4m3x2(__fmul_rn(x0, b.hi), __fmul_rn(x1, b.hi));
-  need |= lo != hi;
+  undecided = lo != hi;
   return lo;
 }
 

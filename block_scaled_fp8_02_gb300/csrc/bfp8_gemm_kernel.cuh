@@ -726,21 +726,24 @@ __global__ void __launch_bounds__(GemmCfg<BN, SWAP, MODE>::kThreads, 1)
           const float scale = group_scale(amax);
           const E4m3Bracket br(scale);
           uint32_t codes[C::kCPT / 4];
-          bool need = false;
+          uint64_t undecided = 0;             // one bit per pair of columns
 #pragma unroll
           for (int i = 0; i < C::kCPT; i += 4) {
-            const uint32_t lo = e4m3_pair_bracketed(acc[i], acc[i + 1], br, need);
-            const uint32_t hi = e4m3_pair_bracketed(acc[i + 2], acc[i + 3], br, need);
+            bool u0 = false, u1 = false;
+            const uint32_t lo = e4m3_pair_bracketed(acc[i], acc[i + 1], br, u0);
+            const uint32_t hi = e4m3_pair_bracketed(acc[i + 2], acc[i + 3], br, u1);
             codes[i / 4] = lo | (hi << 16);
+            undecided |= (static_cast<uint64_t>(u0) << (i / 2)) |
+                         (static_cast<uint64_t>(u1) << (i / 2 + 1));
           }
-          // warp-uniform branch: IEEE divisions only where the bracket does not decide
-          if (__any_sync(0xffffffffu, need)) {
-            if (need) {
+          // warp-uniform branch: IEEE divisions only for the undecided pairs
+          if (__any_sync(0xffffffffu, undecided != 0)) {
 #pragma unroll
-              for (int i = 0; i < C::kCPT; i += 4) {
-                const uint32_t lo = e4m3_pair_divided(acc[i], acc[i + 1], scale);
-                const uint32_t hi = e4m3_pair_divided(acc[i + 2], acc[i + 3], scale);
-                codes[i / 4] = lo | (hi << 16);
+            for (int i = 0; i < C::kCPT; i += 2) {
+              if (undecided & (uint64_t{1} << (i / 2))) {
+                const uint32_t c = e4m3_pair_divided(acc[i], acc[i + 1], scale);
+                const int sh = (i & 2) * 8;
+                codes[i / 4] = (codes[i / 4] & ~(0xFFFFu << sh)) | (c << sh);
               }
             }
           }

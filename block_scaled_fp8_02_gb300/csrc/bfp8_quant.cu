@@ -190,14 +190,17 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32, kBlocksPerSm)
       // in warps where the bracket does not decide a code (warp-uniform branch)
       const E4m3Bracket br(scale);
       uint16_t pk[EPL / 2];
-      bool need = false;
+      uint32_t undecided = 0;                 // one bit per pair
 #pragma unroll
-      for (int e = 0; e < EPL; e += 2) pk[e / 2] = e4m3_pair_bracketed(v[e], v[e + 1], br, need);
-      if (__any_sync(0xffffffffu, need)) {
-        if (need) {
+      for (int e = 0; e < EPL; e += 2) {
+        bool u = false;
+        pk[e / 2] = e4m3_pair_bracketed(v[e], v[e + 1], br, u);
+        undecided |= static_cast<uint32_t>(u) << (e / 2);
+      }
+      if (__any_sync(0xffffffffu, undecided != 0)) {
 #pragma unroll
-          for (int e = 0; e < EPL; e += 2) pk[e / 2] = e4m3_pair_divided(v[e], v[e + 1], scale);
-        }
+        for (int e = 0; e < EPL; e += 2)
+          if (undecided & (1u << (e / 2))) pk[e / 2] = e4m3_pair_divided(v[e], v[e + 1], scale);
       }
       if (!valid) continue;
       uint8_t* qrow = q + static_cast<int64_t>(cur.rw[u]) * ld_q;

@@ -114,3 +114,24 @@ def test_quotients_next_to_e4m3_rounding_boundaries(oracle_mod, dev):
     x = torch.from_numpy(np.stack(rows))
     _check(oracle_mod, dev, x, True)
     _check(oracle_mod, dev, x, False)
+
+
+def test_exact_ties_from_bf16_inputs(oracle_mod, dev):
+    """Groups whose amax is 448 have scale exactly 1, so x / scale = x: every
+    bf16 value that is a midpoint between e4m3 values is an exact tie (to the
+    even code).  bf16 activations meet such exact ties often."""
+    rng = np.random.default_rng(17)
+    tab = oracle_mod.e4m3_table()
+    mags = np.sort(np.unique(np.abs(tab[np.isfinite(tab)])))
+    mids = ((mags[:-1] + mags[1:]) / 2).astype(np.float32)
+    rows = []
+    for r in range(64):
+        vals = rng.choice(mids, size=127) * rng.choice([-1.0, 1.0], size=127)
+        vals = np.concatenate([vals.astype(np.float32), [np.float32(448.0)]])
+        rng.shuffle(vals)
+        rows.append(vals)
+    x32 = torch.from_numpy(np.stack(rows).astype(np.float32))
+    xb = x32.to(torch.bfloat16)
+    assert torch.equal(xb.float(), x32)            # every midpoint is a bf16 value
+    _check(oracle_mod, dev, xb, True)
+    _check(oracle_mod, dev, xb, False)
