@@ -182,8 +182,14 @@ bfp8_status check_options(const bfp8_gemm_options* opt) {
   if (opt->schedule < 0 || opt->schedule > 2)
     return fail(BFP8_ERR_INVALID_ARG, "options.schedule = %d (expected 0, 1 or 2)", opt->schedule);
   if (opt->max_ctas < 0) return fail(BFP8_ERR_INVALID_ARG, "options.max_ctas = %d", opt->max_ctas);
-  if (opt->tile_n != 0 && opt->tile_n != 128 && opt->tile_n != 256)
-    return fail(BFP8_ERR_INVALID_ARG, "options.tile_n = %d (expected 0, 128 or 256)", opt->tile_n);
+  if (opt->tile_n != 0 && opt->tile_n != 16 && opt->tile_n != 32 && opt->tile_n != 64 &&
+      opt->tile_n != 128 && opt->tile_n != 256)
+    return fail(BFP8_ERR_INVALID_ARG, "options.tile_n = %d (expected 0, 16, 32, 64, 128 or 256)",
+                opt->tile_n);
+  if (opt->schedule == BFP8_SCHEDULE_WIDE && opt->tile_n != 0 && opt->tile_n != 128 &&
+      opt->tile_n != 256)
+    return fail(BFP8_ERR_INVALID_ARG, "options.tile_n = %d: wide tiles are 128 or 256 wide",
+                opt->tile_n);
   if (opt->prefetch_weights != 0 && opt->prefetch_weights != 1)
     return fail(BFP8_ERR_INVALID_ARG, "options.prefetch_weights = %d (expected 0 or 1)",
                 opt->prefetch_weights);
@@ -271,7 +277,10 @@ bfp8_status make_plan(int64_t M, int64_t N, int64_t K, int num_sms, const bfp8_g
   const int schedule = opt ? opt->schedule : BFP8_SCHEDULE_AUTO;
   p->swap = schedule == BFP8_SCHEDULE_SWAP_AB ||
             (schedule == BFP8_SCHEDULE_AUTO && M <= kSwapMaxM);
-  p->bn = p->swap ? swap_tile_n(M) : ((opt && opt->tile_n == 128) ? 128 : 256);
+  const int tn = opt ? opt->tile_n : 0;
+  if (!p->swap && tn != 0 && tn != 128 && tn != 256)
+    return fail(BFP8_ERR_INVALID_ARG, "options.tile_n = %d: wide tiles are 128 or 256 wide", tn);
+  p->bn = p->swap ? (tn ? tn : swap_tile_n(M)) : (tn == 128 ? 128 : 256);
   const int64_t G = cdiv(K, 128);
   const int64_t p_tiles = p->swap ? cdiv(N, 128) : cdiv(M, 128);
   const int64_t q_tiles = p->swap ? cdiv(M, p->bn) : cdiv(N, p->bn);

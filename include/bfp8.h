@@ -110,7 +110,9 @@ typedef enum {
 typedef struct {
   int schedule;        /* bfp8_schedule */
   int max_ctas;        /* cap on CTAs; 0 = one per SM */
-  int tile_n;          /* BFP8_SCHEDULE_WIDE only: 128 or 256 (0 = 256) */
+  int tile_n;          /* width of the second MMA operand's tile: wide 128 or
+                          256 (0 = 256); swap-AB 16, 32, 64, 128 or 256 (0 =
+                          the planner's choice for M) */
   int prefetch_weights;/* 1: the GEMM may start streaming B and Bs before the
                           kernel launched just before it on the stream has
                           finished (programmatic dependent launch).  Only valid

@@ -88,8 +88,11 @@ def test_gemm_rejects_bad_arguments_on_the_host(L):
     bad = bf.GemmOptions()
     bad.schedule = 9
     assert _gemm(L, opt=ctypes.pointer(bad)) == 1
-    bad.schedule, bad.tile_n = 0, 64
+    bad.schedule, bad.tile_n = 0, 48
     assert _gemm(L, opt=ctypes.pointer(bad)) == 1
+    bad.schedule, bad.tile_n = 2, 64                # wide tiles are 128 or 256 wide
+    assert _gemm(L, opt=ctypes.pointer(bad)) == 1
+    bad.schedule = 0
     bad.tile_n, bad.k_split = 0, 3
     assert _gemm(L, opt=ctypes.pointer(bad)) == 1
     for cs in (1, 9, -2):
