@@ -20,7 +20,7 @@ BFP8_OK = 0
 BFP8_IN_BF16 = 0
 BFP8_IN_F32 = 1
 SCHEDULE_AUTO, SCHEDULE_SWAP_AB, SCHEDULE_WIDE = 0, 1, 2
-KSPLIT_AUTO, KSPLIT_STREAM_K, KSPLIT_CLUSTER = 0, 1, 2
+KSPLIT_AUTO, KSPLIT_STREAM_K, KSPLIT_CLUSTER, KSPLIT_NONE = 0, 1, 2, 3
 STATUS_NAMES = {0: "BFP8_OK", 1: "BFP8_ERR_INVALID_ARG", 2: "BFP8_ERR_ALIGNMENT",
                 3: "BFP8_ERR_UNSUPPORTED", 4: "BFP8_ERR_CUDA", 5: "BFP8_ERR_WORKSPACE",
                 6: "BFP8_ERR_DEVICE_TIMEOUT"}

@@ -193,8 +193,8 @@ bfp8_status check_options(const bfp8_gemm_options* opt) {
   if (opt->prefetch_weights != 0 && opt->prefetch_weights != 1)
     return fail(BFP8_ERR_INVALID_ARG, "options.prefetch_weights = %d (expected 0 or 1)",
                 opt->prefetch_weights);
-  if (opt->k_split < 0 || opt->k_split > 2)
-    return fail(BFP8_ERR_INVALID_ARG, "options.k_split = %d (expected 0, 1 or 2)", opt->k_split);
+  if (opt->k_split < 0 || opt->k_split > 3)
+    return fail(BFP8_ERR_INVALID_ARG, "options.k_split = %d (expected 0 .. 3)", opt->k_split);
   if (opt->cluster_size != 0 && (opt->cluster_size < 2 || opt->cluster_size > kMaxCluster))
     return fail(BFP8_ERR_INVALID_ARG, "options.cluster_size = %d (expected 0 or 2..8)",
                 opt->cluster_size);
@@ -209,47 +209,96 @@ void estimate_cluster_caps(int sms, int* cap) {
     cap[cs] = cs < 2 ? sms : static_cast<int>(sms * (cs >= 7 ? 0.75 : 0.94) / cs);
 }
 
-// Relative time of the two ways of sharing K among CTAs, in units of one
-// (tile, k-block) step of one CTA.  Stream-K: the busiest CTA's steps plus
-// the fixup of a tile whose steps are spread over c CTAs, which reads the
-// c - 1 other partial tiles (128 x bn fp32 each) one after another from L2,
-// each costing about 1.5 steps of latency plus bn / 128 steps of transfer.
+// Relative time of the ways of sharing the work among CTAs, in units of one
+// (tile, k-block) step of one CTA (a cost model, calibrated on this GB300).
+//
+// Stream-K: the busiest CTA's whole-tile steps and stream-K steps, plus, for
+// each segment end it meets, writing its fp32 partial tile (128 x bn) and,
+// for the tile it finishes, reading the c - 1 other contributors' partials
+// one after another.  For the swap-AB tiles (small bn) the reading chain
+// dominates: 1.5 + bn / 128 steps per partial.  For wide tiles the partials
+// are large (128 KB at bn = 256) and measured on this GPU cost about 8 steps
+// per segment end written and 1.8 per partial read (scaled by bn / 256).
+double stream_k_cost(int64_t tiles, int64_t G, int bn, bool swap, int64_t max_ctas) {
+  const int64_t units = tiles * G;
+  const int64_t grid = max_ctas < units ? max_ctas : units;
+  const int64_t dp_per = (tiles / grid) * G;
+  const double sk_per = static_cast<double>((tiles % grid) * G) / static_cast<double>(grid);
+  if (sk_per <= 0.0) return static_cast<double>(dp_per);
+  const double ctas_per_tile = sk_per >= static_cast<double>(G) ? 1.0 : G / sk_per + 1.0;
+  const double segments = 1.0 + sk_per / static_cast<double>(G);
+  const double write = swap ? 0.0 : 8.0 * bn / 256.0;
+  const double read = swap ? 1.5 + bn / 128.0 : 1.8 * bn / 256.0;
+  return static_cast<double>(dp_per) + std::ceil(sk_per) + segments * write +
+         (ctas_per_tile - 1.0) * read;
+}
+// Whole tiles only: waves of tiles over at most max_ctas CTAs, nothing split.
+double whole_tiles_cost(int64_t tiles, int64_t G, int64_t max_ctas) {
+  return static_cast<double>((tiles + max_ctas - 1) / max_ctas * G);
+}
 // Cluster split-K of size cs: ceil(G / cs) steps per wave of co-resident
 // clusters, plus the reduction through distributed shared memory.
-double stream_k_cost(int64_t tiles, int64_t G, int bn, int64_t grid) {
-  const double per_cta = static_cast<double>(tiles * G) / static_cast<double>(grid);
-  const double ctas_per_tile = per_cta >= static_cast<double>(G) ? 1.0 : G / per_cta + 1.0;
-  return std::ceil(per_cta) + (ctas_per_tile - 1.0) * (1.5 + bn / 128.0);
-}
 double cluster_cost(int64_t tiles, int64_t G, int bn, int cs, int cap) {
   const int64_t waves = cap > 0 ? (tiles + cap - 1) / cap : tiles;
   return static_cast<double>(waves) *
          (static_cast<double>((G + cs - 1) / cs) + 0.5 + 0.5 * bn / 128.0);
 }
 
-// CTAs per tile for cluster split-K, or 0 for the persistent stream-K
-// schedule.  Clusters are considered only when the tiles alone would leave
-// SMs idle, with tiles * cs <= max_ctas and cs <= G.  An explicit
-// cluster_size is taken as given (clamped to G); otherwise the size with the
-// lowest cost above, and under AUTO only when it beats stream-K.
-uint32_t choose_cluster(int64_t tiles, int64_t G, int bn, int64_t max_ctas,
-                        const bfp8_gemm_options* opt, const int* cap) {
+enum class Split { kStreamK, kWholeTiles, kCluster };
+struct SplitChoice {
+  Split kind = Split::kStreamK;
+  uint32_t cs = 0;
+};
+
+// How the tiles and their k-blocks are shared out.  Explicit k_split values
+// are honoured (cluster only when the tiles alone would leave SMs idle, with
+// tiles * cs <= max_ctas and cs <= G; an explicit cluster_size is taken as
+// given, clamped to G); under AUTO the cheapest of the three by the model.
+SplitChoice choose_split(int64_t tiles, int64_t G, int bn, bool swap, int64_t max_ctas,
+                         const bfp8_gemm_options* opt, const int* cap) {
   const int ks = opt ? opt->k_split : BFP8_KSPLIT_AUTO;
-  if (ks == BFP8_KSPLIT_STREAM_K || tiles >= max_ctas || G < 2) return 0;
-  if (opt && opt->cluster_size > 0)
-    return static_cast<uint32_t>(opt->cluster_size < G ? opt->cluster_size : G);
-  int best = 0;
-  double best_cost = 0.0;
-  for (int cs = 2; cs <= kMaxCluster && cs <= G && tiles * cs <= max_ctas; ++cs) {
-    const double c = cluster_cost(tiles, G, bn, cs, cap[cs]);
-    if (best == 0 || c < best_cost) {
-      best = cs;
-      best_cost = c;
+  SplitChoice c;
+  if (ks == BFP8_KSPLIT_STREAM_K) return c;
+  if (ks == BFP8_KSPLIT_NONE) {
+    c.kind = Split::kWholeTiles;
+    return c;
+  }
+  int best_cs = 0;
+  double best_cl = 0.0;
+  if (tiles < max_ctas && G >= 2) {
+    if (opt && opt->cluster_size > 0) {
+      best_cs = static_cast<int>(opt->cluster_size < G ? opt->cluster_size : G);
+      best_cl = cluster_cost(tiles, G, bn, best_cs, cap[best_cs]);
+    } else {
+      for (int cs = 2; cs <= kMaxCluster && cs <= G && tiles * cs <= max_ctas; ++cs) {
+        const double v = cluster_cost(tiles, G, bn, cs, cap[cs]);
+        if (best_cs == 0 || v < best_cl) {
+          best_cs = cs;
+          best_cl = v;
+        }
+      }
     }
   }
-  if (best == 0) return 0;
-  if (ks == BFP8_KSPLIT_AUTO && best_cost >= stream_k_cost(tiles, G, bn, max_ctas)) return 0;
-  return static_cast<uint32_t>(best);
+  if (ks == BFP8_KSPLIT_CLUSTER) {
+    if (best_cs >= 2) {
+      c.kind = Split::kCluster;
+      c.cs = static_cast<uint32_t>(best_cs);
+    }
+    return c;
+  }
+  // AUTO
+  const double sk = stream_k_cost(tiles, G, bn, swap, max_ctas);
+  const double whole = whole_tiles_cost(tiles, G, max_ctas);
+  double best = sk;
+  if (whole < best) {
+    best = whole;
+    c.kind = Split::kWholeTiles;
+  }
+  if (best_cs >= 2 && best_cl < best) {
+    c.kind = Split::kCluster;
+    c.cs = static_cast<uint32_t>(best_cs);
+  }
+  return c;
 }
 
 // Stream-K tiles of a schedule (they each need a counter in the header).
@@ -294,13 +343,15 @@ bfp8_status make_plan(int64_t M, int64_t N, int64_t K, int num_sms, const bfp8_g
     estimate_cluster_caps(num_sms, est);
     cap = est;
   }
-  const uint32_t cs = choose_cluster(p_tiles * q_tiles, G, p->bn, max_ctas, opt, cap);
-  if (cs > 1)
-    p->sched = make_sched_cluster(static_cast<uint32_t>(p_tiles), static_cast<uint32_t>(q_tiles),
-                                  static_cast<uint32_t>(G), cs);
+  const SplitChoice sc = choose_split(p_tiles * q_tiles, G, p->bn, p->swap, max_ctas, opt, cap);
+  const uint32_t pt = static_cast<uint32_t>(p_tiles), qt = static_cast<uint32_t>(q_tiles);
+  const uint32_t g32 = static_cast<uint32_t>(G), mc = static_cast<uint32_t>(max_ctas);
+  if (sc.kind == Split::kCluster)
+    p->sched = make_sched_cluster(pt, qt, g32, sc.cs);
+  else if (sc.kind == Split::kWholeTiles)
+    p->sched = make_sched_whole_tiles(pt, qt, g32, mc);
   else
-    p->sched = make_sched(static_cast<uint32_t>(p_tiles), static_cast<uint32_t>(q_tiles),
-                          static_cast<uint32_t>(G), static_cast<uint32_t>(max_ctas));
+    p->sched = make_sched(pt, qt, g32, mc);
   p->relayout = unaligned || (K % 16) != 0;
   p->kp = p->relayout ? cdiv(K, 16) * 16 : K;
   size_t off = 0;

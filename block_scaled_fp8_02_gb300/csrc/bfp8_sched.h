@@ -40,7 +40,9 @@ struct Sched {
   uint32_t tiles;     // p_tiles * q_tiles
   uint32_t G;         // k-blocks per tile
   uint32_t grid;      // persistent CTAs
-  uint32_t dp_tiles;  // whole tiles handed out round-robin; a multiple of grid
+  uint32_t dp_tiles;  // whole tiles handed out round-robin (CTA p takes tiles
+                      // p, p + grid, ... below dp_tiles); a multiple of grid
+                      // when stream-K units follow
   uint32_t sk_units;  // (tiles - dp_tiles) * G
   uint32_t sk_q;      // stream-K units per CTA ...
   uint32_t sk_r;      // ... plus one for CTAs p < sk_r
@@ -69,12 +71,17 @@ BFP8_HD uint32_t sk_owner(const Sched& s, uint32_t u) {
   return u < big ? u / (s.sk_q + 1) : s.sk_r + (u - big) / s.sk_q;
 }
 
-BFP8_HD uint32_t dp_units(const Sched& s) { return (s.dp_tiles / s.grid) * s.G; }
+// Whole tiles of CTA p (all CTAs get the same number unless the schedule is
+// whole tiles only with a partly filled last wave).
+BFP8_HD uint32_t dp_tiles_of(const Sched& s, uint32_t p) {
+  return p < s.dp_tiles ? (s.dp_tiles - p + s.grid - 1) / s.grid : 0u;
+}
+BFP8_HD uint32_t dp_units(const Sched& s, uint32_t p) { return dp_tiles_of(s, p) * s.G; }
 
 BFP8_HD uint32_t num_units(const Sched& s, uint32_t p) {
   if (s.cluster > 1)
     return cluster_kb_end(s.G, s.cluster, p % s.cluster) - cluster_kb_begin(s.G, s.cluster, p % s.cluster);
-  return dp_units(s) + sk_begin(s, p + 1) - sk_begin(s, p);
+  return dp_units(s, p) + sk_begin(s, p + 1) - sk_begin(s, p);
 }
 
 // CTAs that contribute to stream-K tile ts, in ascending K order.
@@ -119,7 +126,7 @@ struct Cursor {
     grid = s.grid;
     p_tiles = s.p_tiles;
     dp_tiles = s.dp_tiles;
-    dp_per_cta = s.dp_tiles / s.grid;
+    dp_per_cta = dp_tiles_of(s, cta);
     sk_beg = sk_begin(s, cta);
     n = dp_per_cta * s.G + sk_begin(s, cta + 1) - sk_beg;
     j = 0;
@@ -205,6 +212,27 @@ inline Sched make_sched(uint32_t p_tiles, uint32_t q_tiles, uint32_t G, uint32_t
   s.sk_units = (s.tiles - s.dp_tiles) * G;
   s.sk_q = s.sk_units / s.grid;
   s.sk_r = s.sk_units % s.grid;
+  s.cluster = 0;
+  return s;
+}
+
+// Whole tiles only, balanced: waves = ceil(tiles / max_ctas) and grid =
+// ceil(tiles / waves), so every CTA takes waves or waves - 1 tiles and no
+// tile is split (some SMs may stay idle; no partial sums are exchanged).
+inline Sched make_sched_whole_tiles(uint32_t p_tiles, uint32_t q_tiles, uint32_t G,
+                                    uint32_t max_ctas) {
+  Sched s{};
+  s.p_tiles = p_tiles;
+  s.q_tiles = q_tiles;
+  s.tiles = p_tiles * q_tiles;
+  s.G = G;
+  const uint32_t mc = max_ctas < 1 ? 1 : max_ctas;
+  const uint32_t waves = (s.tiles + mc - 1) / mc;
+  s.grid = (s.tiles + waves - 1) / waves;
+  s.dp_tiles = s.tiles;
+  s.sk_units = 0;
+  s.sk_q = 0;
+  s.sk_r = 0;
   s.cluster = 0;
   return s;
 }

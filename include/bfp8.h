@@ -92,18 +92,21 @@ typedef enum {
   BFP8_SCHEDULE_WIDE = 2      /* activations fill it; 128 x 256 output tiles */
 } bfp8_schedule;
 
-/* How the K dimension is shared out when the output has fewer tiles than the
- * device has SMs (decode-sized M, or few weight rows). */
+/* How the output tiles and their K dimension are shared out among CTAs when
+ * the tiles do not fill whole waves of SMs (decode-sized M, few weight rows,
+ * or a partly filled last wave). */
 typedef enum {
-  BFP8_KSPLIT_AUTO = 0,      /* whichever a cost model of the two expects to be
-                                faster for the problem */
+  BFP8_KSPLIT_AUTO = 0,      /* the cheapest of the three below by a cost model
+                                of this GPU */
   BFP8_KSPLIT_STREAM_K = 1,  /* persistent CTAs; tiles left after whole waves are
                                 split into (tile, k-block) units, partial sums
                                 meet in the workspace */
-  BFP8_KSPLIT_CLUSTER = 2    /* thread-block clusters of 2..8 CTAs share a tile,
+  BFP8_KSPLIT_CLUSTER = 2,   /* thread-block clusters of 2..8 CTAs share a tile,
                                 each takes a slice of its k-blocks, and the
                                 partial tiles are added in distributed shared
                                 memory (no workspace traffic) */
+  BFP8_KSPLIT_NONE = 3       /* whole tiles only, balanced over ceil(tiles /
+                                waves) CTAs: nothing is split, some SMs may idle */
 } bfp8_ksplit;
 
 /* Optional tuning / test controls; a NULL options pointer means all zero. */
@@ -196,7 +199,9 @@ typedef struct {
   int relayout;         /* operands re-laid out into the workspace first */
   size_t workspace_bytes;
   int cluster;          /* CTAs per tile: > 1 for cluster split-K (grid =
-                           tiles * cluster, dp_tiles = sk_units = 0), else 1 */
+                           tiles * cluster, dp_tiles = sk_units = 0), else 1.
+                           Whole tiles only: dp_tiles = tiles, sk_units = 0,
+                           grid possibly below the SM count. */
 } bfp8_plan_info;
 
 bfp8_status bfp8_gemm_plan(int64_t M, int64_t N, int64_t K, int num_sms,

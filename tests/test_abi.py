@@ -93,7 +93,7 @@ def test_gemm_rejects_bad_arguments_on_the_host(L):
     bad.schedule, bad.tile_n = 2, 64                # wide tiles are 128 or 256 wide
     assert _gemm(L, opt=ctypes.pointer(bad)) == 1
     bad.schedule = 0
-    bad.tile_n, bad.k_split = 0, 3
+    bad.tile_n, bad.k_split = 0, 4
     assert _gemm(L, opt=ctypes.pointer(bad)) == 1
     for cs in (1, 9, -2):
         bad.k_split, bad.cluster_size = 2, cs
@@ -146,6 +146,8 @@ def _cover(M, N, K, sms, options=None):
     (1, 4096, 4096, 152, {"k_split": 1}), (3, 576, 7168, 152, {"k_split": 2}),
     (1, 4096, 300, 152, {"k_split": 2}), (5, 256, 1024, 152, {"k_split": 2, "cluster_size": 5}),
     (600, 512, 4096, 152, {"schedule": 2}), (7, 1000, 1000, 152, {"k_split": 2, "cluster_size": 7}),
+    (8192, 4096, 4096, 152, None), (1000, 1000, 1000, 152, {"k_split": 3}),
+    (3000, 4096, 512, 152, {"k_split": 3}), (1, 4096, 4096, 152, {"k_split": 3}),
 ])
 def test_work_split_covers_every_unit_once(L, M, N, K, sms, opts):
     _cover(M, N, K, sms, opts)
@@ -206,7 +208,15 @@ def test_plans_choose_the_documented_schedules(L):
     assert p["swap_ab"] == 1 and p["tile_n"] == 64
     p = bf.bfp8_gemm_plan(8192, 4096, 4096, 152)
     assert p["swap_ab"] == 0 and p["tile_n"] == 256 and p["tiles"] == 64 * 16
-    assert p["dp_tiles"] % 152 == 0 and p["dp_tiles"] > 0
+    # 1024 tiles = 6.7 waves: seven balanced waves of whole tiles on 147 CTAs
+    # beat splitting the last 112 tiles' 256-wide partials stream-K
+    assert p["dp_tiles"] == 1024 and p["sk_units"] == 0 and p["grid"] == 147
+    p = bf.bfp8_gemm_plan(1024, 4096, 4096, 152)         # 128 tiles: one wave, 24 SMs idle
+    assert p["grid"] == 128 and p["dp_tiles"] == 128 and p["sk_units"] == 0
+    p = bf.bfp8_gemm_plan(1536, 4096, 4096, 152)         # 192 tiles: stream-K wins
+    assert p["dp_tiles"] == 152 and p["sk_units"] == 40 * 32
+    p = bf.bfp8_gemm_plan(1536, 4096, 4096, 152, {"k_split": 3})
+    assert p["grid"] == 96 and p["dp_tiles"] == 192 and p["sk_units"] == 0
     p = bf.bfp8_gemm_plan(3, 1000, 1000, 152)
     assert p["relayout"] == 1                       # 1000-byte rows break the TMA stride rule
     assert bf.bfp8_gemm_plan(3, 1000, 1024, 152)["relayout"] == 0

@@ -74,7 +74,8 @@ PAGE = wl.correctness_case()
                                      {"schedule": 2, "tile_n": 128}, {"max_ctas": 7},
                                      {"schedule": 2, "max_ctas": 3}, {"schedule": 1, "max_ctas": 150},
                                      {"k_split": 1}, {"k_split": 2}, {"k_split": 2, "cluster_size": 3},
-                                     {"schedule": 2, "k_split": 2}])
+                                     {"schedule": 2, "k_split": 2}, {"k_split": 3},
+                                     {"schedule": 2, "k_split": 3, "max_ctas": 3}])
 def test_page_correctness_case_every_schedule(oracle_mod, dev, col_major, options):
     stats, _ = _run(oracle_mod, dev, PAGE, col_major, options, label=f"page {options}")
     assert stats["rel_diff"] < 1e-3
@@ -163,7 +164,8 @@ def test_cluster_split_k(oracle_mod, dev, M, N, K, cs):
 
 
 @pytest.mark.parametrize("options", [None, {"max_ctas": 5}, {"schedule": 2}, {"k_split": 2},
-                                     {"k_split": 2, "cluster_size": 8}, {"k_split": 1}])
+                                     {"k_split": 2, "cluster_size": 8}, {"k_split": 1},
+                                     {"k_split": 3}])
 def test_deterministic_across_calls(dev, options):
     case = wl.linear_case(96, 1024, 2048, seed=3)
     x = case["x"].to(dev)
