@@ -153,7 +153,13 @@ struct GemmCfg {
   static constexpr int kAsFloats = SWAP ? BN : 128;
   static constexpr int kBsChunks = SWAP ? 1 : BN / 128;
   static constexpr int kSlotFloats = kAsFloats + 4 * kBsChunks;
-  static constexpr int kScaleBytes = kSR * kSlotFloats * 4;
+  static constexpr int kScaleBytes = SWAP ? kSR * kSlotFloats * 4 : 0;
+  // Wide tiles need one activation and one weight scale per thread and unit;
+  // each promotion thread copies its own (cp.async, 4 bytes each) kSQ units
+  // ahead into a private queue in shared memory, so the producer's copy queue
+  // carries operand tiles only.
+  static constexpr int kSQ = 4;
+  static constexpr int kSqBytes = SWAP ? 0 : kSQ * 2 * kNE * 32 * 4;
   static constexpr int kSmemLimit = 232448;      // 227 KB per CTA
   // Wide tiles stage each promotion warp's bf16 output through shared memory,
   // 32 rows x 32 columns at a time (rows padded to 80 bytes: conflict-free),
@@ -162,7 +168,8 @@ struct GemmCfg {
   static constexpr int kOutBytes = SWAP ? 0 : kNE * 32 * kOutPitch;
   static constexpr int kPsumBytes = MODE == kModeGrouped ? kMaxExperts * 4 : 0;
   static constexpr int kStagesFit =
-      (kSmemLimit - 1024 /*align*/ - 384 /*barriers*/ - kScaleBytes - kOutBytes - kPsumBytes) /
+      (kSmemLimit - 1024 /*align*/ - 384 /*barriers*/ - kScaleBytes - kOutBytes - kPsumBytes -
+       kSqBytes) /
       kStageBytes;
   static constexpr int kStages = kStagesFit > 10 ? 10 : kStagesFit;
   static_assert(kStages >= 2, "ring too small");
@@ -173,7 +180,8 @@ struct GemmCfg {
   static constexpr int kOffScale = (kOffFlags + 8 + 15) / 16 * 16;
   static constexpr int kOffOut = (kOffScale + kScaleBytes + 127) / 128 * 128;
   static constexpr int kOffPsum = kOffOut + kOutBytes;
-  static constexpr int kSmemBytes = kOffPsum + kPsumBytes + 1024;
+  static constexpr int kOffSq = kOffPsum + kPsumBytes;
+  static constexpr int kSmemBytes = kOffSq + kSqBytes + 1024;
   // one CTA per SM (the planner's cluster capacities assume it)
   static_assert(2 * kSmemBytes > kSmemLimit + 1024, "two CTAs would fit on one SM");
   static constexpr int kTmemCols = tmem_cols_for(2 * BN);
@@ -393,7 +401,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, SWAP, MODE>::kThreads, 1)
         // B rows of this tile's expert (grouped mode) start at e_cur * N
         const int32_t q_row = static_cast<int32_t>(static_cast<int64_t>(e_cur) * a.N) +
                               static_cast<int32_t>(cur.q_tile * BN);
-        {
+        if (SWAP) {
           if (!mbar_wait_bounded(bar_sempty(ss), sph ^ 1u, a.wait_limit)) {
             fail(kDevTimeoutProducer);
             break;
@@ -523,33 +531,65 @@ __global__ void __launch_bounds__(GemmCfg<BN, SWAP, MODE>::kThreads, 1)
         (kGrouped && a.M > spsum[a.experts - 1]) ? spsum[a.experts - 1] : a.M;
     uint32_t e_tile = 0xFFFFFFFFu, e_cur = 0;      // expert of the current p tile (grouped)
 
+    // Wide tiles: this thread's scale queue (kSQ units of As and Bs values).
+    // One cp.async group per unit, committed even when empty, so that
+    // wait_group<kSQ - 1> always means "the oldest unit's copies have landed".
+    Cursor ahead = cur;
+    uint32_t ea_tile = 0xFFFFFFFFu, ea_cur = 0;    // expert of ahead's p tile (grouped)
+    const uint32_t sq_base = smem_addr(smem + C::kOffSq) + 4u * static_cast<uint32_t>(etid);
+    auto sq_as = [&](uint32_t slot) { return sq_base + 4u * (slot * 2 * C::kNE * 32); };
+    auto sq_bs = [&](uint32_t slot) { return sq_as(slot) + 4u * (C::kNE * 32); };
+    auto issue_scales = [&](uint32_t slot) {
+      if (ahead.valid()) {
+        if (kGrouped && ahead.p_tile != ea_tile) {
+          ea_tile = ahead.p_tile;
+          ea_cur = expert_of(spsum, a.experts, static_cast<int64_t>(ahead.p_tile) * 128);
+        }
+        int64_t m = static_cast<int64_t>(ahead.p_tile) * 128 + r;
+        if (m >= a.M) m = a.M - 1;                 // rows past M: any in-bounds scale
+        uint32_t nb = ahead.q_tile * (BN / 128) + static_cast<uint32_t>(col0 / 128);
+        if (nb >= static_cast<uint32_t>(a.NT)) nb = a.NT - 1;   // columns past N: not stored
+        cp_async_4(sq_as(slot), a.As + static_cast<int64_t>(ahead.kb) * a.ld_as + m, 4u);
+        cp_async_4(sq_bs(slot),
+                   a.Bs + (static_cast<int64_t>(ea_cur) * a.NT + nb) * s.G + ahead.kb, 4u);
+        ahead.next();
+      }
+      cp_async_commit();
+    };
+    if (!SWAP) {
+#pragma unroll 1
+      for (uint32_t d = 0; d < C::kSQ; ++d) issue_scales(d);
+    }
+    const volatile float* sq_as_ptr =
+        reinterpret_cast<const volatile float*>(smem + C::kOffSq) + etid;
+
     unsigned long long t_ewait = 0, t_ework = 0, t_escale = 0, t_efix = 0;
     (void)t_ewait; (void)t_ework; (void)t_escale; (void)t_efix;
     for (; cur.valid(); cur.next()) {
       BFP8_CLK(e0);
       const uint32_t j = cur.j;
-      if (!mbar_wait_bounded(bar_sfull(ss), sph, a.wait_limit)) {
-        fail(kDevTimeoutEpilogue);
-        break;
-      }
-      const float* slot = sRing + ss * C::kSlotFloats;
       float sr;                 // row scale (wide: As * Bs; swap: Bs)
+      const float* sq = nullptr;              // column scales (swap)
       if (!SWAP) {
         if (kGrouped && cur.p_tile != e_tile) {
           e_tile = cur.p_tile;
           e_cur = expert_of(spsum, a.experts, static_cast<int64_t>(cur.p_tile) * 128);
         }
-        const uint32_t hb = col0 / 128;         // this thread's 128-column weight block
-        const uint32_t nb = cur.q_tile * (BN / 128) + hb;
-        const float bsv =
-            nb < static_cast<uint32_t>(a.NT)
-                ? slot[C::kAsFloats + 4 * hb + (((e_cur * a.NT + nb) * s.G + cur.kb) & 3)]
-                : 0.f;
-        sr = slot[r] * bsv;
+        const uint32_t slot = j % C::kSQ;
+        cp_async_wait<C::kSQ - 1>();            // this unit's scales have landed
+        const float asv = sq_as_ptr[slot * 2 * C::kNE * 32];
+        const float bsv = sq_as_ptr[slot * 2 * C::kNE * 32 + C::kNE * 32];
+        sr = asv * bsv;
+        issue_scales(slot);                     // the unit kSQ ahead reuses the slot
       } else {
+        if (!mbar_wait_bounded(bar_sfull(ss), sph, a.wait_limit)) {
+          fail(kDevTimeoutEpilogue);
+          break;
+        }
+        const float* slot = sRing + ss * C::kSlotFloats;
         sr = slot[C::kAsFloats + ((cur.p_tile * s.G + cur.kb) & 3)];
+        sq = slot + col0;
       }
-      const float* sq = slot + col0;          // column scales (swap)
       BFP8_ACC(t_escale, e0);
       BFP8_CLK(e1);
       const int b = j & 1;
@@ -598,9 +638,11 @@ __global__ void __launch_bounds__(GemmCfg<BN, SWAP, MODE>::kThreads, 1)
       __syncwarp();
       if (lane == 0) {
         mbar_arrive(bar_tempty(b));
-        mbar_arrive(bar_sempty(ss));
+        if (SWAP) mbar_arrive(bar_sempty(ss));
       }
-      if (++ss == C::kSR) { ss = 0; sph ^= 1u; }
+      if (SWAP) {
+        if (++ss == C::kSR) { ss = 0; sph ^= 1u; }
+      }
       BFP8_ACC(t_ework, e2);
 
       if (!cur.last()) continue;
@@ -827,6 +869,8 @@ __global__ void __launch_bounds__(GemmCfg<BN, SWAP, MODE>::kThreads, 1)
       }
       BFP8_ACC(t_efix, e3);
     }
+    // no scale copy may still be landing in shared memory when the CTA ends
+    if (!SWAP) cp_async_wait<0>();
     if (s.cluster > 1) {
       // ---- cluster split-K reduction.  After the first cluster barrier every
       // CTA's partial is in its shared memory.  The output tile's valid part,
