@@ -144,22 +144,24 @@ struct GemmCfg {
   static constexpr int kStageBytes = kPBytes + kQBytes;
   // Scales: the producer bulk-copies each unit's activation-scale slice
   // (column-major, contiguous) and a 16-byte chunk holding each weight scale
-  // into a kSR-deep ring of slots, independent of the operand ring so that it
-  // runs further ahead (the library hands the kernel scales in that layout).
-  // Slot layout (floats):
+  // into a kSR-deep ring of slots (the library hands the kernel scales in
+  // that layout).  Slot layout (floats):
   //   [0, kAsFloats)                       As of the tile's rows (wide) / columns (swap)
   //   [kAsFloats + 4h, kAsFloats + 4h + 4) 16-byte chunk containing Bs of block h
-  static constexpr int kSR = 8;
+  // Swap tiles: the ring has its own full / empty barriers and runs ahead of
+  // the operand ring.  Wide tiles: unit j's slot (j mod kSR) is copied with
+  // unit j's operand tiles and completes on the same stage barrier; the MMA
+  // issuer waits for that barrier before the MMAs whose completion the
+  // promotion warps wait for, so no barrier of its own is needed.  The slot
+  // is free again once unit j - kSR has been promoted: the producer writes it
+  // after the MMAs of unit j - kStages have completed, which were issued after
+  // the promotion of unit j - kStages - kTB, hence kSR >= kStages + kTB.
+  static constexpr int kSR = SWAP ? 8 : 12;
+  static constexpr int kSRB = SWAP ? kSR : 0;    // scale-ring barriers (swap only)
   static constexpr int kAsFloats = SWAP ? BN : 128;
   static constexpr int kBsChunks = SWAP ? 1 : BN / 128;
   static constexpr int kSlotFloats = kAsFloats + 4 * kBsChunks;
-  static constexpr int kScaleBytes = SWAP ? kSR * kSlotFloats * 4 : 0;
-  // Wide tiles need one activation and one weight scale per thread and unit;
-  // each promotion thread copies its own (cp.async, 4 bytes each) kSQ units
-  // ahead into a private queue in shared memory, so the producer's copy queue
-  // carries operand tiles only.
-  static constexpr int kSQ = 4;
-  static constexpr int kSqBytes = SWAP ? 0 : kSQ * 2 * kNE * 32 * 4;
+  static constexpr int kScaleBytes = kSR * kSlotFloats * 4;
   static constexpr int kSmemLimit = 232448;      // 227 KB per CTA
   // Wide tiles stage each promotion warp's bf16 output through shared memory,
   // 32 rows x 32 columns at a time (rows padded to 80 bytes: conflict-free),
@@ -168,23 +170,27 @@ struct GemmCfg {
   static constexpr int kOutBytes = SWAP ? 0 : kNE * 32 * kOutPitch;
   static constexpr int kPsumBytes = MODE == kModeGrouped ? kMaxExperts * 4 : 0;
   static constexpr int kStagesFit =
-      (kSmemLimit - 1024 /*align*/ - 384 /*barriers*/ - kScaleBytes - kOutBytes - kPsumBytes -
-       kSqBytes) /
+      (kSmemLimit - 1024 /*align*/ - 384 /*barriers*/ - kScaleBytes - kOutBytes - kPsumBytes) /
       kStageBytes;
   static constexpr int kStages = kStagesFit > 10 ? 10 : kStagesFit;
   static_assert(kStages >= 2, "ring too small");
-  // barriers: full, empty [kStages]; sfull, sempty [kSR]; tfull, tempty [2]
+  // TMEM accumulator buffers: the MMA of a unit may start while the
+  // promotion warps still read the kTB - 1 units before it.  512 columns
+  // hold two 256-column or four 128-column buffers.
+  static constexpr int kTB = (!SWAP && BN == 128) ? 4 : 2;
+  static_assert(SWAP || kSR >= kStages + kTB, "wide scale slots reused too early");
+  // barriers: full, empty [kStages]; sfull, sempty [kSRB]; tfull, tempty [kTB]
   static constexpr int kOffBars = kStages * kStageBytes;
-  static constexpr int kOffTmemPtr = kOffBars + (2 * kStages + 2 * kSR + 4) * 8;
+  static constexpr int kOffTmemPtr = kOffBars + (2 * kStages + 2 * kSRB + 2 * kTB) * 8;
+  static_assert(kOffTmemPtr + 16 - kOffBars <= 384, "barrier area");
   static constexpr int kOffFlags = kOffTmemPtr + 8;
   static constexpr int kOffScale = (kOffFlags + 8 + 15) / 16 * 16;
   static constexpr int kOffOut = (kOffScale + kScaleBytes + 127) / 128 * 128;
   static constexpr int kOffPsum = kOffOut + kOutBytes;
-  static constexpr int kOffSq = kOffPsum + kPsumBytes;
-  static constexpr int kSmemBytes = kOffSq + kSqBytes + 1024;
+  static constexpr int kSmemBytes = kOffPsum + kPsumBytes + 1024;
   // one CTA per SM (the planner's cluster capacities assume it)
   static_assert(2 * kSmemBytes > kSmemLimit + 1024, "two CTAs would fit on one SM");
-  static constexpr int kTmemCols = tmem_cols_for(2 * BN);
+  static constexpr int kTmemCols = tmem_cols_for(kTB * BN);
   // Cluster split-K: a CTA's partial tile goes into its (then idle) operand
   // ring, laid out so that the reduction reads it contiguously along the
   // output's inner dimension (n): swap tiles as [column][row] with a 132-float
@@ -285,10 +291,10 @@ __global__ void __launch_bounds__(GemmCfg<BN, SWAP, MODE>::kThreads, 1)
   auto bar_full = [&](int i) { return sbase + C::kOffBars + 8u * i; };
   auto bar_empty = [&](int i) { return sbase + C::kOffBars + 8u * (C::kStages + i); };
   auto bar_sfull = [&](int i) { return sbase + C::kOffBars + 8u * (2 * C::kStages + i); };
-  auto bar_sempty = [&](int i) { return sbase + C::kOffBars + 8u * (2 * C::kStages + C::kSR + i); };
-  auto bar_tfull = [&](int b) { return sbase + C::kOffBars + 8u * (2 * C::kStages + 2 * C::kSR + b); };
+  auto bar_sempty = [&](int i) { return sbase + C::kOffBars + 8u * (2 * C::kStages + C::kSRB + i); };
+  auto bar_tfull = [&](int b) { return sbase + C::kOffBars + 8u * (2 * C::kStages + 2 * C::kSRB + b); };
   auto bar_tempty = [&](int b) {
-    return sbase + C::kOffBars + 8u * (2 * C::kStages + 2 * C::kSR + 2 + b);
+    return sbase + C::kOffBars + 8u * (2 * C::kStages + 2 * C::kSRB + C::kTB + b);
   };
   auto stage_p = [&](int i) { return sbase + static_cast<uint32_t>(i * C::kStageBytes); };
   auto stage_q = [&](int i) { return sbase + static_cast<uint32_t>(i * C::kStageBytes + C::kPBytes); };
@@ -308,11 +314,11 @@ __global__ void __launch_bounds__(GemmCfg<BN, SWAP, MODE>::kThreads, 1)
       mbar_init(bar_full(i), 1);
       mbar_init(bar_empty(i), 1);
     }
-    for (int i = 0; i < C::kSR; ++i) {
+    for (int i = 0; i < C::kSRB; ++i) {
       mbar_init(bar_sfull(i), 1);
       mbar_init(bar_sempty(i), C::kNE);    // one arrival per promotion warp
     }
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < C::kTB; ++b) {
       mbar_init(bar_tfull(b), 1);
       mbar_init(bar_tempty(b), C::kNE);      // one arrival per promotion warp
     }
@@ -375,6 +381,35 @@ __global__ void __launch_bounds__(GemmCfg<BN, SWAP, MODE>::kThreads, 1)
       int ss = 0;
       uint32_t sph = 0;
       const uint32_t sring = smem_addr(smem + C::kOffScale);
+      // Scales of the unit at c (expert e): the As slice of its rows (wide) /
+      // columns (swap) and the 16-byte chunk holding each weight scale, copied
+      // into ring slot `slot`, completing on barrier `bar`.
+      auto scale_as_bytes = [&](const Cursor& c) -> uint32_t {
+        const int64_t m0 = SWAP ? static_cast<int64_t>(c.q_tile) * BN
+                                : static_cast<int64_t>(c.p_tile) * 128;
+        int64_t n_as = a.ld_as - m0;                   // stay inside the As allocation
+        if (n_as > C::kAsFloats) n_as = C::kAsFloats;
+        return static_cast<uint32_t>(n_as) * 4u;
+      };
+      auto copy_scales = [&](const Cursor& c, uint32_t e, int slot_idx, uint32_t bar) {
+        const int64_t kb = c.kb;
+        const uint32_t slot = sring + 4u * (slot_idx * C::kSlotFloats);
+        const int64_t m0 = SWAP ? static_cast<int64_t>(c.q_tile) * BN
+                                : static_cast<int64_t>(c.p_tile) * 128;
+        bulk_load(slot, a.As + kb * a.ld_as + m0, scale_as_bytes(c), bar);
+#pragma unroll
+        for (int h = 0; h < C::kBsChunks; ++h) {
+          int64_t nb = SWAP ? static_cast<int64_t>(c.p_tile)
+                            : static_cast<int64_t>(c.q_tile) * (BN / 128) + h;
+          if (nb >= a.NT) nb = a.NT - 1;               // block past N: any in-bounds value
+          const int64_t ei = (static_cast<int64_t>(e) * a.NT + nb) * s.G + kb;
+          bulk_load(slot + 4u * (C::kAsFloats + 4 * h), a.Bs + (ei & ~int64_t{3}), 16u, bar);
+        }
+      };
+      // wide tiles: bytes of a unit's stage barrier (operand tiles + scales)
+      auto stage_tx = [&](const Cursor& c) -> uint32_t {
+        return C::kStageBytes + (SWAP ? 0u : scale_as_bytes(c) + 16u * C::kBsChunks);
+      };
       // With prefetch_b, the weight tiles of the first stages are requested
       // before waiting for the preceding grid; their stages are then completed
       // with the activation tiles below.
@@ -382,7 +417,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, SWAP, MODE>::kThreads, 1)
       if (a.prefetch_b) {
         Cursor pc = cur;
         for (; pre < static_cast<uint32_t>(C::kStages) && pc.valid(); ++pre, pc.next()) {
-          mbar_arrive_expect_tx(bar_full(pre), C::kStageBytes);
+          mbar_arrive_expect_tx(bar_full(pre), stage_tx(pc));
           const int32_t x = static_cast<int32_t>(pc.kb * 128);
           if (SWAP)
             tma_load_2d(stage_p(pre), &tmP, bar_full(pre), x, static_cast<int32_t>(pc.p_tile * 128));
@@ -406,24 +441,8 @@ __global__ void __launch_bounds__(GemmCfg<BN, SWAP, MODE>::kThreads, 1)
             fail(kDevTimeoutProducer);
             break;
           }
-          const int64_t kb = cur.kb;
-          const uint32_t slot = sring + 4u * (ss * C::kSlotFloats);
-          const int64_t m0 = SWAP ? static_cast<int64_t>(cur.q_tile) * BN
-                                  : static_cast<int64_t>(cur.p_tile) * 128;
-          int64_t n_as = a.ld_as - m0;                 // stay inside the As allocation
-          if (n_as > C::kAsFloats) n_as = C::kAsFloats;
-          const uint32_t as_bytes = static_cast<uint32_t>(n_as) * 4u;
-          mbar_arrive_expect_tx(bar_sfull(ss), as_bytes + 16u * C::kBsChunks);
-          bulk_load(slot, a.As + kb * a.ld_as + m0, as_bytes, bar_sfull(ss));
-#pragma unroll
-          for (int h = 0; h < C::kBsChunks; ++h) {
-            int64_t nb = SWAP ? static_cast<int64_t>(cur.p_tile)
-                              : static_cast<int64_t>(cur.q_tile) * (BN / 128) + h;
-            if (nb >= a.NT) nb = a.NT - 1;             // block past N: any in-bounds value
-            const int64_t e = (static_cast<int64_t>(e_cur) * a.NT + nb) * s.G + kb;
-            bulk_load(slot + 4u * (C::kAsFloats + 4 * h), a.Bs + (e & ~int64_t{3}), 16u,
-                      bar_sfull(ss));
-          }
+          mbar_arrive_expect_tx(bar_sfull(ss), scale_as_bytes(cur) + 16u * C::kBsChunks);
+          copy_scales(cur, e_cur, ss, bar_sfull(ss));
           ++prod_sissued;
           if (++ss == C::kSR) { ss = 0; sph ^= 1u; }
         }
@@ -440,10 +459,12 @@ __global__ void __launch_bounds__(GemmCfg<BN, SWAP, MODE>::kThreads, 1)
           else
             tma_load_2d(stage_p(st), &tmP, bar_full(st), x, static_cast<int32_t>(cur.p_tile * 128));
         } else {
-          mbar_arrive_expect_tx(bar_full(st), C::kStageBytes);
+          mbar_arrive_expect_tx(bar_full(st), stage_tx(cur));
           tma_load_2d(stage_p(st), &tmP, bar_full(st), x, static_cast<int32_t>(cur.p_tile * 128));
           tma_load_2d(stage_q(st), &tmQ, bar_full(st), x, SWAP ? static_cast<int32_t>(cur.q_tile * BN) : q_row);
         }
+        // wide tiles: this unit's scales complete on the same stage barrier
+        if (!SWAP) copy_scales(cur, e_cur, static_cast<int>(issued % C::kSR), bar_full(st));
         if (issued == 0) trace_event(a.trace, cta, kTrProdFirst);
         ++issued;
         if (++st == C::kStages) { st = 0; ph ^= 1u; }
@@ -451,8 +472,8 @@ __global__ void __launch_bounds__(GemmCfg<BN, SWAP, MODE>::kThreads, 1)
       trace_event(a.trace, cta, kTrProdDone);
       trace_value(a.trace, cta, kTrProdWait, t_wait);
       // When every role finishes normally, every copy has landed (the MMA
-      // issuer waited for each operand stage, the promotion warps for each
-      // scale slot); otherwise the copies are drained at the end.
+      // issuer waited for each operand stage, the swap-tile promotion warps
+      // for each scale slot); otherwise the copies are drained at the end.
       prod_issued = issued;
     } else if (warp == C::kNE + 1 && lane == 0) {
       // -------------------------------------------------------- MMA issuer
@@ -463,8 +484,8 @@ __global__ void __launch_bounds__(GemmCfg<BN, SWAP, MODE>::kThreads, 1)
       unsigned long long t_tmem = 0, t_data = 0;
       (void)t_tmem; (void)t_data;
       for (uint32_t j = 0; j < n; ++j) {
-        const int b = j & 1;
-        const uint32_t tph = (j >> 1) & 1;
+        const int b = static_cast<int>(j % C::kTB);
+        const uint32_t tph = (j / C::kTB) & 1;
         BFP8_CLK(c0);
         const bool ok_t = mbar_wait_bounded(bar_tempty(b), tph ^ 1u, a.wait_limit);
         BFP8_ACC(t_tmem, c0);
@@ -495,7 +516,8 @@ __global__ void __launch_bounds__(GemmCfg<BN, SWAP, MODE>::kThreads, 1)
       // The last commit fires when every MMA issued above has completed.
       if (done > 0 && done < n) {
         const uint32_t j = done - 1;
-        if (!mbar_wait_bounded(bar_tfull(j & 1), (j >> 1) & 1, a.wait_limit)) fail(kDevTimeoutTail);
+        if (!mbar_wait_bounded(bar_tfull(static_cast<int>(j % C::kTB)), (j / C::kTB) & 1, a.wait_limit))
+          fail(kDevTimeoutTail);
       }
     }
     __syncwarp();
@@ -531,56 +553,18 @@ __global__ void __launch_bounds__(GemmCfg<BN, SWAP, MODE>::kThreads, 1)
         (kGrouped && a.M > spsum[a.experts - 1]) ? spsum[a.experts - 1] : a.M;
     uint32_t e_tile = 0xFFFFFFFFu, e_cur = 0;      // expert of the current p tile (grouped)
 
-    // Wide tiles: this thread's scale queue (kSQ units of As and Bs values).
-    // One cp.async group per unit, committed even when empty, so that
-    // wait_group<kSQ - 1> always means "the oldest unit's copies have landed".
-    Cursor ahead = cur;
-    uint32_t ea_tile = 0xFFFFFFFFu, ea_cur = 0;    // expert of ahead's p tile (grouped)
-    const uint32_t sq_base = smem_addr(smem + C::kOffSq) + 4u * static_cast<uint32_t>(etid);
-    auto sq_as = [&](uint32_t slot) { return sq_base + 4u * (slot * 2 * C::kNE * 32); };
-    auto sq_bs = [&](uint32_t slot) { return sq_as(slot) + 4u * (C::kNE * 32); };
-    auto issue_scales = [&](uint32_t slot) {
-      if (ahead.valid()) {
-        if (kGrouped && ahead.p_tile != ea_tile) {
-          ea_tile = ahead.p_tile;
-          ea_cur = expert_of(spsum, a.experts, static_cast<int64_t>(ahead.p_tile) * 128);
-        }
-        int64_t m = static_cast<int64_t>(ahead.p_tile) * 128 + r;
-        if (m >= a.M) m = a.M - 1;                 // rows past M: any in-bounds scale
-        uint32_t nb = ahead.q_tile * (BN / 128) + static_cast<uint32_t>(col0 / 128);
-        if (nb >= static_cast<uint32_t>(a.NT)) nb = a.NT - 1;   // columns past N: not stored
-        cp_async_4(sq_as(slot), a.As + static_cast<int64_t>(ahead.kb) * a.ld_as + m, 4u);
-        cp_async_4(sq_bs(slot),
-                   a.Bs + (static_cast<int64_t>(ea_cur) * a.NT + nb) * s.G + ahead.kb, 4u);
-        ahead.next();
-      }
-      cp_async_commit();
-    };
-    if (!SWAP) {
-#pragma unroll 1
-      for (uint32_t d = 0; d < C::kSQ; ++d) issue_scales(d);
-    }
-    const volatile float* sq_as_ptr =
-        reinterpret_cast<const volatile float*>(smem + C::kOffSq) + etid;
-
     unsigned long long t_ewait = 0, t_ework = 0, t_escale = 0, t_efix = 0;
     (void)t_ewait; (void)t_ework; (void)t_escale; (void)t_efix;
     for (; cur.valid(); cur.next()) {
       BFP8_CLK(e0);
       const uint32_t j = cur.j;
-      float sr;                 // row scale (wide: As * Bs; swap: Bs)
+      float sr = 0.f;           // row scale (wide: As * Bs; swap: Bs)
       const float* sq = nullptr;              // column scales (swap)
       if (!SWAP) {
         if (kGrouped && cur.p_tile != e_tile) {
           e_tile = cur.p_tile;
           e_cur = expert_of(spsum, a.experts, static_cast<int64_t>(cur.p_tile) * 128);
         }
-        const uint32_t slot = j % C::kSQ;
-        cp_async_wait<C::kSQ - 1>();            // this unit's scales have landed
-        const float asv = sq_as_ptr[slot * 2 * C::kNE * 32];
-        const float bsv = sq_as_ptr[slot * 2 * C::kNE * 32 + C::kNE * 32];
-        sr = asv * bsv;
-        issue_scales(slot);                     // the unit kSQ ahead reuses the slot
       } else {
         if (!mbar_wait_bounded(bar_sfull(ss), sph, a.wait_limit)) {
           fail(kDevTimeoutEpilogue);
@@ -592,8 +576,8 @@ __global__ void __launch_bounds__(GemmCfg<BN, SWAP, MODE>::kThreads, 1)
       }
       BFP8_ACC(t_escale, e0);
       BFP8_CLK(e1);
-      const int b = j & 1;
-      if (!mbar_wait_bounded(bar_tfull(b), (j >> 1) & 1, a.wait_limit)) {
+      const int b = static_cast<int>(j % C::kTB);
+      if (!mbar_wait_bounded(bar_tfull(b), (j / C::kTB) & 1, a.wait_limit)) {
         fail(kDevTimeoutEpilogue);
         break;
       }
@@ -614,6 +598,18 @@ __global__ void __launch_bounds__(GemmCfg<BN, SWAP, MODE>::kThreads, 1)
         uint32_t v[C::kBatch];
 #pragma unroll
         for (int h = 0; h < C::kBatch; h += C::kCH) tmem_ld_cols<C::kCH>(taddr + c0 + h, v + h);
+        if (!SWAP && c0 == 0) {
+          // wide tiles: the scale slot landed before the MMAs were issued; it
+          // is read while the first TMEM loads are in flight
+          const float* slot = sRing + (j % C::kSR) * C::kSlotFloats;
+          const uint32_t hb = col0 / 128;       // this thread's 128-column weight block
+          const uint32_t nb = cur.q_tile * (BN / 128) + hb;
+          const float bsv =
+              nb < static_cast<uint32_t>(a.NT)
+                  ? slot[C::kAsFloats + 4 * hb + (((e_cur * a.NT + nb) * s.G + cur.kb) & 3)]
+                  : 0.f;
+          sr = slot[r] * bsv;
+        }
         tmem_wait_ld();
         reg_fence<C::kBatch>(v);
         // element (row r, column c) gets scale sr (wide) or sr * As[c] (swap);
@@ -870,7 +866,6 @@ __global__ void __launch_bounds__(GemmCfg<BN, SWAP, MODE>::kThreads, 1)
       BFP8_ACC(t_efix, e3);
     }
     // no scale copy may still be landing in shared memory when the CTA ends
-    if (!SWAP) cp_async_wait<0>();
     if (s.cluster > 1) {
       // ---- cluster split-K reduction.  After the first cluster barrier every
       // CTA's partial is in its shared memory.  The output tile's valid part,

@@ -248,25 +248,6 @@ __host__ __device__ constexpr uint32_t idesc_e4m3_f32(int m, int n) {
 
 // ------------------------------------------------------ cp.async (sm80) ---
 
-// 4-byte copy global -> shared; src_bytes = 0 writes zero without reading.
-__device__ __forceinline__ void cp_async_4(uint32_t dst, const void* src, uint32_t src_bytes) {
-  asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(dst), "l"(src),
-               "r"(src_bytes)
-               : "memory");
-}
-// Arrives on the barrier (without raising its expected count) once every
-// cp.async this thread issued so far has completed.
-__device__ __forceinline__ void cp_async_mbar_arrive_noinc(uint32_t bar) {
-  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() {
-  asm volatile("cp.async.commit_group;" ::: "memory");
-}
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
-
 // ------------------------------------------ programmatic dependent launch ---
 
 // Waits until the grids this grid depends on (launched before it in the stream)
