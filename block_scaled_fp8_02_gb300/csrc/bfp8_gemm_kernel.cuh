@@ -143,11 +143,13 @@ struct GemmCfg {
   static constexpr int kQBytes = BN * 128;
   static constexpr int kStageBytes = kPBytes + kQBytes;
   // Scales: the producer bulk-copies each unit's activation-scale slice
-  // (column-major, contiguous) and a 16-byte chunk holding each weight scale
-  // into a kSR-deep ring of slots (the library hands the kernel scales in
-  // that layout).  Slot layout (floats):
+  // (column-major, contiguous) into a kSR-deep ring of slots (the library
+  // hands the kernel scales in that layout).  Slot layout (floats):
   //   [0, kAsFloats)                       As of the tile's rows (wide) / columns (swap)
-  //   [kAsFloats + 4h, kAsFloats + 4h + 4) 16-byte chunk containing Bs of block h
+  //   [kAsFloats, kAsFloats + 4)           swap tiles: 16-byte chunk containing Bs
+  // Wide tiles read their weight scales straight from global memory instead
+  // (one load per lane covers 32 units; every bulk copy added to a unit's
+  // stage lengthens the producer's per-unit issue time).
   // Swap tiles: the ring has its own full / empty barriers and runs ahead of
   // the operand ring.  Wide tiles: unit j's slot (j mod kSR) is copied with
   // unit j's operand tiles and completes on the same stage barrier; the MMA
@@ -159,7 +161,7 @@ struct GemmCfg {
   static constexpr int kSR = SWAP ? 8 : 12;
   static constexpr int kSRB = SWAP ? kSR : 0;    // scale-ring barriers (swap only)
   static constexpr int kAsFloats = SWAP ? BN : 128;
-  static constexpr int kBsChunks = SWAP ? 1 : BN / 128;
+  static constexpr int kBsChunks = SWAP ? 1 : 0;
   static constexpr int kSlotFloats = kAsFloats + 4 * kBsChunks;
   static constexpr int kScaleBytes = kSR * kSlotFloats * 4;
   static constexpr int kSmemLimit = 232448;      // 227 KB per CTA
@@ -552,6 +554,11 @@ __global__ void __launch_bounds__(GemmCfg<BN, SWAP, MODE>::kThreads, 1)
     const int64_t m_lim =
         (kGrouped && a.M > spsum[a.experts - 1]) ? spsum[a.experts - 1] : a.M;
     uint32_t e_tile = 0xFFFFFFFFu, e_cur = 0;      // expert of the current p tile (grouped)
+    // Wide tiles: lane i holds the weight scale of this thread's column block
+    // for k-block kb_win + i (loaded at each segment start and every 32
+    // units; a shuffle hands each unit's value to the whole warp)
+    float bs_win = 0.f;
+    uint32_t kb_win = 0;
 
     unsigned long long t_ewait = 0, t_ework = 0, t_escale = 0, t_efix = 0;
     (void)t_ewait; (void)t_ework; (void)t_escale; (void)t_efix;
@@ -564,6 +571,14 @@ __global__ void __launch_bounds__(GemmCfg<BN, SWAP, MODE>::kThreads, 1)
         if (kGrouped && cur.p_tile != e_tile) {
           e_tile = cur.p_tile;
           e_cur = expert_of(spsum, a.experts, static_cast<int64_t>(cur.p_tile) * 128);
+        }
+        if (cur.first() || cur.kb >= kb_win + 32) {
+          kb_win = cur.kb;
+          const uint32_t nb = cur.q_tile * (BN / 128) + static_cast<uint32_t>(col0 / 128);
+          const uint32_t kbl = kb_win + static_cast<uint32_t>(lane);
+          bs_win = (nb < static_cast<uint32_t>(a.NT) && kbl < s.G)
+                       ? __ldg(a.Bs + (static_cast<int64_t>(e_cur) * a.NT + nb) * s.G + kbl)
+                       : 0.f;   // columns past N are not stored
         }
       } else {
         if (!mbar_wait_bounded(bar_sfull(ss), sph, a.wait_limit)) {
@@ -602,12 +617,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, SWAP, MODE>::kThreads, 1)
           // wide tiles: the scale slot landed before the MMAs were issued; it
           // is read while the first TMEM loads are in flight
           const float* slot = sRing + (j % C::kSR) * C::kSlotFloats;
-          const uint32_t hb = col0 / 128;       // this thread's 128-column weight block
-          const uint32_t nb = cur.q_tile * (BN / 128) + hb;
-          const float bsv =
-              nb < static_cast<uint32_t>(a.NT)
-                  ? slot[C::kAsFloats + 4 * hb + (((e_cur * a.NT + nb) * s.G + cur.kb) & 3)]
-                  : 0.f;
+          const float bsv = __shfl_sync(0xffffffffu, bs_win, static_cast<int>(cur.kb - kb_win));
           sr = slot[r] * bsv;
         }
         tmem_wait_ld();
