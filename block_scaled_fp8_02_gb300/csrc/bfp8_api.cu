@@ -217,8 +217,8 @@ void estimate_cluster_caps(int sms, int* cap) {
 // for the tile it finishes, reading the c - 1 other contributors' partials
 // one after another.  For the swap-AB tiles (small bn) the reading chain
 // dominates: 1.5 + bn / 128 steps per partial.  For wide tiles the partials
-// are large (128 KB at bn = 256) and measured on this GPU cost about 8 steps
-// per segment end written and 1.8 per partial read (scaled by bn / 256).
+// are large (128 KB at bn = 256) and measured on this GPU cost about 12 steps
+// per segment end written and 3.5 per partial read (scaled by bn / 256).
 double stream_k_cost(int64_t tiles, int64_t G, int bn, bool swap, int64_t max_ctas) {
   const int64_t units = tiles * G;
   const int64_t grid = max_ctas < units ? max_ctas : units;
@@ -227,8 +227,8 @@ double stream_k_cost(int64_t tiles, int64_t G, int bn, bool swap, int64_t max_ct
   if (sk_per <= 0.0) return static_cast<double>(dp_per);
   const double ctas_per_tile = sk_per >= static_cast<double>(G) ? 1.0 : G / sk_per + 1.0;
   const double segments = 1.0 + sk_per / static_cast<double>(G);
-  const double write = swap ? 0.0 : 8.0 * bn / 256.0;
-  const double read = swap ? 1.5 + bn / 128.0 : 1.8 * bn / 256.0;
+  const double write = swap ? 0.0 : 12.0 * bn / 256.0;
+  const double read = swap ? 1.5 + bn / 128.0 : 3.5 * bn / 256.0;
   return static_cast<double>(dp_per) + std::ceil(sk_per) + segments * write +
          (ctas_per_tile - 1.0) * read;
 }

@@ -213,10 +213,18 @@ def test_plans_choose_the_documented_schedules(L):
     assert p["dp_tiles"] == 1024 and p["sk_units"] == 0 and p["grid"] == 147
     p = bf.bfp8_gemm_plan(1024, 4096, 4096, 152)         # 128 tiles: one wave, 24 SMs idle
     assert p["grid"] == 128 and p["dp_tiles"] == 128 and p["sk_units"] == 0
-    p = bf.bfp8_gemm_plan(1536, 4096, 4096, 152)         # 192 tiles: stream-K wins
-    assert p["dp_tiles"] == 152 and p["sk_units"] == 40 * 32
-    p = bf.bfp8_gemm_plan(1536, 4096, 4096, 152, {"k_split": 3})
+    # 192 tiles: two balanced waves of whole tiles beat splitting 40 tiles'
+    # 256-wide partials over 152 CTAs
+    p = bf.bfp8_gemm_plan(1536, 4096, 4096, 152)
     assert p["grid"] == 96 and p["dp_tiles"] == 192 and p["sk_units"] == 0
+    p = bf.bfp8_gemm_plan(1536, 4096, 4096, 152, {"k_split": 1})
+    assert p["dp_tiles"] == 152 and p["sk_units"] == 40 * 32
+    p = bf.bfp8_gemm_plan(4096, 4096, 4096, 152)         # 512 tiles: four waves of 128
+    assert p["grid"] == 128 and p["sk_units"] == 0
+    # 320 tiles of 64 k-blocks: a third wave of 16 tiles costs more than
+    # sharing their k-blocks stream-K
+    p = bf.bfp8_gemm_plan(2048, 5120, 8192, 152)
+    assert p["dp_tiles"] == 304 and p["sk_units"] == 16 * 64
     p = bf.bfp8_gemm_plan(3, 1000, 1000, 152)
     assert p["relayout"] == 1                       # 1000-byte rows break the TMA stride rule
     assert bf.bfp8_gemm_plan(3, 1000, 1024, 152)["relayout"] == 0

@@ -64,13 +64,14 @@ def test_noalloc_matches_the_regular_entry_point_twice_in_a_row(dev, M, N, K):
 
 
 def test_noalloc_rejects_problems_beyond_its_scratch(dev):
-    M, N, K = 1536, 4096, 4096            # 192 tiles: stream-K needs ~40 MB of partial sums
+    M, N, K = 2048, 5120, 8192            # 320 tiles: stream-K needs ~40 MB of partial sums
     need = bf.bfp8_gemm_workspace_size(M, N, K)
     assert need > ctypes.c_size_t(16 << 20).value
+    G, NT = K // 128, N // 128
     A = torch.zeros((M, K), dtype=torch.uint8, device=dev).view(torch.float8_e4m3fn)
     B = torch.zeros((N, K), dtype=torch.uint8, device=dev).view(torch.float8_e4m3fn)
-    As = torch.ones((32, M), device=dev).t()
-    Bs = torch.ones((32, 32), device=dev)
+    As = torch.ones((G, M), device=dev).t()
+    Bs = torch.ones((NT, G), device=dev)
     out = torch.zeros((M, N), dtype=torch.bfloat16, device=dev)
     assert _call_noalloc(A, B, As, Bs, out) == 5            # BFP8_ERR_WORKSPACE
     assert "scratch" in bf.bfp8_last_error()
