@@ -17,12 +17,13 @@
 // Roles (one CTA per SM, persistent):
 //   warps 0 .. NE-1  promotion / epilogue warps; warp w reads TMEM lanes
 //                    32*(w%4) .. +31 and column half w/4
-//   warp  NE         TMA producer (one lane): A/B tiles into a STAGES-deep ring
+//   warp  NE         TMA producer (one lane): A/B tiles into a STAGES-deep ring,
+//                    and each unit's activation-scale slice
 //   warp  NE+1       TMEM owner and MMA issuer (one lane)
 //   (the 256-wide tile adds two idle warps so that the non-epilogue warps form
 //   a whole warpgroup that can hand registers to the epilogue via setmaxnreg)
-// TMEM holds two partial buffers of BN columns, so the MMA of block kb+1 runs
-// while block kb is promoted.
+// TMEM holds two partial buffers of BN columns (four of 128 on 128-wide
+// tiles), so the MMA of block kb+1 runs while block kb is promoted.
 //
 // SWAP = false: MMA M slot = 128 activation rows, N slot = BN weight rows
 //               (large M).

@@ -120,6 +120,20 @@ def test_edge_shapes(oracle_mod, dev, M, N, K, options):
     _run(oracle_mod, dev, case, options=options, label=f"edge {M}x{N}x{K} {options}")
 
 
+@pytest.mark.parametrize("options", [{"schedule": 2, "k_split": 1, "max_ctas": 7},
+                                     {"schedule": 2, "k_split": 1, "max_ctas": 45},
+                                     {"schedule": 2, "k_split": 3, "max_ctas": 5},
+                                     {"schedule": 2, "tile_n": 128, "k_split": 1, "max_ctas": 11}])
+def test_wide_weight_scale_windows(oracle_mod, dev, options):
+    """Wide tiles read each column block's weight scales 32 k-blocks at a
+    time, reloading at every segment start and every 32 units: stream-K runs
+    over odd CTA counts start segments at k-blocks that are not multiples of
+    32, and 56 k-blocks per tile cross a window boundary inside a segment."""
+    case = wl.ragged_case(1000, 1000, 7168, seed=41)
+    _run(oracle_mod, dev, case, rows=sample_rows(1000, 48, seed=5),
+         label=f"windows {options}")
+
+
 def test_unaligned_operands_and_output(oracle_mod, dev):
     """A and B starting 1 byte past a 16-byte boundary take the re-layout path;
     an output whose rows are not 16-byte aligned takes the element stores."""
