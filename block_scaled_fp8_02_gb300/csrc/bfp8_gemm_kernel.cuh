@@ -231,6 +231,8 @@ enum : int {
   kTrMmaAtSync = 17,   // MMA lane reaches it
   kTrEpiAtSync = 18,   // promotion warp 0 reaches it (partial parked)
   kTrEpiReduced = 19,  // promotion warp 0 done with its share of the reduction
+  kTrMmaLoopCyc = 20,  // SM cycles of the MMA issuer's loop (with kTrMmaFirst /
+                       // kTrMmaDone: the SM clock while it ran)
   kTraceEvents = 24
 };
 #if defined(BFP8_TRACE)
@@ -486,6 +488,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, SWAP, MODE>::kThreads, 1)
       uint32_t done = 0;
       unsigned long long t_tmem = 0, t_data = 0;
       (void)t_tmem; (void)t_data;
+      BFP8_CLK(cl0);
       for (uint32_t j = 0; j < n; ++j) {
         const int b = static_cast<int>(j % C::kTB);
         const uint32_t tph = (j / C::kTB) & 1;
@@ -516,6 +519,9 @@ __global__ void __launch_bounds__(GemmCfg<BN, SWAP, MODE>::kThreads, 1)
       trace_event(a.trace, cta, kTrMmaDone);
       trace_value(a.trace, cta, kTrMmaWaitTmem, t_tmem);
       trace_value(a.trace, cta, kTrMmaWaitData, t_data);
+#if defined(BFP8_TRACE)
+      trace_value(a.trace, cta, kTrMmaLoopCyc, static_cast<unsigned long long>(clock64() - cl0));
+#endif
       // The last commit fires when every MMA issued above has completed.
       if (done > 0 && done < n) {
         const uint32_t j = done - 1;
