@@ -164,6 +164,26 @@ bfp8_status encode_operand(CUtensorMap* map, const void* ptr, int64_t rows, int6
   return BFP8_OK;
 }
 
+// Tensor map over the bf16 output [rows, cols] (row stride cols * 2 bytes,
+// 16-byte aligned), box 32 x 32 with the 64-byte swizzle, for the wide
+// tiles' TMA stores.
+bfp8_status encode_output(CUtensorMap* map, void* ptr, int64_t rows, int64_t cols) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc;
+  bfp8_status st = get_encoder(&enc);
+  if (st != BFP8_OK) return st;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 2u};
+  const cuuint32_t box[2] = {32u, 32u};
+  const cuuint32_t estr[2] = {1u, 1u};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, ptr, dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+                   CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    return fail(BFP8_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d) for the [%lld x %lld] output",
+                (int)r, (long long)rows, (long long)cols);
+  return BFP8_OK;
+}
+
 inline int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 inline size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
@@ -684,6 +704,12 @@ static bfp8_status gemm_impl(const void* A, const void* B, const float* As, int 
   a.counters = reinterpret_cast<int*>(ws ? ws + p.off_counters : nullptr);
   a.partials = reinterpret_cast<float*>(ws ? ws + p.off_partials : nullptr);
   a.vec_store = (!misaligned(out, 16) && (N % 8) == 0) ? 1 : 0;
+  // wide plain / fused tiles store through TMA (grouped tiles mask rows)
+  a.tma_store = 0;
+  if (!p.swap && !psum && a.vec_store) {
+    if ((st = encode_output(&a.tmO, out, M, N)) != BFP8_OK) return st;
+    a.tma_store = 1;
+  }
   // weight prefetch also needs the weight operand untouched by re-layout (and,
   // in grouped mode, the expert of each tile, known only after the wait)
   a.prefetch_b = (opt && opt->prefetch_weights == 1 && !p.relayout && bs_ok && !psum) ? 1 : 0;

@@ -54,6 +54,10 @@ enum : int {
 };
 
 struct GemmArgs {
+  // Tensor map over out ([M, N] bf16, box 32 x 32, 64-byte swizzle) for the
+  // wide tiles' TMA stores; set when tma_store (out 16-byte aligned, N % 8 == 0).
+  CUtensorMap tmO;
+  int32_t tma_store;
   const float* As;       // activation scales, column-major As[kb * ld_as + m],
   int64_t ld_as;         //   16-byte aligned, ld_as % 4 == 0
   int32_t NT;            // rows of Bs = ceil(N / 128); Bs row stride = G
@@ -167,10 +171,15 @@ struct GemmCfg {
   static constexpr int kScaleBytes = kSR * kSlotFloats * 4;
   static constexpr int kSmemLimit = 232448;      // 227 KB per CTA
   // Wide tiles stage each promotion warp's bf16 output through shared memory,
-  // 32 rows x 32 columns at a time (rows padded to 80 bytes: conflict-free),
-  // so that global stores write whole 32-byte sectors along a row.
+  // 32 rows x 32 columns at a time.  Plain and fused tiles: a 2 KB tile in the
+  // TMA store's 64-byte swizzle (conflict-free for lane-per-row 16-byte
+  // writes), stored by one 2-D TMA store.  Grouped tiles, whose rows past the
+  // last expert must not be written: rows padded to 80 bytes, read back and
+  // stored by the warp with row masks (whole 32-byte sectors along a row).
+  static constexpr bool kTmaStore = !SWAP && MODE != kModeGrouped;
   static constexpr int kOutPitch = 80;
-  static constexpr int kOutBytes = SWAP ? 0 : kNE * 32 * kOutPitch;
+  static constexpr int kOutTile = kTmaStore ? 2048 : 32 * kOutPitch;
+  static constexpr int kOutBytes = SWAP ? 0 : kNE * kOutTile;
   static constexpr int kPsumBytes = MODE == kModeGrouped ? kMaxExperts * 4 : 0;
   static constexpr int kStagesFit =
       (kSmemLimit - 1024 /*align*/ - 384 /*barriers*/ - kScaleBytes - kOutBytes - kPsumBytes) /
@@ -188,7 +197,7 @@ struct GemmCfg {
   static_assert(kOffTmemPtr + 16 - kOffBars <= 384, "barrier area");
   static constexpr int kOffFlags = kOffTmemPtr + 8;
   static constexpr int kOffScale = (kOffFlags + 8 + 15) / 16 * 16;
-  static constexpr int kOffOut = (kOffScale + kScaleBytes + 127) / 128 * 128;
+  static constexpr int kOffOut = (kOffScale + kScaleBytes + 1023) / 1024 * 1024;
   static constexpr int kOffPsum = kOffOut + kOutBytes;
   static constexpr int kSmemBytes = kOffPsum + kPsumBytes + 1024;
   // one CTA per SM (the planner's cluster capacities assume it)
@@ -277,7 +286,7 @@ __device__ __forceinline__ void reg_fence(uint32_t* v) {
 template <int BN, bool SWAP, int MODE>
 __global__ void __launch_bounds__(GemmCfg<BN, SWAP, MODE>::kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmP, const __grid_constant__ CUtensorMap tmQ,
-                const GemmArgs a) {
+                const __grid_constant__ GemmArgs a) {
 #if defined(__CUDA_ARCH__)
   using C = GemmCfg<BN, SWAP, MODE>;
   static_assert(MODE == kModePlain || !SWAP, "grouped and fused variants use wide tiles");
@@ -822,11 +831,38 @@ __global__ void __launch_bounds__(GemmCfg<BN, SWAP, MODE>::kThreads, 1)
       }
       if (kFused && !a.store_out) {
         // fused epilogue without the bf16 output
+      } else if (C::kTmaStore && a.tma_store) {
+        // rows of 16-byte-aligned bf16: 32 columns at a time into this warp's
+        // 2 KB tile (16-byte chunk c of row i at 64 i + 16 (c ^ ((i >> 1) & 3)),
+        // the 64-byte swizzle), then one TMA store of the 32 x 32 box; rows
+        // past M and columns past N are not written
+        uint8_t* stg = smem + C::kOffOut + warp * C::kOutTile;
+        const uint32_t stg_s = smem_addr(stg);
+        const int32_t y = static_cast<int32_t>(cur.p_tile * 128 + quad * 32);
+        const int32_t x0 = static_cast<int32_t>(cur.q_tile * BN + col0);
+#pragma unroll
+        for (int ch = 0; ch < C::kCPT; ch += 32) {
+          if (lane == 0) bulk_wait_group_read<0>();   // the previous store has read the tile
+          __syncwarp();
+#pragma unroll
+          for (int g = 0; g < 4; ++g) {
+            const float* f = acc + ch + 8 * g;
+            *reinterpret_cast<uint4*>(stg + lane * 64 + 16 * (g ^ ((lane >> 1) & 3))) =
+                make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]),
+                           pack_bf16x2(f[4], f[5]), pack_bf16x2(f[6], f[7]));
+          }
+          fence_proxy_async_smem();                  // generic writes -> TMA reads
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_2d(&a.tmO, stg_s, x0 + ch, y);
+            bulk_commit_group();
+          }
+        }
       } else if (!SWAP && a.vec_store) {
         // rows of 16-byte-aligned bf16 (N % 8 == 0): through this warp's
         // staging rows, 32 columns at a time; lanes 4i..4i+3 then store one
         // row's 64 contiguous bytes
-        uint8_t* stg = smem + C::kOffOut + warp * (32 * C::kOutPitch);
+        uint8_t* stg = smem + C::kOffOut + warp * C::kOutTile;
         const int64_t mrow0 = static_cast<int64_t>(cur.p_tile) * 128 + quad * 32;
         const int64_t nbase = static_cast<int64_t>(cur.q_tile) * BN + col0;
 #pragma unroll
@@ -882,7 +918,9 @@ __global__ void __launch_bounds__(GemmCfg<BN, SWAP, MODE>::kThreads, 1)
       }
       BFP8_ACC(t_efix, e3);
     }
-    // no scale copy may still be landing in shared memory when the CTA ends
+    // this warp's TMA stores have completed (their staging tile is read and
+    // the output written) before the CTA ends
+    if (C::kTmaStore && lane == 0) bulk_wait_group<0>();
     if (s.cluster > 1) {
       // ---- cluster split-K reduction.  After the first cluster barrier every
       // CTA's partial is in its shared memory.  The output tile's valid part,
