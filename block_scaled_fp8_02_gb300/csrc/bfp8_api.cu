@@ -235,10 +235,10 @@ void estimate_cluster_caps(int sms, int* cap) {
 // Stream-K: the busiest CTA's whole-tile steps and stream-K steps, plus, for
 // each segment end it meets, writing its fp32 partial tile (128 x bn) and,
 // for the tile it finishes, reading the c - 1 other contributors' partials
-// one after another.  For the swap-AB tiles (small bn) the reading chain
-// dominates: 1.5 + bn / 128 steps per partial.  For wide tiles the partials
-// are large (128 KB at bn = 256) and measured on this GPU cost about 12 steps
-// per segment end written and 3.5 per partial read (scaled by bn / 256).
+// one after another.  Fitted to measured times on this GPU, per 256 columns
+// of partial: writing 12 steps on wide tiles and 4 on swap-AB tiles (whose
+// steps are shorter-lived weight streams), reading 3.5 steps on wide tiles
+// and 1.5 + bn / 128 per partial on swap-AB tiles.
 double stream_k_cost(int64_t tiles, int64_t G, int bn, bool swap, int64_t max_ctas) {
   const int64_t units = tiles * G;
   const int64_t grid = max_ctas < units ? max_ctas : units;
@@ -247,7 +247,7 @@ double stream_k_cost(int64_t tiles, int64_t G, int bn, bool swap, int64_t max_ct
   if (sk_per <= 0.0) return static_cast<double>(dp_per);
   const double ctas_per_tile = sk_per >= static_cast<double>(G) ? 1.0 : G / sk_per + 1.0;
   const double segments = 1.0 + sk_per / static_cast<double>(G);
-  const double write = swap ? 0.0 : 12.0 * bn / 256.0;
+  const double write = (swap ? 4.0 : 12.0) * bn / 256.0;
   const double read = swap ? 1.5 + bn / 128.0 : 3.5 * bn / 256.0;
   return static_cast<double>(dp_per) + std::ceil(sk_per) + segments * write +
          (ctas_per_tile - 1.0) * read;

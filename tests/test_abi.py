@@ -196,6 +196,13 @@ def test_plans_choose_the_documented_schedules(L):
     assert bf.bfp8_gemm_plan(83, 576, 7168, 152)["cluster"] == 8
     # 40 tiles of 200 k-blocks: stream-K's 53 steps per CTA beat 67 in clusters of 3
     assert bf.bfp8_gemm_plan(1, 5120, 25600, 152)["cluster"] == 1
+    # ... but not with 256-wide swap tiles, whose 128 KB partials are costly
+    # to write and read (measured: clusters of 3 60.9 us, stream-K 65.8 us)
+    assert bf.bfp8_gemm_plan(256, 5120, 25600, 152)["cluster"] == 3
+    # 80 tiles of 40 k-blocks: stream-K over 152 CTAs beats one wave of 80
+    # whole tiles (measured 37.4 against 39.3 us)
+    p = bf.bfp8_gemm_plan(256, 10240, 5120, 152)
+    assert p["cluster"] == 1 and p["sk_units"] > 0
     # wide tiles: 64 of them at M = 512, clusters of 2
     p = bf.bfp8_gemm_plan(512, 4096, 4096, 152)
     assert p["swap_ab"] == 0 and p["cluster"] == 2 and p["grid"] == 128
