@@ -209,24 +209,34 @@ def barrier(world: int):
 
 # ------------------------------------------------------------ CPU oracle ---
 
-def oracle_sample(Ms, nk, budget_s, seed=1234):
+def oracle_setup(nk, seed=1234):
+    """Weights, weight scales and a one-row calibration of the oracle GEMM
+    (prepared once; not part of any timed sample)."""
+    import numpy as np
+    import oracle
+    from block_scaled_fp8_02_gb300 import workloads as wl
+    B = wl.e4m3_codes(nk, nk, seed).numpy()
+    G = (nk + 127) // 128
+    Bs = (1e-4 + np.random.default_rng(seed).random((G if nk else 1, G)) * (1e-2 - 1e-4)).astype(np.float32)
+    Bs = Bs[: (nk + 127) // 128]
+    x1 = wl.activations(1, nk, seed).view(__import__("torch").int16).numpy().view(np.uint16)
+    A1, As1 = oracle.group_quant(x1, False, True)
+    t0 = time.perf_counter()
+    oracle.blocked_gemm(A1, B, As1, True, Bs, threads=1)
+    per_row_cpu = max(time.perf_counter() - t0, 1e-4)
+    return {"B": B, "Bs": Bs, "per_row_cpu": per_row_cpu, "cores": oracle.default_threads()}
+
+
+def oracle_sample(Ms, nk, budget_s, seed=1234, setup=None):
     """Times the oracle (quantise + blocked GEMM, all host cores) on the first
     rows of each M in the sweep, sized to about `budget_s` seconds of wall time
     on those cores.  Returns (flops, seconds, cores, description)."""
     import numpy as np
     import oracle
     from block_scaled_fp8_02_gb300 import workloads as wl
-    cores = oracle.default_threads()
-    B = wl.e4m3_codes(nk, nk, seed).numpy()
-    G = (nk + 127) // 128
-    Bs = (1e-4 + np.random.default_rng(seed).random((G if nk else 1, G)) * (1e-2 - 1e-4)).astype(np.float32)
-    Bs = Bs[: (nk + 127) // 128]
-    # calibrate: one row of the GEMM
-    x1 = wl.activations(1, nk, seed).view(__import__("torch").int16).numpy().view(np.uint16)
-    A1, As1 = oracle.group_quant(x1, False, True)
-    t0 = time.perf_counter()
-    oracle.blocked_gemm(A1, B, As1, True, Bs, threads=1)
-    per_row_cpu = max(time.perf_counter() - t0, 1e-4)
+    if setup is None:
+        setup = oracle_setup(nk, seed)
+    B, Bs, per_row_cpu, cores = setup["B"], setup["Bs"], setup["per_row_cpu"], setup["cores"]
     # rows the cores get through in the budget, spread evenly over the M
     # values (small M values take all their rows; the rest go to larger ones)
     rows_total = max(len(Ms), int(budget_s * cores / per_row_cpu))
@@ -707,12 +717,14 @@ def run_reference(args, rank, world):
     Ms = sweep_ms(args)
     nk = args.nk
     total_steps = args.steps + args.warmup
-    budget_per_step = max(0.05, min(2.0, 150.0 / max(total_steps, 1)))
+    # about 100 s of oracle work in all, whatever the step count
+    budget_per_step = max(0.05, min(2.0, 100.0 / max(total_steps, 1)))
+    setup = oracle_setup(nk, seed=99)
     times, flops_list = [], []
     cores = None
     desc = None
     for i in range(total_steps):
-        fl, secs, cores, desc = oracle_sample(Ms, nk, budget_per_step, seed=99 + i)
+        fl, secs, cores, desc = oracle_sample(Ms, nk, budget_per_step, seed=99 + i, setup=setup)
         if i >= args.warmup:
             times.append(secs)
             flops_list.append(fl)
