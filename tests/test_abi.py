@@ -5,6 +5,7 @@ import ctypes
 import os
 import re
 
+import numpy as np
 import pytest
 
 import block_scaled_fp8_02_gb300 as bf
@@ -151,6 +152,25 @@ def _cover(M, N, K, sms, options=None):
 ])
 def test_work_split_covers_every_unit_once(L, M, N, K, sms, opts):
     _cover(M, N, K, sms, opts)
+
+
+def test_auto_plans_cover_every_unit_on_random_shapes(L):
+    """The planner's automatic choice (stream-K, whole tiles or clusters,
+    swap-AB or wide tiles) hands every (tile, k-block) unit to exactly one
+    CTA, in contiguous runs, on seeded random shapes and SM counts."""
+    rng = np.random.default_rng(2024)
+    done = 0
+    while done < 40:
+        M = int(rng.integers(1, 6000))
+        N = int(rng.integers(1, 9000))
+        K = int(rng.integers(1, 9000))
+        sms = int(rng.choice([152, 148, 132, 19, 7]))
+        plan = bf.bfp8_gemm_plan(M, N, K, sms)
+        if plan["tiles"] * plan["k_blocks"] > 20000:
+            continue
+        assert 1 <= plan["grid"] <= max(sms, plan["tiles"] * max(plan["cluster"], 1))
+        _cover(M, N, K, sms, None)
+        done += 1
 
 
 def _cluster_units(M, N, K, sms, options):
