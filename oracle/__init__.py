@@ -16,6 +16,12 @@ Functions and the passages they follow:
                              bf16 output, same snippet.
   bf16_from_f64              round-to-nearest-even to bfloat16 (the snippet's
                              out_dtype = torch.bfloat16).
+  ceil_pow2 / group_quant(ue8m0=True)
+                             the UE8M0 scale variant of the transformers DeepGEMM
+                             integration (`_ceil_to_ue8m0`; `_select_fp8_cast_kwargs`
+                             with use_ue8m0): each scale amax/448 rounded up to a
+                             power of two before the codes are computed; weight
+                             scales rounded the same way.
   bias_add_bf16              the bias addition of the transformers DeepGEMM
                              integration's `deepgemm_fp8_fp4_linear`
                              (`output.add_(bias)` on bf16 tensors): one IEEE fp32
@@ -80,6 +86,10 @@ def _load():
             lib.oracle_group_quant.restype = ctypes.c_int
             lib.oracle_group_quant.argtypes = [P, ctypes.c_int, i64, i64, i64, ctypes.c_int, i64,
                                                P, i64, P]
+            lib.oracle_group_quant_ue8m0.restype = ctypes.c_int
+            lib.oracle_group_quant_ue8m0.argtypes = lib.oracle_group_quant.argtypes
+            lib.oracle_ceil_pow2.restype = ctypes.c_float
+            lib.oracle_ceil_pow2.argtypes = [ctypes.c_float]
             lib.oracle_blocked_gemm.restype = ctypes.c_int
             lib.oracle_blocked_gemm.argtypes = [P, P, P, ctypes.c_int, i64, P, i64, i64, i64,
                                                 P, i64, P, P, P, ctypes.c_int]
@@ -124,11 +134,20 @@ def scale_ld(M: int) -> int:
     return (M + 3) // 4 * 4
 
 
-def group_quant(x: np.ndarray, is_f32: bool, col_major: bool, ld_s: int | None = None):
+def ceil_pow2(s) -> np.ndarray:
+    """Each positive finite fp32 scale rounded up to the nearest power of two."""
+    s = np.asarray(s, dtype=np.float32)
+    f = _load().oracle_ceil_pow2
+    return np.array([f(float(v)) for v in s.reshape(-1)], dtype=np.float32).reshape(s.shape)
+
+
+def group_quant(x: np.ndarray, is_f32: bool, col_major: bool, ld_s: int | None = None,
+                ue8m0: bool = False):
     """Quantise x [M, K] (float32 values, or bfloat16 bits as uint16).
 
     Returns (q uint8 [M, K], s float32) where s is [G, ld_s] for column-major
-    scales and [M, ld_s] for row-major ones (G = ceil(K/128)).
+    scales and [M, ld_s] for row-major ones (G = ceil(K/128)).  ue8m0: every
+    scale rounded up to a power of two before the codes are computed.
     """
     x = np.ascontiguousarray(x, dtype=np.float32 if is_f32 else np.uint16)
     M, K = x.shape
@@ -137,8 +156,8 @@ def group_quant(x: np.ndarray, is_f32: bool, col_major: bool, ld_s: int | None =
         ld_s = scale_ld(M) if col_major else G
     q = np.empty((M, K), dtype=np.uint8)
     s = np.empty((G, ld_s) if col_major else (M, ld_s), dtype=np.float32)
-    rc = _load().oracle_group_quant(_ptr(x), int(is_f32), M, K, K, int(col_major), ld_s,
-                                    _ptr(q), K, _ptr(s))
+    fn = _load().oracle_group_quant_ue8m0 if ue8m0 else _load().oracle_group_quant
+    rc = fn(_ptr(x), int(is_f32), M, K, K, int(col_major), ld_s, _ptr(q), K, _ptr(s))
     if rc != 0:
         raise ValueError(f"oracle_group_quant rejected its arguments ({rc})")
     return q, s

@@ -13,7 +13,9 @@
  *        with block_size [128, 128], weight scales [ceil(N/128), ceil(K/128)],
  *        bf16 output.
  *   [P4] transformers integrations/deepgemm.py, _coerce_sf_for_kernel: the
- *        column-major (MN-major) scale layout with a padded leading dimension.
+ *        column-major (MN-major) scale layout with a padded leading dimension;
+ *        _ceil_to_ue8m0 and _select_fp8_cast_kwargs (use_ue8m0): scales rounded
+ *        up to powers of two (UE8M0, the scale format of the SM100 kernels).
  *   OCP 8-bit floating point specification, E4M3: sign, 4 exponent bits
  *        (bias 7), 3 mantissa bits, no infinities, S.1111.111 = NaN.
  */
@@ -123,8 +125,35 @@ static float load_x(const void* x, int in_is_f32, int64_t idx) {
     return f;
 }
 
+/* [P4] _ceil_to_ue8m0: a positive fp32 scale rounded up to the nearest power
+ * of two.  Written from that definition: with s = f * 2^e and f in [0.5, 1),
+ * s is itself a power of two exactly when f = 0.5; otherwise the smallest
+ * power of two above s is 2^e. */
+float oracle_ceil_pow2(float s) {
+    if (!(s > 0.0f) || isinf(s)) return s;   /* defined for positive finite scales */
+    int e;
+    const double f = frexp((double)s, &e);
+    if (f == 0.5) return s;
+    return (float)ldexp(1.0, e);             /* 2^128 and above: +inf */
+}
+
+static int group_quant_impl(const void* x, int in_is_f32, int64_t M, int64_t K, int64_t ld_x,
+                            int col_major, int64_t ld_s, uint8_t* q, int64_t ld_q, float* s,
+                            int ue8m0);
+
 int oracle_group_quant(const void* x, int in_is_f32, int64_t M, int64_t K, int64_t ld_x,
                        int col_major, int64_t ld_s, uint8_t* q, int64_t ld_q, float* s) {
+    return group_quant_impl(x, in_is_f32, M, K, ld_x, col_major, ld_s, q, ld_q, s, 0);
+}
+
+int oracle_group_quant_ue8m0(const void* x, int in_is_f32, int64_t M, int64_t K, int64_t ld_x,
+                             int col_major, int64_t ld_s, uint8_t* q, int64_t ld_q, float* s) {
+    return group_quant_impl(x, in_is_f32, M, K, ld_x, col_major, ld_s, q, ld_q, s, 1);
+}
+
+static int group_quant_impl(const void* x, int in_is_f32, int64_t M, int64_t K, int64_t ld_x,
+                            int col_major, int64_t ld_s, uint8_t* q, int64_t ld_q, float* s,
+                            int ue8m0) {
     if (!x || !q || !s || M < 0 || K < 0 || ld_x < K || ld_q < K) return -1;
     const int64_t G = (K + 127) / 128;
     if (col_major ? ld_s < M : ld_s < G) return -1;
@@ -146,7 +175,8 @@ int oracle_group_quant(const void* x, int in_is_f32, int64_t M, int64_t K, int64
                 if (v > amax) amax = v;
             }
             const float floor_amax = 1e-10f;
-            const float scale = (amax > floor_amax ? amax : floor_amax) / 448.0f;
+            float scale = (amax > floor_amax ? amax : floor_amax) / 448.0f;
+            if (ue8m0) scale = oracle_ceil_pow2(scale);
             for (int64_t k = k0; k < k1; ++k) {
                 const float v = load_x(x, in_is_f32, m * ld_x + k);
                 const float y = v / scale;

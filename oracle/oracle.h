@@ -63,6 +63,16 @@ void oracle_bf16_from_double_array(const double* v, uint16_t* out, int64_t n);
 int oracle_group_quant(const void* x, int in_is_f32, int64_t M, int64_t K, int64_t ld_x,
                        int col_major, int64_t ld_s, uint8_t* q, int64_t ld_q, float* s);
 
+/* UE8M0 variant (transformers integrations/deepgemm.py, _ceil_to_ue8m0 and
+ * the use_ue8m0 cast of _select_fp8_cast_kwargs): oracle_ceil_pow2 rounds a
+ * positive finite fp32 scale up to the nearest power of two;
+ * oracle_group_quant_ue8m0 is oracle_group_quant with every group's scale
+ * max(amax, 1e-10) / 448 so rounded before the codes are computed (the codes
+ * are then encode(x / scale), each division exact). */
+float oracle_ceil_pow2(float s);
+int oracle_group_quant_ue8m0(const void* x, int in_is_f32, int64_t M, int64_t K, int64_t ld_x,
+                             int col_major, int64_t ld_s, uint8_t* q, int64_t ld_q, float* s);
+
 /* Blocked GEMM over selected output rows.
  *   A  : [M, K] e4m3 codes (row stride K), B : [N, K] e4m3 codes (row stride K)
  *   As : activation scales, layout as in oracle_group_quant (as_col_major, ld_as)
