@@ -9,12 +9,22 @@ Acceptance for the GEMM (bf16 outputs):
     2 ulp(ref) + (G + 8) * 2^-24 * sum_kb |D_kb As Bs| -- the worst-case fp32
     accumulation error of G scaled block sums plus the tensor core's fp32
     block sums (the oracle reports that sum of magnitudes).
+Elements beyond 2 ulps are counted; their share of a case's elements must
+stay at or below OVER_2ULP_CEILING.  Every check records its statistics in
+STATS, which the test session prints at the end (tests/conftest.py).
 Quantisation is compared bit for bit (codes and fp32 scales).
 """
 from __future__ import annotations
 
 import numpy as np
 import torch
+
+# Largest share of a case's elements allowed beyond 2 bf16 ulps of the oracle
+# (each of them must still satisfy the cancellation bound); a case of fewer
+# than 1 / OVER_2ULP_CEILING elements may have one.
+OVER_2ULP_CEILING = 1e-4
+
+STATS: list[dict] = []
 
 
 def bf16_bits(t: torch.Tensor) -> np.ndarray:
@@ -53,14 +63,15 @@ def check_gemm(out: torch.Tensor, ref: dict, G: int, rows=None, label: str = "")
             f"{[(int(i), int(j), got[i, j], want[i, j]) for i, j in zip(*bad)][:4]}")
     assert rel < 1e-3, f"{label}: rel_diff {rel}"
     exact = float((got_bits == ref["bf16"]).mean())
-    return {"rel_diff": rel, "over_2ulp": n_over, "bitwise_equal_frac": exact}
-
-
-def sample_rows(M: int, n: int, seed: int = 0) -> list[int]:
-    """First, last, the rows of the last partial 128-row tile and a seeded
-    spread in between."""
-    rows = {0, M - 1}
-    rows.update(range(max(0, (M // 128) * 128), M))
-    rng = np.random.default_rng(seed)
-    rows.update(int(r) for r in rng.integers(0, M, size=n))
-    return sorted(r for r in rows if 0 <= r < M)[: max(n, 2) + 130]
+    frac = n_over / max(got.size, 1)
+    # how much of the cancellation allowance the worst element used, in units
+    # of 2^-24 * sum|terms|
+    excess = 0.0
+    if n_over:
+        excess = float(((err - two_ulp)[over] / (2.0 ** -24 * np.maximum(ref["abs"][over], 1e-300))).max())
+    stats = {"label": label, "elements": int(got.size), "rel_diff": rel, "over_2ulp": n_over,
+             "over_2ulp_frac": frac, "max_excess_units": excess, "bitwise_equal_frac": exact}
+    STATS.append(stats)
+    assert n_over <= max(1, int(OVER_2ULP_CEILING * got.size)), (
+        f"{label}: {n_over} of {got.size} elements beyond 2 ulp ({frac:.2e} > {OVER_2ULP_CEILING})")
+    return stats

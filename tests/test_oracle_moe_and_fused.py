@@ -111,3 +111,63 @@ def test_fused_linear_is_gemm_then_bias_then_group_quant(oracle_mod):
     assert np.array_equal(res["bf16"], y)
     q, s = oracle_mod.group_quant(y, False, True)
     assert np.array_equal(res["q"], q) and np.array_equal(res["s"], s)
+
+
+# Hand-made fused-linear cases.  Every GEMM value below is exact (one nonzero
+# product per output, a power-of-two weight scale), so the expected bf16
+# values, codes and scales follow from the definitions by hand:
+#   e4m3 codes: 0x28 = 0.25, 0x38 = 1, 0x40 = 2, 0x48 = 4, 0x68 = 64, 0x70 = 128, 0x78 = 256,
+#   0x71 = 144, 0x73 = 176, 0x76 = 224, 0x7E = 448 (bias 7, 3 mantissa bits).
+_E4M3 = {1.0: 0x38, 2.0: 0x40, 4.0: 0x48, 64.0: 0x68, 128.0: 0x70, 256.0: 0x78, 0.25: 0x28}
+
+
+def _bf16_bits(vals):
+    return np.array([np.float32(v).view(np.uint32) >> 16 for v in vals], dtype=np.uint16)
+
+
+def _one_group_case(b_rows, bs):
+    """M=1, N=128, K=128; A[0] = (1, 1, 1, 0, ...); row n of B holds the codes
+    b_rows[n] in its first columns; As = 1, Bs = bs."""
+    A = np.zeros((1, 128), dtype=np.uint8)
+    A[0, :3] = 0x38
+    B = np.zeros((128, 128), dtype=np.uint8)
+    for n, vals in b_rows.items():
+        for k, v in enumerate(vals):
+            B[n, k] = _E4M3[v]
+    As = np.ones((1, 1), dtype=np.float32)
+    Bs = np.full((1, 1), bs, dtype=np.float32)
+    return A, B, As, Bs
+
+
+def test_fused_linear_bias_moves_the_group_amax(oracle_mod):
+    """GEMM row = (2, 1, 0, ...), bias = (0, 4, 0, ...): y = (2, 5, 0, ...).
+    The amax is 5 at column 1 (it was 2 at column 0 before the bias), so
+    scale = fl32(5 / 448), column 1 encodes to 448 (0x7E) and column 0 to
+    e4m3(2 / scale) = e4m3(179.2...) = 176 (0x73); zeros stay 0x00."""
+    A, B, As, Bs = _one_group_case({0: [128.0], 1: [64.0]}, 2.0 ** -6)
+    bias = _bf16_bits([0.0, 4.0] + [0.0] * 126)
+    res = oracle_mod.fused_linear(A, B, As, True, Bs, bias)
+    assert res["bf16"][0, :2].tolist() == [0x4000, 0x40A0]          # 2.0, 5.0
+    assert not res["bf16"][0, 2:].any()
+    assert res["q"][0, 0] == 0x73 and res["q"][0, 1] == 0x7E
+    assert not res["q"][0, 2:].any()
+    assert res["s"][0, 0] == np.float32(5.0) / np.float32(448.0)
+
+
+def test_fused_linear_rounds_the_gemm_to_bf16_before_the_bias(oracle_mod):
+    """Column 0: the GEMM value is (256 + 1 + 0.25) * 2^-8 = 1 + 2^-8 + 2^-10,
+    which rounds to bf16 1 + 2^-7; with bias -1 the layer output is
+    bf16(2^-7) = 2^-7.  (Adding the bias before rounding would give
+    2^-8 + 2^-10 = 1.25 * 2^-8 instead.)  Column 1: 4 * 2^-8 = 2^-6, no bias,
+    the group's amax.  So scale = fl32(2^-6 / 448), column 1 encodes to 448
+    (0x7E) and column 0 to e4m3(224) (0x76); the single-rounding value would
+    have encoded to e4m3(140) = 144 (0x71)."""
+    A, B, As, Bs = _one_group_case({0: [256.0, 1.0, 0.25], 1: [4.0]}, 2.0 ** -8)
+    bias = _bf16_bits([-1.0] + [0.0] * 127)
+    res = oracle_mod.fused_linear(A, B, As, True, Bs, bias)
+    gemm = oracle_mod.blocked_gemm(A, B, As, True, Bs)["bf16"]
+    assert gemm[0, 0] == 0x3F81                                      # 1 + 2^-7
+    assert res["bf16"][0, 0] == 0x3C00                               # 2^-7
+    assert res["bf16"][0, 1] == 0x3C80                               # 2^-6
+    assert res["q"][0, 0] == 0x76 and res["q"][0, 1] == 0x7E
+    assert res["s"][0, 0] == np.float32(2.0 ** -6) / np.float32(448.0)
