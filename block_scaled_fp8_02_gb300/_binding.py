@@ -19,6 +19,7 @@ LIB_PATH = os.path.join(_HERE, "_build", "libbfp8.so")
 BFP8_OK = 0
 BFP8_IN_BF16 = 0
 BFP8_IN_F32 = 1
+SCALE_FP32, SCALE_UE8M0 = 0, 1
 SCHEDULE_AUTO, SCHEDULE_SWAP_AB, SCHEDULE_WIDE = 0, 1, 2
 KSPLIT_AUTO, KSPLIT_STREAM_K, KSPLIT_CLUSTER, KSPLIT_NONE = 0, 1, 2, 3
 STATUS_NAMES = {0: "BFP8_OK", 1: "BFP8_ERR_INVALID_ARG", 2: "BFP8_ERR_ALIGNMENT",
@@ -26,7 +27,7 @@ STATUS_NAMES = {0: "BFP8_OK", 1: "BFP8_ERR_INVALID_ARG", 2: "BFP8_ERR_ALIGNMENT"
                 6: "BFP8_ERR_DEVICE_TIMEOUT"}
 
 # Every symbol include/bfp8.h declares.
-EXPORTS = ("bfp8_group_quant", "bfp8_scale_ld", "bfp8_gemm", "bfp8_gemm_ex",
+EXPORTS = ("bfp8_group_quant", "bfp8_group_quant_ex", "bfp8_scale_ceil_ue8m0", "bfp8_scale_ld", "bfp8_gemm", "bfp8_gemm_ex",
            "bfp8_gemm_workspace_size", "bfp8_gemm_plan", "bfp8_plan_unit", "bfp8_last_error",
            "bfp8_status_string", "bfp8_device_status", "bfp8_selftest_bounded_wait",
            "bfp8_version", "bfp8_gemm_noalloc", "bfp8_gemm_grouped",
@@ -70,6 +71,10 @@ def lib():
             P, i64, i32, sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_size_t
             L.bfp8_group_quant.restype = i32
             L.bfp8_group_quant.argtypes = [P, i32, i64, i64, i64, i32, i32, P, i64, P, i64, P]
+            L.bfp8_group_quant_ex.restype = i32
+            L.bfp8_group_quant_ex.argtypes = [P, i32, i64, i64, i64, i32, i32, i32, P, i64, P, i64, P]
+            L.bfp8_scale_ceil_ue8m0.restype = i32
+            L.bfp8_scale_ceil_ue8m0.argtypes = [P, P, i64, P]
             L.bfp8_scale_ld.restype = i64
             L.bfp8_scale_ld.argtypes = [i64]
             L.bfp8_gemm.restype = i32
@@ -161,12 +166,13 @@ def bfp8_scale_ld(M: int) -> int:
 
 def bfp8_group_quant(x: torch.Tensor, col_major: bool = True, group: int = 128,
                      q: torch.Tensor | None = None, s_storage: torch.Tensor | None = None,
-                     stream=None):
+                     stream=None, ue8m0: bool = False):
     """Quantise x [M, K] (bf16 or fp32, CUDA, unit inner stride) per 128-group.
 
     Returns (q, s): q [M, K] float8_e4m3fn and s [M, G] fp32; for col_major the
     scales live in a [G, bfp8_scale_ld(M)] buffer and s is its transposed view
-    (stride (1, ld)), the layout the pages hand to the GEMM.
+    (stride (1, ld)), the layout the pages hand to the GEMM.  ue8m0: every
+    scale rounded up to a power of two (the UE8M0 variant).
     """
     if x.dim() != 2 or x.stride(1) != 1:
         raise ValueError("x must be a 2-D tensor with unit inner stride")
@@ -190,11 +196,26 @@ def bfp8_group_quant(x: torch.Tensor, col_major: bool = True, group: int = 128,
         if s_storage is None:
             s_storage = torch.empty((M, max(ld_s, 1)), dtype=torch.float32, device=x.device)
         s_view = s_storage[:, :G]
-    st = lib().bfp8_group_quant(x.data_ptr(), in_dtype, M, K, x.stride(0), group, int(col_major),
-                                q.data_ptr(), q.stride(0) if M > 0 else K, s_storage.data_ptr(),
-                                ld_s, _stream_ptr(stream))
+    st = lib().bfp8_group_quant_ex(x.data_ptr(), in_dtype, M, K, x.stride(0), group, int(col_major),
+                                   SCALE_UE8M0 if ue8m0 else SCALE_FP32, q.data_ptr(),
+                                   q.stride(0) if M > 0 else K, s_storage.data_ptr(), ld_s,
+                                   _stream_ptr(stream))
     _check(st, "bfp8_group_quant")
     return q, s_view
+
+
+def bfp8_scale_ceil_ue8m0(s: torch.Tensor, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Every element of the fp32 scale tensor s rounded up to a power of two
+    (contiguous tensors; out may be s itself)."""
+    if s.dtype != torch.float32 or not s.is_contiguous():
+        raise ValueError("s must be a contiguous float32 tensor")
+    if out is None:
+        out = torch.empty_like(s)
+    if out.shape != s.shape or out.dtype != torch.float32 or not out.is_contiguous():
+        raise ValueError("out must be a contiguous float32 tensor shaped like s")
+    _check(lib().bfp8_scale_ceil_ue8m0(s.data_ptr(), out.data_ptr(), s.numel(), _stream_ptr(stream)),
+           "bfp8_scale_ceil_ue8m0")
+    return out
 
 
 def _as_layout(As: torch.Tensor, M: int, G: int):
@@ -209,20 +230,36 @@ def _as_layout(As: torch.Tensor, M: int, G: int):
     raise ValueError(f"As strides {As.stride()} are neither row- nor column-major")
 
 
-_ws_cache: dict[int, torch.Tensor] = {}
+_ws_cache: dict[tuple[int, int], torch.Tensor] = {}
 
 
-def workspace_for(nbytes: int, device: torch.device) -> torch.Tensor:
-    """A zero-initialised workspace of at least nbytes on `device` (cached).
+def workspace_for(nbytes: int, device: torch.device, stream=None) -> torch.Tensor:
+    """A zero-initialised workspace of at least nbytes on `device` for calls
+    on `stream` (None: the current stream), cached per (device, stream).
 
     libbfp8 leaves the workspace zeroed after every completed call, so one
-    buffer serves every call that runs on the same stream order."""
+    buffer serves every call issued in order on one stream; calls on streams
+    without ordering between them get separate buffers.  A new buffer is
+    allocated and zeroed on that stream, so its zeroing is ordered before the
+    calls that use it, and a replaced buffer is only ever reused by later work
+    on the same stream (the caching allocator's stream-ordered reuse)."""
     idx = device.index if device.index is not None else torch.cuda.current_device()
-    ws = _ws_cache.get(idx)
+    sp = _stream_ptr(stream)
+    ws = _ws_cache.get((idx, sp))
     if ws is None or ws.numel() < nbytes:
-        ws = torch.zeros(max(nbytes, 256), dtype=torch.uint8, device=device)
-        _ws_cache[idx] = ws
+        s = stream if isinstance(stream, torch.cuda.Stream) else (
+            torch.cuda.current_stream(device) if stream is None else
+            torch.cuda.ExternalStream(sp, device=device))
+        with torch.cuda.stream(s):
+            ws = torch.zeros(max(nbytes, 256), dtype=torch.uint8, device=device)
+        _ws_cache[(idx, sp)] = ws
     return ws
+
+
+def drop_workspaces() -> None:
+    """Forget every cached workspace (after a kernel gave up on a wait, one may
+    hold non-zero stream-K counters)."""
+    _ws_cache.clear()
 
 
 def bfp8_gemm_workspace_size(M: int, N: int, K: int, options=None,
@@ -270,7 +307,7 @@ def bfp8_gemm(A: torch.Tensor, B: torch.Tensor, As: torch.Tensor, Bs: torch.Tens
     unaligned = (A.data_ptr() % 16 != 0) or (B.data_ptr() % 16 != 0)
     if workspace is None:
         need = bfp8_gemm_workspace_size(M, N, K, options, unaligned)
-        workspace = workspace_for(need, A.device)
+        workspace = workspace_for(need, A.device, stream)
     st = lib().bfp8_gemm_ex(A.data_ptr(), B.data_ptr(), As.data_ptr(), col, ld, Bs.data_ptr(),
                             out.data_ptr(), M, N, K, workspace.data_ptr(),
                             workspace.numel() * workspace.element_size(), _opts(options),
@@ -318,7 +355,7 @@ def bfp8_gemm_grouped(A: torch.Tensor, B: torch.Tensor, As: torch.Tensor, Bs: to
     unaligned = (A.data_ptr() % 16 != 0) or (B.data_ptr() % 16 != 0)
     if workspace is None:
         need = bfp8_gemm_grouped_workspace_size(M, N, K, E, options, unaligned)
-        workspace = workspace_for(need, A.device)
+        workspace = workspace_for(need, A.device, stream)
     st = lib().bfp8_gemm_grouped(A.data_ptr(), B.data_ptr(), As.data_ptr(), col, ld,
                                  Bs.data_ptr(), grouped_layout.data_ptr(), E, out.data_ptr(),
                                  M, N, K, workspace.data_ptr(),
@@ -374,7 +411,7 @@ def bfp8_gemm_fused(A: torch.Tensor, B: torch.Tensor, As: torch.Tensor, Bs: torc
         _check(lib().bfp8_gemm_fused_workspace_size(M, N, K, _opts(options), int(unaligned),
                                                     ctypes.byref(n)),
                "bfp8_gemm_fused_workspace_size")
-        workspace = workspace_for(int(n.value), A.device)
+        workspace = workspace_for(int(n.value), A.device, stream)
     st = lib().bfp8_gemm_fused(
         A.data_ptr(), B.data_ptr(), As.data_ptr(), col, ld, Bs.data_ptr(),
         bias.data_ptr() if bias is not None else None, out.data_ptr() if out is not None else None,
@@ -386,8 +423,12 @@ def bfp8_gemm_fused(A: torch.Tensor, B: torch.Tensor, As: torch.Tensor, Bs: torc
 
 
 def bfp8_device_status(clear: bool = True) -> int:
+    """The device failure word (0: no kernel gave up on a wait).  A nonzero
+    word also drops the cached workspaces, which may hold stale counters."""
     code = ctypes.c_int(0)
     _check(lib().bfp8_device_status(ctypes.byref(code), int(clear)), "bfp8_device_status")
+    if code.value != 0:
+        drop_workspaces()
     return int(code.value)
 
 
@@ -400,10 +441,12 @@ def bfp8_selftest_bounded_wait(limit_cycles: int, stream=None):
 
 
 def linear(x: torch.Tensor, B: torch.Tensor, Bs: torch.Tensor, out: torch.Tensor | None = None,
-           stream=None) -> torch.Tensor:
+           stream=None, ue8m0: bool = False) -> torch.Tensor:
     """The whole W8A8 blocked linear layer: quantise x per 128-group (column-major
-    scales) and run the blocked GEMM against e4m3 weights B with scales Bs."""
-    q, s = bfp8_group_quant(x, col_major=True, stream=stream)
+    scales) and run the blocked GEMM against e4m3 weights B with scales Bs.
+    ue8m0: the UE8M0 variant (activation scales rounded up to powers of two;
+    pass weight scales rounded the same way, e.g. by bfp8_scale_ceil_ue8m0)."""
+    q, s = bfp8_group_quant(x, col_major=True, stream=stream, ue8m0=ue8m0)
     # the quantisation kernel writes neither B nor Bs: the GEMM may start
     # streaming the weights while it runs
     return bfp8_gemm(q, B, s, Bs, out=out, options={"prefetch_weights": 1}, stream=stream)

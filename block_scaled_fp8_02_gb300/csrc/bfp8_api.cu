@@ -61,7 +61,10 @@ struct DevInfo {
   int cc_major = 0, cc_minor = 0, sms = 0;
   int* err = nullptr;
   bool caps_ready = false;
-  int cluster_cap[kMaxCluster + 1] = {};   // co-resident GEMM clusters of each size
+  // co-resident GEMM clusters of each size: one-CTA-per-SM instantiations,
+  // and the swap-AB ones sized for two CTAs per SM
+  int cluster_cap[kMaxCluster + 1] = {};
+  int cluster_cap2[kMaxCluster + 1] = {};
 };
 DevInfo g_dev[kMaxDevices];
 std::mutex g_dev_mu;
@@ -110,9 +113,12 @@ bfp8_status current_device_with_caps(DevInfo* out) {
   if (st != BFP8_OK) return st;
   if (out->caps_ready) return BFP8_OK;
   int cap[kMaxCluster + 1] = {};
+  int cap2[kMaxCluster + 1] = {};
   cap[0] = cap[1] = out->sms;
+  cap2[0] = cap2[1] = 2 * out->sms;
   for (int cs = 2; cs <= kMaxCluster; ++cs) {
-    const cudaError_t e = gemm_cluster_capacity(cs, &cap[cs]);
+    cudaError_t e = gemm_cluster_capacity(cs, false, &cap[cs]);
+    if (e == cudaSuccess) e = gemm_cluster_capacity(cs, true, &cap2[cs]);
     if (e != cudaSuccess) {
       cudaGetLastError();
       return fail(BFP8_ERR_CUDA, "cluster occupancy query (size %d): %s", cs, cudaGetErrorString(e));
@@ -121,6 +127,7 @@ bfp8_status current_device_with_caps(DevInfo* out) {
   std::lock_guard<std::mutex> lk(g_dev_mu);
   DevInfo& d = g_dev[dev];
   std::memcpy(d.cluster_cap, cap, sizeof(cap));
+  std::memcpy(d.cluster_cap2, cap2, sizeof(cap2));
   d.caps_ready = true;
   *out = d;
   return BFP8_OK;
@@ -190,6 +197,7 @@ inline size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255);
 struct Plan {
   bool swap = false;
   int bn = 0;
+  int mr = 128;              // wide tiles: activation rows loaded per stage
   bool relayout = false;
   int64_t kp = 0;            // inner extent of the operand tensor maps
   Sched sched{};
@@ -223,10 +231,12 @@ bfp8_status check_options(const bfp8_gemm_options* opt) {
 
 // Co-resident clusters of each size on a device with `sms` SMs when the
 // device itself cannot be asked (host-only planning): its GPCs are not all
-// alike, so a little less than sms / cs, and clearly less for 7 and 8.
-void estimate_cluster_caps(int sms, int* cap) {
+// alike, so a little less than sms / cs, and clearly less for 7 and 8
+// (ctas_per_sm CTAs of the instantiation fit on one SM).
+void estimate_cluster_caps(int sms, int ctas_per_sm, int* cap) {
+  const int slots = sms * ctas_per_sm;
   for (int cs = 0; cs <= kMaxCluster; ++cs)
-    cap[cs] = cs < 2 ? sms : static_cast<int>(sms * (cs >= 7 ? 0.75 : 0.94) / cs);
+    cap[cs] = cs < 2 ? slots : static_cast<int>(slots * (cs >= 7 ? 0.75 : 0.94) / cs);
 }
 
 // Relative time of the ways of sharing the work among CTAs, in units of one
@@ -337,12 +347,13 @@ int swap_tile_n(int64_t M) {
 }
 
 constexpr int64_t kSwapMaxM = 256;
-constexpr size_t kCounterHeaderBytes = 16384;   // 4096 stream-K tile counters
 
-// `cap` = co-resident clusters of each size (nullptr: estimated from num_sms).
-// `experts` > 1: M-grouped mode, B and Bs hold that many experts' weights.
+// `dev` = the device's cached properties, whose co-resident cluster counts
+// the planner uses (nullptr: host-only planning, counts estimated from
+// num_sms).  `experts` > 1: M-grouped mode, B and Bs hold that many experts'
+// weights.
 bfp8_status make_plan(int64_t M, int64_t N, int64_t K, int num_sms, const bfp8_gemm_options* opt,
-                      bool unaligned, const int* cap, Plan* p, int64_t experts = 1) {
+                      bool unaligned, const DevInfo* dev, Plan* p, int64_t experts = 1) {
   const int schedule = opt ? opt->schedule : BFP8_SCHEDULE_AUTO;
   p->swap = schedule == BFP8_SCHEDULE_SWAP_AB ||
             (schedule == BFP8_SCHEDULE_AUTO && M <= kSwapMaxM);
@@ -350,6 +361,9 @@ bfp8_status make_plan(int64_t M, int64_t N, int64_t K, int num_sms, const bfp8_g
   if (!p->swap && tn != 0 && tn != 128 && tn != 256)
     return fail(BFP8_ERR_INVALID_ARG, "options.tile_n = %d: wide tiles are 128 or 256 wide", tn);
   p->bn = p->swap ? (tn ? tn : swap_tile_n(M)) : (tn == 128 ? 128 : 256);
+  // plain 256-wide tiles of a decode-sized M load only the rows that exist
+  // (M-grouped calls keep whole 128-row tiles: experts start on them)
+  p->mr = (!p->swap && p->bn == 256 && experts == 1 && M <= 64) ? (M <= 32 ? 32 : 64) : 128;
   const int64_t G = cdiv(K, 128);
   const int64_t p_tiles = p->swap ? cdiv(N, 128) : cdiv(M, 128);
   const int64_t q_tiles = p->swap ? cdiv(M, p->bn) : cdiv(N, p->bn);
@@ -358,9 +372,13 @@ bfp8_status make_plan(int64_t M, int64_t N, int64_t K, int num_sms, const bfp8_g
                 (long long)(p_tiles * q_tiles), (long long)G);
   int max_ctas = num_sms;
   if (opt && opt->max_ctas > 0 && opt->max_ctas < max_ctas) max_ctas = opt->max_ctas;
+  const bool two = gemm_two_per_sm(p->swap, p->bn);
   int est[kMaxCluster + 1];
-  if (!cap) {
-    estimate_cluster_caps(num_sms, est);
+  const int* cap = nullptr;
+  if (dev) {
+    cap = two ? dev->cluster_cap2 : dev->cluster_cap;
+  } else {
+    estimate_cluster_caps(num_sms, two ? 2 : 1, est);
     cap = est;
   }
   const SplitChoice sc = choose_split(p_tiles * q_tiles, G, p->bn, p->swap, max_ctas, opt, cap);
@@ -471,9 +489,12 @@ const char* bfp8_status_string(int status) {
 
 int64_t bfp8_scale_ld(int64_t M) { return M <= 0 ? 0 : (M + 3) / 4 * 4; }
 
-bfp8_status bfp8_group_quant(const void* x, int in_dtype, int64_t M, int64_t K, int64_t ld_x,
-                             int group, int col_major, void* q, int64_t ld_q, float* s,
-                             int64_t ld_s, void* stream) {
+bfp8_status bfp8_group_quant_ex(const void* x, int in_dtype, int64_t M, int64_t K, int64_t ld_x,
+                                int group, int col_major, int scale_fmt, void* q, int64_t ld_q,
+                                float* s, int64_t ld_s, void* stream) {
+  if (scale_fmt != BFP8_SCALE_FP32 && scale_fmt != BFP8_SCALE_UE8M0)
+    return fail(BFP8_ERR_INVALID_ARG, "scale_fmt = %d (expected BFP8_SCALE_FP32 or BFP8_SCALE_UE8M0)",
+                scale_fmt);
   if (in_dtype != BFP8_IN_BF16 && in_dtype != BFP8_IN_F32)
     return fail(BFP8_ERR_INVALID_ARG, "in_dtype = %d (expected BFP8_IN_BF16 or BFP8_IN_F32)", in_dtype);
   if (group != 128) return fail(BFP8_ERR_INVALID_ARG, "group = %d: only 128 is supported", group);
@@ -497,9 +518,31 @@ bfp8_status bfp8_group_quant(const void* x, int in_dtype, int64_t M, int64_t K, 
   bfp8_status st = current_device(&d, nullptr);
   if (st != BFP8_OK) return st;
   cudaError_t e = launch_group_quant(x, in_dtype == BFP8_IN_F32, M, K, ld_x, static_cast<uint8_t*>(q),
-                                     ld_q, s, col_major, ld_s, d.sms,
+                                     ld_q, s, col_major, ld_s, scale_fmt == BFP8_SCALE_UE8M0, d.sms,
                                      static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return fail(BFP8_ERR_CUDA, "quantisation launch: %s", cudaGetErrorString(e));
+  return ok();
+}
+
+bfp8_status bfp8_group_quant(const void* x, int in_dtype, int64_t M, int64_t K, int64_t ld_x,
+                             int group, int col_major, void* q, int64_t ld_q, float* s,
+                             int64_t ld_s, void* stream) {
+  return bfp8_group_quant_ex(x, in_dtype, M, K, ld_x, group, col_major, BFP8_SCALE_FP32, q, ld_q, s,
+                             ld_s, stream);
+}
+
+bfp8_status bfp8_scale_ceil_ue8m0(const float* in, float* out, int64_t n, void* stream) {
+  if (n < 0) return fail(BFP8_ERR_INVALID_ARG, "n = %lld", (long long)n);
+  if (n == 0) return ok();
+  if (!in || !out) return fail(BFP8_ERR_INVALID_ARG, "null pointer (in=%p out=%p)", (const void*)in,
+                               (void*)out);
+  if (misaligned(in, 4) || misaligned(out, 4))
+    return fail(BFP8_ERR_ALIGNMENT, "in and out must be 4-byte aligned");
+  DevInfo d;
+  bfp8_status st = current_device(&d, nullptr);
+  if (st != BFP8_OK) return st;
+  cudaError_t e = launch_scale_ceil_ue8m0(in, out, n, d.sms, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail(BFP8_ERR_CUDA, "scale rounding launch: %s", cudaGetErrorString(e));
   return ok();
 }
 
@@ -512,19 +555,19 @@ bfp8_status bfp8_gemm_plan(int64_t M, int64_t N, int64_t K, int num_sms,
   if (num_sms < 0) return fail(BFP8_ERR_INVALID_ARG, "num_sms = %d", num_sms);
   if (!info) return fail(BFP8_ERR_INVALID_ARG, "info is null");
   DevInfo d;
-  const int* cap = nullptr;
+  const DevInfo* dp = nullptr;
   if (num_sms == 0) {
     if ((st = current_device_with_caps(&d)) != BFP8_OK) return st;
     num_sms = d.sms;
-    cap = d.cluster_cap;
+    dp = &d;
   }
   Plan p;
-  if ((st = make_plan(M, N, K, num_sms, opt, operands_unaligned != 0, cap, &p)) != BFP8_OK) return st;
+  if ((st = make_plan(M, N, K, num_sms, opt, operands_unaligned != 0, dp, &p)) != BFP8_OK) return st;
   if (stream_k_tiles(p.sched) > static_cast<int64_t>(kCounterHeaderBytes / sizeof(int)))
     return fail(BFP8_ERR_UNSUPPORTED, "more stream-K tiles than the workspace header holds");
   info->swap_ab = p.swap;
   info->tile_n = p.bn;
-  info->stages = gemm_stages(p.swap, p.bn);
+  info->stages = gemm_stages(p.swap, p.bn, p.mr);
   info->grid = p.sched.grid;
   info->tiles = p.sched.tiles;
   info->k_blocks = p.sched.G;
@@ -544,14 +587,14 @@ bfp8_status bfp8_plan_unit(int64_t M, int64_t N, int64_t K, int num_sms,
   if ((st = check_options(opt)) != BFP8_OK) return st;
   if (num_sms < 0) return fail(BFP8_ERR_INVALID_ARG, "num_sms = %d", num_sms);
   DevInfo d;
-  const int* cap = nullptr;
+  const DevInfo* dp = nullptr;
   if (num_sms == 0) {
     if ((st = current_device_with_caps(&d)) != BFP8_OK) return st;
     num_sms = d.sms;
-    cap = d.cluster_cap;
+    dp = &d;
   }
   Plan p;
-  if ((st = make_plan(M, N, K, num_sms, opt, false, cap, &p)) != BFP8_OK) return st;
+  if ((st = make_plan(M, N, K, num_sms, opt, false, dp, &p)) != BFP8_OK) return st;
   if (cta < 0 || static_cast<uint32_t>(cta) >= p.sched.grid)
     return fail(BFP8_ERR_INVALID_ARG, "cta %d out of range", cta);
   const int64_t n = num_units(p.sched, static_cast<uint32_t>(cta));
@@ -578,7 +621,7 @@ bfp8_status bfp8_gemm_workspace_size(int64_t M, int64_t N, int64_t K,
   DevInfo d;
   if ((st = current_device_with_caps(&d)) != BFP8_OK) return st;
   Plan p;
-  if ((st = make_plan(M, N, K, d.sms, opt, operands_unaligned != 0, d.cluster_cap, &p)) != BFP8_OK)
+  if ((st = make_plan(M, N, K, d.sms, opt, operands_unaligned != 0, &d, &p)) != BFP8_OK)
     return st;
   *bytes = p.total;
   return ok();
@@ -641,7 +684,7 @@ static bfp8_status gemm_impl(const void* A, const void* B, const float* As, int 
   if ((st = current_device_with_caps(&d)) != BFP8_OK) return st;
   const bool unaligned = misaligned(A, 16) || misaligned(B, 16);
   Plan p;
-  if ((st = make_plan(M, N, K, d.sms, opt, unaligned, d.cluster_cap, &p, experts)) != BFP8_OK)
+  if ((st = make_plan(M, N, K, d.sms, opt, unaligned, &d, &p, experts)) != BFP8_OK)
     return st;
   if (stream_k_tiles(p.sched) > static_cast<int64_t>(kCounterHeaderBytes / sizeof(int)))
     return fail(BFP8_ERR_UNSUPPORTED, "more stream-K tiles than the workspace header holds");
@@ -689,7 +732,9 @@ static bfp8_status gemm_impl(const void* A, const void* B, const float* As, int 
   const void* q_ptr = p.swap ? a_op : b_op;
   const int64_t p_rows = p.swap ? N : M;
   const int64_t q_rows = p.swap ? M : experts * N;
-  if ((st = encode_operand(&tmP, p_ptr, p_rows, p.kp, 128)) != BFP8_OK) return st;
+  const int mode = psum ? kModeGrouped : (fused ? kModeFused : kModePlain);
+  const int mr = mode == kModePlain ? p.mr : 128;
+  if ((st = encode_operand(&tmP, p_ptr, p_rows, p.kp, p.swap ? 128 : mr)) != BFP8_OK) return st;
   if ((st = encode_operand(&tmQ, q_ptr, q_rows, p.kp, p.bn)) != BFP8_OK) return st;
 
   GemmArgs a{};
@@ -733,9 +778,8 @@ static bfp8_status gemm_impl(const void* A, const void* B, const float* As, int 
     cudaGetLastError();
   }
 #endif
-  const int mode = psum ? kModeGrouped : (fused ? kModeFused : kModePlain);
   cudaError_t e = p.swap ? launch_gemm_swap(p.bn, tmP, tmQ, a, cs)
-                         : launch_gemm_wide(p.bn, mode, tmP, tmQ, a, cs);
+                         : launch_gemm_wide(p.bn, mode, mr, tmP, tmQ, a, cs);
   if (e != cudaSuccess) return fail(BFP8_ERR_CUDA, "GEMM launch: %s", cudaGetErrorString(e));
   return ok();
 }
@@ -789,7 +833,7 @@ bfp8_status bfp8_gemm_grouped_workspace_size(int64_t M, int64_t N, int64_t K, in
   if ((st = current_device_with_caps(&d)) != BFP8_OK) return st;
   const bfp8_gemm_options g = effective_options(opt, true, false);
   Plan p;
-  if ((st = make_plan(M, N, K, d.sms, &g, operands_unaligned != 0, d.cluster_cap, &p,
+  if ((st = make_plan(M, N, K, d.sms, &g, operands_unaligned != 0, &d, &p,
                       num_experts)) != BFP8_OK)
     return st;
   *bytes = p.total;
@@ -843,7 +887,7 @@ bfp8_status bfp8_gemm_fused_workspace_size(int64_t M, int64_t N, int64_t K,
   if ((st = current_device_with_caps(&d)) != BFP8_OK) return st;
   const bfp8_gemm_options g = effective_options(opt, false, true);
   Plan p;
-  if ((st = make_plan(M, N, K, d.sms, &g, operands_unaligned != 0, d.cluster_cap, &p)) != BFP8_OK)
+  if ((st = make_plan(M, N, K, d.sms, &g, operands_unaligned != 0, &d, &p)) != BFP8_OK)
     return st;
   *bytes = p.total;
   return ok();

@@ -62,6 +62,31 @@ __device__ __forceinline__ uint16_t e4m3_pair_bracketed(float x0, float x1, cons
   return lo;
 }
 
+// UE8M0 scales (transformers DeepGEMM integration, _ceil_to_ue8m0): the fp32
+// scale rounded up to the nearest power of two by adding 2^23 - 1 to its bit
+// pattern and clearing the 23 mantissa bits (positive finite scales only).
+__device__ __forceinline__ uint32_t ceil_ue8m0_bits(float s) {
+  return (__float_as_uint(s) + 0x7FFFFFu) & 0xFF800000u;
+}
+
+// Group scale of the UE8M0 variant, and its exact reciprocal: for 2^e with
+// biased exponent E (E = 85 .. 247 here: 2^-42 <= scale < 2^121), 1 / 2^e has
+// biased exponent 254 - E, i.e. bits 0x7F000000 - bits.  x * (1 / scale) is
+// then the correctly rounded x / scale (the same real number, rounded once),
+// so the codes need neither a division nor a bracket.
+struct Ue8m0Scale {
+  float scale, inv;
+  __device__ __forceinline__ explicit Ue8m0Scale(float amax) {
+    const uint32_t b = ceil_ue8m0_bits(group_scale(amax));
+    scale = __uint_as_float(b);
+    inv = __uint_as_float(0x7F000000u - b);
+  }
+};
+
+__device__ __forceinline__ uint16_t e4m3_pair_pow2(float x0, float x1, float inv) {
+  return cvt_e4m3x2(__fmul_rn(x0, inv), __fmul_rn(x1, inv));
+}
+
 // The same codes by the IEEE division.
 __device__ __forceinline__ uint16_t e4m3_pair_divided(float x0, float x1, float scale) {
   return cvt_e4m3x2(__fdiv_rn(x0, scale), __fdiv_rn(x1, scale));

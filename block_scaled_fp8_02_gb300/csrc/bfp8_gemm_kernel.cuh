@@ -51,6 +51,7 @@ enum : int {
   kDevTimeoutMma = 2,
   kDevTimeoutEpilogue = 3,
   kDevTimeoutTail = 4,
+  kDevBadGroupedLayout = 5,   // grouped_layout not non-decreasing multiples of 128
 };
 
 struct GemmArgs {
@@ -116,10 +117,18 @@ __host__ __device__ constexpr int tmem_cols_for(int n) {
   return n <= 32 ? 32 : n <= 64 ? 64 : n <= 128 ? 128 : n <= 256 ? 256 : 512;
 }
 
-template <int BN, bool SWAP, int MODE = kModePlain>
+// MR (wide tiles only): activation rows the producer loads per stage.  The
+// MMA always reads 128 rows of the A operand; with MR < 128 (decode-sized M,
+// M <= MR) the rows past MR are whatever follows in shared memory, their
+// results land in TMEM lanes >= MR and are never read: the promotion warps
+// of those lane quadrants stay idle.
+template <int BN, bool SWAP, int MODE = kModePlain, int MR = 128>
 struct GemmCfg {
   static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "MMA N for M=128 is 16..256 step 16");
   static_assert(SWAP || BN % 128 == 0, "wide tiles cover whole 128-column weight-scale blocks");
+  static_assert(MR == 128 || (!SWAP && MODE == kModePlain && (MR == 32 || MR == 64)),
+                "partial activation tiles: plain wide tiles, 32 or 64 rows");
+  static constexpr int kMR = MR;
 #ifndef BFP8_WIDE_WARPS
 #define BFP8_WIDE_WARPS 8
 #endif
@@ -134,8 +143,10 @@ struct GemmCfg {
 #ifndef BFP8_WIDE_BATCH
 #define BFP8_WIDE_BATCH 64
 #endif
+  // (64-column swap tiles: 32, so that two CTAs' registers fit on one SM)
   static constexpr int kBatch =
-      kNH == 4 ? 32 : (kNH == 2 ? BFP8_WIDE_BATCH : (kCPT >= 64 ? 64 : kCPT));
+      kNH == 4 ? 32
+               : (kNH == 2 ? BFP8_WIDE_BATCH : (kCPT >= 64 ? (SWAP && BN == 64 ? 32 : 64) : kCPT));
   // 8 promotion warps: 12 warps in all so that warps 8..11 are one warpgroup
   // that gives registers to the promotion warpgroups (setmaxnreg).
   static constexpr int kWarps = kNE >= 8 ? kNE + 4 : kNE + 2;
@@ -144,7 +155,7 @@ struct GemmCfg {
   // 8: 256*232 + 128*40 <= 384*168;  16: 512*112 + 128*24 <= 640*96
   static constexpr int kRegsEpi = kNE == 16 ? 112 : 232;
   static constexpr int kRegsOther = kNE == 16 ? 24 : 40;
-  static constexpr int kPBytes = 128 * 128;
+  static constexpr int kPBytes = (SWAP ? 128 : MR) * 128;
   static constexpr int kQBytes = BN * 128;
   static constexpr int kStageBytes = kPBytes + kQBytes;
   // Scales: the producer bulk-copies each unit's activation-scale slice
@@ -156,20 +167,36 @@ struct GemmCfg {
   // (one load per lane covers 32 units; every bulk copy added to a unit's
   // stage lengthens the producer's per-unit issue time).
   // Swap tiles: the ring has its own full / empty barriers and runs ahead of
-  // the operand ring.  Wide tiles: unit j's slot (j mod kSR) is copied with
+  // the operand ring (see kSR below).  Wide tiles: unit j's slot (j mod kSR) is copied with
   // unit j's operand tiles and completes on the same stage barrier; the MMA
   // issuer waits for that barrier before the MMAs whose completion the
   // promotion warps wait for, so no barrier of its own is needed.  The slot
   // is free again once unit j - kSR has been promoted: the producer writes it
   // after the MMAs of unit j - kStages have completed, which were issued after
   // the promotion of unit j - kStages - kTB, hence kSR >= kStages + kTB.
-  static constexpr int kSR = SWAP ? 8 : 12;
-  static constexpr int kSRB = SWAP ? kSR : 0;    // scale-ring barriers (swap only)
+  // Swap tiles up to 64 columns wide are sized for two CTAs per SM, so that
+  // the next launch's CTAs can be resident (and stream their weights) while
+  // this launch finishes; the other instantiations hold one CTA per SM.
+  static constexpr bool kTwoPerSm = SWAP && BN <= 64;
+  // TMEM accumulator buffers: the MMA of a unit may start while the promotion
+  // warps still read the kTB - 1 units before it.  Wide tiles: two 256-column
+  // or four 128-column buffers (512 columns).  Swap tiles: as many as fit in
+  // 256 columns (at most 16), so that the MMAs of a CTA's units run ahead of
+  // their promotion instead of waiting for it unit by unit (512 columns for
+  // the one-CTA-per-SM widths).
+  static constexpr int kTB = !SWAP ? (BN == 128 ? 4 : 2)
+                                   : (BN <= 64 ? (256 / BN > 16 ? 16 : 256 / BN) : 512 / BN);
+  // Swap tiles' scale ring runs ahead of the operand ring: the producer is at
+  // most kStages units ahead of the MMAs, which are at most kTB units ahead of
+  // the promotion, so kStages + kTB slots never hold it back.
+  static constexpr int kSRMax = SWAP ? 10 + kTB : 12;
+  static constexpr int kSRB = SWAP ? kSRMax : 0;   // scale-ring barriers (swap only)
   static constexpr int kAsFloats = SWAP ? BN : 128;
   static constexpr int kBsChunks = SWAP ? 1 : 0;
   static constexpr int kSlotFloats = kAsFloats + 4 * kBsChunks;
-  static constexpr int kScaleBytes = kSR * kSlotFloats * 4;
   static constexpr int kSmemLimit = 232448;      // 227 KB per CTA
+  // two CTAs per SM: 2 x (dynamic shared memory + 1 KB reserved) <= 228 KB
+  static constexpr int kSmemBudget = kTwoPerSm ? 115712 : kSmemLimit;
   // Wide tiles stage each promotion warp's bf16 output through shared memory,
   // 32 rows x 32 columns at a time.  Plain and fused tiles: a 2 KB tile in the
   // TMA store's 64-byte swizzle (conflict-free for lane-per-row 16-byte
@@ -181,27 +208,29 @@ struct GemmCfg {
   static constexpr int kOutTile = kTmaStore ? 2048 : 32 * kOutPitch;
   static constexpr int kOutBytes = SWAP ? 0 : kNE * kOutTile;
   static constexpr int kPsumBytes = MODE == kModeGrouped ? kMaxExperts * 4 : 0;
+  // barriers: full, empty [kStages]; sfull, sempty [kSRB]; tfull, tempty [kTB]
+  static constexpr int kBarBytes = ((2 * 10 + 2 * kSRB + 2 * kTB) * 8 + 16 + 127) / 128 * 128;
   static constexpr int kStagesFit =
-      (kSmemLimit - 1024 /*align*/ - 384 /*barriers*/ - kScaleBytes - kOutBytes - kPsumBytes) /
-      kStageBytes;
+      (kSmemBudget - 1024 /*align*/ - kBarBytes - kSRMax * kSlotFloats * 4 - kOutBytes -
+       kPsumBytes) / kStageBytes;
   static constexpr int kStages = kStagesFit > 10 ? 10 : kStagesFit;
   static_assert(kStages >= 2, "ring too small");
-  // TMEM accumulator buffers: the MMA of a unit may start while the
-  // promotion warps still read the kTB - 1 units before it.  512 columns
-  // hold two 256-column or four 128-column buffers.
-  static constexpr int kTB = (!SWAP && BN == 128) ? 4 : 2;
+  static constexpr int kSR = SWAP ? kStages + kTB : 12;
+  static_assert(kSR <= kSRMax, "scale ring");
+  static constexpr int kScaleBytes = kSR * kSlotFloats * 4;
   static_assert(SWAP || kSR >= kStages + kTB, "wide scale slots reused too early");
-  // barriers: full, empty [kStages]; sfull, sempty [kSRB]; tfull, tempty [kTB]
   static constexpr int kOffBars = kStages * kStageBytes;
   static constexpr int kOffTmemPtr = kOffBars + (2 * kStages + 2 * kSRB + 2 * kTB) * 8;
-  static_assert(kOffTmemPtr + 16 - kOffBars <= 384, "barrier area");
+  static_assert(kOffTmemPtr + 16 - kOffBars <= kBarBytes, "barrier area");
   static constexpr int kOffFlags = kOffTmemPtr + 8;
   static constexpr int kOffScale = (kOffFlags + 8 + 15) / 16 * 16;
   static constexpr int kOffOut = (kOffScale + kScaleBytes + 1023) / 1024 * 1024;
   static constexpr int kOffPsum = kOffOut + kOutBytes;
   static constexpr int kSmemBytes = kOffPsum + kPsumBytes + 1024;
-  // one CTA per SM (the planner's cluster capacities assume it)
-  static_assert(2 * kSmemBytes > kSmemLimit + 1024, "two CTAs would fit on one SM");
+  static_assert(kSmemBytes <= kSmemBudget, "shared memory budget");
+  // one CTA per SM for the other instantiations (the planner's cluster
+  // capacities for them assume it)
+  static_assert(kTwoPerSm || 2 * kSmemBytes > kSmemLimit + 1024, "two CTAs would fit on one SM");
   static constexpr int kTmemCols = tmem_cols_for(kTB * BN);
   // Cluster split-K: a CTA's partial tile goes into its (then idle) operand
   // ring, laid out so that the reduction reads it contiguously along the
@@ -283,12 +312,13 @@ __device__ __forceinline__ void reg_fence(uint32_t* v) {
   for (int i = 0; i < N; i += 16) reg_fence16(*reinterpret_cast<uint32_t(*)[16]>(v + i));
 }
 
-template <int BN, bool SWAP, int MODE>
-__global__ void __launch_bounds__(GemmCfg<BN, SWAP, MODE>::kThreads, 1)
+template <int BN, bool SWAP, int MODE, int MR>
+__global__ void __launch_bounds__(GemmCfg<BN, SWAP, MODE, MR>::kThreads,
+                                  GemmCfg<BN, SWAP, MODE, MR>::kTwoPerSm ? 2 : 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmP, const __grid_constant__ CUtensorMap tmQ,
                 const __grid_constant__ GemmArgs a) {
 #if defined(__CUDA_ARCH__)
-  using C = GemmCfg<BN, SWAP, MODE>;
+  using C = GemmCfg<BN, SWAP, MODE, MR>;
   static_assert(MODE == kModePlain || !SWAP, "grouped and fused variants use wide tiles");
   constexpr bool kGrouped = MODE == kModeGrouped;
   constexpr bool kFused = MODE == kModeFused;
@@ -360,11 +390,24 @@ __global__ void __launch_bounds__(GemmCfg<BN, SWAP, MODE>::kThreads, 1)
   const int32_t* spsum = reinterpret_cast<const int32_t*>(smem + C::kOffPsum);
   if (kGrouped) {
     // grouped mode: every role looks experts up from a shared-memory copy of
-    // psum (written by an earlier kernel, so read after the wait)
+    // psum (written by an earlier kernel, so read after the wait).  A layout
+    // that is not non-decreasing multiples of 128 (one tile would mix
+    // experts) is reported in the failure word and the CTA does nothing else:
+    // no copy has been issued and no TMEM allocated yet (grouped mode never
+    // prefetches weights), and every CTA reaches the same verdict.
     griddep_wait();
     int32_t* dst = reinterpret_cast<int32_t*>(smem + C::kOffPsum);
     for (int i = threadIdx.x; i < a.experts; i += C::kThreads) dst[i] = __ldg(a.psum + i);
     __syncthreads();
+    int bad = 0;
+    for (int i = threadIdx.x; i < a.experts; i += C::kThreads) {
+      const int32_t prev = i > 0 ? dst[i - 1] : 0;
+      if ((dst[i] & 127) != 0 || dst[i] < prev) bad = 1;
+    }
+    if (__syncthreads_or(bad)) {
+      if (threadIdx.x == 0) report_failure(a.err, kDevBadGroupedLayout);
+      return;
+    }
   }
   constexpr uint32_t kTmemSyncThreads = (C::kNE + 1) * 32;
   uint32_t tmem = 0;
@@ -545,7 +588,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, SWAP, MODE>::kThreads, 1)
       if (lane == 0 && warp == C::kNE) trace_event(a.trace, cta, kTrProdAtSync);
       if (lane == 0 && warp == C::kNE + 1) trace_event(a.trace, cta, kTrMmaAtSync);
       cluster_sync();
-      cluster_sync();
+      cluster_sync_relaxed();
     }
   } else {
     // ---------------------------------------------- promotion and epilogue
@@ -555,6 +598,9 @@ __global__ void __launch_bounds__(GemmCfg<BN, SWAP, MODE>::kThreads, 1)
     const int r = quad * 32 + lane;          // TMEM lane = row of the P tile
     const int col0 = half * C::kCPT;         // first TMEM column of this thread
     const int etid = threadIdx.x;            // 0 .. NE*32-1
+    // partial activation tiles: warps whose lane quadrant holds no loaded row
+    // skip the TMEM reads and FMAs (their rows are never stored)
+    const bool idle = MR < 128 && quad * 32 >= MR;
     const float* sRing = reinterpret_cast<const float*>(smem + C::kOffScale);
     int ss = 0;
     uint32_t sph = 0;
@@ -625,7 +671,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, SWAP, MODE>::kThreads, 1)
       const uint32_t taddr = tmem + static_cast<uint32_t>(b * BN + col0) +
                              (static_cast<uint32_t>(quad * 32) << 16);
 #pragma unroll
-      for (int c0 = 0; c0 < C::kCPT; c0 += C::kBatch) {
+      for (int c0 = 0; c0 < (idle ? 0 : C::kCPT); c0 += C::kBatch) {
         uint32_t v[C::kBatch];
 #pragma unroll
         for (int h = 0; h < C::kBatch; h += C::kCH) tmem_ld_cols<C::kCH>(taddr + c0 + h, v + h);
@@ -831,6 +877,8 @@ __global__ void __launch_bounds__(GemmCfg<BN, SWAP, MODE>::kThreads, 1)
       }
       if (kFused && !a.store_out) {
         // fused epilogue without the bf16 output
+      } else if (C::kTmaStore && a.tma_store && idle) {
+        // no row of this warp is stored
       } else if (C::kTmaStore && a.tma_store) {
         // rows of 16-byte-aligned bf16: 32 columns at a time into this warp's
         // 2 KB tile (16-byte chunk c of row i at 64 i + 16 (c ^ ((i >> 1) & 3)),
@@ -927,8 +975,8 @@ __global__ void __launch_bounds__(GemmCfg<BN, SWAP, MODE>::kThreads, 1)
       // cut into runs of 4 elements along n, is divided evenly among the
       // cluster's CTAs; each adds the cs partials of its runs in rank order
       // (deterministic) through distributed shared memory and stores bf16.
-      // The second barrier keeps every CTA (and its shared memory) alive
-      // until all reads of it are done.
+      // The second barrier (relaxed: it orders nothing) keeps every CTA and
+      // its shared memory alive until all reads of it are done.
       if (etid == 0) trace_event(a.trace, cta, kTrEpiAtSync);
       cluster_sync();
       if (etid == 0) trace_event(a.trace, cta, kTrClusterSync);
@@ -969,28 +1017,26 @@ __global__ void __launch_bounds__(GemmCfg<BN, SWAP, MODE>::kThreads, 1)
           rr[u] = off4;
           addr[u] = part0 + 4u * (line * C::kPartPitch + off4);
         }
-        float4 v[kU];
+        // every rank's values are requested before any is added (one
+        // distributed-shared-memory round trip), then summed in rank order
+        float4 t[8][kU];
 #pragma unroll
-        for (int u = 0; u < kU; ++u) v[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-        for (uint32_t q = 0; q < 8; ++q) {
-          if (q >= cs) break;
-          float4 t[kU];
+        for (uint32_t q = 0; q < 8; ++q)
 #pragma unroll
           for (int u = 0; u < kU; ++u)
-            if (i0 + u * kStride < end) t[u] = ld_dsmem_v4(mapa_shared(addr[u], q));
+            if (q < cs && i0 + u * kStride < end) t[q][u] = ld_dsmem_v4(mapa_shared(addr[u], q));
+        float4 v[kU];
+#pragma unroll
+        for (int u = 0; u < kU; ++u) v[u] = t[0][u];
+#pragma unroll
+        for (uint32_t q = 1; q < 8; ++q) {
+          if (q >= cs) break;
 #pragma unroll
           for (int u = 0; u < kU; ++u) {
-            if (i0 + u * kStride < end) {
-              if (q == 0) {
-                v[u] = t[u];
-              } else {
-                v[u].x += t[u].x;
-                v[u].y += t[u].y;
-                v[u].z += t[u].z;
-                v[u].w += t[u].w;
-              }
-            }
+            v[u].x += t[q][u].x;
+            v[u].y += t[q][u].y;
+            v[u].z += t[q][u].z;
+            v[u].w += t[q][u].w;
           }
         }
 #pragma unroll
@@ -1012,7 +1058,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, SWAP, MODE>::kThreads, 1)
       }
       BFP8_ACC(t_efix, e4);
       if (etid == 0) trace_event(a.trace, cta, kTrEpiReduced);
-      cluster_sync();
+      cluster_sync_relaxed();
     }
     if (etid == 0) {
       trace_event(a.trace, cta, kTrEpiEnd);
@@ -1052,17 +1098,17 @@ __global__ void __launch_bounds__(GemmCfg<BN, SWAP, MODE>::kThreads, 1)
 
 // Host side.  The dynamic shared-memory opt-in is per device and set once (a
 // launch captured into a CUDA graph then needs no attribute call).
-template <int BN, bool SWAP, int MODE = kModePlain>
+template <int BN, bool SWAP, int MODE = kModePlain, int MR = 128>
 cudaError_t configure_instance() {
-  using C = GemmCfg<BN, SWAP, MODE>;
+  using C = GemmCfg<BN, SWAP, MODE, MR>;
   static std::atomic<uint64_t> configured{0};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   const uint64_t bit = 1ull << (dev & 63);
   if (!(configured.load(std::memory_order_acquire) & bit)) {
-    e = cudaFuncSetAttribute(gemm_kernel<BN, SWAP, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             C::kSmemBytes);
+    e = cudaFuncSetAttribute(gemm_kernel<BN, SWAP, MODE, MR>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
     if (e != cudaSuccess) return e;
     configured.fetch_or(bit, std::memory_order_acq_rel);
   }
@@ -1087,18 +1133,18 @@ cudaError_t cluster_capacity_instance(int cs, int* clusters) {
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaOccupancyMaxActiveClusters(clusters, gemm_kernel<BN, SWAP, kModePlain>, &cfg);
+  return cudaOccupancyMaxActiveClusters(clusters, gemm_kernel<BN, SWAP, kModePlain, 128>, &cfg);
 }
 
 // Launches one instantiation with programmatic dependent launch (the
 // prologue may overlap the preceding kernel in the stream; the kernel waits
 // for it before reading its inputs) and, for cluster split-K, as 1-D
 // clusters of sched.cluster consecutive CTAs.
-template <int BN, bool SWAP, int MODE = kModePlain>
+template <int BN, bool SWAP, int MODE = kModePlain, int MR = 128>
 cudaError_t launch_instance(const CUtensorMap& tmP, const CUtensorMap& tmQ, const GemmArgs& a,
                             cudaStream_t stream) {
-  using C = GemmCfg<BN, SWAP, MODE>;
-  cudaError_t e = configure_instance<BN, SWAP, MODE>();
+  using C = GemmCfg<BN, SWAP, MODE, MR>;
+  cudaError_t e = configure_instance<BN, SWAP, MODE, MR>();
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(a.sched.grid);
@@ -1117,7 +1163,7 @@ cudaError_t launch_instance(const CUtensorMap& tmP, const CUtensorMap& tmQ, cons
     attr[1].val.clusterDim.z = 1;
     cfg.numAttrs = 2;
   }
-  return cudaLaunchKernelEx(&cfg, gemm_kernel<BN, SWAP, MODE>, tmP, tmQ, a);
+  return cudaLaunchKernelEx(&cfg, gemm_kernel<BN, SWAP, MODE, MR>, tmP, tmQ, a);
 }
 
 }  // namespace bfp8

@@ -74,9 +74,10 @@ cudaError_t launch_gemm_swap(int bn, const CUtensorMap& tmP, const CUtensorMap& 
   }
 }
 
-cudaError_t gemm_cluster_capacity(int cs, int* clusters) {
-  // every instantiation holds one CTA per SM, so one of them answers for all
-  return cluster_capacity_instance<16, true>(cs, clusters);
+cudaError_t gemm_cluster_capacity(int cs, bool two_per_sm, int* clusters) {
+  // the instantiations of each residency class share their answer
+  return two_per_sm ? cluster_capacity_instance<16, true>(cs, clusters)
+                    : cluster_capacity_instance<128, true>(cs, clusters);
 }
 
 cudaError_t launch_relayout(const uint8_t* src, int64_t rows, int64_t K, uint8_t* dst, int64_t kp,

@@ -6,9 +6,15 @@
 
 namespace bfp8 {
 
-cudaError_t launch_gemm_wide(int bn, int mode, const CUtensorMap& tmP, const CUtensorMap& tmQ,
-                             const GemmArgs& a, cudaStream_t stream) {
+cudaError_t launch_gemm_wide(int bn, int mode, int mr, const CUtensorMap& tmP,
+                             const CUtensorMap& tmQ, const GemmArgs& a, cudaStream_t stream) {
   if (mode != kModePlain) return launch_gemm_wide_ext(bn, mode, tmP, tmQ, a, stream);
+  if (mr != 128) {
+    if (bn != 256) return cudaErrorInvalidValue;
+    return mr == 32 ? launch_instance<256, false, kModePlain, 32>(tmP, tmQ, a, stream)
+         : mr == 64 ? launch_instance<256, false, kModePlain, 64>(tmP, tmQ, a, stream)
+                    : cudaErrorInvalidValue;
+  }
   switch (bn) {
     case 128: return launch_instance<128, false>(tmP, tmQ, a, stream);
     case 256: return launch_instance<256, false>(tmP, tmQ, a, stream);
@@ -33,7 +39,11 @@ cudaError_t launch_gemm_wide(int bn, int mode, const CUtensorMap& tmP, const CUt
     default: return 0;                                                          \
   }
 
-int gemm_stages(bool swap, int bn) { BFP8_CFG_CASES(kStages) }
+int gemm_stages(bool swap, int bn, int mr) {
+  if (!swap && bn == 256 && mr == 32) return GemmCfg<256, false, kModePlain, 32>::kStages;
+  if (!swap && bn == 256 && mr == 64) return GemmCfg<256, false, kModePlain, 64>::kStages;
+  BFP8_CFG_CASES(kStages)
+}
 int gemm_threads(bool swap, int bn) { BFP8_CFG_CASES(kThreads) }
 size_t gemm_smem_bytes(bool swap, int bn) { BFP8_CFG_CASES(kSmemBytes) }
 

@@ -18,27 +18,43 @@ bfp8_status set_last_error(bfp8_status st, const char* msg);
 
 struct GemmArgs;
 
-// Per-token group quantisation launcher (bfp8_quant.cu).
+// Per-token group quantisation launcher (bfp8_quant.cu); ue8m0: scales
+// rounded up to powers of two.
 cudaError_t launch_group_quant(const void* x, int in_f32, int64_t M, int64_t K, int64_t ld_x,
                                uint8_t* q, int64_t ld_q, float* s, int col_major, int64_t ld_s,
-                               int num_sms, cudaStream_t stream);
+                               int ue8m0, int num_sms, cudaStream_t stream);
+// n fp32 scales rounded up to powers of two (bfp8_quant.cu).
+cudaError_t launch_scale_ceil_ue8m0(const float* in, float* out, int64_t n, int num_sms,
+                                    cudaStream_t stream);
 
 // GEMM launchers (bfp8_gemm_swap.cu, bfp8_gemm_wide.cu).  `bn` selects the
 // instantiation; returns cudaErrorInvalidValue for one that does not exist.
 cudaError_t launch_gemm_swap(int bn, const CUtensorMap& tmP, const CUtensorMap& tmQ,
                              const GemmArgs& a, cudaStream_t stream);
 // `mode` selects the plain, M-grouped or fused-epilogue variant (wide only;
-// bfp8_gemm_kernel.cuh's kMode* values; the last two live in bfp8_gemm_ext.cu).
-cudaError_t launch_gemm_wide(int bn, int mode, const CUtensorMap& tmP, const CUtensorMap& tmQ,
-                             const GemmArgs& a, cudaStream_t stream);
+// bfp8_gemm_kernel.cuh's kMode* values; the last two live in bfp8_gemm_ext.cu);
+// `mr` the activation rows loaded per stage (128, or 32 / 64 for plain
+// 256-wide tiles of decode-sized M).
+cudaError_t launch_gemm_wide(int bn, int mode, int mr, const CUtensorMap& tmP,
+                             const CUtensorMap& tmQ, const GemmArgs& a, cudaStream_t stream);
 cudaError_t launch_gemm_wide_ext(int bn, int mode, const CUtensorMap& tmP, const CUtensorMap& tmQ,
                                  const GemmArgs& a, cudaStream_t stream);
 
-// Clusters of `cs` GEMM CTAs the current device runs at once (bfp8_gemm_swap.cu).
-cudaError_t gemm_cluster_capacity(int cs, int* clusters);
+// Clusters of `cs` GEMM CTAs the current device runs at once (bfp8_gemm_swap.cu),
+// for the instantiations sized for two CTAs per SM (swap-AB tiles up to 64
+// columns wide) or for the others (one CTA per SM).
+cudaError_t gemm_cluster_capacity(int cs, bool two_per_sm, int* clusters);
+
+// True for the GEMM instantiations sized for two CTAs per SM.
+inline bool gemm_two_per_sm(bool swap, int bn) { return swap && bn <= 64; }
+
+// Bytes at the start of every GEMM workspace that hold the stream-K tile
+// counters (4096 of them); they must read zero when a GEMM starts, and every
+// completed GEMM leaves them zero.
+constexpr size_t kCounterHeaderBytes = 16384;
 
 // Pipeline depth and dynamic shared memory of an instantiation (0 if none).
-int gemm_stages(bool swap, int bn);
+int gemm_stages(bool swap, int bn, int mr = 128);
 int gemm_threads(bool swap, int bn);
 size_t gemm_smem_bytes(bool swap, int bn);
 

@@ -5,7 +5,9 @@
 // The scratch is one file-scope device array.  Host code cannot use the
 // array's name as a device address (on the host it is only a stand-in), so
 // the real address is looked up once per device with cudaGetSymbolAddress,
-// with that device current, and cached.
+// with that device current, and cached.  The cached address belongs to the
+// device's context of that moment: after cudaDeviceReset() on a device, this
+// entry point must not be called on it again in the same process.
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -17,7 +19,6 @@
 namespace {
 
 constexpr size_t kNoAllocScratchBytes = BFP8_NOALLOC_SCRATCH_BYTES;
-constexpr size_t kCounterBytes = 16384;                     // counters that must start at zero
 constexpr int kMaxDevices = 64;
 
 static __device__ __align__(256) unsigned char g_bfp8_noalloc_scratch[kNoAllocScratchBytes];
@@ -64,7 +65,7 @@ extern "C" bfp8_status bfp8_gemm_noalloc(const void* A, const void* B, const flo
   if (need > 0) {
     // The array keeps the previous call's contents; the stream-K counters at
     // its start must read zero when the kernel starts.
-    const size_t clear = need < kCounterBytes ? need : kCounterBytes;
+    const size_t clear = need < bfp8::kCounterHeaderBytes ? need : bfp8::kCounterHeaderBytes;
     if (cudaMemsetAsync(scratch, 0, clear, static_cast<cudaStream_t>(stream)) != cudaSuccess) {
       cudaGetLastError();
       return bfp8::set_last_error(BFP8_ERR_CUDA, "bfp8_gemm_noalloc: clearing the scratch failed");

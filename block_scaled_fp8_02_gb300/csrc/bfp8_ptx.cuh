@@ -297,6 +297,18 @@ __device__ __forceinline__ void cluster_sync() {
       "barrier.cluster.wait.acquire;" ::: "memory");
 }
 
+// A cluster barrier that orders no memory: every thread of the cluster
+// arrives and waits, and nothing else.  Used where the only purpose is to keep
+// every CTA (and its shared memory) alive until all of them are done with
+// their distributed-shared-memory reads -- a load has completed once its value
+// is in a register, so no fence is needed; a release here would instead wait
+// for this thread's outstanding global stores.
+__device__ __forceinline__ void cluster_sync_relaxed() {
+  asm volatile(
+      "barrier.cluster.arrive.relaxed;\n\t"
+      "barrier.cluster.wait;" ::: "memory");
+}
+
 // Address of the same shared-memory location in the CTA of cluster rank `rank`.
 __device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
   uint32_t r;

@@ -9,7 +9,8 @@
 //                                             its code is found from two
 //                                             products that bracket it, with the
 //                                             division only where they disagree)
-// and the scale is stored row-major s[m * ld_s + g] or column-major
+// (the UE8M0 variant rounds each scale up to a power of two first, so the
+// quotients are exact products), and the scale is stored row-major s[m * ld_s + g] or column-major
 // s[g * ld_s + m] (the layout the GEMM kernels read; lmdeploy PR 4830 pads its
 // stride to 16 bytes for TMA, transformers' _coerce_sf_for_kernel calls it
 // MN-major).
@@ -140,7 +141,8 @@ __device__ __forceinline__ void load_batch(const void* x, const ChunkWalk& cw, u
   }
 }
 
-template <bool kF32>
+// kUe8m0: every scale rounded up to a power of two (the UE8M0 variant).
+template <bool kF32, bool kUe8m0>
 __global__ void __launch_bounds__(kWarpsPerBlock * 32, kBlocksPerSm)
     group_quant_kernel(const void* __restrict__ x, int64_t M, int64_t K, int64_t ld_x,
                        uint8_t* __restrict__ q, int64_t ld_q, float* __restrict__ s,
@@ -185,22 +187,31 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32, kBlocksPerSm)
 #pragma unroll
       for (int off = LPG / 2; off > 0; off >>= 1)
         amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
-      const float scale = group_scale(amax);
-      // codes without dividing (bfp8_e4m3.cuh); the IEEE divisions run only
-      // in warps where the bracket does not decide a code (warp-uniform branch)
-      const E4m3Bracket br(scale);
+      float scale;
       uint16_t pk[EPL / 2];
-      uint32_t undecided = 0;                 // one bit per pair
+      if constexpr (kUe8m0) {
+        // power-of-two scale: exact quotients by one multiply each
+        const Ue8m0Scale us(amax);
+        scale = us.scale;
 #pragma unroll
-      for (int e = 0; e < EPL; e += 2) {
-        bool u = false;
-        pk[e / 2] = e4m3_pair_bracketed(v[e], v[e + 1], br, u);
-        undecided |= static_cast<uint32_t>(u) << (e / 2);
-      }
-      if (__any_sync(0xffffffffu, undecided != 0)) {
+        for (int e = 0; e < EPL; e += 2) pk[e / 2] = e4m3_pair_pow2(v[e], v[e + 1], us.inv);
+      } else {
+        scale = group_scale(amax);
+        // codes without dividing (bfp8_e4m3.cuh); the IEEE divisions run only
+        // in warps where the bracket does not decide a code (warp-uniform branch)
+        const E4m3Bracket br(scale);
+        uint32_t undecided = 0;                 // one bit per pair
 #pragma unroll
-        for (int e = 0; e < EPL; e += 2)
-          if (undecided & (1u << (e / 2))) pk[e / 2] = e4m3_pair_divided(v[e], v[e + 1], scale);
+        for (int e = 0; e < EPL; e += 2) {
+          bool u = false;
+          pk[e / 2] = e4m3_pair_bracketed(v[e], v[e + 1], br, u);
+          undecided |= static_cast<uint32_t>(u) << (e / 2);
+        }
+        if (__any_sync(0xffffffffu, undecided != 0)) {
+#pragma unroll
+          for (int e = 0; e < EPL; e += 2)
+            if (undecided & (1u << (e / 2))) pk[e / 2] = e4m3_pair_divided(v[e], v[e + 1], scale);
+        }
       }
       if (!valid) continue;
       uint8_t* qrow = q + static_cast<int64_t>(cur.rw[u]) * ld_q;
@@ -232,11 +243,184 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32, kBlocksPerSm)
   }
 }
 
+// ---------------------------------------------------------------------------
+// The common case on a lean path: bf16 rows of whole 256-element steps (K a
+// multiple of 256, 16-byte aligned rows and codes).  A step is one warp's
+// 512 input bytes -- two groups, a half-warp each, 8 elements per lane.  Each
+// warp walks kStepU steps at a time (all their loads issued before any is
+// used), with 32-bit offsets (the host checks that they fit) and products
+// packed two per instruction.  Same arithmetic, bit for bit, as the general
+// kernel above.
+constexpr int kStepU = 4;
+
+template <bool kUe8m0>
+__global__ void __launch_bounds__(kWarpsPerBlock * 32, kBlocksPerSm)
+    group_quant_bf16_steps_kernel(const uint16_t* __restrict__ x, uint32_t M, uint32_t spr,
+                                  uint32_t ld_x, uint8_t* __restrict__ q, uint32_t ld_q,
+                                  float* __restrict__ s, int32_t col_major, uint32_t ld_s,
+                                  uint32_t adv_row, uint32_t adv_col) {
+  const int lane = threadIdx.x & 31;
+  const uint32_t half = static_cast<uint32_t>(lane) >> 4;     // group within the step
+  const uint32_t warp0 = blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
+  const uint32_t nwarps = gridDim.x * kWarpsPerBlock;
+  // walker u visits steps warp0 + (u + kStepU * i) * nwarps; a step is
+  // (row, column of 256 elements); each advance moves a walker kStepU * nwarps
+  // steps = adv_row rows and adv_col columns (one carry at most, adv_col < spr)
+  uint32_t rw[kStepU], cl[kStepU];
+#pragma unroll
+  for (int u = 0; u < kStepU; ++u) {
+    const uint32_t st = warp0 + static_cast<uint32_t>(u) * nwarps;
+    rw[u] = st / spr;
+    cl[u] = st - rw[u] * spr;
+  }
+  griddep_launch_dependents();
+  griddep_wait();
+  while (rw[0] < M) {
+    uint4 w[kStepU];
+#pragma unroll
+    for (int u = 0; u < kStepU; ++u)
+      if (rw[u] < M)
+        w[u] = __ldg(reinterpret_cast<const uint4*>(x + rw[u] * ld_x + cl[u] * 256u) + lane);
+#pragma unroll
+    for (int u = 0; u < kStepU; ++u) {
+      if (rw[u] >= M) continue;
+      const uint32_t ww[4] = {w[u].x, w[u].y, w[u].z, w[u].w};
+      float v[8];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        v[2 * i] = __uint_as_float(ww[i] << 16);
+        v[2 * i + 1] = __uint_as_float(ww[i] & 0xFFFF0000u);
+      }
+      float amax = fabsf(v[0]);
+#pragma unroll
+      for (int e = 1; e < 8; ++e) amax = fmaxf(amax, fabsf(v[e]));
+#pragma unroll
+      for (int off = 8; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+      float scale;
+      uint32_t pk[4];
+      if constexpr (kUe8m0) {
+        const Ue8m0Scale us(amax);
+        scale = us.scale;
+        const uint64_t inv2 = pack_u32x2(__float_as_uint(us.inv), __float_as_uint(us.inv));
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          float a0, a1;
+          unpack_f32x2(mul_f32x2(pack_u32x2(__float_as_uint(v[2 * i]), __float_as_uint(v[2 * i + 1])), inv2),
+                       a0, a1);
+          pk[i] = cvt_e4m3x2(a0, a1);
+        }
+      } else {
+        scale = group_scale(amax);
+        const E4m3Bracket br(scale);
+        const uint64_t lo2 = pack_u32x2(__float_as_uint(br.lo), __float_as_uint(br.lo));
+        const uint64_t hi2 = pack_u32x2(__float_as_uint(br.hi), __float_as_uint(br.hi));
+        uint32_t undecided = 0;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const uint64_t x2 = pack_u32x2(__float_as_uint(v[2 * i]), __float_as_uint(v[2 * i + 1]));
+          float a0, a1, b0, b1;
+          unpack_f32x2(mul_f32x2(x2, lo2), a0, a1);
+          unpack_f32x2(mul_f32x2(x2, hi2), b0, b1);
+          const uint32_t lo = cvt_e4m3x2(a0, a1), hi = cvt_e4m3x2(b0, b1);
+          pk[i] = lo;
+          undecided |= static_cast<uint32_t>(lo != hi) << i;
+        }
+        // warp-uniform branch: IEEE divisions only for the undecided pairs
+        if (__any_sync(0xffffffffu, undecided != 0)) {
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            if (undecided & (1u << i)) pk[i] = e4m3_pair_divided(v[2 * i], v[2 * i + 1], scale);
+        }
+      }
+      uint2 wq;
+      wq.x = pk[0] | (pk[1] << 16);
+      wq.y = pk[2] | (pk[3] << 16);
+      *reinterpret_cast<uint2*>(q + rw[u] * ld_q + cl[u] * 256u + static_cast<uint32_t>(lane) * 8u) = wq;
+      if ((lane & 15) == 0) {
+        const uint32_t g = cl[u] * 2u + half;
+        if (col_major) s[g * ld_s + rw[u]] = scale;
+        else s[rw[u] * ld_s + g] = scale;
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kStepU; ++u) {
+      cl[u] += adv_col;
+      rw[u] += adv_row;
+      if (cl[u] >= spr) {
+        cl[u] -= spr;
+        ++rw[u];
+      }
+    }
+  }
+}
+
+// Rounds n fp32 scales up to powers of two (the UE8M0 variant's weight scales).
+__global__ void scale_ceil_ue8m0_kernel(const float* __restrict__ in, float* __restrict__ out,
+                                        int64_t n) {
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x)
+    out[i] = __uint_as_float(ceil_ue8m0_bits(in[i]));
+}
+
+}  // namespace
+
+cudaError_t launch_scale_ceil_ue8m0(const float* in, float* out, int64_t n, int num_sms,
+                                    cudaStream_t stream) {
+  int64_t blocks = (n + 255) / 256;
+  if (blocks > static_cast<int64_t>(num_sms) * 4) blocks = static_cast<int64_t>(num_sms) * 4;
+  if (blocks < 1) blocks = 1;
+  scale_ceil_ue8m0_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(in, out, n);
+  return cudaGetLastError();
+}
+
+namespace {
+
+template <bool kF32, bool kUe8m0>
+cudaError_t launch_quant_instance(const cudaLaunchConfig_t& cfg, const void* x, int64_t M,
+                                  int64_t K, int64_t ld_x, uint8_t* q, int64_t ld_q, float* s,
+                                  int32_t cm, int64_t ld_s, int32_t vec_x, int32_t vec_q) {
+  return cudaLaunchKernelEx(&cfg, group_quant_kernel<kF32, kUe8m0>, x, M, K, ld_x, q, ld_q, s, cm,
+                            ld_s, vec_x, vec_q);
+}
+
 }  // namespace
 
 cudaError_t launch_group_quant(const void* x, int in_f32, int64_t M, int64_t K, int64_t ld_x,
                                uint8_t* q, int64_t ld_q, float* s, int col_major, int64_t ld_s,
-                               int num_sms, cudaStream_t stream) {
+                               int ue8m0, int num_sms, cudaStream_t stream) {
+  // lean path: bf16, whole 256-element steps, 16-byte aligned rows of x and
+  // 8-byte aligned rows of q, 32-bit offsets
+  const bool lean = !in_f32 && K % 256 == 0 && reinterpret_cast<uintptr_t>(x) % 16 == 0 &&
+                    ld_x % 8 == 0 && reinterpret_cast<uintptr_t>(q) % 8 == 0 && ld_q % 8 == 0 &&
+                    M * ld_x < (int64_t{1} << 31) && M * ld_q < (int64_t{1} << 31) &&
+                    (col_major ? ((K / 128) * ld_s) : (M * ld_s)) < (int64_t{1} << 31);
+  if (lean) {
+    const uint32_t spr = static_cast<uint32_t>(K / 256);
+    const int64_t steps = M * spr;
+    int64_t blocks = (steps + kWarpsPerBlock - 1) / kWarpsPerBlock;
+    const int64_t cap = static_cast<int64_t>(num_sms) * kBlocksPerSm;
+    if (blocks > cap) blocks = cap;
+    if (blocks < 1) blocks = 1;
+    const uint32_t adv = static_cast<uint32_t>(blocks) * kWarpsPerBlock * kStepU;
+    if (steps + 2 * static_cast<int64_t>(adv) >= (int64_t{1} << 31)) return cudaErrorInvalidValue;
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(static_cast<unsigned>(blocks));
+    cfg.blockDim = dim3(kWarpsPerBlock * 32);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const auto* xb = static_cast<const uint16_t*>(x);
+    const uint32_t Mu = static_cast<uint32_t>(M), ldx = static_cast<uint32_t>(ld_x),
+                   ldq = static_cast<uint32_t>(ld_q), lds = static_cast<uint32_t>(ld_s);
+    const int32_t cm = col_major;
+    return ue8m0 ? cudaLaunchKernelEx(&cfg, group_quant_bf16_steps_kernel<true>, xb, Mu, spr, ldx, q,
+                                      ldq, s, cm, lds, adv / spr, adv % spr)
+                 : cudaLaunchKernelEx(&cfg, group_quant_bf16_steps_kernel<false>, xb, Mu, spr, ldx, q,
+                                      ldq, s, cm, lds, adv / spr, adv % spr);
+  }
   const int64_t G = (K + 127) / 128;
   const int esize = in_f32 ? 4 : 2;
   const int epl = in_f32 ? 4 : 8;
@@ -263,10 +447,10 @@ cudaError_t launch_group_quant(const void* x, int in_f32, int64_t M, int64_t K, 
   cfg.numAttrs = 1;
   const int32_t cm = col_major;
   if (in_f32)
-    return cudaLaunchKernelEx(&cfg, group_quant_kernel<true>, x, M, K, ld_x, q, ld_q, s, cm, ld_s,
-                              vec_x, vec_q);
-  return cudaLaunchKernelEx(&cfg, group_quant_kernel<false>, x, M, K, ld_x, q, ld_q, s, cm, ld_s,
-                            vec_x, vec_q);
+    return ue8m0 ? launch_quant_instance<true, true>(cfg, x, M, K, ld_x, q, ld_q, s, cm, ld_s, vec_x, vec_q)
+                 : launch_quant_instance<true, false>(cfg, x, M, K, ld_x, q, ld_q, s, cm, ld_s, vec_x, vec_q);
+  return ue8m0 ? launch_quant_instance<false, true>(cfg, x, M, K, ld_x, q, ld_q, s, cm, ld_s, vec_x, vec_q)
+               : launch_quant_instance<false, false>(cfg, x, M, K, ld_x, q, ld_q, s, cm, ld_s, vec_x, vec_q);
 }
 
 }  // namespace bfp8

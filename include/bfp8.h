@@ -78,6 +78,37 @@ bfp8_status bfp8_group_quant(const void* x, int in_dtype, int64_t M, int64_t K, 
                              int group, int col_major, void* q, int64_t ld_q, float* s,
                              int64_t ld_s, void* stream);
 
+/* ------------------------------------------------------------------------ */
+/* UE8M0 scale variant                                                       */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * The transformers DeepGEMM integration (`_ceil_to_ue8m0`, and
+ * `_select_fp8_cast_kwargs` with use_ue8m0) rounds every fp32 scale UP to the
+ * nearest power of two -- the UE8M0 format keeps only the biased exponent --
+ * for the SM100 kernels.  That is a different function from the fp32-scale
+ * layer above: activations are quantised with the rounded scale, and weight
+ * scales are rounded the same way.  The blocked GEMM below computes it as it
+ * stands (bfp8_gemm with such As and Bs); the scales stay fp32 values.
+ */
+typedef enum { BFP8_SCALE_FP32 = 0, BFP8_SCALE_UE8M0 = 1 } bfp8_scale_fmt;
+
+/* bfp8_group_quant with a choice of scale format.  BFP8_SCALE_FP32: as
+ * bfp8_group_quant.  BFP8_SCALE_UE8M0: each group's scale max(amax, 1e-10) /
+ * 448 (IEEE fp32 division) is rounded up to a power of two (2^-42 for an
+ * all-zero group), and q = e4m3(x / scale) with the quotient exact; |x / scale|
+ * <= 448, so no code saturates.  Other arguments, layouts and errors as for
+ * bfp8_group_quant; BFP8_ERR_INVALID_ARG for another scale_fmt. */
+bfp8_status bfp8_group_quant_ex(const void* x, int in_dtype, int64_t M, int64_t K, int64_t ld_x,
+                                int group, int col_major, int scale_fmt, void* q, int64_t ld_q,
+                                float* s, int64_t ld_s, void* stream);
+
+/* out[i] = in[i] rounded up to the nearest power of two, for n >= 0 positive
+ * finite fp32 scales (e.g. a weight-scale tensor Bs for the UE8M0 variant);
+ * other inputs give unspecified values.  in == out is allowed.  Device
+ * pointers, 4-byte aligned; asynchronous on `stream`. */
+bfp8_status bfp8_scale_ceil_ue8m0(const float* in, float* out, int64_t n, void* stream);
+
 /* Column-major scale stride the GEMM prefers: M rounded up to a multiple of 4
  * (16 bytes of fp32, the TMA stride rule lmdeploy PR 4830 pads for). */
 int64_t bfp8_scale_ld(int64_t M);
@@ -241,9 +272,10 @@ bfp8_status bfp8_plan_unit(int64_t M, int64_t N, int64_t K, int num_sms,
  * for bfp8_gemm_ex except `schedule` (ignored) and `prefetch_weights`
  * (ignored: the expert of a tile is known only after the wait).  Workspace
  * from bfp8_gemm_grouped_workspace_size.  Requirements as for bfp8_gemm plus
- * 1 <= num_experts <= 1024 and grouped_layout 4-byte aligned; its contents
- * are not validated (a block not a multiple of 128 rows mixes experts in one
- * tile and gives wrong results for its rows).
+ * 1 <= num_experts <= 1024 and grouped_layout 4-byte aligned.  Its contents
+ * live on the device and are checked there: when they are not non-decreasing
+ * multiples of 128, the kernel writes nothing and records
+ * BFP8_DEV_BAD_GROUPED_LAYOUT in the failure word (bfp8_device_status).
  */
 bfp8_status bfp8_gemm_grouped(const void* A, const void* B, const float* As, int as_col_major,
                               int64_t ld_as, const float* Bs, const int32_t* grouped_layout,
@@ -315,7 +347,9 @@ bfp8_status bfp8_gemm_fused_workspace_size(int64_t M, int64_t N, int64_t K,
  *     large-M problems generally do not.
  *   - The first call on each device looks up the scratch's device address
  *     (cudaGetSymbolAddress) with that device current; make that first call
- *     before any stream capture begins.
+ *     before any stream capture begins.  The address is kept for the life of
+ *     the process: after cudaDeviceReset() on a device, do not call this
+ *     entry point on that device again.
  *   - Every call on a device shares the one scratch array, and it keeps the
  *     previous call's contents: each call first clears (cudaMemsetAsync on
  *     `stream`) the part that must start at zero.  Calls whose kernels can
@@ -338,8 +372,16 @@ const char* bfp8_last_error(void);
 const char* bfp8_status_string(int status);
 
 /* Synchronises the current device and reads the library's device-side failure
- * word for it (0 = no kernel-side wait has given up since the last clear);
- * clears it when `clear` is nonzero. */
+ * word for it; clears it when `clear` is nonzero.  The word holds the first
+ * failure a kernel reported since the last clear: */
+#define BFP8_DEV_OK 0                       /* none */
+#define BFP8_DEV_TIMEOUT_PRODUCER 1         /* a bounded wait gave up: operand loader */
+#define BFP8_DEV_TIMEOUT_MMA 2              /*   MMA issuer */
+#define BFP8_DEV_TIMEOUT_EPILOGUE 3         /*   promotion / epilogue warps */
+#define BFP8_DEV_TIMEOUT_TAIL 4             /*   draining copies before exit */
+#define BFP8_DEV_BAD_GROUPED_LAYOUT 5       /* bfp8_gemm_grouped: invalid grouped_layout */
+/* After a timeout code, a workspace the call used may hold non-zero counters:
+ * zero it before reusing it. */
 bfp8_status bfp8_device_status(int* code, int clear);
 
 /* Self-test of the bounded wait every kernel uses: launches one warp that

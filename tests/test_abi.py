@@ -67,6 +67,23 @@ def test_group_quant_rejects_bad_arguments_on_the_host(L):
     assert _quant(L, M=0) == 0 and _quant(L, K=0, x=None) == 0   # empty: nothing to do
 
 
+def test_ue8m0_entry_points_reject_bad_arguments_on_the_host(L):
+    def q(fmt, **kw):
+        a = dict(x=256, in_dtype=0, M=4, K=200, ld_x=200, group=128, col=1, q=256, ld_q=200, s=256,
+                 ld_s=4)
+        a.update(kw)
+        return L.bfp8_group_quant_ex(a["x"], a["in_dtype"], a["M"], a["K"], a["ld_x"], a["group"],
+                                     a["col"], fmt, a["q"], a["ld_q"], a["s"], a["ld_s"], None)
+    assert q(2) == 1 and "scale_fmt" in bf.bfp8_last_error()
+    assert q(-1) == 1
+    assert q(1, group=64) == 1
+    assert q(1, M=0) == 0 and q(0, M=0) == 0
+    assert L.bfp8_scale_ceil_ue8m0(256, 256, -1, None) == 1
+    assert L.bfp8_scale_ceil_ue8m0(None, 256, 4, None) == 1
+    assert L.bfp8_scale_ceil_ue8m0(258, 256, 4, None) == 2
+    assert L.bfp8_scale_ceil_ue8m0(None, None, 0, None) == 0      # empty: nothing to do
+
+
 def _gemm(L, **kw):
     a = dict(A=256, B=256, As=256, col=1, ld_as=4, Bs=256, out=256, M=4, N=128, K=256, ws=256,
              wsb=1 << 30, opt=None, stream=None)

@@ -223,3 +223,22 @@ def test_weight_prefetch_right_after_quantisation(oracle_mod, dev, M, N, K):
     ref = oracle_mod.blocked_gemm(A, case["B"].view(torch.uint8).numpy(), As, True,
                                   case["Bs"].numpy(), want_abs=True)
     check_gemm(out, ref, (K + 127) // 128, label=f"prefetch {M}x{N}x{K}")
+
+
+@pytest.mark.parametrize("M", [1, 16, 32, 33, 64])
+@pytest.mark.parametrize("k_split", [0, 1, 2, 3])
+def test_wide_tiles_with_partial_activation_rows(oracle_mod, dev, M, k_split):
+    """Decode-sized M on 256-wide tiles loads only 32 or 64 activation rows per
+    stage; the MMA still spans 128 rows and the promotion warps of the unused
+    lane quadrants stay idle.  Every schedule, full comparison."""
+    case = wl.linear_case(M, 4096, 4096, seed=900 + M)
+    _run(oracle_mod, dev, case, options={"schedule": 2, "k_split": k_split},
+         label=f"wide-rows M={M} k_split={k_split}")
+
+
+@pytest.mark.parametrize("M,N,K", [(5, 1000, 1000), (40, 576, 7168), (64, 300, 129)])
+def test_wide_partial_rows_ragged(oracle_mod, dev, M, N, K):
+    case = wl.ragged_case(M, N, K, seed=M + N + K)
+    for col_major in (True, False):
+        _run(oracle_mod, dev, case, col_major, options={"schedule": 2},
+             label=f"wide-rows ragged {M}x{N}x{K}")
