@@ -1,35 +1,47 @@
 #!/usr/bin/env python3
 """bench.py -- the blocked W8A8 FP8 linear layer (libbfp8) on GB300.
 
-Workload (the H200 latency table of lmdeploy PR 4830, "Performance"): N = K =
-4096 and M in {1, 8, 9, 16, 24, 32, 64, 128, 160, 192, 224, 256, 512, 1024,
-2048, 4096, 8192}.  One step runs the whole hot path for every M: per-token
-group quantisation of that M's bf16 activations, then the blocked FP8 GEMM
-against that M's own copy of the e4m3 weights (17 weight copies, ~0.65 GB of
-buffers touched once per step, so every kernel reads its inputs cold from
-HBM: the 129 MB L2 cannot carry them from one step to the next).
+Headline workload (the H200 latency table of lmdeploy PR 4830, "Performance"):
+N = K = 4096 and M in {1, 8, 9, 16, 24, 32, 64, 128, 160, 192, 224, 256, 512,
+1024, 2048, 4096, 8192}.  One step runs the whole hot path for every M:
+per-token group quantisation of that M's bf16 activations, then the blocked
+FP8 GEMM against that M's own copy of the e4m3 weights (17 weight copies,
+~0.65 GB of buffers touched once per step, so every kernel reads its inputs
+cold from HBM: the L2 cannot carry them from one step to the next).  Each step
+is one CUDA graph of the 34 kernels (programmatic dependent launch between
+them).  The timed region replays that graph --steps times, bracketed by a
+barrier and torch.cuda.synchronize() on both sides, with CUDA events only at
+its two ends; its duration is the max over ranks.  value = 2*M*N*K summed over
+the sweep, times steps and ranks, over that duration (TFLOP/s).
 
-Timing: each step is one CUDA graph of the 34 kernels (launched with
-programmatic dependent launch, so each GEMM starts streaming its weights while
-its quantisation kernel runs).  The timed region replays that graph --steps
-times, bracketed by a barrier and torch.cuda.synchronize() on both sides, with
-CUDA events only at its two ends; its duration is the max over ranks.
-value = 2*M*N*K summed over the sweep, times steps and ranks, over that
-duration (TFLOP/s).  A second pass replays graphs that carry a timing event
-between consecutive kernels (two sets alternate so the host reads one set's
-events while the GPU runs the other) for the per-kernel breakdown and the
-roofline numbers; event nodes add a few microseconds per kernel, so those
-per-kernel times are slight overestimates.
+Per-kernel figures (per_m, roofline, the other workloads) follow the timing
+protocol of the same page, made stricter: for each configuration a CUDA graph
+of 20 back-to-back launches is replayed; CUDA events on the launching stream
+bracket each replay, and a launch's time is the replay's time / 20.  Every
+configuration is measured in 5 trials that alternate across configurations
+(each trial: a warm-up, then replays for at least --trial-ms), and the
+reported p50 is the median of the trials' medians.  Cold L2 (graded): the
+launches of a replay rotate through enough copies of every buffer that a copy
+is reused only after at least 3 x L2 bytes of other traffic (or a buffer is
+itself larger than 3 x L2).  Hot L2 (the page's "identical preallocated
+inputs"): one copy, reported beside it.
 
---impl reference times the CPU oracle (the test checker) the same way on a
-bounded sample of the same workload; its ratio to the GPU is context only.
-Multi-GPU: the layer does not need an exchange, so N GPUs run N independent
-replicas (scaling "weak").
+Other workloads, timed the same way: the Qwen3-32B-shaped linear stack
+(qkv / o / gate_up / down at M in {1, 16, 64, 256, 2048}), the quantisation
+sweep (M in {2048, 8192} x K in {4096, 7168, 25600}), the ragged/tail shapes
+(reported, not graded), the UE8M0-scale variant and the rows beyond the sweep
+(M-grouped MoE GEMM, fused epilogue).
+
+--impl reference times the CPU oracle (the test checker) on a bounded sample
+of the same workload; its ratio to the GPU is context only.
+Multi-GPU: the layer needs no exchange, so N GPUs run N independent replicas
+(scaling "weak").
 """
 from __future__ import annotations
 
 import argparse
 import json
+import math
 import os
 import statistics
 import subprocess
@@ -41,7 +53,8 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 NK = 4096
-KERNEL_GROUPS = ("quant", "gemm_swap_ab", "gemm_wide")
+BATCH = 20          # launches per timed CUDA-graph replay
+TRIALS = 5
 
 
 def parse_args():
@@ -52,10 +65,13 @@ def parse_args():
     p.add_argument("--impl", choices=("ours", "reference"), default="ours")
     p.add_argument("--ms", type=str, default=None, help="comma-separated M list (default: the sweep)")
     p.add_argument("--nk", type=int, default=NK, help="N = K")
+    p.add_argument("--trial-ms", type=float, default=30.0,
+                   help="measured replay time per configuration per trial")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
-    p.add_argument("--no-extensions", action="store_true",
-                   help="skip timing the grouped (MoE) GEMM and the fused epilogue")
+    p.add_argument("--no-workloads", action="store_true",
+                   help="time only the headline sweep (skip the Qwen3-32B stack, quantisation "
+                        "sweep, ragged shapes, UE8M0 variant and extensions)")
     p.add_argument("--cpu-budget-s", type=float, default=12.0,
                    help="wall seconds (on all host cores) for the oracle baseline sample")
     return p.parse_args()
@@ -207,6 +223,97 @@ def barrier(world: int):
         dist.barrier()
 
 
+def copies_for(bytes_per_copy: int, l2_bytes: int, cold: bool) -> int:
+    """Copies to rotate through so that a copy is reused only after at least
+    3 x L2 bytes of other buffers (1 when a copy alone is that large, or hot);
+    at most two replays' worth of launches (two graphs then alternate)."""
+    if not cold:
+        return 1
+    return max(1, min(2 * BATCH, math.ceil(3 * l2_bytes / max(bytes_per_copy, 1))))
+
+
+# ------------------------------------------------------ graph-batch timing --
+
+class GraphTimer:
+    """Per-launch device time of a configuration: a CUDA graph of BATCH
+    back-to-back launches, replayed with CUDA events around each replay on the
+    launching stream; time per launch = replay time / BATCH.  launch(i) issues
+    launch i; when the configuration rotates through more than BATCH buffer
+    copies (`rotation`), two graphs (launches 0..BATCH-1 and BATCH..2*BATCH-1)
+    alternate."""
+
+    def __init__(self, name: str, launch, meta: dict, rotation: int = 1, keep=()):
+        import torch
+        self.name = name
+        self.meta = meta
+        # the captured launches use these buffers' addresses: they must live as
+        # long as the graphs
+        self.keep = keep
+        self.stream = torch.cuda.Stream()
+        self.trials: list[list[float]] = []
+        n_graphs = 2 if rotation > BATCH else 1
+        with torch.cuda.stream(self.stream):
+            for i in range(BATCH * n_graphs):   # eager pass: first launches set kernel attributes
+                launch(i)
+            torch.cuda.synchronize()
+            self.graphs = []
+            for gi in range(n_graphs):
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=self.stream):
+                    for i in range(BATCH):
+                        launch(gi * BATCH + i)
+                self.graphs.append(g)
+        torch.cuda.synchronize()
+        self.ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                   for _ in range(64)]
+        self.k = 0
+
+    def _replay(self):
+        import torch
+        with torch.cuda.stream(self.stream):     # replay on the stream the events are on
+            self.graphs[self.k % len(self.graphs)].replay()
+        self.k += 1
+
+    def trial(self, measure_ms: float, warmup_replays: int = 4, max_replays: int = 2000):
+        import torch
+        for _ in range(warmup_replays):
+            self._replay()
+        times = []
+        spent = 0.0
+        n = 0
+        while (spent < measure_ms or n < 5) and n < max_replays:
+            k = min(len(self.ev), max(6, n))       # replays between host syncs
+            for j in range(k):
+                self.ev[j][0].record(self.stream)
+                self._replay()
+                self.ev[j][1].record(self.stream)
+            self.ev[k - 1][1].synchronize()
+            for j in range(k):
+                ms = self.ev[j][0].elapsed_time(self.ev[j][1])
+                spent += ms
+                times.append(ms * 1e3 / BATCH)
+            n += k
+        self.trials.append(times)
+        torch.cuda.synchronize()
+
+    def p50_us(self) -> float:
+        return statistics.median(statistics.median(t) for t in self.trials)
+
+    def mean_us(self) -> float:
+        return statistics.mean(statistics.mean(t) for t in self.trials)
+
+    def replays(self) -> int:
+        return sum(len(t) for t in self.trials)
+
+
+def run_trials(timers, measure_ms: float):
+    """TRIALS rounds; in each, every configuration is warmed up and measured in
+    turn (alternating configurations between trials, as the page does)."""
+    for _ in range(TRIALS):
+        for t in timers:
+            t.trial(measure_ms)
+
+
 # ------------------------------------------------------------ CPU oracle ---
 
 def oracle_setup(nk, seed=1234):
@@ -259,6 +366,81 @@ def oracle_sample(Ms, nk, budget_s, seed=1234, setup=None):
     return flops, secs, cores, desc
 
 
+# ------------------------------------------------------------ buffers ------
+
+class Weights:
+    """R copies of one e4m3 weight matrix and its scales (on the device)."""
+
+    def __init__(self, N, K, R, dev, seed):
+        from block_scaled_fp8_02_gb300 import workloads as wl
+        c = wl.linear_case(1, N, K, seed)
+        B0, Bs0 = c["B"].to(dev), c["Bs"].to(dev)
+        self.B = [B0] + [B0.clone() for _ in range(R - 1)]
+        self.Bs = [Bs0] + [Bs0.clone() for _ in range(R - 1)]
+        self.N, self.K = N, K
+
+    def __len__(self):
+        return len(self.B)
+
+
+class Acts:
+    """R copies of one M's activations, codes, scales and output."""
+
+    def __init__(self, M, N, K, R, dev, seed, out=True):
+        import torch
+        import block_scaled_fp8_02_gb300 as bf
+        from block_scaled_fp8_02_gb300 import workloads as wl
+        G = (K + 127) // 128
+        x0 = wl.activations(M, K, seed).to(dev)
+        ld = bf.bfp8_scale_ld(M)
+        self.M, self.N, self.K = M, N, K
+        self.x, self.q, self.s_st, self.s, self.out = [], [], [], [], []
+        for r in range(R):
+            x = x0 if r == 0 else x0.clone()
+            q = torch.empty((M, K), dtype=torch.float8_e4m3fn, device=dev)
+            s_st = torch.empty((G, ld), dtype=torch.float32, device=dev)
+            self.x.append(x)
+            self.q.append(q)
+            self.s_st.append(s_st)
+            self.s.append(s_st[:, :M].t())
+            self.out.append(torch.empty((M, N), dtype=torch.bfloat16, device=dev) if out else None)
+        for r in range(R):
+            bf.bfp8_group_quant(self.x[r], q=self.q[r], s_storage=self.s_st[r])
+
+    def __len__(self):
+        return len(self.x)
+
+
+def gemm_cfg(name, acts, w, ws, opts, meta):
+    import block_scaled_fp8_02_gb300 as bf
+
+    def launch(i):
+        a, b = i % len(acts), i % len(w)
+        bf.bfp8_gemm(acts.q[a], w.B[b], acts.s[a], w.Bs[b], out=acts.out[a], workspace=ws,
+                     options=opts)
+    return GraphTimer(name, launch, meta, max(len(acts), len(w)), keep=(acts, w, ws))
+
+
+def quant_cfg(name, acts, meta, **kw):
+    import block_scaled_fp8_02_gb300 as bf
+
+    def launch(i):
+        a = i % len(acts)
+        bf.bfp8_group_quant(acts.x[a], q=acts.q[a], s_storage=acts.s_st[a], **kw)
+    return GraphTimer(name, launch, meta, len(acts), keep=(acts,))
+
+
+def layer_cfg(name, acts, w, ws, opts, meta):
+    import block_scaled_fp8_02_gb300 as bf
+
+    def launch(i):
+        a, b = i % len(acts), i % len(w)
+        bf.bfp8_group_quant(acts.x[a], q=acts.q[a], s_storage=acts.s_st[a])
+        bf.bfp8_gemm(acts.q[a], w.B[b], acts.s[a], w.Bs[b], out=acts.out[a], workspace=ws,
+                     options=opts)
+    return GraphTimer(name, launch, meta, max(len(acts), len(w)), keep=(acts, w, ws))
+
+
 # ----------------------------------------------------------------- ours ----
 
 def run_ours(args, rank, world, local):
@@ -271,19 +453,26 @@ def run_ours(args, rank, world, local):
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     bf.lib()
+    props = torch.cuda.get_device_properties(dev)
+    l2 = int(getattr(props, "L2_cache_size", 0) or 126 * 2 ** 20)
     Ms = sweep_ms(args)
     N = K = args.nk
     G = (K + 127) // 128
+    peaks = load_peaks()
+    fp8_burst = 2.0 * peaks["bf16_tflops"]
+    hbm = peaks["hbm_gbs"]
+    gemm_opts = {"prefetch_weights": 1}   # each GEMM follows its own quantisation kernel
+
+    # ---------------------------------------------- the headline step (value)
     base = wl.linear_case(1, N, K, seed=4242 + rank)
     B0 = base["B"].to(dev)
     Bs0 = base["Bs"].to(dev)
     bufs = []
-    gemm_opts = {"prefetch_weights": 1}   # each GEMM follows its own quantisation kernel
     for M in Ms:
         x = wl.activations(M, K, seed=1000 + M + 7919 * rank).to(dev)
         ld = bf.bfp8_scale_ld(M)
         s_st = torch.empty((G, ld), dtype=torch.float32, device=dev)
-        wsb = bf.bfp8_gemm_workspace_size(M, N, K)
+        wsb = bf.bfp8_gemm_workspace_size(M, N, K, gemm_opts)
         bufs.append(dict(
             M=M, x=x, B=B0.clone(), Bs=Bs0.clone(),
             q=torch.empty((M, K), dtype=torch.float8_e4m3fn, device=dev), s_st=s_st,
@@ -291,235 +480,238 @@ def run_ours(args, rank, world, local):
             ws=torch.zeros(max(wsb, 256), dtype=torch.uint8, device=dev),
             plan=bf.bfp8_gemm_plan(M, N, K, 0, gemm_opts)))
 
-    def step(events=None):
-        if events is not None:
-            events[0].record()
-        for i, b in enumerate(bufs):
+    def step():
+        for b in bufs:
             bf.bfp8_group_quant(b["x"], col_major=True, q=b["q"], s_storage=b["s_st"])
-            if events is not None:
-                events[2 * i + 1].record()
             bf.bfp8_gemm(b["q"], b["B"], b["s"], b["Bs"], out=b["out"], workspace=b["ws"],
                          options=gemm_opts)
-            if events is not None:
-                events[2 * i + 2].record()
 
-    nk_per_step = 2 * len(bufs)
-    # eager warm-up (first launches set kernel attributes)
-    step()
+    step()                      # eager: first launches set kernel attributes
     torch.cuda.synchronize()
-
-    S = max(1, min(args.steps, 16))
-    use_graphs = True
-    try:
-        torch.cuda.Event(enable_timing=True, external=True)
-    except TypeError:
-        use_graphs = False
-
-    def new_events():
-        if use_graphs:
-            return [torch.cuda.Event(enable_timing=True, external=True) for _ in range(nk_per_step + 1)]
-        return [torch.cuda.Event(enable_timing=True) for _ in range(nk_per_step + 1)]
-
-    sets = [[new_events() for _ in range(S)] for _ in range(2)]
-    graphs = None
-    plain = None
-    if use_graphs:
-        graphs = [[None] * S for _ in range(2)]
-        cap = torch.cuda.Stream()
-        for si in range(2):
-            for gi in range(S):
-                g = torch.cuda.CUDAGraph()
-                with torch.cuda.graph(g, stream=cap):
-                    step(sets[si][gi])
-                graphs[si][gi] = g
-        plain = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(plain, stream=cap):
-            step()
-        torch.cuda.synchronize()
-
-    def replay_plain():
-        if plain is not None:
-            plain.replay()
-        else:
-            step()
-
-    def launch(i):
-        si, gi = (i // S) % 2, i % S
-        if use_graphs:
-            graphs[si][gi].replay()
-        else:
-            step(sets[si][gi])
-        return si, gi
-
-    durations = [[] for _ in range(nk_per_step)]
-
-    def harvest(si, count):
-        sets[si][count - 1][-1].synchronize()
-        for gi in range(count):
-            ev = sets[si][gi]
-            for k in range(nk_per_step):
-                durations[k].append(ev[k].elapsed_time(ev[k + 1]) * 1e3)  # us
-
-    for i in range(args.warmup):
-        launch(i)
-        replay_plain()
+    cap = torch.cuda.Stream()
+    plain = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(plain, stream=cap):
+        step()
+    torch.cuda.synchronize()
+    for _ in range(args.warmup):
+        plain.replay()
     torch.cuda.synchronize()
     sampler = ClockSampler(local)
     sampler.start()
     time.sleep(0.3 if sampler.proc else 0)          # let nvidia-smi start sampling
-    # ---- timed region: --steps plain step graphs, events only at the ends
     barrier(world)
     torch.cuda.synchronize()
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
     t_start.record()
-    for i in range(args.steps):
-        replay_plain()
+    for _ in range(args.steps):
+        plain.replay()
     t_end.record()
     torch.cuda.synchronize()
     barrier(world)
-    elapsed_ms = max_over_ranks(t_start.elapsed_time(t_end), world)
-    # ---- per-kernel pass: graphs with an event between consecutive kernels
-    pending = {}
-    for i in range(args.steps):
-        si, gi = (i // S) % 2, i % S
-        if gi == 0 and si in pending:
-            harvest(si, pending.pop(si))
-        launch(i)
-        pending[si] = gi + 1
-    torch.cuda.synchronize()
     clocks = sampler.stop()
-    for si in sorted(pending):
-        harvest(si, pending[si])
-
+    elapsed_ms = max_over_ranks(t_start.elapsed_time(t_end), world)
     flops_step = sum(mt.gemm_flops(M, N, K) for M in Ms)
     value = flops_step * args.steps * world / (elapsed_ms * 1e-3) / 1e12
+    launches = 2 * len(bufs) * args.steps
+    del plain
 
-    peaks = load_peaks()
-    fp8_sustained = 2.0 * peaks["bf16_tflops_sustained"]
-    hbm = peaks["hbm_gbs"]
+    # ------------------------------------------- per-M graph-batch timings
+    ws_big = torch.zeros(256 << 20, dtype=torch.uint8, device=dev)
+    w_cold = Weights(N, K, copies_for(N * K, l2, True), dev, seed=4243 + rank)
+    w_hot = Weights(N, K, 1, dev, seed=4243 + rank)
+    timers = []
+    per_cfg = {}
+    for M in Ms:
+        act_bytes = 3 * M * K + 4 * M * G + 2 * M * N
+        a_cold = Acts(M, N, K, copies_for(act_bytes, l2, True), dev, seed=2000 + M)
+        a_hot = Acts(M, N, K, 1, dev, seed=2000 + M)
+        for tag, acts, w in (("cold", a_cold, w_cold), ("hot", a_hot, w_hot)):
+            for kind, mk in (("gemm", lambda: gemm_cfg(f"gemm M={M} {tag}", acts, w, ws_big, gemm_opts, {})),
+                             ("quant", lambda: quant_cfg(f"quant M={M} {tag}", acts, {})),
+                             ("layer", lambda: layer_cfg(f"layer M={M} {tag}", acts, w, ws_big,
+                                                         gemm_opts, {}))):
+                if kind == "layer" and tag == "hot":
+                    continue
+                t = mk()
+                per_cfg[(M, kind, tag)] = t
+                timers.append(t)
+    run_trials(timers, args.trial_ms)
+
     per_m = {}
-    groups = {g: {"time_us": 0.0, "flops": 0.0, "bytes": 0.0, "launches": 0} for g in KERNEL_GROUPS}
-    for i, b in enumerate(bufs):
+    for b in bufs:
         M = b["M"]
-        dq, dg = durations[2 * i], durations[2 * i + 1]
-        pq, pg = statistics.median(dq), statistics.median(dg)
+        pg, ph = per_cfg[(M, "gemm", "cold")].p50_us(), per_cfg[(M, "gemm", "hot")].p50_us()
+        pq, pqh = per_cfg[(M, "quant", "cold")].p50_us(), per_cfg[(M, "quant", "hot")].p50_us()
+        pl = per_cfg[(M, "layer", "cold")].p50_us()
         gb = mt.gemm_bytes(M, N, K)
-        bound = mt.gemm_bound(M, N, K, fp8_sustained, hbm)
-        roof = mt.roofline_us(M, N, K, fp8_sustained, hbm)
+        bound = mt.gemm_bound(M, N, K, fp8_burst, hbm)
+        roof = mt.roofline_us(M, N, K, fp8_burst, hbm)
+        plan = b["plan"]
         per_m[str(M)] = {
             "gemm_p50_us": round(pg, 3), "gemm_tflops": round(mt.tflops(M, N, K, pg), 2),
             "gemm_gbs": round(gb / (pg * 1e-6) / 1e9, 1), "gemm_bound": bound,
-            "gemm_roofline_frac": round(roof / pg, 3),
-            "quant_p50_us": round(pq, 3),
+            "gemm_roofline_us": round(roof, 3), "gemm_roofline_frac": round(roof / pg, 3),
+            "gemm_hot_p50_us": round(ph, 3),
+            "quant_p50_us": round(pq, 3), "quant_hot_p50_us": round(pqh, 3),
             "quant_gbs": round(mt.quant_bytes(M, K) / (pq * 1e-6) / 1e9, 1),
-            "schedule": ("swap_ab" if b["plan"]["swap_ab"] else "wide") + f"/n{b['plan']['tile_n']}"
-                        + (f"/cluster{b['plan']['cluster']}" if b["plan"]["cluster"] > 1
-                           else ("/stream-k" if b["plan"]["sk_units"] else "")),
+            "layer_p50_us": round(pl, 3),
+            "schedule": ("swap_ab" if plan["swap_ab"] else "wide") + f"/n{plan['tile_n']}"
+                        + (f"/cluster{plan['cluster']}" if plan["cluster"] > 1
+                           else ("/stream-k" if plan["sk_units"] else "/whole-tiles")),
         }
-        gname = "gemm_swap_ab" if b["plan"]["swap_ab"] else "gemm_wide"
-        for name, ds, fl, by in (("quant", dq, 0.0, mt.quant_bytes(M, K)),
-                                 (gname, dg, mt.gemm_flops(M, N, K), gb)):
-            grp = groups[name]
-            grp["time_us"] += sum(ds)
-            grp["flops"] += fl * len(ds)
-            grp["bytes"] += by * len(ds)
-            grp["launches"] += len(ds)
-    total_kernel_us = sum(g["time_us"] for g in groups.values())
+    del timers, per_cfg
+    torch.cuda.synchronize()
 
-    def roofline_of(name):
-        g = groups[name]
-        if g["launches"] == 0:
+    # ---- roofline families at the M values the targets name
+    def fam_hbm(ms, key, bytes_fn):
+        rows = [(M, per_m[str(M)][key]) for M in ms if str(M) in per_m]
+        if not rows:
             return None
-        avg_us = g["time_us"] / g["launches"]
-        share = g["time_us"] / total_kernel_us if total_kernel_us else 0.0
-        if name == "gemm_wide":
-            ach = g["flops"] / (g["time_us"] * 1e-6) / 1e12
-            return {"kernel": name, "bound": "tensor", "achieved": round(ach, 1),
-                    "peak": round(fp8_sustained, 1), "unit": "TFLOP/s",
-                    "frac": round(ach / fp8_sustained, 4), "share": round(share, 4),
-                    "avg_launch_us": round(avg_us, 3),
-                    "peak_note": f"fp8 dense = 2 x {peaks['source']} sustained bf16 "
-                                 f"({peaks['bf16_tflops_sustained']} TFLOP/s), nominal fp8/bf16 ratio"}
-        ach = g["bytes"] / (g["time_us"] * 1e-6) / 1e9
-        return {"kernel": name, "bound": "hbm", "achieved": round(ach, 1), "peak": hbm,
-                "unit": "GB/s", "frac": round(ach / hbm, 4), "share": round(share, 4),
-                "avg_launch_us": round(avg_us, 3), "peak_note": f"{peaks['source']} copy bandwidth"}
+        fr = [bytes_fn(M) / (t * 1e-6) / 1e9 / hbm for M, t in rows]
+        return {"bound": "hbm", "unit": "GB/s", "peak": hbm,
+                "achieved": round(statistics.median(bytes_fn(M) / (t * 1e-6) / 1e9 for M, t in rows), 1),
+                "frac": round(statistics.median(fr), 4), "frac_min": round(min(fr), 4),
+                "Ms": [M for M, _ in rows], "peak_note": f"{peaks['source']} copy bandwidth"}
 
-    rooflines = {n: roofline_of(n) for n in KERNEL_GROUPS}
+    def fam_tensor(ms):
+        rows = [(M, per_m[str(M)]["gemm_p50_us"]) for M in ms if str(M) in per_m]
+        if not rows:
+            return None
+        ach = [mt.tflops(M, N, K, t) for M, t in rows]
+        return {"bound": "tensor", "unit": "TFLOP/s", "peak": round(fp8_burst, 1),
+                "achieved": round(statistics.median(ach), 1),
+                "frac": round(statistics.median(a / fp8_burst for a in ach), 4),
+                "frac_min": round(min(a / fp8_burst for a in ach), 4), "Ms": [M for M, _ in rows],
+                "peak_note": f"fp8 dense = 2 x {peaks['source']} burst bf16 "
+                             f"({peaks['bf16_tflops']} TFLOP/s), nominal fp8/bf16 ratio"}
 
-    # The roofline object reports the single launch with the largest share of
-    # device time (the widest-M GEMM of the sweep), its achieved rate from the
-    # per-kernel pass's CUDA events.
-    best = None
-    for i, b in enumerate(bufs):
-        for kind, ds in (("quant", durations[2 * i]), ("gemm", durations[2 * i + 1])):
-            if best is None or sum(ds) > best[0]:
-                best = (sum(ds), kind, b, ds)
-    _, kind, b, ds = best
-    M = b["M"]
-    avg_us = sum(ds) / len(ds)
-    total_kernel_all = sum(sum(d) for d in durations)
-    if kind == "gemm" and mt.gemm_bound(M, N, K, fp8_sustained, hbm) == "tensor":
-        ach = mt.gemm_flops(M, N, K) / (avg_us * 1e-6) / 1e12
-        roofline = {"kernel": f"gemm_kernel<{b['plan']['tile_n']}, "
-                              f"{'swap' if b['plan']['swap_ab'] else 'wide'}> M={M} N={N} K={K}",
-                    "bound": "tensor", "achieved": round(ach, 1), "peak": round(fp8_sustained, 1),
-                    "unit": "TFLOP/s", "frac": round(ach / fp8_sustained, 4),
-                    "peak_note": f"fp8 dense = 2 x {peaks['source']} sustained bf16 "
-                                 f"({peaks['bf16_tflops_sustained']} TFLOP/s), nominal fp8/bf16 ratio"}
-        prof = f"gemm_{'swap' if b['plan']['swap_ab'] else 'wide'}_m{M}_n{N}_k{K}"
+    rooflines = {
+        "gemm_swap_ab_decode": fam_hbm([M for M in Ms if M <= 64], "gemm_p50_us",
+                                       lambda M: mt.gemm_bytes(M, N, K)),
+        "gemm_wide_prefill": fam_tensor([M for M in Ms if M >= 2048]),
+        "quant": fam_hbm([max(Ms)], "quant_p50_us", lambda M: mt.quant_bytes(M, K)),
+    }
+
+    # ---- the dominant launch of the step: the widest GEMM of the sweep
+    Mw = max(Ms)
+    t_w = per_m[str(Mw)]["gemm_p50_us"]
+    pw = bufs[Ms.index(Mw)]["plan"]
+    if mt.gemm_bound(Mw, N, K, fp8_burst, hbm) == "tensor":
+        ach = mt.gemm_flops(Mw, N, K) / (t_w * 1e-6) / 1e12
+        roofline = {"kernel": f"gemm_kernel<{pw['tile_n']}, {'swap' if pw['swap_ab'] else 'wide'}> "
+                              f"M={Mw} N={N} K={K}",
+                    "bound": "tensor", "achieved": round(ach, 1), "peak": round(fp8_burst, 1),
+                    "unit": "TFLOP/s", "frac": round(ach / fp8_burst, 4),
+                    "peak_note": f"fp8 dense = 2 x {peaks['source']} burst bf16 "
+                                 f"({peaks['bf16_tflops']} TFLOP/s), nominal fp8/bf16 ratio; burst "
+                                 "because each launch is timed in 20-launch replays of ~ms"}
+        prof = f"gemm_{'swap' if pw['swap_ab'] else 'wide'}_m{Mw}_n{N}_k{K}"
     else:
-        by = mt.gemm_bytes(M, N, K) if kind == "gemm" else mt.quant_bytes(M, K)
-        ach = by / (avg_us * 1e-6) / 1e9
-        roofline = {"kernel": f"{kind} M={M} N={N} K={K}", "bound": "hbm", "achieved": round(ach, 1),
+        ach = mt.gemm_bytes(Mw, N, K) / (t_w * 1e-6) / 1e9
+        roofline = {"kernel": f"gemm M={Mw} N={N} K={K}", "bound": "hbm", "achieved": round(ach, 1),
                     "peak": hbm, "unit": "GB/s", "frac": round(ach / hbm, 4),
                     "peak_note": f"{peaks['source']} copy bandwidth"}
-        prof = f"{kind}_m{M}_k{K}" if kind == "quant" else f"gemm_m{M}_n{N}_k{K}"
-    roofline["avg_launch_us"] = round(avg_us, 3)
-    roofline["share"] = round(sum(ds) / total_kernel_all, 4) if total_kernel_all else None
+        prof = f"gemm_m{Mw}_n{N}_k{K}"
+    roofline["launch_us"] = round(t_w, 3)
+    roofline["timing"] = "p50 of 20-launch CUDA-graph replays, cold L2"
+    step_us = elapsed_ms * 1e3 / args.steps
+    roofline["share"] = round(t_w / step_us, 4) if step_us else None
     roofline["traffic"] = profiled_traffic(prof)
     roofline["traffic_source"] = f"profiles/{prof}.md" if roofline["traffic"] else None
 
     # ---- end to end through the public API with host buffers
     e2e = None
     if not args.no_e2e:
-        e2e_steps = max(1, min(args.steps, 20))
-        x_host = [b["x"].cpu().pin_memory() for b in bufs]
-        out_host = [torch.empty_like(b["out"], device="cpu").pin_memory() for b in bufs]
-        h2d = sum(x.numel() * x.element_size() for x in x_host)
-        d2h = sum(o.numel() * o.element_size() for o in out_host)
+        e2e = measure_e2e(args, bufs, world, flops_step, gemm_opts)
 
-        # Copies are pipelined with the compute as a user would run a stream of
-        # layers: every M's activations go host -> device on a copy stream,
-        # each quant + GEMM waits only for its own input, and each output goes
-        # device -> host on a second copy stream (both directions of the link
-        # at once) while the next M computes.  The step is captured once in a
-        # CUDA graph (copies, quantisation and GEMM calls through the public
-        # API) and replayed every step, as a serving loop would: per-call host
-        # overhead otherwise decides the step time.  The eager loop (the same
-        # calls issued from Python every step, pipelined across steps) is timed
-        # too and reported beside it.
-        cs = torch.cuda.Stream()
-        hs = torch.cuda.Stream()
-        ds = torch.cuda.Stream()
-        nb = len(bufs)
-        ev_in = [torch.cuda.Event() for _ in range(nb)]
-        ev_xfree = [torch.cuda.Event() for _ in range(nb)]
-        ev_out = [torch.cuda.Event() for _ in range(nb)]
-        ev_done = [torch.cuda.Event() for _ in range(nb)]
+    cpu_baseline = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        fl, secs, cores, desc = oracle_sample(Ms, N, args.cpu_budget_s)
+        cpu_baseline = {"value": round(fl / secs / 1e12, 6), "unit": "TFLOP/s", "cores": cores,
+                        "kind": "oracle", "sample": desc, "seconds": round(secs, 2)}
 
-        def e2e_body(cross_step):
-            start = torch.cuda.Event()
-            start.record(cs)
-            hs.wait_event(start)
-            ds.wait_event(start)
+    workloads = None
+    if rank == 0 and not args.no_workloads:
+        del bufs
+        torch.cuda.empty_cache()
+        workloads = measure_workloads(args, dev, l2, fp8_burst, hbm, ws_big)
+
+    if rank == 0:
+        line = {
+            "metric": "block-FP8 GEMM p50 us & TFLOP/s vs M at N=K=4096; % of FP8/HBM roofline",
+            "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(elapsed_ms / args.steps, 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "e4m3",
+            "data": "synthetic",
+            "config": {
+                "workload": f"blocked W8A8 FP8 linear sweep: N=K={N}, M in {Ms}; per M "
+                            "per-token-group quant (bf16 N(0,1) -> e4m3, 1x128, col-major "
+                            "scales) + blocked GEMM (128x128 fp32 weight scales, bf16 out)",
+                "N": N, "K": K, "Ms": Ms,
+                "l2": "value: no flush, each M has its own weights (~0.65 GB read once per step "
+                      "> L2); per_m: cold = buffers rotated over >= 3 x L2, hot = one copy",
+                "parallelism": f"replicas x{world}",
+                "timing": "value: CUDA graph per step (PDL between kernels), events at the region "
+                          "ends; per_m and workloads: 20-launch CUDA-graph replays bracketed by "
+                          "events, 5 alternating trials, median of trial p50s",
+            },
+            "roofline": roofline,
+            "roofline_by_family": rooflines,
+            "per_m": per_m,
+            "gpu_launches": launches,
+            "clocks": clocks,
+            "e2e": e2e,
+            "cpu_baseline": cpu_baseline,
+            "workloads": workloads,
+            "page_context": {"h200_gluon_sweep_gemm_us_sum": 686.64,
+                             "ours_gemm_p50_us_sum": round(sum(v["gemm_p50_us"] for v in per_m.values()), 2),
+                             "ours_gemm_hot_p50_us_sum": round(sum(v["gemm_hot_p50_us"] for v in per_m.values()), 2),
+                             "note": "H200, hot L2, GEMM only (lmdeploy PR 4830 table); context, not a target"},
+        }
+        print(json.dumps(line))
+
+
+# ------------------------------------------------------------------ e2e ----
+
+def measure_e2e(args, bufs, world, flops_step, gemm_opts):
+    """The same sweep through the public Python API with host buffers: every
+    M's bf16 activations go host -> device (pinned) and every bf16 output comes
+    back, each step.  Two modes, both reported: the step's copies and calls
+    captured once in a CUDA graph and replayed, and the same calls issued
+    eagerly from Python each step (pipelined across steps).  The copies alone
+    (each direction, and both at once) are timed too: the step is copy-bound."""
+    import torch
+    import block_scaled_fp8_02_gb300 as bf
+    e2e_steps = max(3, min(args.steps, 20))
+    x_host = [b["x"].cpu().pin_memory() for b in bufs]
+    out_host = [torch.empty_like(b["out"], device="cpu").pin_memory() for b in bufs]
+    h2d = sum(x.numel() * x.element_size() for x in x_host)
+    d2h = sum(o.numel() * o.element_size() for o in out_host)
+    cs, hs, ds = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
+    nb = len(bufs)
+    ev_in = [torch.cuda.Event() for _ in range(nb)]
+    ev_xfree = [torch.cuda.Event() for _ in range(nb)]
+    ev_out = [torch.cuda.Event() for _ in range(nb)]
+    ev_done = [torch.cuda.Event() for _ in range(nb)]
+
+    def body(cross_step, copies_only=None):
+        start = torch.cuda.Event()
+        start.record(cs)
+        hs.wait_event(start)
+        ds.wait_event(start)
+        if copies_only in (None, "h2d", "both"):
             with torch.cuda.stream(hs):
                 for i, (b, xh) in enumerate(zip(bufs, x_host)):
-                    if cross_step:
+                    if cross_step and copies_only is None:
                         hs.wait_event(ev_xfree[i])      # the previous step has read x
                     b["x"].copy_(xh, non_blocking=True)
                     ev_in[i].record(hs)
+        if copies_only in ("d2h", "both"):
+            with torch.cuda.stream(ds):
+                for b, oh in zip(bufs, out_host):
+                    oh.copy_(b["out"], non_blocking=True)
+        if copies_only is None:
             with torch.cuda.stream(cs):
                 for i, (b, oh) in enumerate(zip(bufs, out_host)):
                     cs.wait_event(ev_in[i])
@@ -535,95 +727,170 @@ def run_ours(args, rank, world, local):
                         oh.copy_(b["out"], non_blocking=True)
                         if cross_step:
                             ev_done[i].record(ds)
-            cs.wait_stream(hs)
-            cs.wait_stream(ds)
+        cs.wait_stream(hs)
+        cs.wait_stream(ds)
 
-        def time_steps(step):
-            with torch.cuda.stream(cs):
-                step()
-            torch.cuda.synchronize()
-            barrier(world)
-            e0 = torch.cuda.Event(enable_timing=True)
-            e1 = torch.cuda.Event(enable_timing=True)
-            e0.record(cs)
-            with torch.cuda.stream(cs):
-                for _ in range(e2e_steps):
-                    step()
-            e1.record(cs)
-            torch.cuda.synchronize()
-            return max_over_ranks(e0.elapsed_time(e1), world)
+    def time_steps(fn):
+        with torch.cuda.stream(cs):
+            fn()
+        torch.cuda.synchronize()
+        barrier(world)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(cs)
+        with torch.cuda.stream(cs):
+            for _ in range(e2e_steps):
+                fn()
+        e1.record(cs)
+        torch.cuda.synchronize()
+        return max_over_ranks(e0.elapsed_time(e1), world) / e2e_steps
 
-        eager_ms = time_steps(lambda: e2e_body(True))
-        graph_ms, graph_err = None, None
-        try:
-            g = torch.cuda.CUDAGraph()
-            torch.cuda.synchronize()
-            with torch.cuda.graph(g, stream=cs):
-                e2e_body(False)
-            graph_ms = time_steps(lambda: g.replay())
-        except Exception as ex:  # capture unsupported here: report the eager loop
-            graph_err = f"{type(ex).__name__}: {ex}"[:200]
-            torch.cuda.synchronize()
-        e_ms = graph_ms if graph_ms is not None else eager_ms
-        e2e = {"value": round(flops_step * e2e_steps * world / (e_ms * 1e-3) / 1e12, 2),
-               "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-               "steps": e2e_steps, "ms_per_step": round(e_ms / e2e_steps, 4),
-               "mode": "graph" if graph_ms is not None else "eager",
-               "eager_ms_per_step": round(eager_ms / e2e_steps, 4),
-               "note": "bf16 activations copied in from pinned host memory and bf16 outputs "
-                       "copied back every step, pipelined with the compute on two copy streams; "
-                       "the step's copies and API calls captured in a CUDA graph and replayed "
-                       "(eager_ms_per_step: the same calls issued from Python each step); "
-                       "weights are resident parameters"}
-        if graph_err:
-            e2e["graph_error"] = graph_err
-
-    cpu_baseline = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        fl, secs, cores, desc = oracle_sample(Ms, N, args.cpu_budget_s)
-        cpu_baseline = {"value": round(fl / secs / 1e12, 6), "unit": "TFLOP/s", "cores": cores,
-                        "kind": "oracle", "sample": desc, "seconds": round(secs, 2)}
-
-    extensions = None
-    if rank == 0 and not args.no_extensions:
-        extensions = measure_extensions(dev)
-
-    launches = nk_per_step * args.steps
-    if rank == 0:
-        line = {
-            "metric": "block-FP8 GEMM p50 us & TFLOP/s vs M at N=K=4096; % of FP8/HBM roofline",
-            "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": round(elapsed_ms / args.steps, 4),
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "e4m3",
-            "data": "synthetic",
-            "config": {
-                "workload": f"blocked W8A8 FP8 linear sweep: N=K={N}, M in {Ms}; per M "
-                            "per-token-group quant (bf16 N(0,1) -> e4m3, 1x128, col-major "
-                            "scales) + blocked GEMM (128x128 fp32 weight scales, bf16 out)",
-                "N": N, "K": K, "Ms": Ms,
-                "l2": "no flush: each M has its own weights; ~0.65 GB of buffers are read once "
-                      "per step (> 129 MB L2), so every kernel reads its inputs cold",
-                "parallelism": f"replicas x{world}",
-                "timing": ("value: CUDA graph per step (PDL between kernels), events at the region "
-                           "ends; per_m / roofline: a second pass of graphs with events between "
-                           "kernels" if use_graphs else "eager launches with timing events"),
-            },
-            "roofline": roofline,
-            "roofline_by_kernel": rooflines,
-            "per_m": per_m,
-            "gpu_launches": launches,
-            "clocks": clocks,
-            "e2e": e2e,
-            "cpu_baseline": cpu_baseline,
-            "extensions": extensions,
-            "page_context": {"h200_gluon_sweep_gemm_us_sum": 686.64,
-                             "ours_gemm_p50_us_sum": round(sum(v["gemm_p50_us"] for v in per_m.values()), 2),
-                             "note": "H200, hot L2, GEMM only (lmdeploy PR 4830 table); context, not a target"},
-        }
-        print(json.dumps(line))
+    eager_ms = time_steps(lambda: body(True))
+    graph_ms, graph_err = None, None
+    try:
+        g = torch.cuda.CUDAGraph()
+        torch.cuda.synchronize()
+        with torch.cuda.graph(g, stream=cs):
+            body(False)
+        graph_ms = time_steps(lambda: g.replay())
+    except Exception as ex:  # capture unsupported here: report the eager loop
+        graph_err = f"{type(ex).__name__}: {ex}"[:200]
+        torch.cuda.synchronize()
+    h2d_ms = time_steps(lambda: body(False, "h2d"))
+    d2h_ms = time_steps(lambda: body(False, "d2h"))
+    both_ms = time_steps(lambda: body(False, "both"))
+    modes = {"eager": eager_ms}
+    if graph_ms is not None:
+        modes["graph"] = graph_ms
+    mode = min(modes, key=modes.get)
+    e_ms = modes[mode]
+    res = {"value": round(flops_step * world / (e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps,
+           "ms_per_step": round(e_ms, 4), "mode": mode,
+           "eager_ms_per_step": round(eager_ms, 4),
+           "graph_ms_per_step": round(graph_ms, 4) if graph_ms is not None else None,
+           "copies_only_ms": {"h2d": round(h2d_ms, 4), "d2h": round(d2h_ms, 4),
+                              "both_directions": round(both_ms, 4)},
+           "copy_gbs": {"h2d": round(h2d / (h2d_ms * 1e-3) / 1e9, 1),
+                        "d2h": round(d2h / (d2h_ms * 1e-3) / 1e9, 1),
+                        "both_directions": round((h2d + d2h) / (both_ms * 1e-3) / 1e9, 1)},
+           "note": "bf16 activations in from pinned host memory and bf16 outputs back every step, "
+                   "pipelined with the compute on two copy streams; value from the faster of the "
+                   "two modes (graph: the step's copies and calls captured once and replayed; "
+                   "eager: the same calls issued from Python each step); copies_only_ms times the "
+                   "same copies without compute; weights are resident parameters"}
+    if graph_err:
+        res["graph_error"] = graph_err
+    return res
 
 
-# ------------------------------------------------------------ extensions ---
+# ------------------------------------------------------------ workloads ----
+
+def measure_workloads(args, dev, l2, fp8_burst, hbm, ws):
+    """The configurations beyond the headline sweep, each timed with the
+    graph-batch protocol (cold L2)."""
+    import torch
+    import block_scaled_fp8_02_gb300 as bf
+    from block_scaled_fp8_02_gb300 import metrics as mt
+    from block_scaled_fp8_02_gb300 import workloads as wl
+    res = {}
+    opts = {"prefetch_weights": 1}
+
+    def gemm_row(t, M, N, K):
+        us = t.p50_us()
+        roof = mt.roofline_us(M, N, K, fp8_burst, hbm)
+        return {"p50_us": round(us, 3), "tflops": round(mt.tflops(M, N, K, us), 2),
+                "gbs": round(mt.gemm_bytes(M, N, K) / (us * 1e-6) / 1e9, 1),
+                "bound": mt.gemm_bound(M, N, K, fp8_burst, hbm),
+                "roofline_us": round(roof, 3), "roofline_frac": round(roof / us, 3)}
+
+    # Qwen3-32B-shaped linear stack
+    q_rows = {}
+    for layer, (N, K) in wl.QWEN3_32B_LAYERS.items():
+        w = Weights(N, K, copies_for(N * K, l2, True), dev, seed=N + K)
+        timers = {}
+        for M in wl.QWEN3_32B_MS:
+            G = (K + 127) // 128
+            acts = Acts(M, N, K, copies_for(3 * M * K + 4 * M * G + 2 * M * N, l2, True), dev,
+                        seed=M + N)
+            timers[M] = gemm_cfg(f"{layer} M={M}", acts, w, ws, opts, {})
+        run_trials(list(timers.values()), args.trial_ms)
+        q_rows[layer] = {"N": N, "K": K, **{str(M): gemm_row(t, M, N, K) for M, t in timers.items()}}
+        del w, timers
+        torch.cuda.empty_cache()
+    res["qwen3_32b_stack"] = q_rows
+
+    # quantisation sweep
+    qs = {}
+    timers = {}
+    for M in (2048, 8192):
+        for K in (4096, 7168, 25600):
+            acts = Acts(M, 128, K, copies_for(3 * M * K, l2, True), dev, seed=M + K, out=False)
+            timers[(M, K)] = quant_cfg(f"quant {M}x{K}", acts, {})
+    run_trials(list(timers.values()), args.trial_ms)
+    for (M, K), t in timers.items():
+        us = t.p50_us()
+        gbs = mt.quant_bytes(M, K) / (us * 1e-6) / 1e9
+        qs[f"{M}x{K}"] = {"p50_us": round(us, 3), "gbs": round(gbs, 1), "hbm_frac": round(gbs / hbm, 4)}
+    res["quant_sweep"] = qs
+    del timers
+    torch.cuda.empty_cache()
+
+    # UE8M0 scale variant: power-of-two scales (quantisation and the layer)
+    ue = {}
+    timers = {}
+    for M in (1, 64, 2048, 8192):
+        G = (NK + 127) // 128
+        acts = Acts(M, NK, NK, copies_for(3 * M * NK + 4 * M * G + 2 * M * NK, l2, True), dev,
+                    seed=M + 77)
+        timers[("quant", M)] = quant_cfg(f"ue8m0 quant M={M}", acts, {}, ue8m0=True)
+        if M <= 2048:
+            w = Weights(NK, NK, copies_for(NK * NK, l2, True), dev, seed=78)
+            for b in range(len(w)):
+                bf.bfp8_scale_ceil_ue8m0(w.Bs[b], out=w.Bs[b])
+
+            def launch(i, acts=acts, w=w):
+                a, b = i % len(acts), i % len(w)
+                bf.bfp8_group_quant(acts.x[a], q=acts.q[a], s_storage=acts.s_st[a], ue8m0=True)
+                bf.bfp8_gemm(acts.q[a], w.B[b], acts.s[a], w.Bs[b], out=acts.out[a], workspace=ws,
+                             options=opts)
+            timers[("layer", M)] = GraphTimer(f"ue8m0 layer M={M}", launch, {}, max(len(acts), len(w)),
+                                              keep=(acts, w, ws))
+    run_trials(list(timers.values()), args.trial_ms)
+    for (kind, M), t in timers.items():
+        us = t.p50_us()
+        row = ue.setdefault(str(M), {})
+        if kind == "quant":
+            gbs = mt.quant_bytes(M, NK) / (us * 1e-6) / 1e9
+            row.update(quant_p50_us=round(us, 3), quant_gbs=round(gbs, 1), quant_hbm_frac=round(gbs / hbm, 4))
+        else:
+            row.update(layer_p50_us=round(us, 3))
+    res["ue8m0_variant"] = {"N": NK, "K": NK, **ue,
+                            "note": "activation scales and weight scales rounded up to powers of two; "
+                                    "layer = UE8M0 quantisation + the same blocked GEMM"}
+    del timers
+    torch.cuda.empty_cache()
+
+    # ragged / tail shapes (reported, not graded)
+    rg = {}
+    timers = {}
+    for M in wl.RAGGED_MS:
+        for N in wl.RAGGED_NS:
+            for K in wl.RAGGED_KS:
+                w = Weights(N, K, 1, dev, seed=M * 7 + N + K)
+                acts = Acts(M, N, K, 1, dev, seed=M * 7 + N + K)
+                timers[(M, N, K)] = gemm_cfg(f"ragged {M}x{N}x{K}", acts, w, ws, None, {})
+    run_trials(list(timers.values()), args.trial_ms / 5)
+    for (M, N, K), t in timers.items():
+        us = t.p50_us()
+        rg[f"{M}x{N}x{K}"] = {"p50_us": round(us, 3), "tflops": round(mt.tflops(M, N, K, us), 2)}
+    res["ragged_hot_l2"] = rg
+    del timers
+    torch.cuda.empty_cache()
+
+    res["extensions"] = measure_extensions(dev)
+    return res
+
 
 def _graph_time_us(fn, reps=20, iters=5):
     """Median device time of fn() replayed from a CUDA graph (events at the
@@ -730,20 +997,22 @@ def run_reference(args, rank, world):
             flops_list.append(fl)
     tot_s = sum(times)
     value = sum(flops_list) / tot_s / 1e12 if tot_s > 0 else 0.0
-    flops_step = sum(mt.gemm_flops(M, nk, nk) for M in Ms)
     line = {
         "impl": "reference",
         "metric": "block-FP8 GEMM p50 us & TFLOP/s vs M at N=K=4096; % of FP8/HBM roofline",
         "value": round(value, 6), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup,
-        "ms_per_step": round(flops_step / (value * 1e12) * 1e3, 3) if value else None,
+        "ms_per_step": round(tot_s / max(len(times), 1) * 1e3, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic",
-        "config": {"workload": f"blocked W8A8 FP8 linear sweep: N=K={nk}, M in {Ms} (CPU oracle on "
-                               "a bounded row sample per step; ms_per_step extrapolates to the full sweep)",
-                   "N": nk, "K": nk, "Ms": Ms},
+        "config": {"workload": f"blocked W8A8 FP8 linear sweep: N=K={nk}, M in {Ms}; each step is "
+                               "the CPU oracle (quantise + blocked GEMM) on a bounded row sample of "
+                               "every M; ms_per_step is that sample's measured time",
+                   "N": nk, "K": nk, "Ms": Ms,
+                   "flops_per_step": round(sum(flops_list) / max(len(flops_list), 1), 1),
+                   "full_sweep_flops": sum(mt.gemm_flops(M, nk, nk) for M in Ms)},
         "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "kind": "oracle",
-                         "cores": cores, "sample": desc},
+                         "cores": cores, "sample": desc, "seconds": round(tot_s, 3)},
         "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
