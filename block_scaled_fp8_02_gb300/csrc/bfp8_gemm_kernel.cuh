@@ -129,32 +129,24 @@ struct GemmCfg {
   static_assert(MR == 128 || (!SWAP && MODE == kModePlain && (MR == 32 || MR == 64)),
                 "partial activation tiles: plain wide tiles, 32 or 64 rows");
   static constexpr int kMR = MR;
-#ifndef BFP8_WIDE_WARPS
-#define BFP8_WIDE_WARPS 8
-#endif
-  // promotion warps: 4 per 128 TMEM columns; the wide 256-column tile may use
-  // 16 (four per SM sub-partition, 64 columns each) to hide TMEM load latency
-  static constexpr int kNE = (!SWAP && BN == 256) ? BFP8_WIDE_WARPS : (BN > 128 ? 8 : 4);
+  // promotion warps: 4 per 128 TMEM columns (16 on the 256-wide tile, 64
+  // columns each, ran slower: fewer registers per thread, shallower ring)
+  static constexpr int kNE = BN > 128 ? 8 : 4;
   static constexpr int kNH = kNE / 4;            // column groups per lane quadrant
   static constexpr int kCPT = BN / kNH;          // accumulator columns per thread
   static constexpr int kCH = kCPT >= 32 ? 32 : 16;   // columns per tcgen05.ld
   // columns loaded per tcgen05.wait::ld: every wait costs a full TMEM load
   // latency, so batches are as large as the register budget allows
-#ifndef BFP8_WIDE_BATCH
-#define BFP8_WIDE_BATCH 64
-#endif
   // (64-column swap tiles: 32, so that two CTAs' registers fit on one SM)
-  static constexpr int kBatch =
-      kNH == 4 ? 32
-               : (kNH == 2 ? BFP8_WIDE_BATCH : (kCPT >= 64 ? (SWAP && BN == 64 ? 32 : 64) : kCPT));
+  static constexpr int kBatch = kNH == 2 ? 64 : (kCPT >= 64 ? (SWAP && BN == 64 ? 32 : 64) : kCPT);
   // 8 promotion warps: 12 warps in all so that warps 8..11 are one warpgroup
   // that gives registers to the promotion warpgroups (setmaxnreg).
   static constexpr int kWarps = kNE >= 8 ? kNE + 4 : kNE + 2;
   static constexpr int kThreads = kWarps * 32;
   static constexpr bool kRebalance = kNE >= 8;
-  // 8: 256*232 + 128*40 <= 384*168;  16: 512*112 + 128*24 <= 640*96
-  static constexpr int kRegsEpi = kNE == 16 ? 112 : 232;
-  static constexpr int kRegsOther = kNE == 16 ? 24 : 40;
+  // 8 promotion warps at 232 registers, 4 others at 40: 256*232 + 128*40 <= 384*168
+  static constexpr int kRegsEpi = 232;
+  static constexpr int kRegsOther = 40;
   static constexpr int kPBytes = (SWAP ? 128 : MR) * 128;
   static constexpr int kQBytes = BN * 128;
   static constexpr int kStageBytes = kPBytes + kQBytes;

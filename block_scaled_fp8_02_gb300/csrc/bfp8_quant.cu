@@ -80,15 +80,9 @@ __device__ __forceinline__ void unpack(const uint32_t (&w)[4], float (&v)[QuantS
   }
 }
 
-#ifndef BFP8_QUANT_UNROLL
-#define BFP8_QUANT_UNROLL 2
-#endif
-#ifndef BFP8_QUANT_MIN_BLOCKS
-#define BFP8_QUANT_MIN_BLOCKS 4
-#endif
-constexpr int kUnroll = BFP8_QUANT_UNROLL;       // warp steps per batch
+constexpr int kUnroll = 2;              // warp steps per batch
 constexpr int kWarpsPerBlock = 8;
-constexpr int kBlocksPerSm = BFP8_QUANT_MIN_BLOCKS;
+constexpr int kBlocksPerSm = 4;
 
 // Walks one warp's chunks, kUnroll at a time: chunk c = row * chunks_per_row
 // + col; warp w takes chunks w, w + nwarps, ... (a chunk is one warp step:

@@ -197,18 +197,9 @@ inline Sched make_sched(uint32_t p_tiles, uint32_t q_tiles, uint32_t G, uint32_t
   if (grid > units) grid = units;
   if (grid < 1) grid = 1;
   s.grid = static_cast<uint32_t>(grid);
-#ifndef BFP8_SK_TWO_WAVES
   // Whole waves of tiles are handed out data-parallel; only the remainder
   // (less than one wave) is split stream-K.
   s.dp_tiles = (s.tiles / s.grid) * s.grid;
-#else
-  if (s.tiles % s.grid == 0) {
-    s.dp_tiles = s.tiles;
-  } else {
-    const uint32_t waves = s.tiles / s.grid;
-    s.dp_tiles = waves >= 2 ? (waves - 1) * s.grid : 0;
-  }
-#endif
   s.sk_units = (s.tiles - s.dp_tiles) * G;
   s.sk_q = s.sk_units / s.grid;
   s.sk_r = s.sk_units % s.grid;

@@ -1,7 +1,7 @@
 """Runs one libbfp8 kernel configuration a few times, for profilers.
 
-    python -m block_scaled_fp8_02_gb300.profile_case --M 2048 --N 4096 --K 4096 --iters 2
-    python -m block_scaled_fp8_02_gb300.profile_case --M 8192 --K 4096 --quant --iters 2
+    python profile_case.py --M 2048 --N 4096 --K 4096 --iters 2
+    python profile_case.py --M 8192 --K 4096 --quant --iters 2
 
 Inputs are seeded synthetic data of the bench's distributions (bf16 N(0,1)
 activations, e4m3 weights from U[-448, 448], weight scales U[1e-4, 1e-2)).
@@ -15,8 +15,8 @@ import argparse
 
 import torch
 
-from . import _binding as bf
-from . import workloads as wl
+import block_scaled_fp8_02_gb300 as bf
+from block_scaled_fp8_02_gb300 import workloads as wl
 
 
 def main() -> None:
