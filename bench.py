@@ -72,6 +72,9 @@ def parse_args():
     p.add_argument("--no-workloads", action="store_true",
                    help="time only the headline sweep (skip the Qwen3-32B stack, quantisation "
                         "sweep, ragged shapes, UE8M0 variant and extensions)")
+    p.add_argument("--headline-only", action="store_true",
+                   help="time only the headline step (no per-M, e2e, baseline or workloads; "
+                        "for profiler launch lists)")
     p.add_argument("--cpu-budget-s", type=float, default=12.0,
                    help="wall seconds (on all host cores) for the oracle baseline sample")
     return p.parse_args()
@@ -515,6 +518,15 @@ def run_ours(args, rank, world, local):
     value = flops_step * args.steps * world / (elapsed_ms * 1e-3) / 1e12
     launches = 2 * len(bufs) * args.steps
     del plain
+    if args.headline_only:
+        if rank == 0:
+            print(json.dumps({"metric": "block-FP8 GEMM p50 us & TFLOP/s vs M at N=K=4096; % of FP8/HBM roofline",
+                              "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world,
+                              "steps": args.steps, "warmup": args.warmup,
+                              "ms_per_step": round(elapsed_ms / args.steps, 4),
+                              "higher_is_better": True, "gpu_launches": launches,
+                              "note": "headline step only (profiling run)"}))
+        return
 
     # ------------------------------------------- per-M graph-batch timings
     ws_big = torch.zeros(256 << 20, dtype=torch.uint8, device=dev)

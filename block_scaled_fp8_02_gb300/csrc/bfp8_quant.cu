@@ -238,28 +238,34 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32, kBlocksPerSm)
 }
 
 // ---------------------------------------------------------------------------
-// The common case on a lean path: bf16 rows of whole 256-element steps (K a
-// multiple of 256, 16-byte aligned rows and codes).  A step is one warp's
-// 512 input bytes -- two groups, a half-warp each, 8 elements per lane.  Each
-// warp walks kStepU steps at a time (all their loads issued before any is
-// used), with 32-bit offsets (the host checks that they fit) and products
-// packed two per instruction.  Same arithmetic, bit for bit, as the general
-// kernel above.
-constexpr int kStepU = 4;
-
-template <bool kUe8m0>
+// The common case on a lean path: bf16 rows of whole steps (K a multiple of
+// 32 * EPL), 16-byte aligned rows of x and q.  A step is one warp's
+// 32 * EPL elements of one row: 32 * EPL / 128 groups, 128 / EPL lanes each,
+// EPL elements per lane (16-byte loads).  Each warp walks kStepU steps at a
+// time (all their loads issued before any is used), with 32-bit offsets (the
+// host checks that they fit) and products packed two per instruction.  Same
+// arithmetic, bit for bit, as the general kernel above.  (kStepU: 64 bytes of
+// loads in flight per lane either way.)
+template <int EPL>
+constexpr int kStepUFor = EPL == 16 ? 2 : 4;
+template <bool kUe8m0, int EPL>
 __global__ void __launch_bounds__(kWarpsPerBlock * 32, kBlocksPerSm)
     group_quant_bf16_steps_kernel(const uint16_t* __restrict__ x, uint32_t M, uint32_t spr,
                                   uint32_t ld_x, uint8_t* __restrict__ q, uint32_t ld_q,
                                   float* __restrict__ s, int32_t col_major, uint32_t ld_s,
                                   uint32_t adv_row, uint32_t adv_col) {
+  static_assert(EPL == 8 || EPL == 16, "8 or 16 elements per lane");
+  constexpr int kStepU = kStepUFor<EPL>;
+  constexpr int kLPG = 128 / EPL;                // lanes per group
+  constexpr int kW = EPL / 8;                    // 16-byte words per lane
+  constexpr uint32_t kStep = 32u * EPL;          // elements per step
   const int lane = threadIdx.x & 31;
-  const uint32_t half = static_cast<uint32_t>(lane) >> 4;     // group within the step
+  const uint32_t gi = static_cast<uint32_t>(lane) / kLPG;     // group within the step
   const uint32_t warp0 = blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
   const uint32_t nwarps = gridDim.x * kWarpsPerBlock;
   // walker u visits steps warp0 + (u + kStepU * i) * nwarps; a step is
-  // (row, column of 256 elements); each advance moves a walker kStepU * nwarps
-  // steps = adv_row rows and adv_col columns (one carry at most, adv_col < spr)
+  // (row, column of kStep elements); each advance moves a walker
+  // kStepU * nwarps steps = adv_row rows and adv_col columns (adv_col < spr)
   uint32_t rw[kStepU], cl[kStepU];
 #pragma unroll
   for (int u = 0; u < kStepU; ++u) {
@@ -270,34 +276,41 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32, kBlocksPerSm)
   griddep_launch_dependents();
   griddep_wait();
   while (rw[0] < M) {
-    uint4 w[kStepU];
+    uint4 w[kStepU][kW];
 #pragma unroll
     for (int u = 0; u < kStepU; ++u)
-      if (rw[u] < M)
-        w[u] = __ldg(reinterpret_cast<const uint4*>(x + rw[u] * ld_x + cl[u] * 256u) + lane);
+      if (rw[u] < M) {
+        const uint4* src = reinterpret_cast<const uint4*>(x + rw[u] * ld_x + cl[u] * kStep) + lane * kW;
+#pragma unroll
+        for (int h = 0; h < kW; ++h) w[u][h] = __ldg(src + h);
+      }
 #pragma unroll
     for (int u = 0; u < kStepU; ++u) {
       if (rw[u] >= M) continue;
-      const uint32_t ww[4] = {w[u].x, w[u].y, w[u].z, w[u].w};
-      float v[8];
+      float v[EPL];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        v[2 * i] = __uint_as_float(ww[i] << 16);
-        v[2 * i + 1] = __uint_as_float(ww[i] & 0xFFFF0000u);
+      for (int h = 0; h < kW; ++h) {
+        const uint32_t ww[4] = {w[u][h].x, w[u][h].y, w[u][h].z, w[u][h].w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          v[8 * h + 2 * i] = __uint_as_float(ww[i] << 16);
+          v[8 * h + 2 * i + 1] = __uint_as_float(ww[i] & 0xFFFF0000u);
+        }
       }
       float amax = fabsf(v[0]);
 #pragma unroll
-      for (int e = 1; e < 8; ++e) amax = fmaxf(amax, fabsf(v[e]));
+      for (int e = 1; e < EPL; ++e) amax = fmaxf(amax, fabsf(v[e]));
 #pragma unroll
-      for (int off = 8; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+      for (int off = kLPG / 2; off > 0; off >>= 1)
+        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
       float scale;
-      uint32_t pk[4];
+      uint32_t pk[EPL / 2];
       if constexpr (kUe8m0) {
         const Ue8m0Scale us(amax);
         scale = us.scale;
         const uint64_t inv2 = pack_u32x2(__float_as_uint(us.inv), __float_as_uint(us.inv));
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
+        for (int i = 0; i < EPL / 2; ++i) {
           float a0, a1;
           unpack_f32x2(mul_f32x2(pack_u32x2(__float_as_uint(v[2 * i]), __float_as_uint(v[2 * i + 1])), inv2),
                        a0, a1);
@@ -310,7 +323,7 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32, kBlocksPerSm)
         const uint64_t hi2 = pack_u32x2(__float_as_uint(br.hi), __float_as_uint(br.hi));
         uint32_t undecided = 0;
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
+        for (int i = 0; i < EPL / 2; ++i) {
           const uint64_t x2 = pack_u32x2(__float_as_uint(v[2 * i]), __float_as_uint(v[2 * i + 1]));
           float a0, a1, b0, b1;
           unpack_f32x2(mul_f32x2(x2, lo2), a0, a1);
@@ -322,16 +335,19 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32, kBlocksPerSm)
         // warp-uniform branch: IEEE divisions only for the undecided pairs
         if (__any_sync(0xffffffffu, undecided != 0)) {
 #pragma unroll
-          for (int i = 0; i < 4; ++i)
+          for (int i = 0; i < EPL / 2; ++i)
             if (undecided & (1u << i)) pk[i] = e4m3_pair_divided(v[2 * i], v[2 * i + 1], scale);
         }
       }
-      uint2 wq;
-      wq.x = pk[0] | (pk[1] << 16);
-      wq.y = pk[2] | (pk[3] << 16);
-      *reinterpret_cast<uint2*>(q + rw[u] * ld_q + cl[u] * 256u + static_cast<uint32_t>(lane) * 8u) = wq;
-      if ((lane & 15) == 0) {
-        const uint32_t g = cl[u] * 2u + half;
+      uint8_t* dst = q + rw[u] * ld_q + cl[u] * kStep + static_cast<uint32_t>(lane) * EPL;
+      if constexpr (EPL == 16) {
+        *reinterpret_cast<uint4*>(dst) = make_uint4(pk[0] | (pk[1] << 16), pk[2] | (pk[3] << 16),
+                                                    pk[4] | (pk[5] << 16), pk[6] | (pk[7] << 16));
+      } else {
+        *reinterpret_cast<uint2*>(dst) = make_uint2(pk[0] | (pk[1] << 16), pk[2] | (pk[3] << 16));
+      }
+      if ((static_cast<uint32_t>(lane) % kLPG) == 0) {
+        const uint32_t g = cl[u] * (kStep / 128u) + gi;
         if (col_major) s[g * ld_s + rw[u]] = scale;
         else s[rw[u] * ld_s + g] = scale;
       }
@@ -382,20 +398,23 @@ cudaError_t launch_quant_instance(const cudaLaunchConfig_t& cfg, const void* x, 
 cudaError_t launch_group_quant(const void* x, int in_f32, int64_t M, int64_t K, int64_t ld_x,
                                uint8_t* q, int64_t ld_q, float* s, int col_major, int64_t ld_s,
                                int ue8m0, int num_sms, cudaStream_t stream) {
-  // lean path: bf16, whole 256-element steps, 16-byte aligned rows of x and
-  // 8-byte aligned rows of q, 32-bit offsets
+  // lean path: bf16, whole steps (512 elements: 16 per lane; else 256: 8 per
+  // lane), 16-byte aligned rows of x and q (8-byte for 8 per lane), 32-bit
+  // offsets
+  const int lean_epl = (K % 512 == 0 && reinterpret_cast<uintptr_t>(q) % 16 == 0 && ld_q % 16 == 0) ? 16 : 8;
   const bool lean = !in_f32 && K % 256 == 0 && reinterpret_cast<uintptr_t>(x) % 16 == 0 &&
                     ld_x % 8 == 0 && reinterpret_cast<uintptr_t>(q) % 8 == 0 && ld_q % 8 == 0 &&
                     M * ld_x < (int64_t{1} << 31) && M * ld_q < (int64_t{1} << 31) &&
                     (col_major ? ((K / 128) * ld_s) : (M * ld_s)) < (int64_t{1} << 31);
   if (lean) {
-    const uint32_t spr = static_cast<uint32_t>(K / 256);
+    const uint32_t spr = static_cast<uint32_t>(K / (32 * lean_epl));
     const int64_t steps = M * spr;
     int64_t blocks = (steps + kWarpsPerBlock - 1) / kWarpsPerBlock;
     const int64_t cap = static_cast<int64_t>(num_sms) * kBlocksPerSm;
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;
-    const uint32_t adv = static_cast<uint32_t>(blocks) * kWarpsPerBlock * kStepU;
+    const uint32_t adv =
+        static_cast<uint32_t>(blocks) * kWarpsPerBlock * (lean_epl == 16 ? kStepUFor<16> : kStepUFor<8>);
     if (steps + 2 * static_cast<int64_t>(adv) >= (int64_t{1} << 31)) return cudaErrorInvalidValue;
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(static_cast<unsigned>(blocks));
@@ -410,10 +429,16 @@ cudaError_t launch_group_quant(const void* x, int in_f32, int64_t M, int64_t K, 
     const uint32_t Mu = static_cast<uint32_t>(M), ldx = static_cast<uint32_t>(ld_x),
                    ldq = static_cast<uint32_t>(ld_q), lds = static_cast<uint32_t>(ld_s);
     const int32_t cm = col_major;
-    return ue8m0 ? cudaLaunchKernelEx(&cfg, group_quant_bf16_steps_kernel<true>, xb, Mu, spr, ldx, q,
-                                      ldq, s, cm, lds, adv / spr, adv % spr)
-                 : cudaLaunchKernelEx(&cfg, group_quant_bf16_steps_kernel<false>, xb, Mu, spr, ldx, q,
-                                      ldq, s, cm, lds, adv / spr, adv % spr);
+    const uint32_t ar = adv / spr, ac = adv % spr;
+    if (lean_epl == 16)
+      return ue8m0 ? cudaLaunchKernelEx(&cfg, group_quant_bf16_steps_kernel<true, 16>, xb, Mu, spr, ldx,
+                                        q, ldq, s, cm, lds, ar, ac)
+                   : cudaLaunchKernelEx(&cfg, group_quant_bf16_steps_kernel<false, 16>, xb, Mu, spr, ldx,
+                                        q, ldq, s, cm, lds, ar, ac);
+    return ue8m0 ? cudaLaunchKernelEx(&cfg, group_quant_bf16_steps_kernel<true, 8>, xb, Mu, spr, ldx, q,
+                                      ldq, s, cm, lds, ar, ac)
+                 : cudaLaunchKernelEx(&cfg, group_quant_bf16_steps_kernel<false, 8>, xb, Mu, spr, ldx, q,
+                                      ldq, s, cm, lds, ar, ac);
   }
   const int64_t G = (K + 127) / 128;
   const int esize = in_f32 ? 4 : 2;
