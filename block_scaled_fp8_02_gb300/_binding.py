@@ -31,7 +31,8 @@ EXPORTS = ("bfp8_group_quant", "bfp8_group_quant_ex", "bfp8_scale_ceil_ue8m0", "
            "bfp8_gemm_workspace_size", "bfp8_gemm_plan", "bfp8_plan_unit", "bfp8_last_error",
            "bfp8_status_string", "bfp8_device_status", "bfp8_selftest_bounded_wait",
            "bfp8_version", "bfp8_gemm_noalloc", "bfp8_gemm_grouped",
-           "bfp8_gemm_grouped_workspace_size", "bfp8_gemm_fused", "bfp8_gemm_fused_workspace_size")
+           "bfp8_gemm_grouped_workspace_size", "bfp8_gemm_fused", "bfp8_gemm_fused_workspace_size",
+           "bfp8_linear", "bfp8_linear_workspace_size")
 
 
 class BFP8Error(RuntimeError):
@@ -112,6 +113,12 @@ def lib():
             L.bfp8_gemm_fused_workspace_size.restype = i32
             L.bfp8_gemm_fused_workspace_size.argtypes = [i64, i64, i64, ctypes.POINTER(GemmOptions),
                                                          i32, ctypes.POINTER(sz)]
+            L.bfp8_linear.restype = i32
+            L.bfp8_linear.argtypes = [P, i64, P, P, P, i64, i64, i64, P, sz,
+                                      ctypes.POINTER(GemmOptions), P]
+            L.bfp8_linear_workspace_size.restype = i32
+            L.bfp8_linear_workspace_size.argtypes = [i64, i64, i64, ctypes.POINTER(GemmOptions), i32,
+                                                     ctypes.POINTER(sz)]
             L.bfp8_gemm_grouped_workspace_size.restype = i32
             L.bfp8_gemm_grouped_workspace_size.argtypes = [i64, i64, i64, i32,
                                                            ctypes.POINTER(GemmOptions), i32,
@@ -440,12 +447,52 @@ def bfp8_selftest_bounded_wait(limit_cycles: int, stream=None):
     return int(st), int(el.value)
 
 
+def bfp8_linear_workspace_size(M: int, N: int, K: int, options=None,
+                               weights_unaligned: bool = False) -> int:
+    n = ctypes.c_size_t(0)
+    _check(lib().bfp8_linear_workspace_size(M, N, K, _opts(options), int(weights_unaligned),
+                                            ctypes.byref(n)), "bfp8_linear_workspace_size")
+    return int(n.value)
+
+
+def bfp8_linear(x: torch.Tensor, B: torch.Tensor, Bs: torch.Tensor, out: torch.Tensor | None = None,
+                workspace: torch.Tensor | None = None, options=None, stream=None) -> torch.Tensor:
+    """out [M, N] bf16 = the blocked linear layer of bf16 x [M, K] (rows may be
+    strided) against e4m3 weights B [N, K] with scales Bs: the 1 x 128 group
+    quantisation into the workspace, then the GEMM, in one library call."""
+    if x.dtype != torch.bfloat16 or x.dim() != 2 or x.stride(1) != 1:
+        raise ValueError("x must be a 2-D bfloat16 tensor with unit column stride")
+    if B.dtype != torch.float8_e4m3fn or not B.is_contiguous() or not Bs.is_contiguous():
+        raise ValueError("B must be contiguous float8_e4m3fn and Bs contiguous")
+    M, K = x.shape
+    N, K2 = B.shape
+    if K2 != K:
+        raise ValueError("x and B disagree on K")
+    G = (K + 127) // 128
+    if Bs.shape != ((N + 127) // 128, G) or Bs.dtype != torch.float32:
+        raise ValueError(f"Bs must be float32 of shape {((N + 127) // 128, G)}")
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
+    if workspace is None:
+        need = bfp8_linear_workspace_size(M, N, K, options, B.data_ptr() % 16 != 0)
+        workspace = workspace_for(need, x.device, stream)
+    st = lib().bfp8_linear(x.data_ptr(), x.stride(0), B.data_ptr(), Bs.data_ptr(), out.data_ptr(),
+                           M, N, K, workspace.data_ptr(),
+                           workspace.numel() * workspace.element_size(), _opts(options),
+                           _stream_ptr(stream))
+    _check(st, "bfp8_linear")
+    return out
+
+
 def linear(x: torch.Tensor, B: torch.Tensor, Bs: torch.Tensor, out: torch.Tensor | None = None,
            stream=None, ue8m0: bool = False) -> torch.Tensor:
     """The whole W8A8 blocked linear layer: quantise x per 128-group (column-major
-    scales) and run the blocked GEMM against e4m3 weights B with scales Bs.
-    ue8m0: the UE8M0 variant (activation scales rounded up to powers of two;
-    pass weight scales rounded the same way, e.g. by bfp8_scale_ceil_ue8m0)."""
+    scales) and run the blocked GEMM against e4m3 weights B with scales Bs
+    (bfp8_linear).  ue8m0: the UE8M0 variant (activation scales rounded up to
+    powers of two; pass weight scales rounded the same way, e.g. by
+    bfp8_scale_ceil_ue8m0) and fp32 activations run as two calls."""
+    if not ue8m0 and x.dtype == torch.bfloat16:
+        return bfp8_linear(x, B, Bs, out=out, stream=stream)
     q, s = bfp8_group_quant(x, col_major=True, stream=stream, ue8m0=ue8m0)
     # the quantisation kernel writes neither B nor Bs: the GEMM may start
     # streaming the weights while it runs

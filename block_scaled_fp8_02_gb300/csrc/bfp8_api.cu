@@ -653,6 +653,16 @@ static bfp8_gemm_options effective_options(const bfp8_gemm_options* opt, bool gr
   return o;
 }
 
+// Timeline-trace builds: the kernels record into g_bfp8_trace.
+static void set_trace(GemmArgs* a) {
+  a->trace = nullptr;
+#if defined(BFP8_TRACE)
+  void* tp = nullptr;
+  if (cudaGetSymbolAddress(&tp, g_bfp8_trace) == cudaSuccess) a->trace = static_cast<unsigned long long*>(tp);
+  cudaGetLastError();
+#endif
+}
+
 // The GEMM proper (internal linkage: not part of the exported interface).
 static bfp8_status gemm_impl(const void* A, const void* B, const float* As, int as_col_major,
                              int64_t ld_as, const float* Bs, void* out, int64_t M, int64_t N,
@@ -710,8 +720,8 @@ static bfp8_status gemm_impl(const void* A, const void* B, const float* As, int 
     a_op = ws + p.off_a;
     b_op = ws + p.off_b;
   }
-  // scales in the layout the kernel bulk-copies
   const int64_t NTv = cdiv(N, 128);
+  // scales in the layout the kernel bulk-copies
   const bool as_ok = as_col_major && ld_as % 4 == 0 && !misaligned(As, 16);
   const bool bs_ok = !misaligned(Bs, 16) && (experts * NTv * G) % 4 == 0;
   const float* as_k = As;
@@ -770,14 +780,7 @@ static bfp8_status gemm_impl(const void* A, const void* B, const float* As, int 
   a.q_vec = (x.q && !misaligned(x.q, 16) && N % 16 == 0) ? 1 : 0;
   a.err = d.err;
   a.wait_limit = kWaitLimitCycles;
-  a.trace = nullptr;
-#if defined(BFP8_TRACE)
-  {
-    void* tp = nullptr;
-    if (cudaGetSymbolAddress(&tp, g_bfp8_trace) == cudaSuccess) a.trace = static_cast<unsigned long long*>(tp);
-    cudaGetLastError();
-  }
-#endif
+  set_trace(&a);
   cudaError_t e = p.swap ? launch_gemm_swap(p.bn, tmP, tmQ, a, cs)
                          : launch_gemm_wide(p.bn, mode, mr, tmP, tmQ, a, cs);
   if (e != cudaSuccess) return fail(BFP8_ERR_CUDA, "GEMM launch: %s", cudaGetErrorString(e));
@@ -931,6 +934,79 @@ bfp8_status bfp8_selftest_bounded_wait(uint64_t limit_cycles, uint64_t* elapsed,
   if (elapsed) *elapsed = el;
   if (!done) return fail(BFP8_ERR_DEVICE_TIMEOUT, "the wait gave up after %llu cycles", el);
   return ok();
+}
+
+
+// bfp8_linear: workspace = [GEMM workspace | q (M x K e4m3) | s (G x ld fp32)].
+static bfp8_status linear_plan(int64_t M, int64_t N, int64_t K, const bfp8_gemm_options* opt,
+                               bool b_unaligned, const DevInfo& d, Plan* p, size_t* off_q,
+                               size_t* off_s, size_t* total) {
+  bfp8_status st = check_gemm_sizes(M, N, K);
+  if (st != BFP8_OK) return st;
+  if ((st = check_options(opt)) != BFP8_OK) return st;
+  if ((st = make_plan(M, N, K, d.sms, opt, b_unaligned, &d, p)) != BFP8_OK) return st;
+  if (stream_k_tiles(p->sched) > static_cast<int64_t>(kCounterHeaderBytes / sizeof(int)))
+    return fail(BFP8_ERR_UNSUPPORTED, "more stream-K tiles than the workspace header holds");
+  *off_q = p->total;
+  *off_s = *off_q + align256(static_cast<size_t>(M) * static_cast<size_t>(K));
+  *total = *off_s + align256(static_cast<size_t>(cdiv(K, 128)) * static_cast<size_t>(bfp8_scale_ld(M)) *
+                             sizeof(float));
+  return BFP8_OK;
+}
+
+bfp8_status bfp8_linear_workspace_size(int64_t M, int64_t N, int64_t K, const bfp8_gemm_options* opt,
+                                       int weights_unaligned, size_t* bytes) {
+  if (!bytes) return fail(BFP8_ERR_INVALID_ARG, "bytes is null");
+  bfp8_status st = check_gemm_sizes(M, N, K);
+  if (st != BFP8_OK) return st;
+  if ((st = check_options(opt)) != BFP8_OK) return st;
+  DevInfo d;
+  st = current_device_with_caps(&d);
+  if (st != BFP8_OK) return st;
+  Plan p;
+  size_t oq = 0, os = 0;
+  if ((st = linear_plan(M, N, K, opt, weights_unaligned != 0, d, &p, &oq, &os, bytes)) != BFP8_OK)
+    return st;
+  return ok();
+}
+
+bfp8_status bfp8_linear(const void* x, int64_t ld_x, const void* B, const float* Bs, void* out,
+                        int64_t M, int64_t N, int64_t K, void* workspace, size_t workspace_bytes,
+                        const bfp8_gemm_options* opt, void* stream) {
+  bfp8_status st = check_gemm_sizes(M, N, K);
+  if (st != BFP8_OK) return st;
+  if ((st = check_options(opt)) != BFP8_OK) return st;
+  if (!x || !B || !Bs || !out)
+    return fail(BFP8_ERR_INVALID_ARG, "null pointer (x=%p B=%p Bs=%p out=%p)", x, B,
+                (const void*)Bs, out);
+  if (ld_x < K) return fail(BFP8_ERR_INVALID_ARG, "ld_x = %lld < K = %lld", (long long)ld_x, (long long)K);
+  if (misaligned(x, 2) || misaligned(out, 2)) return fail(BFP8_ERR_ALIGNMENT, "x and out must be 2-byte aligned");
+  if (misaligned(Bs, 4)) return fail(BFP8_ERR_ALIGNMENT, "Bs must be 4-byte aligned");
+  DevInfo d;
+  st = current_device_with_caps(&d);
+  if (st != BFP8_OK) return st;
+  Plan p;
+  size_t off_q = 0, off_s = 0, total = 0;
+  if ((st = linear_plan(M, N, K, opt, misaligned(B, 16), d, &p, &off_q, &off_s, &total)) != BFP8_OK)
+    return st;
+  if (!workspace) return fail(BFP8_ERR_WORKSPACE, "this layer needs %zu workspace bytes; got none", total);
+  if (workspace_bytes < total)
+    return fail(BFP8_ERR_WORKSPACE, "workspace of %zu bytes is smaller than the %zu needed",
+                workspace_bytes, total);
+  if (misaligned(workspace, 256)) return fail(BFP8_ERR_WORKSPACE, "workspace must be 256-byte aligned");
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  // quantise into the workspace, then the GEMM (which may stream the weights
+  // while the quantisation runs: it writes neither B nor Bs)
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  uint8_t* q = ws + off_q;
+  float* s = reinterpret_cast<float*>(ws + off_s);
+  const int64_t ld_s = bfp8_scale_ld(M);
+  cudaError_t e = launch_group_quant(x, 0, M, K, ld_x, q, K, s, 1, ld_s, 0, d.sms, cs);
+  if (e != cudaSuccess) return fail(BFP8_ERR_CUDA, "quantisation launch: %s", cudaGetErrorString(e));
+  bfp8_gemm_options o{};
+  if (opt) o = *opt;
+  o.prefetch_weights = 1;
+  return gemm_impl(q, B, s, 1, ld_s, Bs, out, M, N, K, workspace, off_q, &o, stream, GemmExtras{});
 }
 
 }  // extern "C"

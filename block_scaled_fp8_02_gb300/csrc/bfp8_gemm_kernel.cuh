@@ -263,6 +263,7 @@ enum : int {
   kTrEpiReduced = 19,  // promotion warp 0 done with its share of the reduction
   kTrMmaLoopCyc = 20,  // SM cycles of the MMA issuer's loop (with kTrMmaFirst /
                        // kTrMmaDone: the SM clock while it ran)
+  kTrSmid = 21,        // the SM the CTA ran on
   kTraceEvents = 24
 };
 #if defined(BFP8_TRACE)
@@ -370,7 +371,14 @@ __global__ void __launch_bounds__(GemmCfg<BN, SWAP, MODE, MR>::kThreads,
   // streaming while the MMA warp allocates TMEM.  The TMEM address reaches the
   // MMA and promotion warps through named barrier 2 (producer not included).
   __syncthreads();
-  if (threadIdx.x == 0) trace_event(a.trace, cta, kTrStart);
+  if (threadIdx.x == 0) {
+    trace_event(a.trace, cta, kTrStart);
+#if defined(BFP8_TRACE)
+    uint32_t smid;
+    asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
+    trace_value(a.trace, cta, kTrSmid, smid);
+#endif
+  }
   // Everything above overlaps the tail of the preceding kernel in the stream
   // (programmatic dependent launch).  Global memory that kernel may have
   // written (A, As, the workspace; B and Bs unless prefetch_b) is touched only

@@ -323,6 +323,34 @@ bfp8_status bfp8_gemm_fused_workspace_size(int64_t M, int64_t N, int64_t K,
                                            size_t* bytes);
 
 /*
+ * bfp8_linear -- the whole W8A8 blocked linear layer from bf16 activations in
+ * one call:
+ *   out = bfp8_gemm(q, B, s, Bs)  with  (q, s) = bfp8_group_quant(x, group 128,
+ *   column-major scales)
+ * (per_token_group_quant_fp8 followed by w8a8_block_fp8_matmul, the two steps
+ * of the vLLM PR 49932 digest's blocked FP8 linear), bitwise what those two
+ * calls give with the same options.  Two kernels: the quantisation writes q
+ * and s into the workspace, and the GEMM, launched behind it with
+ * programmatic dependent launch, streams the weights while it runs.
+ *   x    bf16 [M, K], row stride ld_x elements (ld_x >= K), 2-byte aligned.
+ *   B, Bs, out, M, N, K, opt, stream as for bfp8_gemm_ex (opt.prefetch_weights
+ *        is always on).
+ *   workspace / workspace_bytes
+ *        at least bfp8_linear_workspace_size bytes, 256-byte aligned, zero-filled
+ *        once after allocation: its first part serves the GEMM as for
+ *        bfp8_gemm (left ready for the next call), the rest holds q and s.
+ * Errors: BFP8_ERR_INVALID_ARG / ALIGNMENT / WORKSPACE as for bfp8_gemm_ex.
+ */
+bfp8_status bfp8_linear(const void* x, int64_t ld_x, const void* B, const float* Bs, void* out,
+                        int64_t M, int64_t N, int64_t K, void* workspace, size_t workspace_bytes,
+                        const bfp8_gemm_options* opt, void* stream);
+
+/* Workspace bytes bfp8_linear needs (current device); weights_unaligned: B
+ * not 16-byte aligned. */
+bfp8_status bfp8_linear_workspace_size(int64_t M, int64_t N, int64_t K, const bfp8_gemm_options* opt,
+                                       int weights_unaligned, size_t* bytes);
+
+/*
  * bfp8_gemm_noalloc -- bfp8_gemm for callers that cannot allocate device
  * memory.  (Not from the pages: they have no counterpart; this is a
  * convenience of this library.)

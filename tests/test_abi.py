@@ -273,3 +273,22 @@ def test_plans_choose_the_documented_schedules(L):
     assert p["relayout"] == 1                       # 1000-byte rows break the TMA stride rule
     assert bf.bfp8_gemm_plan(3, 1000, 1024, 152)["relayout"] == 0
     assert bf.bfp8_gemm_plan(3, 1000, 1024, 152, operands_unaligned=True)["relayout"] == 1
+
+
+def test_linear_rejects_bad_arguments_on_the_host(L):
+    P = 256  # any 256-aligned fake device address: nothing is dereferenced on the host
+    def lin(x=P, ld_x=256, B=P, Bs=P, out=P, M=4, N=8, K=256, ws=P, wsb=1 << 20, opt=None):
+        return L.bfp8_linear(x, ld_x, B, Bs, out, M, N, K, ws, wsb, opt, None)
+    assert lin(M=0) == 1
+    assert lin(K=-1) == 1
+    assert lin(x=None) == 1
+    assert lin(out=None) == 1
+    assert lin(ld_x=255) == 1                       # ld_x >= K
+    assert lin(x=P + 1) == 2                        # bf16 rows: 2-byte aligned
+    assert lin(Bs=P + 2) == 2
+    bad = bf.GemmOptions()
+    bad.k_split = 7
+    assert lin(opt=ctypes.pointer(bad)) == 1
+    n = ctypes.c_size_t(0)
+    assert L.bfp8_linear_workspace_size(4, 8, 0, None, 0, ctypes.byref(n)) == 1
+    assert L.bfp8_linear_workspace_size(4, 8, 256, None, 0, None) == 1

@@ -37,6 +37,39 @@ def test_linear_end_to_end(oracle_mod, dev, M, N, K):
     check_gemm(out, ref, (K + 127) // 128, label=f"linear {M}x{N}x{K}")
 
 
+def _quant_then_gemm(x, B, Bs, options):
+    q, s = bf.bfp8_group_quant(x, col_major=True)
+    return bf.bfp8_gemm(q, B, s, Bs, options=options)
+
+
+@pytest.mark.parametrize("M,N,K,ld_pad,options", [
+    (1, 4096, 4096, 0, None), (16, 4096, 4096, 64, None), (3, 576, 7168, 0, {"k_split": 2}),
+    (3, 1000, 1040, 0, None),          # K % 128 != 0
+    (4, 4096, 4096, 3, None),          # rows of x not 16-byte aligned
+    (100, 1000, 1024, 0, {"k_split": 1}),
+    (1, 5120, 25600, 0, None),
+    (2048, 4096, 4096, 0, None)])
+def test_bfp8_linear(oracle_mod, dev, M, N, K, ld_pad, options):
+    """bfp8_linear (one library call: quantisation into the workspace, then
+    the GEMM) is bitwise the two-call result and matches the oracle; x may
+    have a row stride other than K."""
+    case = wl.ragged_case(M, N, K, seed=5 * M + K)
+    xs = torch.zeros((M, K + ld_pad), dtype=torch.bfloat16)
+    xs[:, :K] = case["x"]
+    x = xs.to(dev)[:, :K]
+    B, Bs = case["B"].to(dev), case["Bs"].to(dev)
+    out = bf.bfp8_linear(x, B, Bs, options=options)
+    two = _quant_then_gemm(x, B, Bs, dict(options or {}, prefetch_weights=1))
+    torch.cuda.synchronize()
+    assert bf.bfp8_device_status() == 0
+    assert torch.equal(out.view(torch.int16), two.view(torch.int16))
+    rows = None if M * N * K <= 2e9 else np.arange(0, M, 97)
+    A, As = oracle_mod.group_quant(case["x"].view(torch.int16).numpy().view(np.uint16), False, True)
+    ref = oracle_mod.blocked_gemm(A, case["B"].view(torch.uint8).numpy(), As, True,
+                                  case["Bs"].numpy(), rows=rows, want_abs=True)
+    check_gemm(out, ref, (K + 127) // 128, rows=rows, label=f"bfp8_linear {M}x{N}x{K}")
+
+
 def test_bounded_wait_gives_up_and_reports(dev):
     """A wait on a barrier nothing arrives on returns an error status after its
     cycle budget instead of hanging the GPU; the context stays usable."""
