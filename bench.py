@@ -568,7 +568,8 @@ def run_ours(args, rank, world, local):
             "quant_p50_us": round(pq, 3), "quant_hot_p50_us": round(pqh, 3),
             "quant_gbs": round(mt.quant_bytes(M, K) / (pq * 1e-6) / 1e9, 1),
             "layer_p50_us": round(pl, 3),
-            "schedule": ("swap_ab" if plan["swap_ab"] else "wide") + f"/n{plan['tile_n']}"
+            "schedule": "gemv/mma.sync-m16n8k32" if plan.get("gemv") else
+                        ("swap_ab" if plan["swap_ab"] else "wide") + f"/n{plan['tile_n']}"
                         + (f"/cluster{plan['cluster']}" if plan["cluster"] > 1
                            else ("/stream-k" if plan["sk_units"] else "/whole-tiles")),
         }
@@ -599,7 +600,7 @@ def run_ours(args, rank, world, local):
                              f"({peaks['bf16_tflops']} TFLOP/s), nominal fp8/bf16 ratio"}
 
     rooflines = {
-        "gemm_swap_ab_decode": fam_hbm([M for M in Ms if M <= 64], "gemm_p50_us",
+        "gemm_decode": fam_hbm([M for M in Ms if M <= 64], "gemm_p50_us",
                                        lambda M: mt.gemm_bytes(M, N, K)),
         "gemm_wide_prefill": fam_tensor([M for M in Ms if M >= 2048]),
         "quant": fam_hbm([max(Ms)], "quant_p50_us", lambda M: mt.quant_bytes(M, K)),

@@ -20,7 +20,7 @@ BFP8_OK = 0
 BFP8_IN_BF16 = 0
 BFP8_IN_F32 = 1
 SCALE_FP32, SCALE_UE8M0 = 0, 1
-SCHEDULE_AUTO, SCHEDULE_SWAP_AB, SCHEDULE_WIDE = 0, 1, 2
+SCHEDULE_AUTO, SCHEDULE_SWAP_AB, SCHEDULE_WIDE, SCHEDULE_GEMV = 0, 1, 2, 3
 KSPLIT_AUTO, KSPLIT_STREAM_K, KSPLIT_CLUSTER, KSPLIT_NONE = 0, 1, 2, 3
 STATUS_NAMES = {0: "BFP8_OK", 1: "BFP8_ERR_INVALID_ARG", 2: "BFP8_ERR_ALIGNMENT",
                 3: "BFP8_ERR_UNSUPPORTED", 4: "BFP8_ERR_CUDA", 5: "BFP8_ERR_WORKSPACE",
@@ -52,7 +52,7 @@ class PlanInfo(ctypes.Structure):
                 ("grid", ctypes.c_int), ("tiles", ctypes.c_int64), ("k_blocks", ctypes.c_int64),
                 ("dp_tiles", ctypes.c_int64), ("sk_units", ctypes.c_int64),
                 ("relayout", ctypes.c_int), ("workspace_bytes", ctypes.c_size_t),
-                ("cluster", ctypes.c_int)]
+                ("cluster", ctypes.c_int), ("gemv", ctypes.c_int)]
 
 
 _lock = threading.Lock()

@@ -198,6 +198,7 @@ struct Plan {
   bool swap = false;
   int bn = 0;
   int mr = 128;              // wide tiles: activation rows loaded per stage
+  bool gemv = false;         // the matrix-vector kernel (few activation rows)
   bool relayout = false;
   int64_t kp = 0;            // inner extent of the operand tensor maps
   Sched sched{};
@@ -207,8 +208,8 @@ struct Plan {
 
 bfp8_status check_options(const bfp8_gemm_options* opt) {
   if (!opt) return BFP8_OK;
-  if (opt->schedule < 0 || opt->schedule > 2)
-    return fail(BFP8_ERR_INVALID_ARG, "options.schedule = %d (expected 0, 1 or 2)", opt->schedule);
+  if (opt->schedule < 0 || opt->schedule > 3)
+    return fail(BFP8_ERR_INVALID_ARG, "options.schedule = %d (expected 0 .. 3)", opt->schedule);
   if (opt->max_ctas < 0) return fail(BFP8_ERR_INVALID_ARG, "options.max_ctas = %d", opt->max_ctas);
   if (opt->tile_n != 0 && opt->tile_n != 16 && opt->tile_n != 32 && opt->tile_n != 64 &&
       opt->tile_n != 128 && opt->tile_n != 256)
@@ -347,6 +348,18 @@ int swap_tile_n(int64_t M) {
 }
 
 constexpr int64_t kSwapMaxM = 256;
+// AUTO runs the matrix-vector kernel (for M <= kGemvMaxM) when its 16-row
+// tiles fill their waves of CTA slots (two per SM) to at least 2/3: it runs a
+// tile per CTA per wave, so a barely started last wave (e.g. 320 tiles on 304
+// slots) costs a whole wave.  Measured on this GPU at M = 1: N = K = 4096
+// (256 tiles) 6.1 against 8.9 us, N = 10240 (640 tiles) 14.9 against 18.5,
+// N = 51200 25.6 % faster; N = 5120, K = 25600 (320 tiles) 42.9 against 36.5.
+bool gemv_preferred(int64_t N, int num_sms) {
+  const int64_t tiles = (N + 15) / 16;
+  const int64_t slots = 2 * static_cast<int64_t>(num_sms > 0 ? num_sms : 1);
+  const int64_t waves = (tiles + slots - 1) / slots;
+  return 3 * tiles >= 2 * waves * slots;
+}
 
 // `dev` = the device's cached properties, whose co-resident cluster counts
 // the planner uses (nullptr: host-only planning, counts estimated from
@@ -355,7 +368,14 @@ constexpr int64_t kSwapMaxM = 256;
 bfp8_status make_plan(int64_t M, int64_t N, int64_t K, int num_sms, const bfp8_gemm_options* opt,
                       bool unaligned, const DevInfo* dev, Plan* p, int64_t experts = 1) {
   const int schedule = opt ? opt->schedule : BFP8_SCHEDULE_AUTO;
-  p->swap = schedule == BFP8_SCHEDULE_SWAP_AB ||
+  p->gemv = experts == 1 && !unaligned && K % 16 == 0 && M <= kGemvMaxM &&
+            (schedule == BFP8_SCHEDULE_GEMV ||
+             (schedule == BFP8_SCHEDULE_AUTO && gemv_preferred(N, num_sms)));
+  if (schedule == BFP8_SCHEDULE_GEMV && !p->gemv)
+    return fail(BFP8_ERR_UNSUPPORTED,
+                "options.schedule = GEMV needs M <= %d, K %% 16 == 0 and 16-byte aligned A and B "
+                "(got M=%lld K=%lld)", kGemvMaxM, (long long)M, (long long)K);
+  p->swap = schedule == BFP8_SCHEDULE_SWAP_AB || schedule == BFP8_SCHEDULE_GEMV ||
             (schedule == BFP8_SCHEDULE_AUTO && M <= kSwapMaxM);
   const int tn = opt ? opt->tile_n : 0;
   if (!p->swap && tn != 0 && tn != 128 && tn != 256)
@@ -576,6 +596,7 @@ bfp8_status bfp8_gemm_plan(int64_t M, int64_t N, int64_t K, int num_sms,
   info->relayout = p.relayout;
   info->workspace_bytes = p.total;
   info->cluster = p.sched.cluster > 1 ? static_cast<int>(p.sched.cluster) : 1;
+  info->gemv = p.gemv ? 1 : 0;
   return ok();
 }
 
@@ -708,6 +729,15 @@ static bfp8_status gemm_impl(const void* A, const void* B, const float* As, int 
       return fail(BFP8_ERR_WORKSPACE, "workspace must be 256-byte aligned");
   }
   cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  if (p.gemv) {
+    // matrix-vector kernel: A, As (either layout), B and Bs read where they are
+    const cudaError_t e =
+        launch_gemv(static_cast<const uint8_t*>(A), K, As, as_col_major, ld_as,
+                    static_cast<const uint8_t*>(B), Bs, static_cast<__nv_bfloat16*>(out),
+                    static_cast<int>(M), N, K, (opt && opt->prefetch_weights == 1) ? 1 : 0, d.sms, cs);
+    if (e != cudaSuccess) return fail(BFP8_ERR_CUDA, "GEMV launch: %s", cudaGetErrorString(e));
+    return ok();
+  }
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   const void* a_op = A;
   const void* b_op = B;

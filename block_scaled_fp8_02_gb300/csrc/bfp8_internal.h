@@ -4,6 +4,7 @@
 
 #include <cuda.h>
 #include <cuda_runtime.h>
+#include <cuda_bf16.h>
 
 #include <cstddef>
 #include <cstdint>
@@ -39,6 +40,15 @@ cudaError_t launch_gemm_wide(int bn, int mode, int mr, const CUtensorMap& tmP,
                              const CUtensorMap& tmQ, const GemmArgs& a, cudaStream_t stream);
 cudaError_t launch_gemm_wide_ext(int bn, int mode, const CUtensorMap& tmP, const CUtensorMap& tmQ,
                                  const GemmArgs& a, cudaStream_t stream);
+
+// The GEMM for M <= kGemvMaxM activation rows on warp-level MMAs
+// (bfp8_gemv.cu): A [M, K] e4m3 with row stride lda, As in either layout,
+// B [N, K] e4m3 (row stride K), Bs [ceil(N/128), G]; K % 16 == 0 and A, B
+// 16-byte aligned.
+constexpr int kGemvMaxM = 8;
+cudaError_t launch_gemv(const uint8_t* A, int64_t lda, const float* As, int as_col_major,
+                        int64_t ld_as, const uint8_t* B, const float* Bs, __nv_bfloat16* out, int M,
+                        int64_t N, int64_t K, int prefetch_b, int num_sms, cudaStream_t stream);
 
 // Clusters of `cs` GEMM CTAs the current device runs at once (bfp8_gemm_swap.cu),
 // for the instantiations sized for two CTAs per SM (swap-AB tiles up to 64

@@ -120,7 +120,11 @@ int64_t bfp8_scale_ld(int64_t M);
 typedef enum {
   BFP8_SCHEDULE_AUTO = 0,
   BFP8_SCHEDULE_SWAP_AB = 1,  /* weights fill the 128-row MMA slot (small M) */
-  BFP8_SCHEDULE_WIDE = 2      /* activations fill it; 128 x 256 output tiles */
+  BFP8_SCHEDULE_WIDE = 2,     /* activations fill it; 128 x 256 output tiles */
+  BFP8_SCHEDULE_GEMV = 3      /* M <= 8 only: a matrix-vector kernel on warp-level
+                                 MMAs (16 weight rows per CTA, k split over its 8
+                                 warps, no workspace use); needs K % 16 == 0 and
+                                 16-byte aligned A and B */
 } bfp8_schedule;
 
 /* How the output tiles and their K dimension are shared out among CTAs when
@@ -233,6 +237,9 @@ typedef struct {
                            tiles * cluster, dp_tiles = sk_units = 0), else 1.
                            Whole tiles only: dp_tiles = tiles, sk_units = 0,
                            grid possibly below the SM count. */
+  int gemv;             /* 1: the matrix-vector kernel runs (BFP8_SCHEDULE_GEMV);
+                           the tile fields above then describe the tensor-core
+                           plan it replaces */
 } bfp8_plan_info;
 
 bfp8_status bfp8_gemm_plan(int64_t M, int64_t N, int64_t K, int num_sms,

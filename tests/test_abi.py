@@ -106,6 +106,8 @@ def test_gemm_rejects_bad_arguments_on_the_host(L):
     bad = bf.GemmOptions()
     bad.schedule = 9
     assert _gemm(L, opt=ctypes.pointer(bad)) == 1
+    bad.schedule = 4
+    assert _gemm(L, opt=ctypes.pointer(bad)) == 1
     bad.schedule, bad.tile_n = 0, 48
     assert _gemm(L, opt=ctypes.pointer(bad)) == 1
     bad.schedule, bad.tile_n = 2, 64                # wide tiles are 128 or 256 wide
@@ -292,3 +294,21 @@ def test_linear_rejects_bad_arguments_on_the_host(L):
     n = ctypes.c_size_t(0)
     assert L.bfp8_linear_workspace_size(4, 8, 0, None, 0, ctypes.byref(n)) == 1
     assert L.bfp8_linear_workspace_size(4, 8, 256, None, 0, None) == 1
+
+
+def test_gemv_plans(L):
+    """BFP8_SCHEDULE_GEMV: M <= 8, K % 16 == 0, aligned operands; else refused."""
+    G = {"schedule": bf.SCHEDULE_GEMV}
+    for M in (1, 2, 3, 4, 8):
+        assert bf.bfp8_gemm_plan(M, 4096, 4096, 152, G)["gemv"] == 1
+    for M, N, K, kw in ((9, 4096, 4096, {}), (1, 4096, 1000, {}), (2, 64, 4096, {"operands_unaligned": True})):
+        with pytest.raises(bf.BFP8Error):
+            bf.bfp8_gemm_plan(M, N, K, 152, G, **kw)
+    assert bf.bfp8_gemm_plan(64, 4096, 4096, 152)["gemv"] == 0
+    # AUTO, M <= 8: when the 16-row tiles fill their waves of 2 x SM slots to 2/3
+    assert bf.bfp8_gemm_plan(1, 4096, 4096, 152)["gemv"] == 1       # 256 of 304
+    assert bf.bfp8_gemm_plan(8, 10240, 5120, 152)["gemv"] == 1      # 640 of 912
+    assert bf.bfp8_gemm_plan(1, 5120, 25600, 152)["gemv"] == 0      # 320 of 608
+    assert bf.bfp8_gemm_plan(1, 576, 7168, 152)["gemv"] == 0        # 36 of 304
+    assert bf.bfp8_gemm_plan(9, 4096, 4096, 152)["gemv"] == 0
+    assert bf.bfp8_gemm_plan(1, 4096, 4096, 152, {"schedule": bf.SCHEDULE_SWAP_AB})["gemv"] == 0

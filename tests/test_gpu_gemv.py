@@ -1,0 +1,79 @@
+"""GPU parity of the matrix-vector kernel for a few activation rows (M <= 8,
+BFP8_SCHEDULE_GEMV, warp-level MMAs): every output element against the
+oracle, on the decode sweep shape, the Qwen3-32B layer shapes, ragged N and K
+(a partial last 64-byte window and k-block, fewer k-blocks than warps), both
+scale layouts and weight prefetch."""
+import numpy as np
+import pytest
+import torch
+
+import block_scaled_fp8_02_gb300 as bf
+from block_scaled_fp8_02_gb300 import build as bfbuild
+from block_scaled_fp8_02_gb300 import workloads as wl
+
+from parity import check_gemm
+
+pytestmark = pytest.mark.gpu
+
+GEMV = {"schedule": bf.SCHEDULE_GEMV}
+
+
+@pytest.fixture(scope="module")
+def dev():
+    bfbuild.build()
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    return torch.device("cuda:0")
+
+
+def _run(oracle_mod, dev, case, col_major=True, options=GEMV, label=""):
+    x = case["x"]
+    M, N, K = case["M"], case["N"], case["K"]
+    A, As = oracle_mod.group_quant(x.view(torch.int16).numpy().view(np.uint16), False, col_major)
+    B = case["B"].view(torch.uint8).numpy()
+    Bs = case["Bs"].numpy()
+    A_d = torch.from_numpy(A).to(dev).view(torch.float8_e4m3fn)
+    B_d = torch.from_numpy(B).to(dev).view(torch.float8_e4m3fn)
+    As_st = torch.from_numpy(As).to(dev)
+    As_d = As_st[:, :M].t() if col_major else As_st
+    Bs_d = torch.from_numpy(Bs).to(dev)
+    plan = bf.bfp8_gemm_plan(M, N, K, 0, options)
+    assert plan["gemv"] == 1
+    out = bf.bfp8_gemm(A_d, B_d, As_d, Bs_d, options=options)
+    torch.cuda.synchronize()
+    ref = oracle_mod.blocked_gemm(A, B, As, col_major, Bs, want_abs=True)
+    return check_gemm(out, ref, (K + 127) // 128, label=label)
+
+
+@pytest.mark.parametrize("M", [1, 2, 3, 4, 5, 7, 8])
+def test_decode_sweep_shape(oracle_mod, dev, M):
+    _run(oracle_mod, dev, wl.linear_case(M, 4096, 4096, seed=100 + M), label=f"gemv decode M={M}")
+
+
+@pytest.mark.parametrize("layer", list(wl.QWEN3_32B_LAYERS))
+def test_qwen3_32b_layers_m1(oracle_mod, dev, layer):
+    N, K = wl.QWEN3_32B_LAYERS[layer]
+    _run(oracle_mod, dev, wl.linear_case(1, N, K, seed=N + K), label=f"gemv {layer} M=1")
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 1, 16), (2, 130, 144), (3, 1000, 1040), (4, 576, 7168),
+                                   (1, 300, 528), (8, 129, 4112), (6, 8, 2000 + 16 * 3),
+                                   (8, 4100, 1024)])
+@pytest.mark.parametrize("col_major", [True, False])
+def test_ragged(oracle_mod, dev, M, N, K, col_major):
+    _run(oracle_mod, dev, wl.ragged_case(M, N, K, seed=M + N + K), col_major,
+         label=f"gemv ragged {M}x{N}x{K}")
+
+
+def test_prefetch_weights(oracle_mod, dev):
+    _run(oracle_mod, dev, wl.linear_case(2, 4096, 4096, seed=5),
+         options=dict(GEMV, prefetch_weights=1), label="gemv prefetch")
+
+
+def test_deterministic(dev):
+    case = wl.linear_case(6, 2048, 4096, seed=9)
+    q, s = bf.bfp8_group_quant(case["x"].to(dev))
+    B, Bs = case["B"].to(dev), case["Bs"].to(dev)
+    outs = [bf.bfp8_gemm(q, B, s, Bs, options=GEMV).clone() for _ in range(4)]
+    torch.cuda.synchronize()
+    for o in outs[1:]:
+        assert torch.equal(o.view(torch.int16), outs[0].view(torch.int16))

@@ -135,3 +135,24 @@ def test_exact_ties_from_bf16_inputs(oracle_mod, dev):
     assert torch.equal(xb.float(), x32)            # every midpoint is a bf16 value
     _check(oracle_mod, dev, xb, True)
     _check(oracle_mod, dev, xb, False)
+
+
+@pytest.mark.parametrize("M,K,frac", [(300, 4096, 1.0), (97, 768, 1.0), (512, 4096, 0.02),
+                                      (64, 25600, 0.3)])
+def test_exact_ties_on_the_bf16_fast_path(oracle_mod, dev, M, K, frac):
+    """Exact ties on the bf16 fast path (K a multiple of 256): a fraction
+    `frac` of the elements are e4m3 midpoints in groups whose amax is 448
+    (scale 1), up to every element of every warp step, so that the
+    bracketing products disagree everywhere and the IEEE divisions decide."""
+    rng = np.random.default_rng(M + K)
+    tab = oracle_mod.e4m3_table()
+    mags = np.sort(np.unique(np.abs(tab[np.isfinite(tab)])))
+    mids = ((mags[:-1] + mags[1:]) / 2).astype(np.float32)
+    x = rng.standard_normal((M, K)).astype(np.float32) * 40.0
+    tie = rng.random((M, K)) < frac
+    x[tie] = rng.choice(mids, size=int(tie.sum())) * rng.choice([-1.0, 1.0], size=int(tie.sum()))
+    x = np.clip(x, -447.0, 447.0)
+    x[:, ::128] = 448.0                                  # every group's amax: scale 1
+    xb = torch.from_numpy(x).to(torch.bfloat16)
+    _check(oracle_mod, dev, xb, True)
+    _check(oracle_mod, dev, xb, False)
