@@ -279,6 +279,7 @@ enum class Split { kStreamK, kWholeTiles, kCluster };
 struct SplitChoice {
   Split kind = Split::kStreamK;
   uint32_t cs = 0;
+  double cost = 0.0;    // the model's relative time of the chosen split
 };
 
 // How the tiles and their k-blocks are shared out.  Explicit k_split values
@@ -289,9 +290,13 @@ SplitChoice choose_split(int64_t tiles, int64_t G, int bn, bool swap, int64_t ma
                          const bfp8_gemm_options* opt, const int* cap) {
   const int ks = opt ? opt->k_split : BFP8_KSPLIT_AUTO;
   SplitChoice c;
+  const double sk = stream_k_cost(tiles, G, bn, swap, max_ctas);
+  const double whole = whole_tiles_cost(tiles, G, max_ctas);
+  c.cost = sk;
   if (ks == BFP8_KSPLIT_STREAM_K) return c;
   if (ks == BFP8_KSPLIT_NONE) {
     c.kind = Split::kWholeTiles;
+    c.cost = whole;
     return c;
   }
   int best_cs = 0;
@@ -314,20 +319,19 @@ SplitChoice choose_split(int64_t tiles, int64_t G, int bn, bool swap, int64_t ma
     if (best_cs >= 2) {
       c.kind = Split::kCluster;
       c.cs = static_cast<uint32_t>(best_cs);
+      c.cost = best_cl;
     }
     return c;
   }
   // AUTO
-  const double sk = stream_k_cost(tiles, G, bn, swap, max_ctas);
-  const double whole = whole_tiles_cost(tiles, G, max_ctas);
-  double best = sk;
-  if (whole < best) {
-    best = whole;
+  if (whole < c.cost) {
+    c.cost = whole;
     c.kind = Split::kWholeTiles;
   }
-  if (best_cs >= 2 && best_cl < best) {
+  if (best_cs >= 2 && best_cl < c.cost) {
     c.kind = Split::kCluster;
     c.cs = static_cast<uint32_t>(best_cs);
+    c.cost = best_cl;
   }
   return c;
 }
@@ -375,33 +379,55 @@ bfp8_status make_plan(int64_t M, int64_t N, int64_t K, int num_sms, const bfp8_g
     return fail(BFP8_ERR_UNSUPPORTED,
                 "options.schedule = GEMV needs M <= %d, K %% 16 == 0 and 16-byte aligned A and B "
                 "(got M=%lld K=%lld)", kGemvMaxM, (long long)M, (long long)K);
-  p->swap = schedule == BFP8_SCHEDULE_SWAP_AB || schedule == BFP8_SCHEDULE_GEMV ||
-            (schedule == BFP8_SCHEDULE_AUTO && M <= kSwapMaxM);
   const int tn = opt ? opt->tile_n : 0;
+  // swap-AB when asked for, and under AUTO only for the tile widths that
+  // exist only as swap-AB tiles (16, 32, 64)
+  p->swap = schedule == BFP8_SCHEDULE_SWAP_AB || schedule == BFP8_SCHEDULE_GEMV ||
+            (schedule == BFP8_SCHEDULE_AUTO && M <= kSwapMaxM && tn != 0 && tn < 128);
   if (!p->swap && tn != 0 && tn != 128 && tn != 256)
     return fail(BFP8_ERR_INVALID_ARG, "options.tile_n = %d: wide tiles are 128 or 256 wide", tn);
-  p->bn = p->swap ? (tn ? tn : swap_tile_n(M)) : (tn == 128 ? 128 : 256);
+  const int64_t G = cdiv(K, 128);
+  int max_ctas = num_sms;
+  if (opt && opt->max_ctas > 0 && opt->max_ctas < max_ctas) max_ctas = opt->max_ctas;
+  // the split of one tile shape, with the cluster capacities of its class
+  auto split_for = [&](bool swap, int bn, int64_t tiles) -> SplitChoice {
+    const bool two = gemm_two_per_sm(swap, bn);
+    int est[kMaxCluster + 1];
+    const int* cap = nullptr;
+    if (dev) {
+      cap = two ? dev->cluster_cap2 : dev->cluster_cap;
+    } else {
+      estimate_cluster_caps(num_sms, two ? 2 : 1, est);
+      cap = est;
+    }
+    return choose_split(tiles, G, bn, swap, max_ctas, opt, cap);
+  };
+  if (p->swap) {
+    p->bn = tn ? tn : swap_tile_n(M);
+  } else if (tn) {
+    p->bn = tn;
+  } else if (schedule == BFP8_SCHEDULE_AUTO && M <= kSwapMaxM && experts == 1) {
+    // up to 256 rows: 256- or 128-wide tiles by the split model, a 128-wide
+    // step weighted 0.7 of a 256-wide one (fitted to this GPU's times at
+    // M = 9 .. 256 on the sweep and Qwen3-32B shapes; swap-AB tiles, the
+    // pages' small-M design, were never faster by more than 1 % there and
+    // up to 1.6x slower, so AUTO does not take them)
+    const int64_t mt = cdiv(M, 128);
+    const double c256 = split_for(false, 256, mt * cdiv(N, 256)).cost;
+    const double c128 = 0.7 * split_for(false, 128, mt * cdiv(N, 128)).cost;
+    p->bn = c128 < c256 ? 128 : 256;
+  } else {
+    p->bn = 256;
+  }
   // plain 256-wide tiles of a decode-sized M load only the rows that exist
   // (M-grouped calls keep whole 128-row tiles: experts start on them)
   p->mr = (!p->swap && p->bn == 256 && experts == 1 && M <= 64) ? (M <= 32 ? 32 : 64) : 128;
-  const int64_t G = cdiv(K, 128);
   const int64_t p_tiles = p->swap ? cdiv(N, 128) : cdiv(M, 128);
   const int64_t q_tiles = p->swap ? cdiv(M, p->bn) : cdiv(N, p->bn);
   if (p_tiles * q_tiles * G >= (int64_t{1} << 31))
     return fail(BFP8_ERR_UNSUPPORTED, "problem too large: %lld tiles x %lld k-blocks",
                 (long long)(p_tiles * q_tiles), (long long)G);
-  int max_ctas = num_sms;
-  if (opt && opt->max_ctas > 0 && opt->max_ctas < max_ctas) max_ctas = opt->max_ctas;
-  const bool two = gemm_two_per_sm(p->swap, p->bn);
-  int est[kMaxCluster + 1];
-  const int* cap = nullptr;
-  if (dev) {
-    cap = two ? dev->cluster_cap2 : dev->cluster_cap;
-  } else {
-    estimate_cluster_caps(num_sms, two ? 2 : 1, est);
-    cap = est;
-  }
-  const SplitChoice sc = choose_split(p_tiles * q_tiles, G, p->bn, p->swap, max_ctas, opt, cap);
+  const SplitChoice sc = split_for(p->swap, p->bn, p_tiles * q_tiles);
   const uint32_t pt = static_cast<uint32_t>(p_tiles), qt = static_cast<uint32_t>(q_tiles);
   const uint32_t g32 = static_cast<uint32_t>(G), mc = static_cast<uint32_t>(max_ctas);
   if (sc.kind == Split::kCluster)

@@ -226,32 +226,54 @@ def test_cluster_split_gives_each_rank_one_nonempty_contiguous_slice(L, M, N, K,
 
 
 def test_plans_choose_the_documented_schedules(L):
-    p = bf.bfp8_gemm_plan(1, 4096, 4096, 152)
+    SW = {"schedule": bf.SCHEDULE_SWAP_AB}
+    p = bf.bfp8_gemm_plan(1, 4096, 4096, 152, SW)
     assert p["swap_ab"] == 1 and p["tile_n"] == 16 and p["cluster"] == 4 and p["grid"] == 128
-    p = bf.bfp8_gemm_plan(1, 4096, 4096, 152, {"k_split": 1})
+    p = bf.bfp8_gemm_plan(1, 4096, 4096, 152, dict(SW, k_split=1))
     assert p["cluster"] == 1 and p["grid"] == 152 and p["dp_tiles"] == 0
-    # the cost model: five tiles of 56 k-blocks would be spread over ~30 CTAs
-    # each by stream-K (a long fixup chain); clusters of 8 win
-    assert bf.bfp8_gemm_plan(83, 576, 7168, 152)["cluster"] == 8
+    # AUTO, M <= 256: 256- or 128-wide tiles by the split model (a 128-wide
+    # step weighs 0.7 of a 256-wide one).  N = K = 4096: 128-wide tiles in
+    # clusters of 4 up to M = 128 (measured 8.96 against 10.13 us at M = 32,
+    # 10.61 against 14.33 at M = 128), 256-wide from M = 160 (13.58 against 14.09)
+    for M in (9, 32, 128):
+        p = bf.bfp8_gemm_plan(M, 4096, 4096, 152)
+        assert (p["swap_ab"], p["tile_n"], p["cluster"]) == (0, 128, 4)
+    for M in (160, 256):
+        p = bf.bfp8_gemm_plan(M, 4096, 4096, 152)
+        assert (p["swap_ab"], p["tile_n"], p["cluster"]) == (0, 256, 4)
+    # Qwen3-32B shapes: 256-wide (qkv at M = 256: 23.6 us against 36.3 with
+    # swap-AB tiles; down at M = 64: 30.0 against 41.5)
+    assert bf.bfp8_gemm_plan(256, 10240, 5120, 152)["tile_n"] == 256
+    p = bf.bfp8_gemm_plan(64, 5120, 25600, 152)
+    assert p["swap_ab"] == 0 and p["tile_n"] == 256 and p["cluster"] == 6
+    # five narrow tiles (N = 576): 128-wide in clusters of 8 (7.99 us at M =
+    # 83, against 9.50 swap-AB and 11.72 256-wide)
+    p = bf.bfp8_gemm_plan(83, 576, 7168, 152)
+    assert (p["swap_ab"], p["tile_n"], p["cluster"]) == (0, 128, 8)
+    # swap-AB tiles, explicitly: five tiles of 56 k-blocks would be spread over
+    # ~30 CTAs each by stream-K (a long fixup chain); clusters of 8 win
+    assert bf.bfp8_gemm_plan(83, 576, 7168, 152, SW)["cluster"] == 8
     # 40 tiles of 200 k-blocks: stream-K's 53 steps per CTA beat 67 in clusters of 3
-    assert bf.bfp8_gemm_plan(1, 5120, 25600, 152)["cluster"] == 1
+    assert bf.bfp8_gemm_plan(1, 5120, 25600, 152, SW)["cluster"] == 1
     # ... but not with 256-wide swap tiles, whose 128 KB partials are costly
     # to write and read (measured: clusters of 3 60.9 us, stream-K 65.8 us)
-    assert bf.bfp8_gemm_plan(256, 5120, 25600, 152)["cluster"] == 3
+    assert bf.bfp8_gemm_plan(256, 5120, 25600, 152, SW)["cluster"] == 3
     # 80 tiles of 40 k-blocks: stream-K over 152 CTAs beats one wave of 80
     # whole tiles (measured 37.4 against 39.3 us)
-    p = bf.bfp8_gemm_plan(256, 10240, 5120, 152)
+    p = bf.bfp8_gemm_plan(256, 10240, 5120, 152, SW)
     assert p["cluster"] == 1 and p["sk_units"] > 0
     # wide tiles: 64 of them at M = 512, clusters of 2
     p = bf.bfp8_gemm_plan(512, 4096, 4096, 152)
     assert p["swap_ab"] == 0 and p["cluster"] == 2 and p["grid"] == 128
     # 80 tiles: not even clusters of 2 fit in one wave
-    assert bf.bfp8_gemm_plan(1, 10240, 5120, 152)["cluster"] == 1
+    assert bf.bfp8_gemm_plan(1, 10240, 5120, 152, SW)["cluster"] == 1
     # cluster schedules need no stream-K partials in the workspace
-    assert (bf.bfp8_gemm_plan(1, 4096, 4096, 152)["workspace_bytes"]
-            < bf.bfp8_gemm_plan(1, 4096, 4096, 152, {"k_split": 1})["workspace_bytes"])
-    p = bf.bfp8_gemm_plan(64, 4096, 4096, 152)
+    assert (bf.bfp8_gemm_plan(1, 4096, 4096, 152, SW)["workspace_bytes"]
+            < bf.bfp8_gemm_plan(1, 4096, 4096, 152, dict(SW, k_split=1))["workspace_bytes"])
+    p = bf.bfp8_gemm_plan(64, 4096, 4096, 152, SW)
     assert p["swap_ab"] == 1 and p["tile_n"] == 64
+    # an explicit narrow tile width exists only as a swap-AB tile
+    assert bf.bfp8_gemm_plan(64, 4096, 4096, 152, {"tile_n": 32})["swap_ab"] == 1
     p = bf.bfp8_gemm_plan(8192, 4096, 4096, 152)
     assert p["swap_ab"] == 0 and p["tile_n"] == 256 and p["tiles"] == 64 * 16
     # 1024 tiles = 6.7 waves: seven balanced waves of whole tiles on 147 CTAs

@@ -82,9 +82,12 @@ def test_page_correctness_case_every_schedule(oracle_mod, dev, col_major, option
 
 
 @pytest.mark.parametrize("M", wl.DECODE_MS)
-def test_decode_sweep_full(oracle_mod, dev, M):
+@pytest.mark.parametrize("options", [None, {"schedule": 1}, {"schedule": 2, "tile_n": 256}])
+def test_decode_sweep_full(oracle_mod, dev, M, options):
+    """AUTO (matrix-vector kernel or wide tiles) and, explicitly, swap-AB and
+    256-wide tiles with partial activation rows."""
     case = wl.linear_case(M, 4096, 4096, seed=100 + M)
-    _run(oracle_mod, dev, case, label=f"decode M={M}")
+    _run(oracle_mod, dev, case, options=options, label=f"decode M={M} {options}")
 
 
 @pytest.mark.parametrize("M", wl.PREFILL_MS)
@@ -157,11 +160,12 @@ def test_unaligned_operands_and_output(oracle_mod, dev):
                                    (100, 1000, 1000), (129, 16, 300), (256, 4096, 1024),
                                    (600, 512, 4096), (257, 384, 256), (2, 130, 129)])
 @pytest.mark.parametrize("cs", [0, 2, 3, 5, 8])
-def test_cluster_split_k(oracle_mod, dev, M, N, K, cs):
+@pytest.mark.parametrize("schedule", [0, 1])
+def test_cluster_split_k(oracle_mod, dev, M, N, K, cs, schedule):
     """Cluster split-K at every cluster size the planner may pick (0 = its
     own choice; explicit sizes are clamped to the tile's k-blocks): swap and
     wide tiles, ragged M, N and K, re-laid-out operands."""
-    opts = {"k_split": 2, "cluster_size": cs}
+    opts = {"k_split": 2, "cluster_size": cs, "schedule": schedule}
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     plan = bf.bfp8_gemm_plan(M, N, K, 0, opts)          # this device's plan
     G = plan["k_blocks"]
@@ -170,7 +174,7 @@ def test_cluster_split_k(oracle_mod, dev, M, N, K, cs):
     elif G >= 2 and 2 * plan["tiles"] <= sms:
         assert 2 <= plan["cluster"] <= min(8, G) and plan["grid"] <= sms
     case = wl.ragged_case(M, N, K, seed=5 * M + N + K + cs)
-    _run(oracle_mod, dev, case, options=opts, label=f"cluster {cs} {M}x{N}x{K}")
+    _run(oracle_mod, dev, case, options=opts, label=f"cluster {cs} s{schedule} {M}x{N}x{K}")
 
 
 @pytest.mark.parametrize("options", [None, {"max_ctas": 5}, {"schedule": 2}, {"k_split": 2},

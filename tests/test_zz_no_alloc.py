@@ -5,9 +5,13 @@ whose host framework owns every device allocation, latency-critical loops that
 must not allocate) cannot hand libbfp8 a workspace; this entry point uses the
 scratch array built into the library instead.  Its results must equal the
 regular entry point's bit for bit on two calls in a row (the second call finds
-the first call's leftovers in the shared scratch), including a shape whose
-stream-K counters and partial sums live in that scratch, and must meet the
-GEMM acceptance against the oracle.  This file is collected last on purpose.
+the first call's leftovers in the shared scratch) on every kernel family a
+decode-sized call can take -- the matrix-vector kernel, 128- and 256-wide
+tiles in clusters, swap-AB tiles, re-laid-out operands and scales in the
+scratch -- and must meet the GEMM acceptance against the oracle.  (The
+default plans split no decode-sized problem stream-K within the scratch: a
+wide tile's fp32 partials need ~38 MB on a full grid; such problems are
+rejected.)  This file is collected last on purpose.
 """
 import ctypes
 
@@ -40,20 +44,12 @@ def _call_noalloc(A, B, As, Bs, out):
         M, N, K, torch.cuda.current_stream().cuda_stream)
 
 
-def _stream_k_shape():
-    """A decode-sized shape whose plan on this device splits tiles stream-K
-    (partial sums and counters in the scratch, no cluster reduction) and whose
-    workspace fits the built-in scratch."""
-    for M, N, K in [(32, 24576, 2048), (16, 20480, 7168), (64, 20480, 4096), (1, 20480, 7168)]:
-        p = bf.bfp8_gemm_plan(M, N, K, 0)
-        if p["sk_units"] > 0 and p["cluster"] == 1 and p["workspace_bytes"] <= (16 << 20):
-            return M, N, K
-    raise AssertionError("no stream-K shape found for this device")
-
-
 def _shapes():
-    return [(1, 4096, 4096), (16, 4096, 4096), (64, 4096, 4096), (32, 576, 7168), (3, 1000, 1000),
-            "stream-k"]
+    # M = 1: matrix-vector kernel; 16, 64: 128-wide tiles, clusters of 4;
+    # 200 x 2048: 256-wide tiles; 32 x 576: 128-wide, clusters of 8;
+    # 3 x 1000 x 1000: re-laid-out operands and scales in the scratch
+    return [(1, 4096, 4096), (16, 4096, 4096), (64, 4096, 4096), (200, 2048, 4096),
+            (32, 576, 7168), (3, 1000, 1000)]
 
 
 @pytest.mark.parametrize("shape", _shapes())
@@ -61,10 +57,7 @@ def test_noalloc_matches_the_regular_entry_point_twice_in_a_row(oracle_mod, dev,
     """Bit for bit equal to bfp8_gemm (same plan, same kernels) on two calls in
     a row -- the second call finds the first call's leftovers in the shared
     scratch -- and, once, within the GEMM acceptance of the oracle."""
-    M, N, K = _stream_k_shape() if shape == "stream-k" else shape
-    if shape == "stream-k":
-        plan = bf.bfp8_gemm_plan(M, N, K, 0)
-        assert plan["sk_units"] > 0 and plan["cluster"] == 1
+    M, N, K = shape
     case = wl.ragged_case(M, N, K, seed=11 * M + N)
     q, s = bf.bfp8_group_quant(case["x"].to(dev))
     B = case["B"].to(dev)
