@@ -9,7 +9,7 @@ and `metrics` holds the FLOP / byte accounting.
 """
 from ._binding import (  # noqa: F401
     BFP8Error, BFP8_OK, EXPORTS, GemmOptions,
-    KSPLIT_AUTO, KSPLIT_CLUSTER, KSPLIT_NONE, KSPLIT_STREAM_K,
+    KSPLIT_AUTO, KSPLIT_CLUSTER, KSPLIT_NONE, KSPLIT_STREAM_K, PAIRS_ALWAYS, PAIRS_AUTO, PAIRS_NEVER,
     SCALE_FP32, SCALE_UE8M0, SCHEDULE_AUTO, SCHEDULE_GEMV, SCHEDULE_SWAP_AB, SCHEDULE_WIDE,
     LIB_PATH, bfp8_device_status, bfp8_gemm, bfp8_gemm_fused, bfp8_gemm_grouped,
     bfp8_gemm_grouped_workspace_size, bfp8_gemm_plan, bfp8_linear, bfp8_linear_workspace_size, bfp8_gemm_workspace_size, bfp8_group_quant,

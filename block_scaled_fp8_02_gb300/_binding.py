@@ -22,6 +22,7 @@ BFP8_IN_F32 = 1
 SCALE_FP32, SCALE_UE8M0 = 0, 1
 SCHEDULE_AUTO, SCHEDULE_SWAP_AB, SCHEDULE_WIDE, SCHEDULE_GEMV = 0, 1, 2, 3
 KSPLIT_AUTO, KSPLIT_STREAM_K, KSPLIT_CLUSTER, KSPLIT_NONE = 0, 1, 2, 3
+PAIRS_AUTO, PAIRS_NEVER, PAIRS_ALWAYS = 0, 1, 2
 STATUS_NAMES = {0: "BFP8_OK", 1: "BFP8_ERR_INVALID_ARG", 2: "BFP8_ERR_ALIGNMENT",
                 3: "BFP8_ERR_UNSUPPORTED", 4: "BFP8_ERR_CUDA", 5: "BFP8_ERR_WORKSPACE",
                 6: "BFP8_ERR_DEVICE_TIMEOUT"}
@@ -44,7 +45,8 @@ class BFP8Error(RuntimeError):
 class GemmOptions(ctypes.Structure):
     _fields_ = [("schedule", ctypes.c_int), ("max_ctas", ctypes.c_int), ("tile_n", ctypes.c_int),
                 ("prefetch_weights", ctypes.c_int), ("k_split", ctypes.c_int),
-                ("cluster_size", ctypes.c_int), ("reserved", ctypes.c_int * 2)]
+                ("cluster_size", ctypes.c_int), ("pairs", ctypes.c_int),
+                ("reserved", ctypes.c_int * 1)]
 
 
 class PlanInfo(ctypes.Structure):
@@ -52,7 +54,7 @@ class PlanInfo(ctypes.Structure):
                 ("grid", ctypes.c_int), ("tiles", ctypes.c_int64), ("k_blocks", ctypes.c_int64),
                 ("dp_tiles", ctypes.c_int64), ("sk_units", ctypes.c_int64),
                 ("relayout", ctypes.c_int), ("workspace_bytes", ctypes.c_size_t),
-                ("cluster", ctypes.c_int), ("gemv", ctypes.c_int)]
+                ("cluster", ctypes.c_int), ("gemv", ctypes.c_int), ("pair", ctypes.c_int)]
 
 
 _lock = threading.Lock()
@@ -156,8 +158,9 @@ def _opts(options) -> ctypes.POINTER(GemmOptions) | None:
     o.prefetch_weights = int(options.get("prefetch_weights", 0))
     o.k_split = int(options.get("k_split", 0))
     o.cluster_size = int(options.get("cluster_size", 0))
+    o.pairs = int(options.get("pairs", 0))
     unknown = set(options) - {"schedule", "max_ctas", "tile_n", "prefetch_weights", "k_split",
-                              "cluster_size"}
+                              "cluster_size", "pairs"}
     if unknown:
         raise ValueError(f"unknown GEMM options {sorted(unknown)}")
     return ctypes.pointer(o)

@@ -19,7 +19,8 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libbfp8.so")
 SOURCES = ["bfp8_api.cu", "bfp8_quant.cu", "bfp8_gemm_swap.cu", "bfp8_gemm_wide.cu",
-           "bfp8_gemm_ext.cu", "bfp8_gemv.cu", "bfp8_noalloc.cu"]
+           "bfp8_gemm_ext.cu", "bfp8_gemm_pair.cu", "bfp8_gemv.cu",
+           "bfp8_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
          "--expt-relaxed-constexpr", "-I", os.path.join(ROOT, "include")]

@@ -199,6 +199,7 @@ struct Plan {
   int bn = 0;
   int mr = 128;              // wide tiles: activation rows loaded per stage
   bool gemv = false;         // the matrix-vector kernel (few activation rows)
+  bool pair = false;         // 256 x 256 tiles on CTA pairs (sched counts pairs)
   bool relayout = false;
   int64_t kp = 0;            // inner extent of the operand tensor maps
   Sched sched{};
@@ -227,6 +228,8 @@ bfp8_status check_options(const bfp8_gemm_options* opt) {
   if (opt->cluster_size != 0 && (opt->cluster_size < 2 || opt->cluster_size > kMaxCluster))
     return fail(BFP8_ERR_INVALID_ARG, "options.cluster_size = %d (expected 0 or 2..8)",
                 opt->cluster_size);
+  if (opt->pairs < 0 || opt->pairs > 2)
+    return fail(BFP8_ERR_INVALID_ARG, "options.pairs = %d (expected 0, 1 or 2)", opt->pairs);
   return BFP8_OK;
 }
 
@@ -365,6 +368,15 @@ bool gemv_preferred(int64_t N, int num_sms) {
   return 3 * tiles >= 2 * waves * slots;
 }
 
+// AUTO never takes the paired tiles: on this GPU they ran slower than 128-row
+// tiles at every size measured (N = K = 4096: M = 256 24.3 against 14.0 us,
+// M = 2048 47.2 against 37.9, M = 8192 155.2 against 124.1; M = 2048,
+// N = 5120, K = 25600 386.7 against 246.7).  Both kernels are bound by the
+// promotion warps, and a pair's promotion costs more per unit (its activation
+// scales come through a ring the warps wait on, its TMEM releases cross the
+// pair); whole-tile schedules on pairs also leave SMs idle at small M.
+bool pairs_preferred(int64_t /*M*/) { return false; }
+
 // `dev` = the device's cached properties, whose co-resident cluster counts
 // the planner uses (nullptr: host-only planning, counts estimated from
 // num_sms).  `experts` > 1: M-grouped mode, B and Bs hold that many experts'
@@ -406,7 +418,8 @@ bfp8_status make_plan(int64_t M, int64_t N, int64_t K, int num_sms, const bfp8_g
     p->bn = tn ? tn : swap_tile_n(M);
   } else if (tn) {
     p->bn = tn;
-  } else if (schedule == BFP8_SCHEDULE_AUTO && M <= kSwapMaxM && experts == 1) {
+  } else if (schedule == BFP8_SCHEDULE_AUTO && M <= kSwapMaxM && experts == 1 &&
+             !(opt && opt->pairs == BFP8_PAIRS_ALWAYS)) {
     // up to 256 rows: 256- or 128-wide tiles by the split model, a 128-wide
     // step weighted 0.7 of a 256-wide one (fitted to this GPU's times at
     // M = 9 .. 256 on the sweep and Qwen3-32B shapes; swap-AB tiles, the
@@ -436,6 +449,26 @@ bfp8_status make_plan(int64_t M, int64_t N, int64_t K, int num_sms, const bfp8_g
     p->sched = make_sched_whole_tiles(pt, qt, g32, mc);
   else
     p->sched = make_sched(pt, qt, g32, mc);
+  // 256 x 256 tiles on CTA pairs (bfp8_pairs), whole tiles over the pairs
+  const int pairs_opt = opt ? opt->pairs : BFP8_PAIRS_AUTO;
+  const int ks = opt ? opt->k_split : BFP8_KSPLIT_AUTO;
+  const bool pair_ok = !p->gemv && !p->swap && p->bn == 256 && p->mr == 128 && experts == 1 &&
+                       (ks == BFP8_KSPLIT_AUTO || ks == BFP8_KSPLIT_NONE);
+  if (pairs_opt == BFP8_PAIRS_ALWAYS && !pair_ok)
+    return fail(BFP8_ERR_UNSUPPORTED,
+                "options.pairs = ALWAYS needs a plain call on 256-wide tiles with more than 64 rows "
+                "and no explicit stream-K or cluster split (M=%lld N=%lld)", (long long)M, (long long)N);
+  if (pair_ok && (pairs_opt == BFP8_PAIRS_ALWAYS || (pairs_opt == BFP8_PAIRS_AUTO && pairs_preferred(M)))) {
+    int est2[kMaxCluster + 1];
+    if (!dev) estimate_cluster_caps(num_sms, 1, est2);
+    const int cap_pairs = dev ? dev->cluster_cap[2] : est2[2];
+    int64_t max_pairs = max_ctas / 2;
+    if (cap_pairs > 0 && cap_pairs < max_pairs) max_pairs = cap_pairs;
+    if (max_pairs < 1) max_pairs = 1;
+    p->pair = true;
+    p->sched = make_sched_whole_tiles(static_cast<uint32_t>(cdiv(M, 256)), static_cast<uint32_t>(cdiv(N, 256)),
+                                      g32, static_cast<uint32_t>(max_pairs));
+  }
   p->relayout = unaligned || (K % 16) != 0;
   p->kp = p->relayout ? cdiv(K, 16) * 16 : K;
   size_t off = 0;
@@ -613,8 +646,8 @@ bfp8_status bfp8_gemm_plan(int64_t M, int64_t N, int64_t K, int num_sms,
     return fail(BFP8_ERR_UNSUPPORTED, "more stream-K tiles than the workspace header holds");
   info->swap_ab = p.swap;
   info->tile_n = p.bn;
-  info->stages = gemm_stages(p.swap, p.bn, p.mr);
-  info->grid = p.sched.grid;
+  info->stages = p.pair ? gemm_pair_stages() : gemm_stages(p.swap, p.bn, p.mr);
+  info->grid = p.pair ? 2 * p.sched.grid : p.sched.grid;
   info->tiles = p.sched.tiles;
   info->k_blocks = p.sched.G;
   info->dp_tiles = p.sched.dp_tiles;
@@ -623,6 +656,7 @@ bfp8_status bfp8_gemm_plan(int64_t M, int64_t N, int64_t K, int num_sms,
   info->workspace_bytes = p.total;
   info->cluster = p.sched.cluster > 1 ? static_cast<int>(p.sched.cluster) : 1;
   info->gemv = p.gemv ? 1 : 0;
+  info->pair = p.pair ? 1 : 0;
   return ok();
 }
 
@@ -695,7 +729,10 @@ static bfp8_gemm_options effective_options(const bfp8_gemm_options* opt, bool gr
                                            bool fused) {
   bfp8_gemm_options o{};
   if (opt) o = *opt;
-  if (grouped || fused) o.schedule = BFP8_SCHEDULE_WIDE;
+  if (grouped || fused) {
+    o.schedule = BFP8_SCHEDULE_WIDE;
+    o.pairs = BFP8_PAIRS_NEVER;
+  }
   if (fused) o.k_split = BFP8_KSPLIT_STREAM_K;
   return o;
 }
@@ -801,7 +838,7 @@ static bfp8_status gemm_impl(const void* A, const void* B, const float* As, int 
   const int mode = psum ? kModeGrouped : (fused ? kModeFused : kModePlain);
   const int mr = mode == kModePlain ? p.mr : 128;
   if ((st = encode_operand(&tmP, p_ptr, p_rows, p.kp, p.swap ? 128 : mr)) != BFP8_OK) return st;
-  if ((st = encode_operand(&tmQ, q_ptr, q_rows, p.kp, p.bn)) != BFP8_OK) return st;
+  if ((st = encode_operand(&tmQ, q_ptr, q_rows, p.kp, p.pair ? p.bn / 2 : p.bn)) != BFP8_OK) return st;
 
   GemmArgs a{};
   a.As = as_k;
@@ -837,8 +874,9 @@ static bfp8_status gemm_impl(const void* A, const void* B, const float* As, int 
   a.err = d.err;
   a.wait_limit = kWaitLimitCycles;
   set_trace(&a);
-  cudaError_t e = p.swap ? launch_gemm_swap(p.bn, tmP, tmQ, a, cs)
-                         : launch_gemm_wide(p.bn, mode, mr, tmP, tmQ, a, cs);
+  cudaError_t e = p.pair ? launch_gemm_pair(tmP, tmQ, a, cs)
+                 : p.swap ? launch_gemm_swap(p.bn, tmP, tmQ, a, cs)
+                          : launch_gemm_wide(p.bn, mode, mr, tmP, tmQ, a, cs);
   if (e != cudaSuccess) return fail(BFP8_ERR_CUDA, "GEMM launch: %s", cudaGetErrorString(e));
   return ok();
 }

@@ -97,8 +97,14 @@ constexpr int kMaxExperts = 1024;   // psum entries cached in shared memory
 
 // Kernel variants (compile-time, so that the plain GEMM carries none of the
 // others' code): the plain GEMM, the M-grouped (MoE) GEMM and the GEMM with
-// the fused epilogue (the last two on wide tiles only).
-enum : int { kModePlain = 0, kModeGrouped = 1, kModeFused = 2 };
+// the fused epilogue (the last two on wide tiles only), and the paired plain
+// GEMM (256-wide tiles only): a 1-D cluster of two CTAs, the pair computing
+// 256 x 256 output tiles with 2-SM MMAs (tcgen05.mma.cta_group::2, M = 256).
+// Each CTA loads its 128 activation rows and half of the 256 weight rows of a
+// unit (32 KB against 48 KB unpaired, the per-SM operand ingest being what
+// bounds the unpaired tile); the even CTA issues the MMAs for both, and each
+// CTA promotes and stores its own 128 x 256 rows from its own TMEM.
+enum : int { kModePlain = 0, kModeGrouped = 1, kModeFused = 2, kModePair = 3 };
 
 // Expert of the 128-row tile starting at row m0: the first e with psum[e] >
 // m0 (psum in shared memory); past the last expert, the last one (its
@@ -129,6 +135,8 @@ struct GemmCfg {
   static_assert(MR == 128 || (!SWAP && MODE == kModePlain && (MR == 32 || MR == 64)),
                 "partial activation tiles: plain wide tiles, 32 or 64 rows");
   static constexpr int kMR = MR;
+  static constexpr bool kPair = !SWAP && MODE == kModePair;
+  static_assert(!kPair || (BN == 256 && MR == 128), "paired tiles: 256 wide, 128 rows per CTA");
   // promotion warps: 4 per 128 TMEM columns (16 on the 256-wide tile, 64
   // columns each, ran slower: fewer registers per thread, shallower ring)
   static constexpr int kNE = BN > 128 ? 8 : 4;
@@ -138,7 +146,10 @@ struct GemmCfg {
   // columns loaded per tcgen05.wait::ld: every wait costs a full TMEM load
   // latency, so batches are as large as the register budget allows
   // (64-column swap tiles: 32, so that two CTAs' registers fit on one SM)
-  static constexpr int kBatch = kNH == 2 ? 64 : (kCPT >= 64 ? (SWAP && BN == 64 ? 32 : 64) : kCPT);
+  // (paired tiles: 32, their scale ring and rank bookkeeping leave fewer
+  // registers to the promotion warps)
+  static constexpr int kBatch = (!SWAP && MODE == kModePair) ? 32
+                                : kNH == 2 ? 64 : (kCPT >= 64 ? (SWAP && BN == 64 ? 32 : 64) : kCPT);
   // 8 promotion warps: 12 warps in all so that warps 8..11 are one warpgroup
   // that gives registers to the promotion warpgroups (setmaxnreg).
   static constexpr int kWarps = kNE >= 8 ? kNE + 4 : kNE + 2;
@@ -148,7 +159,7 @@ struct GemmCfg {
   static constexpr int kRegsEpi = 232;
   static constexpr int kRegsOther = 40;
   static constexpr int kPBytes = (SWAP ? 128 : MR) * 128;
-  static constexpr int kQBytes = BN * 128;
+  static constexpr int kQBytes = (kPair ? BN / 2 : BN) * 128;   // paired: half the weight rows
   static constexpr int kStageBytes = kPBytes + kQBytes;
   // Scales: the producer bulk-copies each unit's activation-scale slice
   // (column-major, contiguous) into a kSR-deep ring of slots (the library
@@ -181,8 +192,11 @@ struct GemmCfg {
   // Swap tiles' scale ring runs ahead of the operand ring: the producer is at
   // most kStages units ahead of the MMAs, which are at most kTB units ahead of
   // the promotion, so kStages + kTB slots never hold it back.
-  static constexpr int kSRMax = SWAP ? 10 + kTB : 12;
-  static constexpr int kSRB = SWAP ? kSRMax : 0;   // scale-ring barriers (swap only)
+  // Paired tiles use the swap tiles' ring too: a unit's stage completes on
+  // the even CTA's barrier, so each CTA tracks its own scale copies.
+  static constexpr bool kRing = SWAP || kPair;
+  static constexpr int kSRMax = kRing ? 10 + kTB : 12;
+  static constexpr int kSRB = kRing ? kSRMax : 0;   // scale-ring barriers
   static constexpr int kAsFloats = SWAP ? BN : 128;
   static constexpr int kBsChunks = SWAP ? 1 : 0;
   static constexpr int kSlotFloats = kAsFloats + 4 * kBsChunks;
@@ -207,7 +221,7 @@ struct GemmCfg {
        kPsumBytes) / kStageBytes;
   static constexpr int kStages = kStagesFit > 10 ? 10 : kStagesFit;
   static_assert(kStages >= 2, "ring too small");
-  static constexpr int kSR = SWAP ? kStages + kTB : 12;
+  static constexpr int kSR = kRing ? kStages + kTB : 12;
   static_assert(kSR <= kSRMax, "scale ring");
   static constexpr int kScaleBytes = kSR * kSlotFloats * 4;
   static_assert(SWAP || kSR >= kStages + kTB, "wide scale slots reused too early");
@@ -234,7 +248,7 @@ struct GemmCfg {
   static constexpr int kPartLines = SWAP ? BN : 128;
   static_assert(kPartLines * kPartPitch * 4 <= kStages * kStageBytes,
                 "partial tile does not fit the ring");
-  static constexpr uint32_t kIdesc = idesc_e4m3_f32(128, BN);
+  static constexpr uint32_t kIdesc = idesc_e4m3_f32(kPair ? 256 : 128, BN);
 };
 
 // Optional timeline trace (compiled in only with -DBFP8_TRACE): %globaltimer
@@ -323,7 +337,15 @@ __global__ void __launch_bounds__(GemmCfg<BN, SWAP, MODE, MR>::kThreads,
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const Sched& s = a.sched;
-  const uint32_t cta = blockIdx.x;
+  constexpr bool kPair = C::kPair;
+  // paired tiles: the pair is the scheduling unit; rank 0 issues the MMAs
+  const uint32_t prank = kPair ? cluster_ctarank() : 0u;
+  const uint32_t cta = kPair ? blockIdx.x >> 1 : blockIdx.x;
+  // first output row of this CTA's share of the tile at p_tile
+  auto row0 = [&](uint32_t p_tile) -> int64_t {
+    return kPair ? static_cast<int64_t>(p_tile) * 256 + static_cast<int64_t>(prank) * 128
+                 : static_cast<int64_t>(p_tile) * 128;
+  };
 
   auto bar_full = [&](int i) { return sbase + C::kOffBars + 8u * i; };
   auto bar_empty = [&](int i) { return sbase + C::kOffBars + 8u * (C::kStages + i); };
@@ -357,7 +379,8 @@ __global__ void __launch_bounds__(GemmCfg<BN, SWAP, MODE, MR>::kThreads,
     }
     for (int b = 0; b < C::kTB; ++b) {
       mbar_init(bar_tfull(b), 1);
-      mbar_init(bar_tempty(b), C::kNE);      // one arrival per promotion warp
+      // one arrival per promotion warp (paired: of both CTAs, on rank 0's)
+      mbar_init(bar_tempty(b), kPair ? 2 * C::kNE : C::kNE);
     }
     *s_last_flag = 0;
     *s_fail = 0;
@@ -371,12 +394,15 @@ __global__ void __launch_bounds__(GemmCfg<BN, SWAP, MODE, MR>::kThreads,
   // streaming while the MMA warp allocates TMEM.  The TMEM address reaches the
   // MMA and promotion warps through named barrier 2 (producer not included).
   __syncthreads();
+  // paired tiles: both CTAs' barriers are initialised before either CTA's
+  // copies or arrivals reach the other's
+  if (kPair) cluster_sync();
   if (threadIdx.x == 0) {
-    trace_event(a.trace, cta, kTrStart);
+    trace_event(a.trace, blockIdx.x, kTrStart);
 #if defined(BFP8_TRACE)
     uint32_t smid;
     asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
-    trace_value(a.trace, cta, kTrSmid, smid);
+    trace_value(a.trace, blockIdx.x, kTrSmid, smid);
 #endif
   }
   // Everything above overlaps the tail of the preceding kernel in the stream
@@ -412,8 +438,13 @@ __global__ void __launch_bounds__(GemmCfg<BN, SWAP, MODE, MR>::kThreads,
   constexpr uint32_t kTmemSyncThreads = (C::kNE + 1) * 32;
   uint32_t tmem = 0;
   if (warp == C::kNE + 1) {
-    tmem_alloc(smem_addr(tmem_slot), C::kTmemCols);
-    tmem_relinquish();
+    if (kPair) {
+      tmem_alloc_pair(smem_addr(tmem_slot), C::kTmemCols);   // both CTAs, same address
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(smem_addr(tmem_slot), C::kTmemCols);
+      tmem_relinquish();
+    }
     tc_fence_before();
     named_bar_sync(2, kTmemSyncThreads);
     tc_fence_after();
@@ -441,19 +472,22 @@ __global__ void __launch_bounds__(GemmCfg<BN, SWAP, MODE, MR>::kThreads,
       // Scales of the unit at c (expert e): the As slice of its rows (wide) /
       // columns (swap) and the 16-byte chunk holding each weight scale, copied
       // into ring slot `slot`, completing on barrier `bar`.
+      // first row of the unit's As slice; a paired tile's second half may lie
+      // wholly past M (and past ld_as): it then copies row 0's slice instead,
+      // whose values no stored row uses
+      auto scale_m0 = [&](const Cursor& c) -> int64_t {
+        const int64_t m0 = SWAP ? static_cast<int64_t>(c.q_tile) * BN : row0(c.p_tile);
+        return m0 < a.ld_as ? m0 : 0;
+      };
       auto scale_as_bytes = [&](const Cursor& c) -> uint32_t {
-        const int64_t m0 = SWAP ? static_cast<int64_t>(c.q_tile) * BN
-                                : static_cast<int64_t>(c.p_tile) * 128;
-        int64_t n_as = a.ld_as - m0;                   // stay inside the As allocation
+        int64_t n_as = a.ld_as - scale_m0(c);          // stay inside the As allocation
         if (n_as > C::kAsFloats) n_as = C::kAsFloats;
         return static_cast<uint32_t>(n_as) * 4u;
       };
       auto copy_scales = [&](const Cursor& c, uint32_t e, int slot_idx, uint32_t bar) {
         const int64_t kb = c.kb;
         const uint32_t slot = sring + 4u * (slot_idx * C::kSlotFloats);
-        const int64_t m0 = SWAP ? static_cast<int64_t>(c.q_tile) * BN
-                                : static_cast<int64_t>(c.p_tile) * 128;
-        bulk_load(slot, a.As + kb * a.ld_as + m0, scale_as_bytes(c), bar);
+        bulk_load(slot, a.As + kb * a.ld_as + scale_m0(c), scale_as_bytes(c), bar);
 #pragma unroll
         for (int h = 0; h < C::kBsChunks; ++h) {
           int64_t nb = SWAP ? static_cast<int64_t>(c.p_tile)
@@ -463,9 +497,20 @@ __global__ void __launch_bounds__(GemmCfg<BN, SWAP, MODE, MR>::kThreads,
           bulk_load(slot + 4u * (C::kAsFloats + 4 * h), a.Bs + (ei & ~int64_t{3}), 16u, bar);
         }
       };
-      // wide tiles: bytes of a unit's stage barrier (operand tiles + scales)
+      // wide tiles: bytes of a unit's stage barrier (operand tiles + scales;
+      // paired: both CTAs' operand tiles, on rank 0's barrier)
       auto stage_tx = [&](const Cursor& c) -> uint32_t {
+        if (kPair) return 2u * C::kStageBytes;
         return C::kStageBytes + (SWAP ? 0u : scale_as_bytes(c) + 16u * C::kBsChunks);
+      };
+      // paired: this CTA's halves of the unit, counted on rank 0's barrier
+      auto pair_load_p = [&](int stg, const Cursor& c, int32_t x) {
+        tma_load_2d_pair(stage_p(stg), &tmP, mapa_shared(bar_full(stg), 0), x,
+                         static_cast<int32_t>(row0(c.p_tile)));
+      };
+      auto pair_load_q = [&](int stg, const Cursor& c, int32_t x) {
+        tma_load_2d_pair(stage_q(stg), &tmQ, mapa_shared(bar_full(stg), 0), x,
+                         static_cast<int32_t>(c.q_tile * BN + prank * (BN / 2)));
       };
       // With prefetch_b, the weight tiles of the first stages are requested
       // before waiting for the preceding grid; their stages are then completed
@@ -474,9 +519,11 @@ __global__ void __launch_bounds__(GemmCfg<BN, SWAP, MODE, MR>::kThreads,
       if (a.prefetch_b) {
         Cursor pc = cur;
         for (; pre < static_cast<uint32_t>(C::kStages) && pc.valid(); ++pre, pc.next()) {
-          mbar_arrive_expect_tx(bar_full(pre), stage_tx(pc));
+          if (prank == 0) mbar_arrive_expect_tx(bar_full(pre), stage_tx(pc));
           const int32_t x = static_cast<int32_t>(pc.kb * 128);
-          if (SWAP)
+          if (kPair)
+            pair_load_q(static_cast<int>(pre), pc, x);
+          else if (SWAP)
             tma_load_2d(stage_p(pre), &tmP, bar_full(pre), x, static_cast<int32_t>(pc.p_tile * 128));
           else
             tma_load_2d(stage_q(pre), &tmQ, bar_full(pre), x, static_cast<int32_t>(pc.q_tile * BN));
@@ -493,7 +540,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, SWAP, MODE, MR>::kThreads,
         // B rows of this tile's expert (grouped mode) start at e_cur * N
         const int32_t q_row = static_cast<int32_t>(static_cast<int64_t>(e_cur) * a.N) +
                               static_cast<int32_t>(cur.q_tile * BN);
-        if (SWAP) {
+        if (C::kRing) {
           if (!mbar_wait_bounded(bar_sempty(ss), sph ^ 1u, a.wait_limit)) {
             fail(kDevTimeoutProducer);
             break;
@@ -511,30 +558,37 @@ __global__ void __launch_bounds__(GemmCfg<BN, SWAP, MODE, MR>::kThreads,
         const int32_t x = static_cast<int32_t>(cur.kb * 128);
         if (issued < pre) {
           // weight tile already requested: add the activation tile
-          if (SWAP)
+          if (kPair)
+            pair_load_p(st, cur, x);
+          else if (SWAP)
             tma_load_2d(stage_q(st), &tmQ, bar_full(st), x, static_cast<int32_t>(cur.q_tile * BN));
           else
             tma_load_2d(stage_p(st), &tmP, bar_full(st), x, static_cast<int32_t>(cur.p_tile * 128));
+        } else if (kPair) {
+          if (prank == 0) mbar_arrive_expect_tx(bar_full(st), stage_tx(cur));
+          pair_load_p(st, cur, x);
+          pair_load_q(st, cur, x);
         } else {
           mbar_arrive_expect_tx(bar_full(st), stage_tx(cur));
           tma_load_2d(stage_p(st), &tmP, bar_full(st), x, static_cast<int32_t>(cur.p_tile * 128));
           tma_load_2d(stage_q(st), &tmQ, bar_full(st), x, SWAP ? static_cast<int32_t>(cur.q_tile * BN) : q_row);
         }
         // wide tiles: this unit's scales complete on the same stage barrier
-        if (!SWAP) copy_scales(cur, e_cur, static_cast<int>(issued % C::kSR), bar_full(st));
-        if (issued == 0) trace_event(a.trace, cta, kTrProdFirst);
+        if (!C::kRing) copy_scales(cur, e_cur, static_cast<int>(issued % C::kSR), bar_full(st));
+        if (issued == 0) trace_event(a.trace, blockIdx.x, kTrProdFirst);
         ++issued;
         if (++st == C::kStages) { st = 0; ph ^= 1u; }
       }
-      trace_event(a.trace, cta, kTrProdDone);
-      trace_value(a.trace, cta, kTrProdWait, t_wait);
+      trace_event(a.trace, blockIdx.x, kTrProdDone);
+      trace_value(a.trace, blockIdx.x, kTrProdWait, t_wait);
       // When every role finishes normally, every copy has landed (the MMA
       // issuer waited for each operand stage, the swap-tile promotion warps
       // for each scale slot); otherwise the copies are drained at the end.
       prod_issued = issued;
     } else if (warp == C::kNE + 1 && lane == 0) {
       // -------------------------------------------------------- MMA issuer
-      const uint32_t n = num_units(s, cta);
+      // (paired tiles: rank 0 issues for both CTAs; rank 1's lane idles)
+      const uint32_t n = (kPair && prank != 0) ? 0u : num_units(s, cta);
       int st = 0;
       uint32_t ph = 0;
       uint32_t done = 0;
@@ -554,25 +608,34 @@ __global__ void __launch_bounds__(GemmCfg<BN, SWAP, MODE, MR>::kThreads,
         }
         BFP8_ACC(t_data, c1);
         tc_fence_after();
-        if (j == 0) trace_event(a.trace, cta, kTrMmaFirst);
+        if (j == 0) trace_event(a.trace, blockIdx.x, kTrMmaFirst);
         const uint32_t d_tmem = tmem + static_cast<uint32_t>(b * BN);
         const uint64_t adesc = sdesc_k_sw128(stage_p(st));
         const uint64_t bdesc = sdesc_k_sw128(stage_q(st));
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
           // advancing 32 fp8 elements along K = 32 bytes = 2 descriptor units
-          mma_f8f6f4(d_tmem, adesc + 2u * k, bdesc + 2u * k, C::kIdesc, k > 0 ? 1u : 0u);
+          if (kPair)
+            mma_f8f6f4_pair(d_tmem, adesc + 2u * k, bdesc + 2u * k, C::kIdesc, k > 0 ? 1u : 0u);
+          else
+            mma_f8f6f4(d_tmem, adesc + 2u * k, bdesc + 2u * k, C::kIdesc, k > 0 ? 1u : 0u);
         }
-        mma_commit(bar_empty(st));
-        mma_commit(bar_tfull(b));
+        if (kPair) {
+          // both CTAs' stages are free and both halves of the tile are in TMEM
+          mma_commit_pair(bar_empty(st), static_cast<uint16_t>(3));
+          mma_commit_pair(bar_tfull(b), static_cast<uint16_t>(3));
+        } else {
+          mma_commit(bar_empty(st));
+          mma_commit(bar_tfull(b));
+        }
         done = j + 1;
         if (++st == C::kStages) { st = 0; ph ^= 1u; }
       }
-      trace_event(a.trace, cta, kTrMmaDone);
-      trace_value(a.trace, cta, kTrMmaWaitTmem, t_tmem);
-      trace_value(a.trace, cta, kTrMmaWaitData, t_data);
+      trace_event(a.trace, blockIdx.x, kTrMmaDone);
+      trace_value(a.trace, blockIdx.x, kTrMmaWaitTmem, t_tmem);
+      trace_value(a.trace, blockIdx.x, kTrMmaWaitData, t_data);
 #if defined(BFP8_TRACE)
-      trace_value(a.trace, cta, kTrMmaLoopCyc, static_cast<unsigned long long>(clock64() - cl0));
+      trace_value(a.trace, blockIdx.x, kTrMmaLoopCyc, static_cast<unsigned long long>(clock64() - cl0));
 #endif
       // The last commit fires when every MMA issued above has completed.
       if (done > 0 && done < n) {
@@ -585,8 +648,8 @@ __global__ void __launch_bounds__(GemmCfg<BN, SWAP, MODE, MR>::kThreads,
     if (s.cluster > 1) {
       // every thread of the cluster takes part in both cluster barriers of
       // the split-K reduction (see the promotion warps)
-      if (lane == 0 && warp == C::kNE) trace_event(a.trace, cta, kTrProdAtSync);
-      if (lane == 0 && warp == C::kNE + 1) trace_event(a.trace, cta, kTrMmaAtSync);
+      if (lane == 0 && warp == C::kNE) trace_event(a.trace, blockIdx.x, kTrProdAtSync);
+      if (lane == 0 && warp == C::kNE + 1) trace_event(a.trace, blockIdx.x, kTrMmaAtSync);
       cluster_sync();
       cluster_sync_relaxed();
     }
@@ -642,6 +705,11 @@ __global__ void __launch_bounds__(GemmCfg<BN, SWAP, MODE, MR>::kThreads,
                        ? __ldg(a.Bs + (static_cast<int64_t>(e_cur) * a.NT + nb) * s.G + kbl)
                        : 0.f;   // columns past N are not stored
         }
+        // paired tiles: this CTA's As slice comes through its own ring
+        if (kPair && !mbar_wait_bounded(bar_sfull(ss), sph, a.wait_limit)) {
+          fail(kDevTimeoutEpilogue);
+          break;
+        }
       } else {
         if (!mbar_wait_bounded(bar_sfull(ss), sph, a.wait_limit)) {
           fail(kDevTimeoutEpilogue);
@@ -661,8 +729,8 @@ __global__ void __launch_bounds__(GemmCfg<BN, SWAP, MODE, MR>::kThreads,
       tc_fence_after();
       BFP8_ACC(t_ewait, e1);
       BFP8_CLK(e2);
-      if (j == 0 && etid == 0) trace_event(a.trace, cta, kTrEpiFirst);
-      if (j + 1 == cur.n && etid == 0) trace_event(a.trace, cta, kTrEpiLoop);
+      if (j == 0 && etid == 0) trace_event(a.trace, blockIdx.x, kTrEpiFirst);
+      if (j + 1 == cur.n && etid == 0) trace_event(a.trace, blockIdx.x, kTrEpiLoop);
 
       if (cur.first()) {
 #pragma unroll
@@ -678,7 +746,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, SWAP, MODE, MR>::kThreads,
         if (!SWAP && c0 == 0) {
           // wide tiles: the scale slot landed before the MMAs were issued; it
           // is read while the first TMEM loads are in flight
-          const float* slot = sRing + (j % C::kSR) * C::kSlotFloats;
+          const float* slot = sRing + (kPair ? ss : static_cast<int>(j % C::kSR)) * C::kSlotFloats;
           const float bsv = __shfl_sync(0xffffffffu, bs_win, static_cast<int>(cur.kb - kb_win));
           sr = slot[r] * bsv;
         }
@@ -705,10 +773,13 @@ __global__ void __launch_bounds__(GemmCfg<BN, SWAP, MODE, MR>::kThreads,
       tc_fence_before();
       __syncwarp();
       if (lane == 0) {
-        mbar_arrive(bar_tempty(b));
-        if (SWAP) mbar_arrive(bar_sempty(ss));
+        // paired tiles: the buffer is free once both CTAs' warps have read it;
+        // rank 0's MMA lane counts them on its barrier
+        if (kPair) mbar_arrive_cluster(mapa_shared(bar_tempty(b), 0));
+        else mbar_arrive(bar_tempty(b));
+        if (C::kRing) mbar_arrive(bar_sempty(ss));
       }
-      if (SWAP) {
+      if (C::kRing) {
         if (++ss == C::kSR) { ss = 0; sph ^= 1u; }
       }
       BFP8_ACC(t_ework, e2);
@@ -886,7 +957,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, SWAP, MODE, MR>::kThreads,
         // past M and columns past N are not written
         uint8_t* stg = smem + C::kOffOut + warp * C::kOutTile;
         const uint32_t stg_s = smem_addr(stg);
-        const int32_t y = static_cast<int32_t>(cur.p_tile * 128 + quad * 32);
+        const int32_t y = static_cast<int32_t>(row0(cur.p_tile) + quad * 32);
         const int32_t x0 = static_cast<int32_t>(cur.q_tile * BN + col0);
 #pragma unroll
         for (int ch = 0; ch < C::kCPT; ch += 32) {
@@ -911,7 +982,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, SWAP, MODE, MR>::kThreads,
         // staging rows, 32 columns at a time; lanes 4i..4i+3 then store one
         // row's 64 contiguous bytes
         uint8_t* stg = smem + C::kOffOut + warp * C::kOutTile;
-        const int64_t mrow0 = static_cast<int64_t>(cur.p_tile) * 128 + quad * 32;
+        const int64_t mrow0 = row0(cur.p_tile) + quad * 32;
         const int64_t nbase = static_cast<int64_t>(cur.q_tile) * BN + col0;
 #pragma unroll
         for (int ch = 0; ch < C::kCPT; ch += 32) {
@@ -935,7 +1006,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, SWAP, MODE, MR>::kThreads,
           __syncwarp();
         }
       } else if (!SWAP) {
-        const int64_t m = static_cast<int64_t>(cur.p_tile) * 128 + r;
+        const int64_t m = row0(cur.p_tile) + r;
         if (m < m_lim) {
           __nv_bfloat16* row = a.out + m * a.N;
           const int64_t nbase = static_cast<int64_t>(cur.q_tile) * BN + col0;
@@ -977,9 +1048,9 @@ __global__ void __launch_bounds__(GemmCfg<BN, SWAP, MODE, MR>::kThreads,
       // (deterministic) through distributed shared memory and stores bf16.
       // The second barrier (relaxed: it orders nothing) keeps every CTA and
       // its shared memory alive until all reads of it are done.
-      if (etid == 0) trace_event(a.trace, cta, kTrEpiAtSync);
+      if (etid == 0) trace_event(a.trace, blockIdx.x, kTrEpiAtSync);
       cluster_sync();
-      if (etid == 0) trace_event(a.trace, cta, kTrClusterSync);
+      if (etid == 0) trace_event(a.trace, blockIdx.x, kTrClusterSync);
       BFP8_CLK(e4);
       const uint32_t cs = s.cluster;
       const uint32_t rank = cta % cs;            // 1-D clusters of consecutive CTAs
@@ -1057,15 +1128,15 @@ __global__ void __launch_bounds__(GemmCfg<BN, SWAP, MODE, MR>::kThreads,
         }
       }
       BFP8_ACC(t_efix, e4);
-      if (etid == 0) trace_event(a.trace, cta, kTrEpiReduced);
+      if (etid == 0) trace_event(a.trace, blockIdx.x, kTrEpiReduced);
       cluster_sync_relaxed();
     }
     if (etid == 0) {
-      trace_event(a.trace, cta, kTrEpiEnd);
-      trace_value(a.trace, cta, kTrEpiWaitCyc, t_ewait);
-      trace_value(a.trace, cta, kTrEpiWorkCyc, t_ework);
-      trace_value(a.trace, cta, kTrEpiScaleCyc, t_escale);
-      trace_value(a.trace, cta, kTrEpiFixCyc, t_efix);
+      trace_event(a.trace, blockIdx.x, kTrEpiEnd);
+      trace_value(a.trace, blockIdx.x, kTrEpiWaitCyc, t_ewait);
+      trace_value(a.trace, blockIdx.x, kTrEpiWorkCyc, t_ework);
+      trace_value(a.trace, blockIdx.x, kTrEpiScaleCyc, t_escale);
+      trace_value(a.trace, blockIdx.x, kTrEpiFixCyc, t_efix);
     }
   }
 
@@ -1074,8 +1145,11 @@ __global__ void __launch_bounds__(GemmCfg<BN, SWAP, MODE, MR>::kThreads,
   tc_fence_after();
   if (warp == C::kNE && lane == 0 && *s_fail) {
     // a role gave up: do not leave while copies into this CTA's shared memory
-    // may still be in flight
-    const uint32_t tail = prod_issued < static_cast<uint32_t>(C::kStages) ? prod_issued : C::kStages;
+    // may still be in flight (paired tiles: rank 0's stage barriers count
+    // both CTAs' operand copies, and rank 1 leaves only after the closing
+    // cluster barrier, which rank 0 reaches after draining them)
+    const uint32_t tail = (kPair && prank != 0) ? 0u
+                          : (prod_issued < static_cast<uint32_t>(C::kStages) ? prod_issued : C::kStages);
     for (uint32_t t = 0; t < tail; ++t) {
       const uint32_t j = prod_issued - 1 - t;
       if (!mbar_wait_bounded(bar_full(j % C::kStages), (j / C::kStages) & 1u, a.wait_limit)) {
@@ -1092,7 +1166,15 @@ __global__ void __launch_bounds__(GemmCfg<BN, SWAP, MODE, MR>::kThreads,
       }
     }
   }
-  if (warp == C::kNE + 1) tmem_dealloc(tmem, C::kTmemCols);
+  if (kPair) {
+    // rank 0's MMAs read rank 1's shared memory and both CTAs arrive on rank
+    // 0's barriers: neither leaves (nor frees the pair's TMEM) before both
+    // are done
+    cluster_sync();
+    if (warp == C::kNE + 1) tmem_dealloc_pair(tmem, C::kTmemCols);
+  } else if (warp == C::kNE + 1) {
+    tmem_dealloc(tmem, C::kTmemCols);
+  }
 #endif
 }
 
@@ -1147,7 +1229,8 @@ cudaError_t launch_instance(const CUtensorMap& tmP, const CUtensorMap& tmQ, cons
   cudaError_t e = configure_instance<BN, SWAP, MODE, MR>();
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg{};
-  cfg.gridDim = dim3(a.sched.grid);
+  // paired tiles: sched.grid counts pairs; each is a 1-D cluster of two CTAs
+  cfg.gridDim = dim3(a.sched.grid * (C::kPair ? 2u : 1u));
   cfg.blockDim = dim3(C::kThreads);
   cfg.dynamicSmemBytes = C::kSmemBytes;
   cfg.stream = stream;
@@ -1156,9 +1239,9 @@ cudaError_t launch_instance(const CUtensorMap& tmP, const CUtensorMap& tmQ, cons
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (a.sched.cluster > 1) {
+  if (C::kPair || a.sched.cluster > 1) {
     attr[1].id = cudaLaunchAttributeClusterDimension;
-    attr[1].val.clusterDim.x = a.sched.cluster;
+    attr[1].val.clusterDim.x = C::kPair ? 2u : a.sched.cluster;
     attr[1].val.clusterDim.y = 1;
     attr[1].val.clusterDim.z = 1;
     cfg.numAttrs = 2;

@@ -50,6 +50,12 @@ cudaError_t launch_gemv(const uint8_t* A, int64_t lda, const float* As, int as_c
                         int64_t ld_as, const uint8_t* B, const float* Bs, __nv_bfloat16* out, int M,
                         int64_t N, int64_t K, int prefetch_b, int num_sms, cudaStream_t stream);
 
+// The paired wide-tile GEMM (bfp8_gemm_pair.cu): sched.grid counts CTA pairs,
+// whole tiles of 256 x 256 only.
+cudaError_t launch_gemm_pair(const CUtensorMap& tmP, const CUtensorMap& tmQ, const GemmArgs& a,
+                             cudaStream_t stream);
+int gemm_pair_stages();
+
 // Clusters of `cs` GEMM CTAs the current device runs at once (bfp8_gemm_swap.cu),
 // for the instantiations sized for two CTAs per SM (swap-AB tiles up to 64
 // columns wide) or for the others (one CTA per SM).

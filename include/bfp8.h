@@ -144,6 +144,23 @@ typedef enum {
                                 waves) CTAs: nothing is split, some SMs may idle */
 } bfp8_ksplit;
 
+/* Wide tiles on CTA pairs: a 1-D cluster of two CTAs computes 256 x 256
+ * output tiles with 2-SM MMAs (tcgen05.mma.cta_group::2), each CTA loading its
+ * 128 activation rows and half of the 256 weight rows of every unit, so each
+ * SM takes in a third less operand data per FLOP than with 128 x 256 tiles.
+ * Whole tiles only (no k split), plain GEMM calls only (not grouped, not
+ * fused), tiles of 256 weight rows. */
+typedef enum {
+  BFP8_PAIRS_AUTO = 0,    /* when the planner prefers them: never in this
+                             version (they measured slower than 128 x 256
+                             tiles on every shape tried) */
+  BFP8_PAIRS_NEVER = 1,
+  BFP8_PAIRS_ALWAYS = 2   /* whenever the call allows them; BFP8_ERR_UNSUPPORTED
+                             when it does not (swap-AB or 128-wide tiles, at
+                             most 64 rows, an explicit stream-K or cluster
+                             split, grouped or fused calls) */
+} bfp8_pairs;
+
 /* Optional tuning / test controls; a NULL options pointer means all zero. */
 typedef struct {
   int schedule;        /* bfp8_schedule */
@@ -162,7 +179,8 @@ typedef struct {
   int cluster_size;    /* CLUSTER: CTAs per tile, 2..8, clamped to ceil(K/128);
                           0 = the size the cost model prefers among those with
                           tiles * size <= max_ctas */
-  int reserved[2];
+  int pairs;           /* bfp8_pairs: 256 x 256 tiles on CTA pairs (2-SM MMAs) */
+  int reserved[1];
 } bfp8_gemm_options;
 
 /*
@@ -240,6 +258,8 @@ typedef struct {
   int gemv;             /* 1: the matrix-vector kernel runs (BFP8_SCHEDULE_GEMV);
                            the tile fields above then describe the tensor-core
                            plan it replaces */
+  int pair;             /* 1: 256 x 256 tiles on CTA pairs (grid counts CTAs,
+                           tiles the 256 x 256 tiles) */
 } bfp8_plan_info;
 
 bfp8_status bfp8_gemm_plan(int64_t M, int64_t N, int64_t K, int num_sms,

@@ -334,3 +334,22 @@ def test_gemv_plans(L):
     assert bf.bfp8_gemm_plan(1, 576, 7168, 152)["gemv"] == 0        # 36 of 304
     assert bf.bfp8_gemm_plan(9, 4096, 4096, 152)["gemv"] == 0
     assert bf.bfp8_gemm_plan(1, 4096, 4096, 152, {"schedule": bf.SCHEDULE_SWAP_AB})["gemv"] == 0
+
+
+def test_pair_plans(L):
+    """Paired 256 x 256 tiles: plain calls on 256-wide tiles with more than 64
+    rows, whole tiles over the pairs; refused otherwise when forced."""
+    P = {"pairs": bf.PAIRS_ALWAYS}
+    p = bf.bfp8_gemm_plan(2048, 4096, 4096, 152, P)
+    assert p["pair"] == 1 and p["tiles"] == 8 * 16 and p["grid"] % 2 == 0 and p["sk_units"] == 0
+    p = bf.bfp8_gemm_plan(8192, 4096, 4096, 152, P)
+    assert p["pair"] == 1 and p["tiles"] == 32 * 16 and p["dp_tiles"] == p["tiles"]
+    assert bf.bfp8_gemm_plan(2048, 4096, 4096, 152, {"pairs": bf.PAIRS_NEVER})["pair"] == 0
+    assert bf.bfp8_gemm_plan(2048, 4096, 4096, 152, dict(P, max_ctas=10))["grid"] == 10
+    for M, o in ((64, {}), (2048, {"k_split": 1}), (2048, {"tile_n": 128}), (2048, {"schedule": 1})):
+        with pytest.raises(bf.BFP8Error):
+            bf.bfp8_gemm_plan(M, 4096, 4096, 152, dict(P, **o))
+    bad = bf.GemmOptions()
+    bad.pairs = 3
+    assert _gemm(L, opt=ctypes.pointer(bad)) == 1
+
