@@ -171,6 +171,28 @@ bfp8_status encode_operand(CUtensorMap* map, const void* ptr, int64_t rows, int6
   return BFP8_OK;
 }
 
+// Tensor map over a [rows, K] uint8 matrix (row stride K bytes, K % 128 == 0)
+// viewed as [rows][K / 128][128]: box 128 x 8 x box_rows, i.e. eight k-blocks
+// of box_rows rows, landing as [row][k-block][128 bytes]; 128-byte swizzle,
+// zero fill outside the matrix (rows past `rows`, k-blocks past K / 128).
+bfp8_status encode_kblocks(CUtensorMap* map, const void* ptr, int64_t rows, int64_t K,
+                           int box_rows) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc;
+  bfp8_status st = get_encoder(&enc);
+  if (st != BFP8_OK) return st;
+  const cuuint64_t dims[3] = {128u, static_cast<cuuint64_t>(K / 128), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[2] = {128u, static_cast<cuuint64_t>(K)};
+  const cuuint32_t box[3] = {128u, 8u, static_cast<cuuint32_t>(box_rows)};
+  const cuuint32_t estr[3] = {1u, 1u, 1u};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(ptr), dims, strides, box,
+                   estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    return fail(BFP8_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d) for [%lld x %lld] in k-blocks, box %d",
+                (int)r, (long long)rows, (long long)K, box_rows);
+  return BFP8_OK;
+}
+
 // Tensor map over the bf16 output [rows, cols] (row stride cols * 2 bytes,
 // 16-byte aligned), box 32 x 32 with the 64-byte swizzle, for the wide
 // tiles' TMA stores.
@@ -355,17 +377,18 @@ int swap_tile_n(int64_t M) {
 }
 
 constexpr int64_t kSwapMaxM = 256;
-// AUTO runs the matrix-vector kernel (for M <= kGemvMaxM) when its 16-row
-// tiles fill their waves of CTA slots (two per SM) to at least 2/3: it runs a
-// tile per CTA per wave, so a barely started last wave (e.g. 320 tiles on 304
-// slots) costs a whole wave.  Measured on this GPU at M = 1: N = K = 4096
-// (256 tiles) 6.1 against 8.9 us, N = 10240 (640 tiles) 14.9 against 18.5,
-// N = 51200 25.6 % faster; N = 5120, K = 25600 (320 tiles) 42.9 against 36.5.
-bool gemv_preferred(int64_t N, int num_sms) {
+// AUTO runs the warp-MMA kernel for M <= 8 (measured faster than the tcgen05
+// kernel on every decode and Qwen3-32B shape with K % 128 == 0: N = K = 4096
+// 5.6 against 8.8 us, N = 51200, K = 5120 42.3 against 64.2, N = 5120,
+// K = 25600 35.6 against 36.3, N = 576, K = 7168 6.1 against 7.6) and for
+// M <= 16 when its 16-row tiles fit in one wave of two CTAs per SM (N = K =
+// 4096 at M = 16: 7.5 against 9.0 us; beyond one wave the doubled MMA work
+// per weight byte and the last wave's imbalance lose, e.g. N = 5120,
+// K = 25600: 51 against 36 us).
+bool gemv_preferred(int64_t M, int64_t N, int num_sms) {
+  if (M <= 8) return true;
   const int64_t tiles = (N + 15) / 16;
-  const int64_t slots = 2 * static_cast<int64_t>(num_sms > 0 ? num_sms : 1);
-  const int64_t waves = (tiles + slots - 1) / slots;
-  return 3 * tiles >= 2 * waves * slots;
+  return M <= 16 && tiles <= 2 * static_cast<int64_t>(num_sms > 0 ? num_sms : 1);
 }
 
 // AUTO never takes the paired tiles: on this GPU they ran slower than 128-row
@@ -384,12 +407,12 @@ bool pairs_preferred(int64_t /*M*/) { return false; }
 bfp8_status make_plan(int64_t M, int64_t N, int64_t K, int num_sms, const bfp8_gemm_options* opt,
                       bool unaligned, const DevInfo* dev, Plan* p, int64_t experts = 1) {
   const int schedule = opt ? opt->schedule : BFP8_SCHEDULE_AUTO;
-  p->gemv = experts == 1 && !unaligned && K % 16 == 0 && M <= kGemvMaxM &&
+  p->gemv = experts == 1 && !unaligned && K % 128 == 0 && M <= kGemvMaxM &&
             (schedule == BFP8_SCHEDULE_GEMV ||
-             (schedule == BFP8_SCHEDULE_AUTO && gemv_preferred(N, num_sms)));
+             (schedule == BFP8_SCHEDULE_AUTO && gemv_preferred(M, N, num_sms)));
   if (schedule == BFP8_SCHEDULE_GEMV && !p->gemv)
     return fail(BFP8_ERR_UNSUPPORTED,
-                "options.schedule = GEMV needs M <= %d, K %% 16 == 0 and 16-byte aligned A and B "
+                "options.schedule = GEMV needs M <= %d, K %% 128 == 0 and 16-byte aligned A and B "
                 "(got M=%lld K=%lld)", kGemvMaxM, (long long)M, (long long)K);
   const int tn = opt ? opt->tile_n : 0;
   // swap-AB when asked for, and under AUTO only for the tile widths that
@@ -793,11 +816,25 @@ static bfp8_status gemm_impl(const void* A, const void* B, const float* As, int 
   }
   cudaStream_t cs = static_cast<cudaStream_t>(stream);
   if (p.gemv) {
-    // matrix-vector kernel: A, As (either layout), B and Bs read where they are
+    // warp-MMA kernel: A and B streamed by TMA in k-block boxes; As (either
+    // layout) and Bs read where they are
+    CUtensorMap tmW, tmX;
+    if ((st = encode_kblocks(&tmW, B, N, K, 16)) != BFP8_OK) return st;
+    if ((st = encode_kblocks(&tmX, A, M, K, static_cast<int>(M))) != BFP8_OK) return st;
+    GemvArgs ga{};
+    ga.As = As;
+    ga.ld_as = ld_as;
+    ga.as_col_major = as_col_major;
+    ga.Bs = Bs;
+    ga.out = static_cast<__nv_bfloat16*>(out);
+    ga.M = static_cast<int32_t>(M);
+    ga.N = N;
+    ga.G = K / 128;
+    ga.prefetch_b = (opt && opt->prefetch_weights == 1) ? 1 : 0;
+    ga.err = d.err;
+    ga.wait_limit = kWaitLimitCycles;
     const cudaError_t e =
-        launch_gemv(static_cast<const uint8_t*>(A), K, As, as_col_major, ld_as,
-                    static_cast<const uint8_t*>(B), Bs, static_cast<__nv_bfloat16*>(out),
-                    static_cast<int>(M), N, K, (opt && opt->prefetch_weights == 1) ? 1 : 0, d.sms, cs);
+        launch_gemv(tmW, tmX, ga, d.sms, (opt && opt->max_ctas > 0) ? opt->max_ctas : 0, cs);
     if (e != cudaSuccess) return fail(BFP8_ERR_CUDA, "GEMV launch: %s", cudaGetErrorString(e));
     return ok();
   }

@@ -38,21 +38,12 @@
 #include <atomic>
 #include <cstdint>
 
+#include "bfp8_devstatus.cuh"
 #include "bfp8_e4m3.cuh"
 #include "bfp8_ptx.cuh"
 #include "bfp8_sched.h"
 
 namespace bfp8 {
-
-// Device-side failure codes (the first failure of a launch wins).
-enum : int {
-  kDevOk = 0,
-  kDevTimeoutProducer = 1,
-  kDevTimeoutMma = 2,
-  kDevTimeoutEpilogue = 3,
-  kDevTimeoutTail = 4,
-  kDevBadGroupedLayout = 5,   // grouped_layout not non-decreasing multiples of 128
-};
 
 struct GemmArgs {
   // Tensor map over out ([M, N] bf16, box 32 x 32, 64-byte swizzle) for the
@@ -298,10 +289,6 @@ __device__ __forceinline__ void trace_value(unsigned long long*, uint32_t, int, 
 #define BFP8_CLK(var)
 #define BFP8_ACC(acc, since)
 #endif
-
-__device__ __forceinline__ void report_failure(int* err, int code) {
-  if (err != nullptr) atomicCAS(err, 0, code);
-}
 
 template <int N>
 __device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, uint32_t* v) {

@@ -1,30 +1,51 @@
-// bfp8_gemv.cu -- the blocked FP8 GEMM for a handful of activation rows
-// (M <= 8): a matrix-vector product bound by the weight stream.
+// bfp8_gemv.cu -- the blocked FP8 GEMM for a few activation rows (M <= 32):
+// a matrix-vector-like product bound by the weight stream.
 //
-// At M <= 8 the layer reads 16 MB of e4m3 weights (N = K = 4096) for at most
-// 0.27 GFLOP.  The tcgen05 kernel spreads 32 weight tiles over the SMs by
-// cluster split-K, with TMEM, a distributed reduction and one 128 x 16 MMA per
-// 4 KB of weights; here the contraction is small enough for the warp-level
-// tensor-core instruction mma.sync.m16n8k32 (e4m3 x e4m3 -> fp32), whose
-// operands come straight from registers: no shared-memory staging, no TMEM, no
-// clusters, no workspace.
+// At M <= 32 the layer reads 16.8 MB of e4m3 weights (N = K = 4096) for at
+// most 1.1 GFLOP.  Here the contraction runs on the warp-level tensor-core
+// instruction mma.sync.m16n8k32 (e4m3 x e4m3 -> fp32), with the weight rows
+// in its 16-row slot (swap-AB: N in the MMA's M slot) and up to four 8-column
+// groups of activation rows; no TMEM, no clusters, no workspace.
 //
-// A CTA (8 warps) owns 16 weight rows (output columns n0 .. n0 + 15); warp w
-// takes a contiguous 1/8 of the k-blocks.  Per k-block each lane loads 16
-// bytes of weight rows g and g + 8 (g = lane / 4) and 16 bytes of activation
-// row g at the same k offsets (64 bytes per group of 4 lanes, two 64-byte
-// windows per 128-wide k-block) and feeds them to two MMAs per window.  The
-// fragment slots are filled with the same absolute k positions on both
-// operands, so each MMA sums 32 exact e4m3 products per output, in fp32; the
-// four MMAs of a k-block start from zero, and the k-block's 16 x 8 partial is
-// scaled by Bs[n/128, kb] * As[m, kb] into an fp32 accumulator (the blocked
-// definition of the vLLM PR 49932 digest's matmul).  The 8 warps' partials
-// are added in warp order in shared memory (deterministic) and rounded to bf16.
+// The weights stream through TMA.  B [N, K] is viewed as [N][K/128][128]
+// bytes; one 3-D box is 16 weight rows x 8 k-blocks (16 KB, landing as
+// [row][k-block][128 bytes] with the 128-byte swizzle), and the activations
+// of the same 8 k-blocks come as one box of M rows: a stage.  A producer lane
+// keeps a ring of 3 .. 4 stages in flight (192 KB per SM), across tile
+// boundaries, so each SM has a large share of the weights requested at once
+// -- plain per-thread loads were limited by the requests a warp can keep
+// outstanding.  With the weight prefetch, the first ring of weights and
+// weight scales is requested before the preceding kernel completes.
+// A third role, the scale warp, reads each stage's scales (Bs of the tile's
+// 128-row block and As of the M rows, for its 8 k-blocks) with plain loads
+// several stages ahead and parks them in a per-stage slot that completes on
+// the stage's barrier: the MMA warps never wait on a global load (reading
+// the scales themselves, a few stages ahead, cost a third of the bandwidth
+// on long weight streams).
+//
+// A CTA (8 MMA warps, a TMA warp and a scale warp; two CTAs per SM for
+// M <= 16, one above, so that each SM keeps 192 KB in flight) takes 16-row
+// weight tiles n0 = 16 * (blockIdx.x + i * gridDim.x).  In every stage warp w
+// takes k-block w: lane (g = lane / 4, t = lane % 4) reads 16 bytes of weight
+// rows g and g + 8 at k = 16t and k = 64 + 16t of the block, and the same k of
+// activation row g of each column group, and issues four MMAs per group whose
+// fragment slots hold the same absolute k on both operands (the MMA's k order
+// is a permutation of the block's, which a dot product does not see), as two
+// chains of two that are added at the end.  The k-block's 16 x 8 partial is
+// scaled by Bs[n/128, kb] * As[m, kb] into fp32 accumulators (the blocked
+// definition of the vLLM PR 49932 digest's matmul).  At the end of a tile the
+// 8 warps' partials are added in warp order in shared memory (deterministic)
+// and rounded to bf16.
+//
+// Every barrier wait is bounded: a wait that gives up records
+// BFP8_DEV_TIMEOUT_* in the failure word and the kernel winds down.
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
 #include <cstdint>
 
+#include "bfp8_devstatus.cuh"
 #include "bfp8_internal.h"
 #include "bfp8_ptx.cuh"
 
@@ -32,8 +53,30 @@ namespace bfp8 {
 
 namespace {
 
-constexpr int kGemvWarps = 8;      // warps per CTA = k-slices of a 16-row tile
-constexpr int kAhead = 2;          // k-blocks of loads in flight ahead of the one in use
+constexpr int kGvWarps = 8;                 // MMA warps = k-blocks per stage
+constexpr int kGvThreads = (kGvWarps + 2) * 32;   // + TMA warp + scale warp
+constexpr int kGvRows = 16;                 // weight rows per tile
+constexpr int kGvBoxKb = 8;                 // k-blocks per TMA box = per stage
+constexpr int kGvRingPerSm = 192 * 1024;    // bytes of stages in flight per SM
+
+template <int NG>   // 8-column groups of activation rows (M <= 8 * NG)
+struct GvCfg {
+  static constexpr int kCtas = NG <= 2 ? 2 : 1;                 // CTAs per SM
+  static constexpr int kWBytes = kGvRows * kGvBoxKb * 128;      // one weight box
+  static constexpr int kXBytes = 8 * NG * kGvBoxKb * 128;       // room for one activation box
+  static constexpr int kStageBytes = kWBytes + kXBytes;         // 8 k-blocks
+  static constexpr int kStages = kGvRingPerSm / kCtas / kStageBytes;   // 4, 3, 4, 4
+  // scale slot of a stage: Bs of its 8 k-blocks, then As[k-block][column]
+  static constexpr int kScFloats = kGvBoxKb + kGvBoxKb * 8 * NG;
+  static constexpr int kRedPitch = 8 * NG + 1;                  // padded row of partials
+  static constexpr int kOffSc = kStages * kStageBytes;
+  static constexpr int kOffRed = kOffSc + kStages * kScFloats * 4;
+  static constexpr int kOffBar = kOffRed + kGvWarps * kGvRows * kRedPitch * 4;
+  static constexpr int kSmemBytes = kOffBar + 2 * kStages * 8 + 1024;   // + alignment slack
+  static_assert(kXBytes % 1024 == 0 && kWBytes % 1024 == 0, "swizzled boxes start on 1 KB");
+  static_assert(kScFloats % 4 == 0 && kOffBar % 8 == 0, "slot and barrier alignment");
+  static_assert(kCtas * (kSmemBytes + 1024) <= 228 * 1024, "shared memory per SM");
+};
 
 // d += a (16 x 32 e4m3, row) * b (32 x 8 e4m3, col), fp32.  Fragments: lane
 // (g = lane / 4, t = lane % 4) holds A rows g (a0, a2) and g + 8 (a1, a3) at
@@ -48,148 +91,297 @@ __device__ __forceinline__ void mma_e4m3_16x8x32(float (&d)[4], uint32_t a0, uin
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-// One k-block's operands for this lane: weight rows g and g + 8 and
-// activation row g, 16 bytes each, in each of the block's two windows, and
-// the k-block's scales (Bs of the 16 rows; As of this lane's two columns),
-// all requested kAhead k-blocks before they are used.
-struct KbWords {
-  uint4 w0[2], w1[2], x[2];
-  float sb, sa0, sa1;
-};
+// Byte offset, inside a box landed as [row][8 k-blocks][128 bytes] with the
+// 128-byte swizzle (16-byte chunk index XOR the 128-byte line index mod 8), of
+// chunk c of k-block j of row r.
+__device__ __forceinline__ uint32_t box_off(int r, int j, int c) {
+  const int line = r * kGvBoxKb + j;
+  return static_cast<uint32_t>(line * 128 + ((c ^ (line & 7)) << 4));
+}
 
-// Requires K % 16 == 0 and A, B 16-byte aligned (a 16-byte word of a row is
-// wholly inside or wholly past K).  M <= 8.  Persistent: CTA b takes the
-// 16-row tiles b, b + gridDim.x, ...; each warp walks the (tile, k-block)
-// positions of its k-slice through all of them, with the loads of the next
-// kAhead positions in flight (across tile boundaries too).
-__global__ void __launch_bounds__(kGemvWarps * 32, 2)
-    gemv_kernel(const uint8_t* __restrict__ A, int64_t lda, const float* __restrict__ As,
-                int32_t as_col_major, int64_t ld_as, const uint8_t* __restrict__ B,
-                const float* __restrict__ Bs, __nv_bfloat16* __restrict__ out, int32_t M, int64_t N,
-                int64_t K, int32_t prefetch_b) {
-  __shared__ float red[kGemvWarps][16][9];          // partial 16 x 8 tiles (padded)
+template <int NG>
+__global__ void __launch_bounds__(kGvThreads, GvCfg<NG>::kCtas)
+    gemv_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
+                const __grid_constant__ GemvArgs a) {
+  using C = GvCfg<NG>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  const uint32_t sbase = smem_addr(smem);
+  auto bar_full = [&](int s) { return sbase + static_cast<uint32_t>(C::kOffBar + 8 * s); };
+  auto bar_empty = [&](int s) {
+    return sbase + static_cast<uint32_t>(C::kOffBar + 8 * (C::kStages + s));
+  };
+  float* sc_slots = reinterpret_cast<float*>(smem + C::kOffSc);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int g = lane >> 2, t = lane & 3;
-  const int64_t G = (K + 127) / 128;
-  const int64_t tiles = (N + 15) / 16;
-  const int64_t step = gridDim.x;
-  const int64_t kb_begin = (G * warp) / kGemvWarps, kb_end = (G * (warp + 1)) / kGemvWarps;
-  const bool x_row = g < M;
-  const int c0 = 2 * t, c1 = 2 * t + 1;                 // this lane's output columns (m)
-  // (tile, kb) -> the position `ahead` k-blocks later in this warp's walk
-  auto advance = [&](int64_t& tile, int64_t& kb, int64_t ahead) {
-    if (kb_end <= kb_begin) return;                     // no k-slice: nothing to walk
-    kb += ahead;
-    while (kb >= kb_end) {
-      kb -= kb_end - kb_begin;
-      tile += step;
+  const int64_t G = a.G;
+  const int64_t tiles = (a.N + kGvRows - 1) / kGvRows;
+  const int64_t S = (G + kGvBoxKb - 1) / kGvBoxKb;            // stages per tile
+  const int64_t my_tiles =
+      tiles > blockIdx.x ? (tiles - 1 - blockIdx.x) / gridDim.x + 1 : 0;
+  const int64_t total = my_tiles * S;                         // stages of this CTA
+  // (tile, stage) cursor over this CTA's stages
+  auto advance = [&](int64_t& tile, int64_t& st) {
+    if (++st == S) {
+      st = 0;
+      tile += gridDim.x;
     }
   };
-  auto load_w = [&](int64_t tile, int64_t kb, KbWords& o) {
-    const int64_t r0 = tile * 16 + g, r1 = r0 + 8;
-    const bool live = tile < tiles;
-    o.sb = live ? __ldg(Bs + (tile / 8) * G + kb) : 0.f;
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const int64_t k = kb * 128 + h * 64 + t * 16;
-      const bool in = live && k < K;
-      o.w0[h] = (in && r0 < N) ? __ldg(reinterpret_cast<const uint4*>(B + r0 * K + k)) : make_uint4(0u, 0u, 0u, 0u);
-      o.w1[h] = (in && r1 < N) ? __ldg(reinterpret_cast<const uint4*>(B + r1 * K + k)) : make_uint4(0u, 0u, 0u, 0u);
+
+  if (threadIdx.x == kGvWarps * 32) {
+    for (int s = 0; s < C::kStages; ++s) {
+      mbar_init(bar_full(s), 1 + 32);          // TMA bytes + the scale warp's lanes
+      mbar_init(bar_empty(s), kGvWarps);
     }
-  };
-  auto load_x = [&](int64_t tile, int64_t kb, KbWords& o) {
-    const bool live = tile < tiles;
-    o.sa0 = (live && c0 < M) ? (as_col_major ? __ldg(As + kb * ld_as + c0) : __ldg(As + c0 * ld_as + kb)) : 0.f;
-    o.sa1 = (live && c1 < M) ? (as_col_major ? __ldg(As + kb * ld_as + c1) : __ldg(As + c1 * ld_as + kb)) : 0.f;
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const int64_t k = kb * 128 + h * 64 + t * 16;
-      o.x[h] = (live && k < K && x_row) ? __ldg(reinterpret_cast<const uint4*>(A + g * lda + k))
-                                        : make_uint4(0u, 0u, 0u, 0u);
-    }
-  };
-  const bool has_slice = kb_end > kb_begin;               // G < 8: some warps have none
-  KbWords ring[kAhead + 1];
-  // the weights are not written by the preceding kernel: with prefetch_b they
-  // are requested before waiting for it; the activations only after
-  if (prefetch_b && has_slice) {
-    int64_t tt = blockIdx.x, kk = kb_begin;
-#pragma unroll
-    for (int s = 0; s <= kAhead; ++s) {
-      load_w(tt, kk, ring[s]);
-      advance(tt, kk, 1);
-    }
+    fence_barrier_init();
   }
+  __syncthreads();
   griddep_launch_dependents();
-  griddep_wait();
-  if (has_slice) {
-    int64_t tt = blockIdx.x, kk = kb_begin;
-#pragma unroll
-    for (int s = 0; s <= kAhead; ++s) {
-      if (!prefetch_b) load_w(tt, kk, ring[s]);
-      load_x(tt, kk, ring[s]);
-      advance(tt, kk, 1);
-    }
-  }
-  for (int64_t tile = blockIdx.x; tile < tiles; tile += step) {
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};
-    for (int64_t kb = kb_begin; kb < kb_end; ++kb) {
-      float d[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const uint4 w0 = ring[0].w0[h], w1 = ring[0].w1[h], x = ring[0].x[h];
-        mma_e4m3_16x8x32(d, w0.x, w1.x, w0.y, w1.y, x.x, x.y);
-        mma_e4m3_16x8x32(d, w0.z, w1.z, w0.w, w1.w, x.z, x.w);
+
+  if (warp == kGvWarps) {
+    // ------------------------------------------------------------ TMA warp
+    if (lane != 0) return;
+    tma_prefetch_desc(&tmW);
+    tma_prefetch_desc(&tmX);
+    const uint32_t stage_bytes = static_cast<uint32_t>(C::kWBytes + a.M * kGvBoxKb * 128);
+    auto issue = [&](int64_t q, int64_t tile, int64_t st, bool w, bool x) {
+      const int slot = static_cast<int>(q % C::kStages);
+      const uint32_t stage = sbase + static_cast<uint32_t>(slot * C::kStageBytes);
+      const int32_t kb = static_cast<int32_t>(st * kGvBoxKb);
+      if (w) tma_load_3d(stage, &tmW, bar_full(slot), 0, kb, static_cast<int32_t>(tile * kGvRows));
+      if (x) tma_load_3d(stage + C::kWBytes, &tmX, bar_full(slot), 0, kb, 0);
+    };
+    int64_t q = 0, tile = blockIdx.x, st = 0;
+    if (a.prefetch_b) {
+      // the weights are not written by the preceding kernel: the first ring's
+      // worth is requested before waiting for it; the activations only after
+      const int64_t pre = total < C::kStages ? total : C::kStages;
+      for (; q < pre; ++q, advance(tile, st)) {
+        mbar_arrive_expect_tx(bar_full(static_cast<int>(q)), stage_bytes);
+        issue(q, tile, st, true, false);
       }
-      const float s0 = __fmul_rn(ring[0].sb, ring[0].sa0), s1 = __fmul_rn(ring[0].sb, ring[0].sa1);
-      acc[0] = fmaf(d[0], s0, acc[0]);
-      acc[1] = fmaf(d[1], s1, acc[1]);
-      acc[2] = fmaf(d[2], s0, acc[2]);
-      acc[3] = fmaf(d[3], s1, acc[3]);
-#pragma unroll
-      for (int s = 0; s < kAhead; ++s) ring[s] = ring[s + 1];
-      int64_t tt = tile, kk = kb;
-      advance(tt, kk, kAhead + 1);
-      load_w(tt, kk, ring[kAhead]);
-      load_x(tt, kk, ring[kAhead]);
+      griddep_wait();
+      int64_t t2 = blockIdx.x, s2 = 0;
+      for (int64_t p = 0; p < pre; ++p, advance(t2, s2)) issue(p, t2, s2, false, true);
+    } else {
+      griddep_wait();
     }
-    red[warp][g][c0] = acc[0];
-    red[warp][g][c1] = acc[1];
-    red[warp][g + 8][c0] = acc[2];
-    red[warp][g + 8][c1] = acc[3];
-    __syncthreads();
-    if (threadIdx.x < 128) {
-      const int row = threadIdx.x >> 3, col = threadIdx.x & 7;
-      float v = red[0][row][col];
-#pragma unroll
-      for (int w = 1; w < kGemvWarps; ++w) v += red[w][row][col];
-      const int64_t n = tile * 16 + row;
-      if (col < M && n < N) out[static_cast<int64_t>(col) * N + n] = __float2bfloat16_rn(v);
+    for (; q < total; ++q, advance(tile, st)) {
+      const int slot = static_cast<int>(q % C::kStages);
+      const uint32_t ph = static_cast<uint32_t>((q / C::kStages) & 1);
+      if (!mbar_wait_bounded(bar_empty(slot), ph ^ 1u, a.wait_limit)) {
+        report_failure(a.err, kDevTimeoutProducer);
+        break;
+      }
+      mbar_arrive_expect_tx(bar_full(slot), stage_bytes);
+      issue(q, tile, st, true, true);
     }
-    __syncthreads();                                      // red is reused by the next tile
+    // no copy may still be landing in shared memory when the CTA exits
+    for (int64_t p = q > C::kStages ? q - C::kStages : 0; p < q; ++p) {
+      if (!mbar_wait_bounded(bar_full(static_cast<int>(p % C::kStages)),
+                             static_cast<uint32_t>((p / C::kStages) & 1), a.wait_limit)) {
+        report_failure(a.err, kDevTimeoutTail);
+        break;
+      }
+    }
+    return;
+  }
+
+  if (warp == kGvWarps + 1) {
+    // ---------------------------------------------------------- scale warp
+    // lane holds elements lane + 32 i of each stage's slot, kD stages ahead
+    constexpr int kPer = (C::kScFloats + 31) / 32;
+    constexpr int kD = 4;
+    // part 1: the Bs elements (slot 0 .. 7), part 2: the As elements
+    auto load = [&](int64_t tile, int64_t st, float (&o)[kPer], int part) {
+      const bool live = tile < tiles;
+#pragma unroll
+      for (int i = 0; i < kPer; ++i) {
+        const int e = lane + 32 * i;
+        if (e < kGvBoxKb) {
+          if (part != 1) continue;
+          const int64_t kb = st * kGvBoxKb + e;
+          o[i] = (live && kb < G) ? __ldg(a.Bs + (tile >> 3) * G + kb) : 0.f;
+        } else {
+          if (part != 2) continue;
+          float v = 0.f;
+          if (live && e < C::kScFloats) {
+            const int kbc = (e - kGvBoxKb) / (8 * NG), m = (e - kGvBoxKb) % (8 * NG);
+            const int64_t kb = st * kGvBoxKb + kbc;
+            if (kb < G && m < a.M)
+              v = __ldg(a.as_col_major ? a.As + kb * a.ld_as + m : a.As + m * a.ld_as + kb);
+          }
+          o[i] = v;
+        }
+      }
+    };
+    float v[kD][kPer];
+    int64_t lt = blockIdx.x, ls = 0;
+    {
+      // Bs is not written by the preceding kernel: with the weight prefetch
+      // its first stages are requested before waiting for it; As only after
+      if (a.prefetch_b) {
+        int64_t t2 = blockIdx.x, s2 = 0;
+#pragma unroll
+        for (int d = 0; d < kD; ++d) {
+          load(t2, s2, v[d], 1);
+          advance(t2, s2);
+        }
+      }
+      griddep_wait();
+#pragma unroll
+      for (int d = 0; d < kD; ++d) {
+        if (!a.prefetch_b) load(lt, ls, v[d], 1);
+        load(lt, ls, v[d], 2);
+        advance(lt, ls);
+      }
+    }
+    for (int64_t q = 0; q < total; ++q) {
+      const int slot = static_cast<int>(q % C::kStages);
+      const uint32_t ph = static_cast<uint32_t>((q / C::kStages) & 1);
+      if (!mbar_wait_bounded(bar_empty(slot), ph ^ 1u, a.wait_limit)) {
+        report_failure(a.err, kDevTimeoutProducer);
+        break;
+      }
+      float* dst = sc_slots + slot * C::kScFloats;
+#pragma unroll
+      for (int i = 0; i < kPer; ++i)
+        if (lane + 32 * i < C::kScFloats) dst[lane + 32 * i] = v[0][i];
+      mbar_arrive(bar_full(slot));             // each lane releases its own stores
+#pragma unroll
+      for (int d = 0; d + 1 < kD; ++d)
+#pragma unroll
+        for (int i = 0; i < kPer; ++i) v[d][i] = v[d + 1][i];
+      load(lt, ls, v[kD - 1], 1);
+      load(lt, ls, v[kD - 1], 2);
+      advance(lt, ls);
+    }
+    return;
+  }
+
+  // ------------------------------------------------------------- MMA warps
+  const int g = lane >> 2, t = lane & 3;
+  // per-lane offsets inside a stage: weight rows g and g + 8, chunks t and
+  // t + 4 (k = 16t .., 64 + 16t ..) of k-block `warp`
+  const uint32_t w0a = box_off(g, warp, t);
+  const uint32_t w0b = box_off(g, warp, t + 4);
+  const uint32_t w1a = box_off(g + 8, warp, t);
+  const uint32_t w1b = box_off(g + 8, warp, t + 4);
+  uint32_t xa[NG], xb[NG];                   // activation row 8 grp + g (rows past M: row M-1)
+#pragma unroll
+  for (int grp = 0; grp < NG; ++grp) {
+    const int m = (8 * grp + g < a.M) ? 8 * grp + g : a.M - 1;
+    xa[grp] = C::kWBytes + box_off(m, warp, t);
+    xb[grp] = C::kWBytes + box_off(m, warp, t + 4);
+  }
+  // the output belongs to the preceding kernel's stream order
+  griddep_wait();
+  float* red = reinterpret_cast<float*>(smem + C::kOffRed);
+  float acc[NG][4];
+#pragma unroll
+  for (int grp = 0; grp < NG; ++grp) acc[grp][0] = acc[grp][1] = acc[grp][2] = acc[grp][3] = 0.f;
+  bool ok = true;
+  int64_t tile = blockIdx.x, st = 0;
+  for (int64_t q = 0; q < total; ++q, advance(tile, st)) {
+    const int slot = static_cast<int>(q % C::kStages);
+    if (ok && !mbar_wait_bounded(bar_full(slot), static_cast<uint32_t>((q / C::kStages) & 1),
+                                 a.wait_limit)) {
+      report_failure(a.err, kDevTimeoutEpilogue);
+      ok = false;
+    }
+    if (ok && st * kGvBoxKb + warp < G) {
+      const uint8_t* stage = smem + slot * C::kStageBytes;
+      const float* sc = sc_slots + slot * C::kScFloats;
+      const float sb = sc[warp];
+      const uint4 u0a = *reinterpret_cast<const uint4*>(stage + w0a);
+      const uint4 u0b = *reinterpret_cast<const uint4*>(stage + w0b);
+      const uint4 u1a = *reinterpret_cast<const uint4*>(stage + w1a);
+      const uint4 u1b = *reinterpret_cast<const uint4*>(stage + w1b);
+#pragma unroll
+      for (int grp = 0; grp < NG; ++grp) {
+        const uint4 va = *reinterpret_cast<const uint4*>(stage + xa[grp]);
+        const uint4 vb = *reinterpret_cast<const uint4*>(stage + xb[grp]);
+        // two independent chains of two MMAs (k = 16t .. and 64 + 16t ..)
+        float d[4] = {0.f, 0.f, 0.f, 0.f}, e[4] = {0.f, 0.f, 0.f, 0.f};
+        mma_e4m3_16x8x32(d, u0a.x, u1a.x, u0a.y, u1a.y, va.x, va.y);
+        mma_e4m3_16x8x32(e, u0b.x, u1b.x, u0b.y, u1b.y, vb.x, vb.y);
+        mma_e4m3_16x8x32(d, u0a.z, u1a.z, u0a.w, u1a.w, va.z, va.w);
+        mma_e4m3_16x8x32(e, u0b.z, u1b.z, u0b.w, u1b.w, vb.z, vb.w);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) d[i] += e[i];
+        const float2 sa = *reinterpret_cast<const float2*>(
+            sc + kGvBoxKb + warp * 8 * NG + 8 * grp + 2 * t);
+        const float s0 = __fmul_rn(sb, sa.x), s1 = __fmul_rn(sb, sa.y);
+        acc[grp][0] = fmaf(d[0], s0, acc[grp][0]);
+        acc[grp][1] = fmaf(d[1], s1, acc[grp][1]);
+        acc[grp][2] = fmaf(d[2], s0, acc[grp][2]);
+        acc[grp][3] = fmaf(d[3], s1, acc[grp][3]);
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bar_empty(slot));
+
+    if (st == S - 1) {
+      // tile done: the 8 warps' partials, added in warp order
+#pragma unroll
+      for (int grp = 0; grp < NG; ++grp) {
+        float* r0 = red + (warp * kGvRows + g) * C::kRedPitch + 8 * grp + 2 * t;
+        float* r1 = r0 + 8 * C::kRedPitch;
+        r0[0] = acc[grp][0];
+        r0[1] = acc[grp][1];
+        r1[0] = acc[grp][2];
+        r1[1] = acc[grp][3];
+        acc[grp][0] = acc[grp][1] = acc[grp][2] = acc[grp][3] = 0.f;
+      }
+      named_bar_sync(1, kGvWarps * 32);
+      for (int i = threadIdx.x; i < kGvRows * 8 * NG; i += kGvWarps * 32) {
+        const int m = i / kGvRows, r = i % kGvRows;     // consecutive threads: consecutive n
+        float v = red[r * C::kRedPitch + m];
+#pragma unroll
+        for (int w = 1; w < kGvWarps; ++w) v += red[(w * kGvRows + r) * C::kRedPitch + m];
+        const int64_t n = tile * kGvRows + r;
+        if (ok && m < a.M && n < a.N) a.out[static_cast<int64_t>(m) * a.N + n] = __float2bfloat16_rn(v);
+      }
+      named_bar_sync(1, kGvWarps * 32);              // red is rewritten by the next tile
+    }
   }
 }
 
-}  // namespace
-
-cudaError_t launch_gemv(const uint8_t* A, int64_t lda, const float* As, int as_col_major,
-                        int64_t ld_as, const uint8_t* B, const float* Bs, __nv_bfloat16* out, int M,
-                        int64_t N, int64_t K, int prefetch_b, int num_sms, cudaStream_t stream) {
-  if (M < 1 || M > kGemvMaxM) return cudaErrorInvalidValue;
-  // one wave: two CTAs per SM
-  int64_t blocks = (N + 15) / 16;
-  if (blocks > 2 * static_cast<int64_t>(num_sms)) blocks = 2 * static_cast<int64_t>(num_sms);
+template <int NG>
+cudaError_t launch_ng(const CUtensorMap& tmW, const CUtensorMap& tmX, const GemvArgs& a,
+                      int num_sms, int max_ctas, cudaStream_t stream) {
+  using C = GvCfg<NG>;
+  cudaError_t e = cudaFuncSetAttribute(gemv_kernel<NG>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       C::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  const int64_t tiles = (a.N + kGvRows - 1) / kGvRows;
+  int64_t slots = static_cast<int64_t>(C::kCtas) * num_sms;           // persistent
+  if (max_ctas > 0 && max_ctas < slots) slots = max_ctas;
+  const int64_t blocks = tiles < slots ? tiles : slots;
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(static_cast<unsigned>(blocks));
-  cfg.blockDim = dim3(kGemvWarps * 32);
+  cfg.blockDim = dim3(kGvThreads);
+  cfg.dynamicSmemBytes = C::kSmemBytes;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, gemv_kernel, A, lda, As, static_cast<int32_t>(as_col_major), ld_as,
-                            B, Bs, out, static_cast<int32_t>(M), N, K, static_cast<int32_t>(prefetch_b));
+  return cudaLaunchKernelEx(&cfg, gemv_kernel<NG>, tmW, tmX, a);
+}
+
+}  // namespace
+
+cudaError_t launch_gemv(const CUtensorMap& tmW, const CUtensorMap& tmX, const GemvArgs& a,
+                        int num_sms, int max_ctas, cudaStream_t stream) {
+  if (a.M < 1 || a.M > kGemvMaxM || a.N < 1 || a.G < 1 || num_sms < 1) return cudaErrorInvalidValue;
+  switch ((a.M + 7) / 8) {
+    case 1: return launch_ng<1>(tmW, tmX, a, num_sms, max_ctas, stream);
+    case 2: return launch_ng<2>(tmW, tmX, a, num_sms, max_ctas, stream);
+    case 3: return launch_ng<3>(tmW, tmX, a, num_sms, max_ctas, stream);
+    default: return launch_ng<4>(tmW, tmX, a, num_sms, max_ctas, stream);
+  }
 }
 
 }  // namespace bfp8

@@ -42,13 +42,26 @@ cudaError_t launch_gemm_wide_ext(int bn, int mode, const CUtensorMap& tmP, const
                                  const GemmArgs& a, cudaStream_t stream);
 
 // The GEMM for M <= kGemvMaxM activation rows on warp-level MMAs
-// (bfp8_gemv.cu): A [M, K] e4m3 with row stride lda, As in either layout,
-// B [N, K] e4m3 (row stride K), Bs [ceil(N/128), G]; K % 16 == 0 and A, B
-// 16-byte aligned.
-constexpr int kGemvMaxM = 8;
-cudaError_t launch_gemv(const uint8_t* A, int64_t lda, const float* As, int as_col_major,
-                        int64_t ld_as, const uint8_t* B, const float* Bs, __nv_bfloat16* out, int M,
-                        int64_t N, int64_t K, int prefetch_b, int num_sms, cudaStream_t stream);
+// (bfp8_gemv.cu).  tmW: B [N, K] e4m3 viewed as [N][K/128][128] bytes, box
+// 128 x 8 x 16 (eight k-blocks of 16 weight rows), 128-byte swizzle, zero
+// fill; tmX: A [M, K] viewed the same way, box 128 x 8 x M.  K % 128 == 0.
+constexpr int kGemvMaxM = 32;
+struct GemvArgs {
+  const float* As;       // activation scales, either layout (4-byte aligned)
+  int64_t ld_as;
+  int32_t as_col_major;
+  const float* Bs;       // [ceil(N/128), G]
+  __nv_bfloat16* out;    // [M, N] row-major
+  int32_t M;
+  int64_t N;
+  int64_t G;             // K / 128
+  int32_t prefetch_b;    // request the first weights before the grid dependency
+  int* err;              // device failure word
+  unsigned long long wait_limit;
+};
+// max_ctas > 0 caps the grid (persistent CTAs; two per SM for M <= 16).
+cudaError_t launch_gemv(const CUtensorMap& tmW, const CUtensorMap& tmX, const GemvArgs& a,
+                        int num_sms, int max_ctas, cudaStream_t stream);
 
 // The paired wide-tile GEMM (bfp8_gemm_pair.cu): sched.grid counts CTA pairs,
 // whole tiles of 256 x 256 only.

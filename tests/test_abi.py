@@ -319,20 +319,21 @@ def test_linear_rejects_bad_arguments_on_the_host(L):
 
 
 def test_gemv_plans(L):
-    """BFP8_SCHEDULE_GEMV: M <= 8, K % 16 == 0, aligned operands; else refused."""
+    """BFP8_SCHEDULE_GEMV: M <= 32, K % 128 == 0, aligned operands; else refused."""
     G = {"schedule": bf.SCHEDULE_GEMV}
-    for M in (1, 2, 3, 4, 8):
+    for M in (1, 2, 3, 4, 8, 9, 16, 24, 32):
         assert bf.bfp8_gemm_plan(M, 4096, 4096, 152, G)["gemv"] == 1
-    for M, N, K, kw in ((9, 4096, 4096, {}), (1, 4096, 1000, {}), (2, 64, 4096, {"operands_unaligned": True})):
+    for M, N, K, kw in ((33, 4096, 4096, {}), (1, 4096, 1000, {}), (1, 4096, 4112, {}),
+                        (2, 64, 4096, {"operands_unaligned": True})):
         with pytest.raises(bf.BFP8Error):
             bf.bfp8_gemm_plan(M, N, K, 152, G, **kw)
     assert bf.bfp8_gemm_plan(64, 4096, 4096, 152)["gemv"] == 0
-    # AUTO, M <= 8: when the 16-row tiles fill their waves of 2 x SM slots to 2/3
-    assert bf.bfp8_gemm_plan(1, 4096, 4096, 152)["gemv"] == 1       # 256 of 304
-    assert bf.bfp8_gemm_plan(8, 10240, 5120, 152)["gemv"] == 1      # 640 of 912
-    assert bf.bfp8_gemm_plan(1, 5120, 25600, 152)["gemv"] == 0      # 320 of 608
-    assert bf.bfp8_gemm_plan(1, 576, 7168, 152)["gemv"] == 0        # 36 of 304
-    assert bf.bfp8_gemm_plan(9, 4096, 4096, 152)["gemv"] == 0
+    # AUTO: M <= 8 always; M <= 16 when the 16-row tiles fit in one wave of 2 x SMs
+    for M, N, K in ((1, 4096, 4096), (8, 10240, 5120), (1, 5120, 25600), (1, 576, 7168),
+                    (9, 4096, 4096), (16, 4864, 4096)):
+        assert bf.bfp8_gemm_plan(M, N, K, 152)["gemv"] == 1, (M, N, K)
+    for M, N, K in ((16, 10240, 5120), (16, 4880, 4096), (17, 4096, 4096), (1, 4096, 4112)):
+        assert bf.bfp8_gemm_plan(M, N, K, 152)["gemv"] == 0, (M, N, K)
     assert bf.bfp8_gemm_plan(1, 4096, 4096, 152, {"schedule": bf.SCHEDULE_SWAP_AB})["gemv"] == 0
 
 

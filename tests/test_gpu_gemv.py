@@ -1,8 +1,8 @@
-"""GPU parity of the matrix-vector kernel for a few activation rows (M <= 8,
-BFP8_SCHEDULE_GEMV, warp-level MMAs): every output element against the
-oracle, on the decode sweep shape, the Qwen3-32B layer shapes, ragged N and K
-(a partial last 64-byte window and k-block, fewer k-blocks than warps), both
-scale layouts and weight prefetch."""
+"""GPU parity of the warp-MMA kernel for a few activation rows (M <= 32,
+BFP8_SCHEDULE_GEMV, TMA-fed mma.sync): every output element against the
+oracle, on the decode sweep shapes, the Qwen3-32B layer shapes, ragged M and
+N (a partial last weight tile, partial column groups, fewer k-blocks than a
+stage or a box holds), both scale layouts and weight prefetch."""
 import numpy as np
 import pytest
 import torch
@@ -40,37 +40,48 @@ def _run(oracle_mod, dev, case, col_major=True, options=GEMV, label=""):
     assert plan["gemv"] == 1
     out = bf.bfp8_gemm(A_d, B_d, As_d, Bs_d, options=options)
     torch.cuda.synchronize()
+    assert bf.bfp8_device_status() == 0
     ref = oracle_mod.blocked_gemm(A, B, As, col_major, Bs, want_abs=True)
     return check_gemm(out, ref, (K + 127) // 128, label=label)
 
 
-@pytest.mark.parametrize("M", [1, 2, 3, 4, 5, 7, 8])
+@pytest.mark.parametrize("M", [1, 2, 3, 4, 5, 7, 8, 9, 12, 16, 17, 24, 25, 31, 32])
 def test_decode_sweep_shape(oracle_mod, dev, M):
     _run(oracle_mod, dev, wl.linear_case(M, 4096, 4096, seed=100 + M), label=f"gemv decode M={M}")
 
 
+@pytest.mark.parametrize("M", [1, 16])
 @pytest.mark.parametrize("layer", list(wl.QWEN3_32B_LAYERS))
-def test_qwen3_32b_layers_m1(oracle_mod, dev, layer):
+def test_qwen3_32b_layers(oracle_mod, dev, layer, M):
     N, K = wl.QWEN3_32B_LAYERS[layer]
-    _run(oracle_mod, dev, wl.linear_case(1, N, K, seed=N + K), label=f"gemv {layer} M=1")
+    _run(oracle_mod, dev, wl.linear_case(M, N, K, seed=N + K + M), label=f"gemv {layer} M={M}")
 
 
-@pytest.mark.parametrize("M,N,K", [(1, 1, 16), (2, 130, 144), (3, 1000, 1040), (4, 576, 7168),
-                                   (1, 300, 528), (8, 129, 4112), (6, 8, 2000 + 16 * 3),
-                                   (8, 4100, 1024)])
+@pytest.mark.parametrize("M,N,K", [(1, 1, 128), (2, 130, 256), (3, 1000, 1024), (4, 576, 7168),
+                                   (1, 300, 640), (8, 129, 4224), (6, 8, 2048 + 128),
+                                   (8, 4100, 1024), (13, 1000, 7168), (32, 200, 384),
+                                   (20, 4100, 1152), (27, 16, 512 + 128 * 3)])
 @pytest.mark.parametrize("col_major", [True, False])
 def test_ragged(oracle_mod, dev, M, N, K, col_major):
     _run(oracle_mod, dev, wl.ragged_case(M, N, K, seed=M + N + K), col_major,
          label=f"gemv ragged {M}x{N}x{K}")
 
 
-def test_prefetch_weights(oracle_mod, dev):
-    _run(oracle_mod, dev, wl.linear_case(2, 4096, 4096, seed=5),
-         options=dict(GEMV, prefetch_weights=1), label="gemv prefetch")
+@pytest.mark.parametrize("M", [2, 24])
+def test_prefetch_weights(oracle_mod, dev, M):
+    _run(oracle_mod, dev, wl.linear_case(M, 4096, 4096, seed=5 + M),
+         options=dict(GEMV, prefetch_weights=1), label=f"gemv prefetch M={M}")
+
+
+@pytest.mark.parametrize("M,max_ctas", [(5, 1), (5, 3), (1, 7), (13, 5), (30, 2)])
+def test_max_ctas(oracle_mod, dev, M, max_ctas):
+    """Few persistent CTAs: many tiles per CTA, the stage ring wraps many times."""
+    _run(oracle_mod, dev, wl.linear_case(M, 1000, 2048 + 384, seed=M + max_ctas),
+         options=dict(GEMV, max_ctas=max_ctas), label=f"gemv M={M} max_ctas={max_ctas}")
 
 
 def test_deterministic(dev):
-    case = wl.linear_case(6, 2048, 4096, seed=9)
+    case = wl.linear_case(20, 2048, 4096, seed=9)
     q, s = bf.bfp8_group_quant(case["x"].to(dev))
     B, Bs = case["B"].to(dev), case["Bs"].to(dev)
     outs = [bf.bfp8_gemm(q, B, s, Bs, options=GEMV).clone() for _ in range(4)]
