@@ -23,8 +23,8 @@
 // the scales themselves, a few stages ahead, cost a third of the bandwidth
 // on long weight streams).
 //
-// A CTA (8 MMA warps, a TMA warp and a scale warp; two CTAs per SM for
-// M <= 16, one above, so that each SM keeps 192 KB in flight) takes 16-row
+// A CTA (8 MMA warps, a TMA warp and a scale warp; two or three CTAs per SM
+// for M <= 16, one above, so that each SM keeps ~192 KB in flight) takes 16-row
 // weight tiles n0 = 16 * (blockIdx.x + i * gridDim.x).  In every stage warp w
 // takes k-block w: lane (g = lane / 4, t = lane % 4) reads 16 bytes of weight
 // rows g and g + 8 at k = 16t and k = 64 + 16t of the block, and the same k of
@@ -59,13 +59,16 @@ constexpr int kGvRows = 16;                 // weight rows per tile
 constexpr int kGvBoxKb = 8;                 // k-blocks per TMA box = per stage
 constexpr int kGvRingPerSm = 192 * 1024;    // bytes of stages in flight per SM
 
-template <int NG>   // 8-column groups of activation rows (M <= 8 * NG)
+// NG: 8-column groups of activation rows (M <= 8 * NG); CTAS: CTAs per SM
+template <int NG, int CTAS>
 struct GvCfg {
-  static constexpr int kCtas = NG <= 2 ? 2 : 1;                 // CTAs per SM
+  static constexpr int kCtas = CTAS;
   static constexpr int kWBytes = kGvRows * kGvBoxKb * 128;      // one weight box
   static constexpr int kXBytes = 8 * NG * kGvBoxKb * 128;       // room for one activation box
   static constexpr int kStageBytes = kWBytes + kXBytes;         // 8 k-blocks
-  static constexpr int kStages = kGvRingPerSm / kCtas / kStageBytes;   // 4, 3, 4, 4
+  static constexpr int kStages = kGvRingPerSm / kCtas / kStageBytes;
+  // stages of scales the scale warp has in flight
+  static constexpr int kScAhead = kCtas >= 3 ? 2 : 4;
   // scale slot of a stage: Bs of its 8 k-blocks, then As[k-block][column]
   static constexpr int kScFloats = kGvBoxKb + kGvBoxKb * 8 * NG;
   static constexpr int kRedPitch = 8 * NG + 1;                  // padded row of partials
@@ -99,11 +102,11 @@ __device__ __forceinline__ uint32_t box_off(int r, int j, int c) {
   return static_cast<uint32_t>(line * 128 + ((c ^ (line & 7)) << 4));
 }
 
-template <int NG>
-__global__ void __launch_bounds__(kGvThreads, GvCfg<NG>::kCtas)
+template <int NG, int CTAS>
+__global__ void __launch_bounds__(kGvThreads, CTAS)
     gemv_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
                 const __grid_constant__ GemvArgs a) {
-  using C = GvCfg<NG>;
+  using C = GvCfg<NG, CTAS>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -191,7 +194,7 @@ __global__ void __launch_bounds__(kGvThreads, GvCfg<NG>::kCtas)
     // ---------------------------------------------------------- scale warp
     // lane holds elements lane + 32 i of each stage's slot, kD stages ahead
     constexpr int kPer = (C::kScFloats + 31) / 32;
-    constexpr int kD = 4;
+    constexpr int kD = C::kScAhead;
     // part 1: the Bs elements (slot 0 .. 7), part 2: the As elements
     auto load = [&](int64_t tile, int64_t st, float (&o)[kPer], int part) {
       const bool live = tile < tiles;
@@ -347,12 +350,12 @@ __global__ void __launch_bounds__(kGvThreads, GvCfg<NG>::kCtas)
   }
 }
 
-template <int NG>
+template <int NG, int CTAS>
 cudaError_t launch_ng(const CUtensorMap& tmW, const CUtensorMap& tmX, const GemvArgs& a,
                       int num_sms, int max_ctas, cudaStream_t stream) {
-  using C = GvCfg<NG>;
-  cudaError_t e = cudaFuncSetAttribute(gemv_kernel<NG>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       C::kSmemBytes);
+  using C = GvCfg<NG, CTAS>;
+  cudaError_t e = cudaFuncSetAttribute(gemv_kernel<NG, CTAS>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;
   const int64_t tiles = (a.N + kGvRows - 1) / kGvRows;
   int64_t slots = static_cast<int64_t>(C::kCtas) * num_sms;           // persistent
@@ -368,7 +371,7 @@ cudaError_t launch_ng(const CUtensorMap& tmW, const CUtensorMap& tmX, const Gemv
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, gemv_kernel<NG>, tmW, tmX, a);
+  return cudaLaunchKernelEx(&cfg, gemv_kernel<NG, CTAS>, tmW, tmX, a);
 }
 
 }  // namespace
@@ -376,11 +379,20 @@ cudaError_t launch_ng(const CUtensorMap& tmW, const CUtensorMap& tmX, const Gemv
 cudaError_t launch_gemv(const CUtensorMap& tmW, const CUtensorMap& tmX, const GemvArgs& a,
                         int num_sms, int max_ctas, cudaStream_t stream) {
   if (a.M < 1 || a.M > kGemvMaxM || a.N < 1 || a.G < 1 || num_sms < 1) return cudaErrorInvalidValue;
+  // M <= 8: two CTAs per SM with a 4-stage ring (a 4096-deep tile in flight
+  // at once) while the tiles fit in one such wave, else three with a 2-stage
+  // ring (more streams per SM, a shorter last wave): measured N = K = 4096
+  // 6.2 against 6.8 us, N = 5120, K = 25600 42.7 against 32.0, N = 51200,
+  // K = 5120 50.3 against 44.9 (two against three)
+  const int64_t tiles = (a.N + kGvRows - 1) / kGvRows;
   switch ((a.M + 7) / 8) {
-    case 1: return launch_ng<1>(tmW, tmX, a, num_sms, max_ctas, stream);
-    case 2: return launch_ng<2>(tmW, tmX, a, num_sms, max_ctas, stream);
-    case 3: return launch_ng<3>(tmW, tmX, a, num_sms, max_ctas, stream);
-    default: return launch_ng<4>(tmW, tmX, a, num_sms, max_ctas, stream);
+    case 1:
+      return tiles > 2 * static_cast<int64_t>(num_sms)
+                 ? launch_ng<1, 3>(tmW, tmX, a, num_sms, max_ctas, stream)
+                 : launch_ng<1, 2>(tmW, tmX, a, num_sms, max_ctas, stream);
+    case 2: return launch_ng<2, 2>(tmW, tmX, a, num_sms, max_ctas, stream);
+    case 3: return launch_ng<3, 1>(tmW, tmX, a, num_sms, max_ctas, stream);
+    default: return launch_ng<4, 1>(tmW, tmX, a, num_sms, max_ctas, stream);
   }
 }
 

@@ -60,7 +60,8 @@ def test_qwen3_32b_layers(oracle_mod, dev, layer, M):
 @pytest.mark.parametrize("M,N,K", [(1, 1, 128), (2, 130, 256), (3, 1000, 1024), (4, 576, 7168),
                                    (1, 300, 640), (8, 129, 4224), (6, 8, 2048 + 128),
                                    (8, 4100, 1024), (13, 1000, 7168), (32, 200, 384),
-                                   (20, 4100, 1152), (27, 16, 512 + 128 * 3)])
+                                   (20, 4100, 1152), (27, 16, 512 + 128 * 3), (7, 5000, 1152),
+                                   (3, 6000, 128 * 3)])
 @pytest.mark.parametrize("col_major", [True, False])
 def test_ragged(oracle_mod, dev, M, N, K, col_major):
     _run(oracle_mod, dev, wl.ragged_case(M, N, K, seed=M + N + K), col_major,
