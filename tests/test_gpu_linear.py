@@ -48,6 +48,8 @@ def _quant_then_gemm(x, B, Bs, options):
     (4, 4096, 4096, 3, None),          # rows of x not 16-byte aligned
     (100, 1000, 1024, 0, {"k_split": 1}),
     (1, 5120, 25600, 0, None),
+    (8, 1000, 128, 0, None), (5, 4100, 384, 8, None), (13, 2000, 1152, 0, None),
+    (7, 16, 4096, 0, {"max_ctas": 3}), (2, 51200, 5120, 0, None),
     (2048, 4096, 4096, 0, None)])
 def test_bfp8_linear(oracle_mod, dev, M, N, K, ld_pad, options):
     """bfp8_linear (one library call: quantisation into the workspace, then
