@@ -985,7 +985,62 @@ def measure_extensions(dev):
         "config": {"M": M, "N": N, "K": K, "bias": True, "outputs": "e4m3 codes + scales"},
         "fused_us": round(t_f, 2), "unfused_us": round(t_u, 2),
         "unfused": "GEMM (bf16 out) -> torch bf16 bias add -> bfp8_group_quant"}
+    res["sm_budget"] = measure_sm_budget(dev)
     return res
+
+
+def measure_sm_budget(dev):
+    """SM budget (options.max_ctas): a compute-bound GEMM (M=2048, N=K=4096)
+    capped to fewer CTAs, co-running on a second stream with an independent
+    HBM-bound quantisation (M=8192, K=4096), against the two run back to back
+    on one stream (CUDA-graph replays, inputs resident)."""
+    import torch
+    import block_scaled_fp8_02_gb300 as bf
+    from block_scaled_fp8_02_gb300 import workloads as wl
+    M, N, K = 2048, 4096, 4096
+    lc = wl.linear_case(M, N, K, seed=23)
+    q, s = bf.bfp8_group_quant(lc["x"].to(dev))
+    B, Bs = lc["B"].to(dev), lc["Bs"].to(dev)
+    y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    Mq, Kq = 8192, 4096
+    x2 = wl.activations(Mq, Kq, seed=24).to(dev)
+    q2 = torch.empty((Mq, Kq), dtype=torch.float8_e4m3fn, device=dev)
+    s2 = torch.empty((Kq // 128, bf.bfp8_scale_ld(Mq)), dtype=torch.float32, device=dev)
+    ws = torch.zeros(bf.bfp8_gemm_workspace_size(M, N, K) + (1 << 20), dtype=torch.uint8, device=dev)
+    side = torch.cuda.Stream()
+
+    def gemm(cap):
+        bf.bfp8_gemm(q, B, s, Bs, out=y, workspace=ws, options={"max_ctas": cap} if cap else None)
+
+    def quant():
+        bf.bfp8_group_quant(x2, q=q2, s_storage=s2)
+
+    def both(cap):
+        main = torch.cuda.current_stream()
+        fork = torch.cuda.Event()
+        fork.record(main)
+        side.wait_event(fork)
+        with torch.cuda.stream(side):
+            quant()
+        gemm(cap)
+        join = torch.cuda.Event()
+        join.record(side)
+        main.wait_event(join)
+
+    t_q = _graph_time_us(quant)
+    out = {"config": {"gemm": {"M": M, "N": N, "K": K}, "quant": {"M": Mq, "K": Kq},
+                      "sms": torch.cuda.get_device_properties(dev).multi_processor_count},
+           "quant_alone_us": round(t_q, 2)}
+    rows = []
+    for cap in (0, 120, 104, 88):
+        t_g = _graph_time_us(lambda: gemm(cap))
+        t_s = _graph_time_us(lambda: (gemm(cap), quant()))
+        t_c = _graph_time_us(lambda: both(cap))
+        rows.append({"max_ctas": cap or "auto", "grid": bf.bfp8_gemm_plan(M, N, K, 0, {"max_ctas": cap})["grid"],
+                     "gemm_alone_us": round(t_g, 2), "back_to_back_us": round(t_s, 2),
+                     "co_running_us": round(t_c, 2)})
+    out["by_cap"] = rows
+    return out
 
 
 # ------------------------------------------------------------ reference ----
