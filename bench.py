@@ -568,7 +568,7 @@ def run_ours(args, rank, world, local):
             "quant_p50_us": round(pq, 3), "quant_hot_p50_us": round(pqh, 3),
             "quant_gbs": round(mt.quant_bytes(M, K) / (pq * 1e-6) / 1e9, 1),
             "layer_p50_us": round(pl, 3),
-            "schedule": "gemv/mma.sync-m16n8k32" if plan.get("gemv") else
+            "schedule": "warp-mma/tma+mma.sync-m16n8k32" if plan.get("gemv") else
                         ("swap_ab" if plan["swap_ab"] else "wide") + f"/n{plan['tile_n']}"
                         + (f"/cluster{plan['cluster']}" if plan["cluster"] > 1
                            else ("/stream-k" if plan["sk_units"] else "/whole-tiles")),

@@ -121,10 +121,12 @@ typedef enum {
   BFP8_SCHEDULE_AUTO = 0,
   BFP8_SCHEDULE_SWAP_AB = 1,  /* weights fill the 128-row MMA slot (small M) */
   BFP8_SCHEDULE_WIDE = 2,     /* activations fill it; 128 x 256 output tiles */
-  BFP8_SCHEDULE_GEMV = 3      /* M <= 8 only: a matrix-vector kernel on warp-level
-                                 MMAs (16 weight rows per CTA, k split over its 8
-                                 warps, no workspace use); needs K % 16 == 0 and
-                                 16-byte aligned A and B */
+  BFP8_SCHEDULE_GEMV = 3      /* M <= 32 only: the decode kernel on warp-level
+                                 MMAs (16-row weight tiles streamed by TMA, one
+                                 k-block per MMA warp, no workspace use); needs
+                                 K % 128 == 0 and 16-byte aligned A and B.  AUTO
+                                 takes it for M <= 8, and for M <= 16 when
+                                 ceil(N / 16) <= 2 x SMs */
 } bfp8_schedule;
 
 /* How the output tiles and their K dimension are shared out among CTAs when
@@ -255,7 +257,7 @@ typedef struct {
                            tiles * cluster, dp_tiles = sk_units = 0), else 1.
                            Whole tiles only: dp_tiles = tiles, sk_units = 0,
                            grid possibly below the SM count. */
-  int gemv;             /* 1: the matrix-vector kernel runs (BFP8_SCHEDULE_GEMV);
+  int gemv;             /* 1: the warp-MMA decode kernel runs (BFP8_SCHEDULE_GEMV);
                            the tile fields above then describe the tensor-core
                            plan it replaces */
   int pair;             /* 1: 256 x 256 tiles on CTA pairs (grid counts CTAs,

@@ -84,7 +84,7 @@ def test_page_correctness_case_every_schedule(oracle_mod, dev, col_major, option
 @pytest.mark.parametrize("M", wl.DECODE_MS)
 @pytest.mark.parametrize("options", [None, {"schedule": 1}, {"schedule": 2, "tile_n": 256}])
 def test_decode_sweep_full(oracle_mod, dev, M, options):
-    """AUTO (matrix-vector kernel or wide tiles) and, explicitly, swap-AB and
+    """AUTO (warp-MMA decode kernel or wide tiles) and, explicitly, swap-AB and
     256-wide tiles with partial activation rows."""
     case = wl.linear_case(M, 4096, 4096, seed=100 + M)
     _run(oracle_mod, dev, case, options=options, label=f"decode M={M} {options}")

@@ -6,7 +6,7 @@ must not allocate) cannot hand libbfp8 a workspace; this entry point uses the
 scratch array built into the library instead.  Its results must equal the
 regular entry point's bit for bit on two calls in a row (the second call finds
 the first call's leftovers in the shared scratch) on every kernel family a
-decode-sized call can take -- the matrix-vector kernel, 128- and 256-wide
+decode-sized call can take -- the warp-MMA decode kernel, 128- and 256-wide
 tiles in clusters, swap-AB tiles, re-laid-out operands and scales in the
 scratch -- and must meet the GEMM acceptance against the oracle.  (The
 default plans split no decode-sized problem stream-K within the scratch: a
@@ -45,7 +45,7 @@ def _call_noalloc(A, B, As, Bs, out):
 
 
 def _shapes():
-    # M = 1: matrix-vector kernel; 16, 64: 128-wide tiles, clusters of 4;
+    # M = 1, 16: warp-MMA decode kernel; 64: 128-wide tiles, clusters of 4;
     # 200 x 2048: 256-wide tiles; 32 x 576: 128-wide, clusters of 8;
     # 3 x 1000 x 1000: re-laid-out operands and scales in the scratch
     return [(1, 4096, 4096), (16, 4096, 4096), (64, 4096, 4096), (200, 2048, 4096),
