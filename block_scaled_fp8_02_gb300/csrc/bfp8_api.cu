@@ -377,18 +377,29 @@ int swap_tile_n(int64_t M) {
 }
 
 constexpr int64_t kSwapMaxM = 256;
-// AUTO runs the warp-MMA kernel for M <= 8 (measured faster than the tcgen05
-// kernel on every decode and Qwen3-32B shape with K % 128 == 0: N = K = 4096
-// 5.6 against 8.8 us, N = 51200, K = 5120 42.3 against 64.2, N = 5120,
-// K = 25600 35.6 against 36.3, N = 576, K = 7168 6.1 against 7.6) and for
-// M <= 16 when its 16-row tiles fit in one wave of two CTAs per SM (N = K =
-// 4096 at M = 16: 7.5 against 9.0 us; beyond one wave the doubled MMA work
-// per weight byte and the last wave's imbalance lose, e.g. N = 5120,
-// K = 25600: 51 against 36 us).
-bool gemv_preferred(int64_t M, int64_t N, int num_sms) {
-  if (M <= 8) return true;
+// AUTO runs the warp-MMA kernel for M <= 8 and, for M <= 16, when its 16-row
+// tiles fit in one wave of two CTAs per SM.  Measured on this GPU against the
+// tcgen05 plans AUTO would otherwise take (256- or 128-wide tiles, split-K),
+// M = 1, µs: N = K = 4096 6.2 against 9.1, N = 576, K = 7168 6.5 against
+// 8.5, N = 10240, K = 5120 13.7 against 14.1, N = 5120, K = 8192 11.7 against
+// 12.7, N = 51200, K = 5120 44.7 against 61.1, but N = 5120, K = 25600 31.9
+// against 26.3: past one wave the kernel's CTAs take whole tiles round-robin
+// (the CTAs stream the same k offsets together, which the DRAM favours: a
+// stream-K split of (tile, stage) ranges measured slower everywhere), so an
+// SM carries ceil(tiles / SMs) tiles against tiles / SMs on average; below 3/4
+// of that balance on a long weight stream (> 64 MB) the tcgen05 split-K plan
+// wins.  M = 16: N = K = 4096 7.5 against 9.0; beyond one wave the doubled
+// MMA work per weight byte loses (N = 5120, K = 25600: 51 against 36).
+bool gemv_preferred(int64_t M, int64_t N, int64_t K, int num_sms) {
   const int64_t tiles = (N + 15) / 16;
-  return M <= 16 && tiles <= 2 * static_cast<int64_t>(num_sms > 0 ? num_sms : 1);
+  const int64_t sms = num_sms > 0 ? num_sms : 1;
+  if (M <= 8) {
+    if (tiles <= 2 * sms) return true;
+    const int64_t most = (tiles + sms - 1) / sms;          // tiles on the busiest SM
+    const bool balanced = 4 * tiles >= 3 * most * sms;
+    return balanced || N * K <= (int64_t{64} << 20);
+  }
+  return M <= 16 && tiles <= 2 * sms;
 }
 
 // AUTO never takes the paired tiles: on this GPU they ran slower than 128-row
@@ -409,7 +420,7 @@ bfp8_status make_plan(int64_t M, int64_t N, int64_t K, int num_sms, const bfp8_g
   const int schedule = opt ? opt->schedule : BFP8_SCHEDULE_AUTO;
   p->gemv = experts == 1 && !unaligned && K % 128 == 0 && M <= kGemvMaxM &&
             (schedule == BFP8_SCHEDULE_GEMV ||
-             (schedule == BFP8_SCHEDULE_AUTO && gemv_preferred(M, N, num_sms)));
+             (schedule == BFP8_SCHEDULE_AUTO && gemv_preferred(M, N, K, num_sms)));
   if (schedule == BFP8_SCHEDULE_GEMV && !p->gemv)
     return fail(BFP8_ERR_UNSUPPORTED,
                 "options.schedule = GEMV needs M <= %d, K %% 128 == 0 and 16-byte aligned A and B "

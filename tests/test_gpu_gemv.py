@@ -74,6 +74,28 @@ def test_prefetch_weights(oracle_mod, dev, M):
          options=dict(GEMV, prefetch_weights=1), label=f"gemv prefetch M={M}")
 
 
+@pytest.mark.parametrize("M,N,K,max_ctas", [(2, 5000, 2048, 7), (8, 6000, 1024, 0), (20, 3000, 1152, 0),
+                                             (13, 5200, 640, 11), (1, 4880, 384, 0)])
+def test_multi_wave(oracle_mod, dev, M, N, K, max_ctas):
+    """More 16-row tiles than a wave of CTAs: persistent CTAs take tiles
+    round-robin (three per SM up to 8 rows; few CTAs when capped; three
+    activation column groups)."""
+    options = dict(GEMV, max_ctas=max_ctas) if max_ctas else GEMV
+    _run(oracle_mod, dev, wl.ragged_case(M, N, K, seed=M + N + K + max_ctas), True,
+         options=options, label=f"gemv multi-wave {M}x{N}x{K} cap {max_ctas}")
+
+
+def test_multi_wave_deterministic(dev):
+    case = wl.linear_case(3, 5120, 25600, seed=11)
+    q, s = bf.bfp8_group_quant(case["x"].to(dev))
+    B, Bs = case["B"].to(dev), case["Bs"].to(dev)
+    outs = [bf.bfp8_gemm(q, B, s, Bs, options=GEMV).clone() for _ in range(3)]
+    torch.cuda.synchronize()
+    assert bf.bfp8_device_status() == 0
+    for o in outs[1:]:
+        assert torch.equal(o.view(torch.int16), outs[0].view(torch.int16))
+
+
 @pytest.mark.parametrize("M,max_ctas", [(5, 1), (5, 3), (1, 7), (13, 5), (30, 2)])
 def test_max_ctas(oracle_mod, dev, M, max_ctas):
     """Few persistent CTAs: many tiles per CTA, the stage ring wraps many times."""
