@@ -55,6 +55,16 @@ def test_quant_bitwise_vs_oracle(oracle_mod, dev, M, K, dist, col_major):
     _check(oracle_mod, dev, x, col_major)
 
 
+@pytest.mark.parametrize("M,K,dist", [(1001, 4608, "normal"), (1024, 7168, "student_t3"),
+                                      (4097, 1024, "normal")])
+@pytest.mark.parametrize("col_major", [True, False])
+def test_quant_large_dense_inputs(oracle_mod, dev, M, K, dist, col_major):
+    """Large dense bf16 inputs: a step count that is not a multiple of the
+    warps' walk, heavy tails, rows of two 512-element steps."""
+    x = wl.activations(M, K, seed=M + 7 * K, dist=dist)
+    _check(oracle_mod, dev, x, col_major)
+
+
 @pytest.mark.parametrize("col_major", [True, False])
 def test_quant_page_fp32_inputs(oracle_mod, dev, col_major):
     c = wl.correctness_case()
@@ -138,7 +148,7 @@ def test_exact_ties_from_bf16_inputs(oracle_mod, dev):
 
 
 @pytest.mark.parametrize("M,K,frac", [(300, 4096, 1.0), (97, 768, 1.0), (512, 4096, 0.02),
-                                      (64, 25600, 0.3)])
+                                      (64, 25600, 0.3), (1024, 4096, 1.0), (1100, 4096, 0.3)])
 def test_exact_ties_on_the_bf16_fast_path(oracle_mod, dev, M, K, frac):
     """Exact ties on the bf16 fast path (K a multiple of 256): a fraction
     `frac` of the elements are e4m3 midpoints in groups whose amax is 448
