@@ -844,6 +844,7 @@ static bfp8_status gemm_impl(const void* A, const void* B, const float* As, int 
     ga.prefetch_b = (opt && opt->prefetch_weights == 1) ? 1 : 0;
     ga.err = d.err;
     ga.wait_limit = kWaitLimitCycles;
+    ga.as_bulk = (as_col_major && ld_as % 4 == 0 && ld_as <= 8 * cdiv(M, 8) && !misaligned(As, 16)) ? 1 : 0;
     const cudaError_t e =
         launch_gemv(tmW, tmX, ga, d.sms, (opt && opt->max_ctas > 0) ? opt->max_ctas : 0, cs);
     if (e != cudaSuccess) return fail(BFP8_ERR_CUDA, "GEMV launch: %s", cudaGetErrorString(e));

@@ -146,13 +146,27 @@ __global__ void __launch_bounds__(kGvThreads, CTAS)
     if (lane != 0) return;
     tma_prefetch_desc(&tmW);
     tma_prefetch_desc(&tmX);
-    const uint32_t stage_bytes = static_cast<uint32_t>(C::kWBytes + a.M * kGvBoxKb * 128);
+    // bytes of a stage: the weight and activation boxes, and (as_bulk) the
+    // As slice of its k-blocks that exist
+    auto as_bytes = [&](int64_t st) -> uint32_t {
+      if (!a.as_bulk) return 0u;
+      const int64_t kbs = G - st * kGvBoxKb < kGvBoxKb ? G - st * kGvBoxKb : kGvBoxKb;
+      return static_cast<uint32_t>(kbs * a.ld_as * 4);
+    };
+    auto stage_bytes = [&](int64_t st) {
+      return static_cast<uint32_t>(C::kWBytes + a.M * kGvBoxKb * 128) + as_bytes(st);
+    };
     auto issue = [&](int64_t q, int64_t tile, int64_t st, bool w, bool x) {
       const int slot = static_cast<int>(q % C::kStages);
       const uint32_t stage = sbase + static_cast<uint32_t>(slot * C::kStageBytes);
       const int32_t kb = static_cast<int32_t>(st * kGvBoxKb);
       if (w) tma_load_3d(stage, &tmW, bar_full(slot), 0, kb, static_cast<int32_t>(tile * kGvRows));
-      if (x) tma_load_3d(stage + C::kWBytes, &tmX, bar_full(slot), 0, kb, 0);
+      if (x) {
+        tma_load_3d(stage + C::kWBytes, &tmX, bar_full(slot), 0, kb, 0);
+        if (a.as_bulk)
+          bulk_load(sbase + static_cast<uint32_t>(C::kOffSc + (slot * C::kScFloats + kGvBoxKb) * 4),
+                    a.As + static_cast<int64_t>(kb) * a.ld_as, as_bytes(st), bar_full(slot));
+      }
     };
     int64_t q = 0, tile = blockIdx.x, st = 0;
     if (a.prefetch_b) {
@@ -160,7 +174,7 @@ __global__ void __launch_bounds__(kGvThreads, CTAS)
       // worth is requested before waiting for it; the activations only after
       const int64_t pre = total < C::kStages ? total : C::kStages;
       for (; q < pre; ++q, advance(tile, st)) {
-        mbar_arrive_expect_tx(bar_full(static_cast<int>(q)), stage_bytes);
+        mbar_arrive_expect_tx(bar_full(static_cast<int>(q)), stage_bytes(st));
         issue(q, tile, st, true, false);
       }
       griddep_wait();
@@ -176,7 +190,7 @@ __global__ void __launch_bounds__(kGvThreads, CTAS)
         report_failure(a.err, kDevTimeoutProducer);
         break;
       }
-      mbar_arrive_expect_tx(bar_full(slot), stage_bytes);
+      mbar_arrive_expect_tx(bar_full(slot), stage_bytes(st));
       issue(q, tile, st, true, true);
     }
     // no copy may still be landing in shared memory when the CTA exits
@@ -206,7 +220,7 @@ __global__ void __launch_bounds__(kGvThreads, CTAS)
           const int64_t kb = st * kGvBoxKb + e;
           o[i] = (live && kb < G) ? __ldg(a.Bs + (tile >> 3) * G + kb) : 0.f;
         } else {
-          if (part != 2) continue;
+          if (part != 2 || a.as_bulk) continue;
           float v = 0.f;
           if (live && e < C::kScFloats) {
             const int kbc = (e - kGvBoxKb) / (8 * NG), m = (e - kGvBoxKb) % (8 * NG);
@@ -249,7 +263,7 @@ __global__ void __launch_bounds__(kGvThreads, CTAS)
       float* dst = sc_slots + slot * C::kScFloats;
 #pragma unroll
       for (int i = 0; i < kPer; ++i)
-        if (lane + 32 * i < C::kScFloats) dst[lane + 32 * i] = v[0][i];
+        if (lane + 32 * i < (a.as_bulk ? kGvBoxKb : C::kScFloats)) dst[lane + 32 * i] = v[0][i];
       mbar_arrive(bar_full(slot));             // each lane releases its own stores
 #pragma unroll
       for (int d = 0; d + 1 < kD; ++d)
@@ -279,6 +293,9 @@ __global__ void __launch_bounds__(kGvThreads, CTAS)
   }
   // the output belongs to the preceding kernel's stream order
   griddep_wait();
+  // As of a k-block in the scale slot: the bulk-copied slice keeps the
+  // caller's column stride, the scale warp packs 8 * NG columns
+  const int sa_ld = a.as_bulk ? static_cast<int>(a.ld_as) : 8 * NG;
   float* red = reinterpret_cast<float*>(smem + C::kOffRed);
   float acc[NG][4];
 #pragma unroll
@@ -313,7 +330,7 @@ __global__ void __launch_bounds__(kGvThreads, CTAS)
 #pragma unroll
         for (int i = 0; i < 4; ++i) d[i] += e[i];
         const float2 sa = *reinterpret_cast<const float2*>(
-            sc + kGvBoxKb + warp * 8 * NG + 8 * grp + 2 * t);
+            sc + kGvBoxKb + warp * sa_ld + 8 * grp + 2 * t);
         const float s0 = __fmul_rn(sb, sa.x), s1 = __fmul_rn(sb, sa.y);
         acc[grp][0] = fmaf(d[0], s0, acc[grp][0]);
         acc[grp][1] = fmaf(d[1], s1, acc[grp][1]);

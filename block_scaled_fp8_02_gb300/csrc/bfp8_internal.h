@@ -58,6 +58,10 @@ struct GemvArgs {
   int32_t prefetch_b;    // request the first weights before the grid dependency
   int* err;              // device failure word
   unsigned long long wait_limit;
+  // 1: As is column-major with ld_as % 4 == 0, ld_as <= 8 * ceil(M / 8) and
+  // 16-byte aligned: each stage's As slice (8 k-blocks x ld_as floats,
+  // contiguous) is bulk-copied with the stage; 0: read by the scale warp
+  int32_t as_bulk;
 };
 // max_ctas > 0 caps the grid (persistent CTAs; two per SM for M <= 16).
 cudaError_t launch_gemv(const CUtensorMap& tmW, const CUtensorMap& tmX, const GemvArgs& a,

@@ -195,7 +195,9 @@ typedef struct {
  *   B    [N, K] float8_e4m3fn, row-major, row stride K bytes (the "NT" form:
  *        out = A @ B^T).
  *   As   activation scales, G = ceil(K / 128) per row:
- *          as_col_major = 1: As[kb * ld_as + m], ld_as >= M
+ *          as_col_major = 1: As[kb * ld_as + m], ld_as >= M; the buffer holds
+ *                            G * ld_as floats (rows are copied whole, as the
+ *                            [G, bfp8_scale_ld(M)] buffers of bfp8_group_quant)
  *          as_col_major = 0: As[m * ld_as + kb], ld_as >= G
  *   Bs   [ceil(N / 128), G] fp32, row-major, one scale per 128 x 128 weight tile.
  *   out  [M, N] bfloat16, row-major; each element is the fp32 accumulation of

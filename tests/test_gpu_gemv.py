@@ -68,6 +68,29 @@ def test_ragged(oracle_mod, dev, M, N, K, col_major):
          label=f"gemv ragged {M}x{N}x{K}")
 
 
+@pytest.mark.parametrize("M,ld", [(3, 16), (5, 5), (8, 12), (13, 36)])
+def test_column_major_scale_strides(oracle_mod, dev, M, ld):
+    """Column-major As whose stride rules out copying each stage's slice whole
+    (ld_as above 8 x the column groups, or not a multiple of 4): the scale
+    warp reads the scales instead."""
+    case = wl.linear_case(M, 1000, 2048 + 128, seed=M + ld)
+    x = case["x"]
+    N, K = case["N"], case["K"]
+    A, As = oracle_mod.group_quant(x.view(torch.int16).numpy().view(np.uint16), False, True)
+    G = (K + 127) // 128
+    wide = np.zeros((G, ld), dtype=np.float32)
+    wide[:, :M] = As[:, :M]
+    A_d = torch.from_numpy(A).to(dev).view(torch.float8_e4m3fn)
+    B_d = case["B"].to(dev)
+    As_d = torch.from_numpy(wide).to(dev)[:, :M].t()
+    out = bf.bfp8_gemm(A_d, B_d, As_d, case["Bs"].to(dev), options=GEMV)
+    torch.cuda.synchronize()
+    assert bf.bfp8_device_status() == 0
+    ref = oracle_mod.blocked_gemm(A, case["B"].view(torch.uint8).numpy(), As, True, case["Bs"].numpy(),
+                                  want_abs=True)
+    check_gemm(out, ref, G, label=f"gemv As ld={ld} M={M}")
+
+
 @pytest.mark.parametrize("M", [2, 24])
 def test_prefetch_weights(oracle_mod, dev, M):
     _run(oracle_mod, dev, wl.linear_case(M, 4096, 4096, seed=5 + M),
