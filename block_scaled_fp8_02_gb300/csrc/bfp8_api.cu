@@ -377,29 +377,30 @@ int swap_tile_n(int64_t M) {
 }
 
 constexpr int64_t kSwapMaxM = 256;
-// AUTO runs the warp-MMA kernel for M <= 8 and, for M <= 16, when its 16-row
-// tiles fit in one wave of two CTAs per SM.  Measured on this GPU against the
-// tcgen05 plans AUTO would otherwise take (256- or 128-wide tiles, split-K),
-// M = 1, µs: N = K = 4096 6.2 against 9.1, N = 576, K = 7168 6.5 against
-// 8.5, N = 10240, K = 5120 13.7 against 14.1, N = 5120, K = 8192 11.7 against
-// 12.7, N = 51200, K = 5120 44.7 against 61.1, but N = 5120, K = 25600 31.9
-// against 26.3: past one wave the kernel's CTAs take whole tiles round-robin
-// (the CTAs stream the same k offsets together, which the DRAM favours: a
-// stream-K split of (tile, stage) ranges measured slower everywhere), so an
-// SM carries ceil(tiles / SMs) tiles against tiles / SMs on average; below 3/4
-// of that balance on a long weight stream (> 64 MB) the tcgen05 split-K plan
-// wins.  M = 16: N = K = 4096 7.5 against 9.0; beyond one wave the doubled
-// MMA work per weight byte loses (N = 5120, K = 25600: 51 against 36).
+// AUTO runs the warp-MMA kernel for M <= 16 when its 16-row tiles fit in one
+// wave of two CTAs per SM, or past that when they keep the SMs balanced:
+// the CTAs take whole tiles round-robin (all CTAs streaming the same k
+// offsets together, which the DRAM favours: a stream-K split of (tile, stage)
+// ranges measured slower everywhere), so an SM carries ceil(tiles / SMs)
+// tiles against tiles / SMs on average, and below 3/4 of that balance the
+// tcgen05 split-K plan wins -- except for M <= 8 on weight streams up to
+// 64 MB, where the tcgen05 plans pay more for their cluster reductions.
+// Measured on this GPU (µs, against the tcgen05 plan AUTO would otherwise
+// take): M = 1: N = K = 4096 5.1 against 9.1, N = 576, K = 7168 4.7 against
+// 8.5, N = 10240, K = 5120 12.5 against 14.2, N = 5120, K = 8192 10.4 against
+// 12.8 (balance 0.70, 42 MB), N = 51200, K = 5120 40.6 against 60.6, N = 5120,
+// K = 25600 27.2 against 26.0 (0.70, 131 MB); M = 16: N = K = 4096 6.4
+// against 9.6, N = 10240 14.0 against 14.7 (0.84), N = 51200 54.5 against
+// 61.3, N = 5120, K = 8192 13.8 against 13.3 (0.70); M = 24 / 32 (one CTA per
+// SM, four MMA column groups) lose on the larger shapes and stay on tcgen05.
 bool gemv_preferred(int64_t M, int64_t N, int64_t K, int num_sms) {
+  if (M > 16) return false;
   const int64_t tiles = (N + 15) / 16;
   const int64_t sms = num_sms > 0 ? num_sms : 1;
-  if (M <= 8) {
-    if (tiles <= 2 * sms) return true;
-    const int64_t most = (tiles + sms - 1) / sms;          // tiles on the busiest SM
-    const bool balanced = 4 * tiles >= 3 * most * sms;
-    return balanced || N * K <= (int64_t{64} << 20);
-  }
-  return M <= 16 && tiles <= 2 * sms;
+  if (tiles <= 2 * sms) return true;
+  const int64_t most = (tiles + sms - 1) / sms;          // tiles on the busiest SM
+  const bool balanced = 4 * tiles >= 3 * most * sms;
+  return balanced || (M <= 8 && N * K <= (int64_t{64} << 20));
 }
 
 // AUTO never takes the paired tiles: on this GPU they ran slower than 128-row
