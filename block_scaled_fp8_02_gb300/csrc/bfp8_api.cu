@@ -377,8 +377,9 @@ int swap_tile_n(int64_t M) {
 }
 
 constexpr int64_t kSwapMaxM = 256;
-// AUTO runs the warp-MMA kernel for M <= 16 when its 16-row tiles fit in one
-// wave of two CTAs per SM, or past that when they keep the SMs balanced:
+// AUTO runs the warp-MMA kernel for M <= 24 when its 16-row tiles fit in one
+// wave of two CTAs per SM, and for M <= 16 past that when they keep the SMs
+// balanced:
 // the CTAs take whole tiles round-robin (all CTAs streaming the same k
 // offsets together, which the DRAM favours: a stream-K split of (tile, stage)
 // ranges measured slower everywhere), so an SM carries ceil(tiles / SMs)
@@ -391,13 +392,17 @@ constexpr int64_t kSwapMaxM = 256;
 // 12.8 (balance 0.70, 42 MB), N = 51200, K = 5120 40.6 against 60.6, N = 5120,
 // K = 25600 27.2 against 26.0 (0.70, 131 MB); M = 16: N = K = 4096 6.4
 // against 9.6, N = 10240 14.0 against 14.7 (0.84), N = 51200 54.5 against
-// 61.3, N = 5120, K = 8192 13.8 against 13.3 (0.70); M = 24 / 32 (one CTA per
-// SM, four MMA column groups) lose on the larger shapes and stay on tcgen05.
+// 61.3, N = 5120, K = 8192 13.8 against 13.3 (0.70).  M = 17 .. 24 (three
+// MMA column groups, two CTAs per SM) only in one wave: N = K = 4096 at
+// M = 17 / 24 7.2 / 7.3 against 9.0 / 8.9, but N = 10240, K = 5120 at M = 24
+// 17.9 against 15.0; M = 25 .. 32 (one CTA per SM) loses (N = K = 4096 at
+// M = 32: 10.3 against 8.9).
 bool gemv_preferred(int64_t M, int64_t N, int64_t K, int num_sms) {
-  if (M > 16) return false;
+  if (M > 24) return false;
   const int64_t tiles = (N + 15) / 16;
   const int64_t sms = num_sms > 0 ? num_sms : 1;
   if (tiles <= 2 * sms) return true;
+  if (M > 16) return false;
   const int64_t most = (tiles + sms - 1) / sms;          // tiles on the busiest SM
   const bool balanced = 4 * tiles >= 3 * most * sms;
   return balanced || (M <= 8 && N * K <= (int64_t{64} << 20));

@@ -24,7 +24,7 @@
 // on long weight streams).
 //
 // A CTA (8 MMA warps, a TMA warp and a scale warp; two or three CTAs per SM
-// for M <= 16, one above, so that each SM keeps ~192 KB in flight) takes 16-row
+// for M <= 24, one above, so that each SM keeps ~192 KB in flight) takes 16-row
 // weight tiles n0 = 16 * (blockIdx.x + i * gridDim.x).  In every stage warp w
 // takes k-block w: lane (g = lane / 4, t = lane % 4) reads 16 bytes of weight
 // rows g and g + 8 at k = 16t and k = 64 + 16t of the block, and the same k of
@@ -408,7 +408,7 @@ cudaError_t launch_gemv(const CUtensorMap& tmW, const CUtensorMap& tmX, const Ge
                  ? launch_ng<1, 3>(tmW, tmX, a, num_sms, max_ctas, stream)
                  : launch_ng<1, 2>(tmW, tmX, a, num_sms, max_ctas, stream);
     case 2: return launch_ng<2, 2>(tmW, tmX, a, num_sms, max_ctas, stream);
-    case 3: return launch_ng<3, 1>(tmW, tmX, a, num_sms, max_ctas, stream);
+    case 3: return launch_ng<3, 2>(tmW, tmX, a, num_sms, max_ctas, stream);
     default: return launch_ng<4, 1>(tmW, tmX, a, num_sms, max_ctas, stream);
   }
 }

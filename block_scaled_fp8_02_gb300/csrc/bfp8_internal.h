@@ -63,7 +63,7 @@ struct GemvArgs {
   // contiguous) is bulk-copied with the stage; 0: read by the scale warp
   int32_t as_bulk;
 };
-// max_ctas > 0 caps the grid (persistent CTAs; two per SM for M <= 16).
+// max_ctas > 0 caps the grid (persistent CTAs; two or three per SM up to M = 24).
 cudaError_t launch_gemv(const CUtensorMap& tmW, const CUtensorMap& tmX, const GemvArgs& a,
                         int num_sms, int max_ctas, cudaStream_t stream);
 

@@ -125,10 +125,10 @@ typedef enum {
                                  MMAs (16-row weight tiles streamed by TMA, one
                                  k-block per MMA warp, no workspace use); needs
                                  K % 128 == 0 and 16-byte aligned A and B.  AUTO
-                                 takes it for M <= 16 when its 16-row tiles fit
-                                 one wave of 2 x SMs or spread evenly enough
-                                 over the SMs (M <= 8: also for weights up to
-                                 64 MB) */
+                                 takes it for M <= 24 when its 16-row tiles fit
+                                 one wave of 2 x SMs, and for M <= 16 when they
+                                 spread evenly enough over the SMs (M <= 8:
+                                 also for weights up to 64 MB) */
 } bfp8_schedule;
 
 /* How the output tiles and their K dimension are shared out among CTAs when
