@@ -172,17 +172,18 @@ bfp8_status encode_operand(CUtensorMap* map, const void* ptr, int64_t rows, int6
 }
 
 // Tensor map over a [rows, K] uint8 matrix (row stride K bytes, K % 128 == 0)
-// viewed as [rows][K / 128][128]: box 128 x 8 x box_rows, i.e. eight k-blocks
-// of box_rows rows, landing as [row][k-block][128 bytes]; 128-byte swizzle,
-// zero fill outside the matrix (rows past `rows`, k-blocks past K / 128).
+// viewed as 128-byte k-block lines indexed (byte, row, k-block) -- strides K
+// and 128 bytes: box 128 x box_rows x 8, i.e. eight k-blocks of box_rows rows,
+// landing as [k-block][row][128 bytes]; 128-byte swizzle, zero fill outside
+// the matrix (rows past `rows`, k-blocks past K / 128).
 bfp8_status encode_kblocks(CUtensorMap* map, const void* ptr, int64_t rows, int64_t K,
                            int box_rows) {
   PFN_cuTensorMapEncodeTiled_v12000 enc;
   bfp8_status st = get_encoder(&enc);
   if (st != BFP8_OK) return st;
-  const cuuint64_t dims[3] = {128u, static_cast<cuuint64_t>(K / 128), static_cast<cuuint64_t>(rows)};
-  const cuuint64_t strides[2] = {128u, static_cast<cuuint64_t>(K)};
-  const cuuint32_t box[3] = {128u, 8u, static_cast<cuuint32_t>(box_rows)};
+  const cuuint64_t dims[3] = {128u, static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(K / 128)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(K), 128u};
+  const cuuint32_t box[3] = {128u, static_cast<cuuint32_t>(box_rows), 8u};
   const cuuint32_t estr[3] = {1u, 1u, 1u};
   CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(ptr), dims, strides, box,
                    estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,

@@ -7,10 +7,12 @@
 // in its 16-row slot (swap-AB: N in the MMA's M slot) and up to four 8-column
 // groups of activation rows; no TMEM, no clusters, no workspace.
 //
-// The weights stream through TMA.  B [N, K] is viewed as [N][K/128][128]
-// bytes; one 3-D box is 16 weight rows x 8 k-blocks (16 KB, landing as
-// [row][k-block][128 bytes] with the 128-byte swizzle), and the activations
-// of the same 8 k-blocks come as one box of M rows: a stage.  A producer lane
+// The weights stream through TMA.  B [N, K] is viewed as a 3-D tensor of
+// 128-byte k-block lines indexed (byte, row, k-block); one box is 16 weight
+// rows x 8 k-blocks (16 KB, landing k-block-major as [k-block][row][128
+// bytes] with the 128-byte swizzle, so that the 8 rows a warp's lanes read
+// at once sit in different swizzle phases: no bank conflicts), and the
+// activations of the same 8 k-blocks come as one box of M rows: a stage.  A producer lane
 // keeps a ring of 3 .. 4 stages in flight (192 KB per SM), across tile
 // boundaries, so each SM has a large share of the weights requested at once
 // -- plain per-thread loads were limited by the requests a warp can keep
@@ -94,11 +96,11 @@ __device__ __forceinline__ void mma_e4m3_16x8x32(float (&d)[4], uint32_t a0, uin
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-// Byte offset, inside a box landed as [row][8 k-blocks][128 bytes] with the
-// 128-byte swizzle (16-byte chunk index XOR the 128-byte line index mod 8), of
-// chunk c of k-block j of row r.
-__device__ __forceinline__ uint32_t box_off(int r, int j, int c) {
-  const int line = r * kGvBoxKb + j;
+// Byte offset, inside a box of `rows` rows landed as [8 k-blocks][rows][128
+// bytes] with the 128-byte swizzle (16-byte chunk index XOR the 128-byte line
+// index mod 8, the box starting on 1 KB), of chunk c of k-block j of row r.
+__device__ __forceinline__ uint32_t box_off(int r, int j, int c, int rows) {
+  const int line = j * rows + r;
   return static_cast<uint32_t>(line * 128 + ((c ^ (line & 7)) << 4));
 }
 
@@ -160,9 +162,9 @@ __global__ void __launch_bounds__(kGvThreads, CTAS)
       const int slot = static_cast<int>(q % C::kStages);
       const uint32_t stage = sbase + static_cast<uint32_t>(slot * C::kStageBytes);
       const int32_t kb = static_cast<int32_t>(st * kGvBoxKb);
-      if (w) tma_load_3d(stage, &tmW, bar_full(slot), 0, kb, static_cast<int32_t>(tile * kGvRows));
+      if (w) tma_load_3d(stage, &tmW, bar_full(slot), 0, static_cast<int32_t>(tile * kGvRows), kb);
       if (x) {
-        tma_load_3d(stage + C::kWBytes, &tmX, bar_full(slot), 0, kb, 0);
+        tma_load_3d(stage + C::kWBytes, &tmX, bar_full(slot), 0, 0, kb);
         if (a.as_bulk)
           bulk_load(sbase + static_cast<uint32_t>(C::kOffSc + (slot * C::kScFloats + kGvBoxKb) * 4),
                     a.As + static_cast<int64_t>(kb) * a.ld_as, as_bytes(st), bar_full(slot));
@@ -280,16 +282,16 @@ __global__ void __launch_bounds__(kGvThreads, CTAS)
   const int g = lane >> 2, t = lane & 3;
   // per-lane offsets inside a stage: weight rows g and g + 8, chunks t and
   // t + 4 (k = 16t .., 64 + 16t ..) of k-block `warp`
-  const uint32_t w0a = box_off(g, warp, t);
-  const uint32_t w0b = box_off(g, warp, t + 4);
-  const uint32_t w1a = box_off(g + 8, warp, t);
-  const uint32_t w1b = box_off(g + 8, warp, t + 4);
+  const uint32_t w0a = box_off(g, warp, t, kGvRows);
+  const uint32_t w0b = box_off(g, warp, t + 4, kGvRows);
+  const uint32_t w1a = box_off(g + 8, warp, t, kGvRows);
+  const uint32_t w1b = box_off(g + 8, warp, t + 4, kGvRows);
   uint32_t xa[NG], xb[NG];                   // activation row 8 grp + g (rows past M: row M-1)
 #pragma unroll
   for (int grp = 0; grp < NG; ++grp) {
     const int m = (8 * grp + g < a.M) ? 8 * grp + g : a.M - 1;
-    xa[grp] = C::kWBytes + box_off(m, warp, t);
-    xb[grp] = C::kWBytes + box_off(m, warp, t + 4);
+    xa[grp] = C::kWBytes + box_off(m, warp, t, a.M);
+    xb[grp] = C::kWBytes + box_off(m, warp, t + 4, a.M);
   }
   // the output belongs to the preceding kernel's stream order
   griddep_wait();
