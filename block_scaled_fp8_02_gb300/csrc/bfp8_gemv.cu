@@ -12,21 +12,22 @@
 // rows x 8 k-blocks (16 KB, landing k-block-major as [k-block][row][128
 // bytes] with the 128-byte swizzle, so that the 8 rows a warp's lanes read
 // at once sit in different swizzle phases: no bank conflicts), and the
-// activations of the same 8 k-blocks come as one box of M rows: a stage.  A producer lane
-// keeps a ring of 3 .. 4 stages in flight (192 KB per SM), across tile
-// boundaries, so each SM has a large share of the weights requested at once
+// activations of the same 8 k-blocks come as one box of M rows: a stage.  A
+// producer lane keeps a ring of 2 .. 4 stages in flight (up to 192 KB per
+// SM), across tile boundaries, so each SM has a large share of the weights requested at once
 // -- plain per-thread loads were limited by the requests a warp can keep
 // outstanding.  With the weight prefetch, the first ring of weights and
 // weight scales is requested before the preceding kernel completes.
-// A third role, the scale warp, reads each stage's scales (Bs of the tile's
-// 128-row block and As of the M rows, for its 8 k-blocks) with plain loads
-// several stages ahead and parks them in a per-stage slot that completes on
-// the stage's barrier: the MMA warps never wait on a global load (reading
-// the scales themselves, a few stages ahead, cost a third of the bandwidth
-// on long weight streams).
+// Each stage's scales land in a per-stage slot that completes on the stage's
+// barrier, so the MMA warps never wait on a global load (reading the scales
+// themselves, a few stages ahead, cost a third of the bandwidth on long
+// weight streams): the As slice of the stage's 8 k-blocks (contiguous in the
+// column-major layout) is bulk-copied with the activation box, and a third
+// role, the scale warp, reads the Bs of the tile's 128-row block (and As in
+// other layouts) with plain loads several stages ahead.
 //
 // A CTA (8 MMA warps, a TMA warp and a scale warp; two or three CTAs per SM
-// for M <= 24, one above, so that each SM keeps ~192 KB in flight) takes 16-row
+// for M <= 24, one above) takes 16-row
 // weight tiles n0 = 16 * (blockIdx.x + i * gridDim.x).  In every stage warp w
 // takes k-block w: lane (g = lane / 4, t = lane % 4) reads 16 bytes of weight
 // rows g and g + 8 at k = 16t and k = 64 + 16t of the block, and the same k of
@@ -59,16 +60,16 @@ constexpr int kGvWarps = 8;                 // MMA warps = k-blocks per stage
 constexpr int kGvThreads = (kGvWarps + 2) * 32;   // + TMA warp + scale warp
 constexpr int kGvRows = 16;                 // weight rows per tile
 constexpr int kGvBoxKb = 8;                 // k-blocks per TMA box = per stage
-constexpr int kGvRingPerSm = 192 * 1024;    // bytes of stages in flight per SM
 
-// NG: 8-column groups of activation rows (M <= 8 * NG); CTAS: CTAs per SM
-template <int NG, int CTAS>
+// NG: 8-column groups of activation rows (M <= 8 * NG); CTAS: CTAs per SM;
+// STAGES: depth of the ring
+template <int NG, int CTAS, int STAGES>
 struct GvCfg {
   static constexpr int kCtas = CTAS;
   static constexpr int kWBytes = kGvRows * kGvBoxKb * 128;      // one weight box
   static constexpr int kXBytes = 8 * NG * kGvBoxKb * 128;       // room for one activation box
   static constexpr int kStageBytes = kWBytes + kXBytes;         // 8 k-blocks
-  static constexpr int kStages = kGvRingPerSm / kCtas / kStageBytes;
+  static constexpr int kStages = STAGES;
   // stages of scales the scale warp has in flight
   static constexpr int kScAhead = kCtas >= 3 ? 2 : 4;
   // scale slot of a stage: Bs of its 8 k-blocks, then As[k-block][column]
@@ -104,11 +105,11 @@ __device__ __forceinline__ uint32_t box_off(int r, int j, int c, int rows) {
   return static_cast<uint32_t>(line * 128 + ((c ^ (line & 7)) << 4));
 }
 
-template <int NG, int CTAS>
+template <int NG, int CTAS, int STAGES>
 __global__ void __launch_bounds__(kGvThreads, CTAS)
     gemv_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
                 const __grid_constant__ GemvArgs a) {
-  using C = GvCfg<NG, CTAS>;
+  using C = GvCfg<NG, CTAS, STAGES>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -369,11 +370,11 @@ __global__ void __launch_bounds__(kGvThreads, CTAS)
   }
 }
 
-template <int NG, int CTAS>
+template <int NG, int CTAS, int STAGES>
 cudaError_t launch_ng(const CUtensorMap& tmW, const CUtensorMap& tmX, const GemvArgs& a,
                       int num_sms, int max_ctas, cudaStream_t stream) {
-  using C = GvCfg<NG, CTAS>;
-  cudaError_t e = cudaFuncSetAttribute(gemv_kernel<NG, CTAS>,
+  using C = GvCfg<NG, CTAS, STAGES>;
+  cudaError_t e = cudaFuncSetAttribute(gemv_kernel<NG, CTAS, STAGES>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;
   const int64_t tiles = (a.N + kGvRows - 1) / kGvRows;
@@ -390,7 +391,7 @@ cudaError_t launch_ng(const CUtensorMap& tmW, const CUtensorMap& tmX, const Gemv
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, gemv_kernel<NG, CTAS>, tmW, tmX, a);
+  return cudaLaunchKernelEx(&cfg, gemv_kernel<NG, CTAS, STAGES>, tmW, tmX, a);
 }
 
 }  // namespace
@@ -398,20 +399,23 @@ cudaError_t launch_ng(const CUtensorMap& tmW, const CUtensorMap& tmX, const Gemv
 cudaError_t launch_gemv(const CUtensorMap& tmW, const CUtensorMap& tmX, const GemvArgs& a,
                         int num_sms, int max_ctas, cudaStream_t stream) {
   if (a.M < 1 || a.M > kGemvMaxM || a.N < 1 || a.G < 1 || num_sms < 1) return cudaErrorInvalidValue;
-  // M <= 8: two CTAs per SM with a 4-stage ring (a 4096-deep tile in flight
-  // at once) while the tiles fit in one such wave, else three with a 2-stage
-  // ring (more streams per SM, a shorter last wave): measured N = K = 4096
-  // 6.2 against 6.8 us, N = 5120, K = 25600 42.7 against 32.0, N = 51200,
-  // K = 5120 50.3 against 44.9 (two against three)
+  // M <= 8: two CTAs per SM while the tiles fit in one such wave, else three
+  // with a 2-stage ring (more streams per SM, a shorter last wave): measured
+  // N = K = 4096 6.2 against 6.8 us, N = 5120, K = 25600 42.7 against 32.0,
+  // N = 51200, K = 5120 50.3 against 44.9 (two against three).  In one wave,
+  // a 4-stage ring (a 4096-deep tile in flight at once) while each SM holds
+  // one tile, a 3-stage ring once SMs hold two: N = K = 4096 4.96 against
+  // 5.08 us, N = 4864 5.44 against 5.63, but N = 2048 4.40 against 4.20.
   const int64_t tiles = (a.N + kGvRows - 1) / kGvRows;
+  const int64_t sms = num_sms;
   switch ((a.M + 7) / 8) {
     case 1:
-      return tiles > 2 * static_cast<int64_t>(num_sms)
-                 ? launch_ng<1, 3>(tmW, tmX, a, num_sms, max_ctas, stream)
-                 : launch_ng<1, 2>(tmW, tmX, a, num_sms, max_ctas, stream);
-    case 2: return launch_ng<2, 2>(tmW, tmX, a, num_sms, max_ctas, stream);
-    case 3: return launch_ng<3, 2>(tmW, tmX, a, num_sms, max_ctas, stream);
-    default: return launch_ng<4, 1>(tmW, tmX, a, num_sms, max_ctas, stream);
+      if (tiles > 2 * sms) return launch_ng<1, 3, 2>(tmW, tmX, a, num_sms, max_ctas, stream);
+      if (tiles > sms) return launch_ng<1, 2, 3>(tmW, tmX, a, num_sms, max_ctas, stream);
+      return launch_ng<1, 2, 4>(tmW, tmX, a, num_sms, max_ctas, stream);
+    case 2: return launch_ng<2, 2, 3>(tmW, tmX, a, num_sms, max_ctas, stream);
+    case 3: return launch_ng<3, 2, 2>(tmW, tmX, a, num_sms, max_ctas, stream);
+    default: return launch_ng<4, 1, 4>(tmW, tmX, a, num_sms, max_ctas, stream);
   }
 }
 
