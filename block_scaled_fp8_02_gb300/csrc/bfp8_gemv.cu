@@ -10,12 +10,12 @@
 // The weights stream through TMA.  B [N, K] is viewed as a 3-D tensor of
 // 128-byte k-block lines indexed (byte, row, k-block); one box is 16 weight
 // rows x 8 k-blocks (16 KB, landing k-block-major as [k-block][row][128
-// bytes] with the 128-byte swizzle, so that the 8 rows a warp's lanes read
-// at once sit in different swizzle phases: no bank conflicts), and the
-// activations of the same 8 k-blocks come as one box of M rows: a stage.  A
-// producer lane keeps a ring of 2 .. 4 stages in flight (up to 192 KB per
-// SM), across tile boundaries, so each SM has a large share of the weights requested at once
-// -- plain per-thread loads were limited by the requests a warp can keep
+// bytes] with the 128-byte swizzle, so that rows four apart in a k-block sit
+// four swizzle phases apart), and the activations of the same 8 k-blocks
+// come as one box of M rows: a stage.  A producer lane keeps a ring of
+// 2 .. 4 stages in flight (up to 192 KB per SM), across tile boundaries, so
+// each SM has a large share of the weights requested at once -- plain
+// per-thread loads were limited by the requests a warp can keep
 // outstanding.  With the weight prefetch, the first ring of weights and
 // weight scales is requested before the preceding kernel completes.
 // Each stage's scales land in a per-stage slot that completes on the stage's
@@ -30,8 +30,10 @@
 // for M <= 24, one above) takes 16-row
 // weight tiles n0 = 16 * (blockIdx.x + i * gridDim.x).  In every stage warp w
 // takes k-block w: lane (g = lane / 4, t = lane % 4) reads 16 bytes of weight
-// rows g and g + 8 at k = 16t and k = 64 + 16t of the block, and the same k of
-// activation row g of each column group, and issues four MMAs per group whose
+// rows p and p + 8 at k = 16t and k = 64 + 16t of the block, p = g / 2 +
+// 4 (g % 2), and the same k of activation row p of each column group (the
+// permutation spreads each quarter-warp's rows over all banks), and issues
+// four MMAs per group whose
 // fragment slots hold the same absolute k on both operands (the MMA's k order
 // is a permutation of the block's, which a dot product does not see), as two
 // chains of two that are added at the end.  The k-block's 16 x 8 partial is
@@ -281,16 +283,22 @@ __global__ void __launch_bounds__(kGvThreads, CTAS)
 
   // ------------------------------------------------------------- MMA warps
   const int g = lane >> 2, t = lane & 3;
-  // per-lane offsets inside a stage: weight rows g and g + 8, chunks t and
+  // Fragment row (and column) g holds weight row (activation row) pg: a
+  // 16-byte shared load is served a quarter-warp (lanes of g = 2q, 2q + 1) at
+  // a time, and pg = q, q + 4 puts those two rows four swizzle phases apart,
+  // on disjoint banks.  D column c therefore belongs to activation row
+  // p(c): columns 2t, 2t + 1 to rows t, t + 4 of the column group.
+  const int pg = (g >> 1) + 4 * (g & 1);
+  // per-lane offsets inside a stage: weight rows pg and pg + 8, chunks t and
   // t + 4 (k = 16t .., 64 + 16t ..) of k-block `warp`
-  const uint32_t w0a = box_off(g, warp, t, kGvRows);
-  const uint32_t w0b = box_off(g, warp, t + 4, kGvRows);
-  const uint32_t w1a = box_off(g + 8, warp, t, kGvRows);
-  const uint32_t w1b = box_off(g + 8, warp, t + 4, kGvRows);
-  uint32_t xa[NG], xb[NG];                   // activation row 8 grp + g (rows past M: row M-1)
+  const uint32_t w0a = box_off(pg, warp, t, kGvRows);
+  const uint32_t w0b = box_off(pg, warp, t + 4, kGvRows);
+  const uint32_t w1a = box_off(pg + 8, warp, t, kGvRows);
+  const uint32_t w1b = box_off(pg + 8, warp, t + 4, kGvRows);
+  uint32_t xa[NG], xb[NG];                   // activation row 8 grp + pg (rows past M: row M-1)
 #pragma unroll
   for (int grp = 0; grp < NG; ++grp) {
-    const int m = (8 * grp + g < a.M) ? 8 * grp + g : a.M - 1;
+    const int m = (8 * grp + pg < a.M) ? 8 * grp + pg : a.M - 1;
     xa[grp] = C::kWBytes + box_off(m, warp, t, a.M);
     xb[grp] = C::kWBytes + box_off(m, warp, t + 4, a.M);
   }
@@ -332,9 +340,8 @@ __global__ void __launch_bounds__(kGvThreads, CTAS)
         mma_e4m3_16x8x32(e, u0b.z, u1b.z, u0b.w, u1b.w, vb.z, vb.w);
 #pragma unroll
         for (int i = 0; i < 4; ++i) d[i] += e[i];
-        const float2 sa = *reinterpret_cast<const float2*>(
-            sc + kGvBoxKb + warp * sa_ld + 8 * grp + 2 * t);
-        const float s0 = __fmul_rn(sb, sa.x), s1 = __fmul_rn(sb, sa.y);
+        const float* sa = sc + kGvBoxKb + warp * sa_ld + 8 * grp + t;   // rows t, t + 4
+        const float s0 = __fmul_rn(sb, sa[0]), s1 = __fmul_rn(sb, sa[4]);
         acc[grp][0] = fmaf(d[0], s0, acc[grp][0]);
         acc[grp][1] = fmaf(d[1], s1, acc[grp][1]);
         acc[grp][2] = fmaf(d[2], s0, acc[grp][2]);
@@ -348,12 +355,13 @@ __global__ void __launch_bounds__(kGvThreads, CTAS)
       // tile done: the 8 warps' partials, added in warp order
 #pragma unroll
       for (int grp = 0; grp < NG; ++grp) {
-        float* r0 = red + (warp * kGvRows + g) * C::kRedPitch + 8 * grp + 2 * t;
+        // weight rows pg, pg + 8; activation rows 8 grp + t, 8 grp + t + 4
+        float* r0 = red + (warp * kGvRows + pg) * C::kRedPitch + 8 * grp + t;
         float* r1 = r0 + 8 * C::kRedPitch;
         r0[0] = acc[grp][0];
-        r0[1] = acc[grp][1];
+        r0[4] = acc[grp][1];
         r1[0] = acc[grp][2];
-        r1[1] = acc[grp][3];
+        r1[4] = acc[grp][3];
         acc[grp][0] = acc[grp][1] = acc[grp][2] = acc[grp][3] = 0.f;
       }
       named_bar_sync(1, kGvWarps * 32);
