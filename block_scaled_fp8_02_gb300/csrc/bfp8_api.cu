@@ -380,24 +380,24 @@ int swap_tile_n(int64_t M) {
 constexpr int64_t kSwapMaxM = 256;
 // AUTO runs the warp-MMA kernel for M <= 24 when its 16-row tiles fit in one
 // wave of two CTAs per SM, and for M <= 16 past that when they keep the SMs
-// balanced:
-// the CTAs take whole tiles round-robin (all CTAs streaming the same k
-// offsets together, which the DRAM favours: a stream-K split of (tile, stage)
-// ranges measured slower everywhere), so an SM carries ceil(tiles / SMs)
-// tiles against tiles / SMs on average, and below 3/4 of that balance the
-// tcgen05 split-K plan wins -- except for M <= 8 on weight streams up to
-// 64 MB, where the tcgen05 plans pay more for their cluster reductions.
-// Measured on this GPU (µs, against the tcgen05 plan AUTO would otherwise
-// take): M = 1: N = K = 4096 5.1 against 9.1, N = 576, K = 7168 4.7 against
-// 8.5, N = 10240, K = 5120 12.5 against 14.2, N = 5120, K = 8192 10.4 against
-// 12.8 (balance 0.70, 42 MB), N = 51200, K = 5120 40.6 against 60.6, N = 5120,
-// K = 25600 27.2 against 26.0 (0.70, 131 MB); M = 16: N = K = 4096 6.4
-// against 9.6, N = 10240 14.0 against 14.7 (0.84), N = 51200 54.5 against
-// 61.3, N = 5120, K = 8192 13.8 against 13.3 (0.70).  M = 17 .. 24 (three
+// balanced or the weight stream is short: the CTAs take whole tiles
+// round-robin (all CTAs streaming the same k offsets together, which the
+// DRAM favours: a stream-K split of (tile, stage) ranges measured slower
+// everywhere), so an SM carries ceil(tiles / SMs) tiles against tiles / SMs
+// on average; below 3/4 of that balance the tcgen05 split-K plan wins on
+// long streams, while up to 64 MB of weights the tcgen05 plans pay more for
+// their cluster reductions.  Measured on this GPU (µs, against the tcgen05
+// plan AUTO would otherwise take): M = 1: N = K = 4096 4.9 against 9.1,
+// N = 576, K = 7168 4.7 against 8.5, N = 51200, K = 5120 40.3 against 60.6,
+// N = 5120, K = 25600 26.3 against 26.4 (balance 0.70, 131 MB); M = 16:
+// N = K = 4096 5.9 against 9.6, N = 4880 7.95 against 10.3 (305 tiles,
+// balance 0.67), N = 5120, K = 8192 12.8 against 13.4 (0.70, 42 MB), N =
+// 10240, K = 5120 12.8 against 12.8 (0.84), N = 51200 50.9 against 61.3,
+// N = 5120, K = 25600 34.2 against 27.6 (0.70, 131 MB).  M = 17 .. 24 (three
 // MMA column groups, two CTAs per SM) only in one wave: N = K = 4096 at
-// M = 17 / 24 7.2 / 7.3 against 9.0 / 8.9, but N = 10240, K = 5120 at M = 24
-// 17.9 against 15.0; M = 25 .. 32 (one CTA per SM) loses (N = K = 4096 at
-// M = 32: 10.3 against 8.9).
+// M = 24 6.8 against 8.9, but N = 10240, K = 5120 16.5 against 15.0 and
+// N = 51200 65.3 against 61.2; M = 25 .. 32 (one CTA per SM) loses (N = K =
+// 4096 at M = 32: 9.4 against 8.9).
 bool gemv_preferred(int64_t M, int64_t N, int64_t K, int num_sms) {
   if (M > 24) return false;
   const int64_t tiles = (N + 15) / 16;
@@ -406,7 +406,7 @@ bool gemv_preferred(int64_t M, int64_t N, int64_t K, int num_sms) {
   if (M > 16) return false;
   const int64_t most = (tiles + sms - 1) / sms;          // tiles on the busiest SM
   const bool balanced = 4 * tiles >= 3 * most * sms;
-  return balanced || (M <= 8 && N * K <= (int64_t{64} << 20));
+  return balanced || N * K <= (int64_t{64} << 20);
 }
 
 // AUTO never takes the paired tiles: on this GPU they ran slower than 128-row

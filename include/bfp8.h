@@ -127,8 +127,8 @@ typedef enum {
                                  K % 128 == 0 and 16-byte aligned A and B.  AUTO
                                  takes it for M <= 24 when its 16-row tiles fit
                                  one wave of 2 x SMs, and for M <= 16 when they
-                                 spread evenly enough over the SMs (M <= 8:
-                                 also for weights up to 64 MB) */
+                                 spread evenly enough over the SMs or the
+                                 weights take up to 64 MB */
 } bfp8_schedule;
 
 /* How the output tiles and their K dimension are shared out among CTAs when

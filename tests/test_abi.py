@@ -328,15 +328,15 @@ def test_gemv_plans(L):
         with pytest.raises(bf.BFP8Error):
             bf.bfp8_gemm_plan(M, N, K, 152, G, **kw)
     assert bf.bfp8_gemm_plan(64, 4096, 4096, 152)["gemv"] == 0
-    # AUTO, M <= 16: one wave of 2 x SMs, or past it SMs balanced to 3/4
-    # (M <= 8 also on weight streams up to 64 MB)
+    # AUTO, M <= 16: one wave of 2 x SMs, or past it SMs balanced to 3/4 or
+    # weight streams up to 64 MB
     for M, N, K in ((1, 4096, 4096), (8, 10240, 5120), (1, 5120, 8192), (1, 51200, 5120),
                     (1, 576, 7168), (9, 4096, 4096), (16, 4864, 4096), (16, 10240, 5120),
-                    (16, 51200, 5120), (12, 6144, 4096)):
+                    (16, 51200, 5120), (12, 6144, 4096), (16, 5120, 8192), (16, 4880, 4096)):
         assert bf.bfp8_gemm_plan(M, N, K, 152)["gemv"] == 1, (M, N, K)
     for M, N, K in ((17, 4096, 4096), (24, 4864, 4096)):          # M 17..24: one wave only
         assert bf.bfp8_gemm_plan(M, N, K, 152)["gemv"] == 1, (M, N, K)
-    for M, N, K in ((1, 5120, 25600), (16, 5120, 8192), (16, 4880, 4096), (24, 10240, 5120),
+    for M, N, K in ((1, 5120, 25600), (16, 5120, 25600), (17, 4880, 4096), (24, 10240, 5120),
                     (25, 4096, 4096), (1, 4096, 4112)):
         assert bf.bfp8_gemm_plan(M, N, K, 152)["gemv"] == 0, (M, N, K)
     assert bf.bfp8_gemm_plan(1, 4096, 4096, 152, {"schedule": bf.SCHEDULE_SWAP_AB})["gemv"] == 0
