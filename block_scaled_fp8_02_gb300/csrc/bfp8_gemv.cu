@@ -27,20 +27,19 @@
 // other layouts) with plain loads several stages ahead.
 //
 // A CTA (8 MMA warps, a TMA warp and a scale warp; two or three CTAs per SM
-// for M <= 24, one above) takes 16-row
-// weight tiles n0 = 16 * (blockIdx.x + i * gridDim.x).  In every stage warp w
-// takes k-block w: lane (g = lane / 4, t = lane % 4) reads 16 bytes of weight
-// rows p and p + 8 at k = 16t and k = 64 + 16t of the block, p = g / 2 +
-// 4 (g % 2), and the same k of activation row p of each column group (the
-// permutation spreads each quarter-warp's rows over all banks), and issues
-// four MMAs per group whose
-// fragment slots hold the same absolute k on both operands (the MMA's k order
-// is a permutation of the block's, which a dot product does not see), as two
-// chains of two that are added at the end.  The k-block's 16 x 8 partial is
-// scaled by Bs[n/128, kb] * As[m, kb] into fp32 accumulators (the blocked
-// definition of the vLLM PR 49932 digest's matmul).  At the end of a tile the
-// 8 warps' partials are added in warp order in shared memory (deterministic)
-// and rounded to bf16.
+// for M <= 24, one above) takes 16-row weight tiles n0 = 16 * (blockIdx.x +
+// i * gridDim.x).  In every stage warp w takes k-block w: lane (g = lane / 4,
+// t = lane % 4) reads 16 bytes of weight rows p and p + 8 at k = 16t and
+// k = 64 + 16t of the block, p = g / 2 + 4 (g % 2), and the same k of
+// activation row p of each column group (the permutation spreads each
+// quarter-warp's rows over all banks), and issues four MMAs per group whose
+// fragment slots hold the same absolute k on both operands (the MMA's k
+// order is a permutation of the block's, which a dot product does not see),
+// as two chains of two that are added at the end.  The k-block's 16 x 8
+// partial is scaled by Bs[n/128, kb] * As[m, kb] into fp32 accumulators (the
+// blocked definition of the vLLM PR 49932 digest's matmul).  At the end of a
+// tile the 8 warps' partials are added in warp order in shared memory
+// (deterministic) and rounded to bf16.
 //
 // Every barrier wait is bounded: a wait that gives up records
 // BFP8_DEV_TIMEOUT_* in the failure word and the kernel winds down.
